@@ -1,0 +1,586 @@
+"""FlashMap one-jump block-draft step: the oracle.
+
+TEST INFRASTRUCTURE ONLY. This module is a plain, slow, obviously correct CPU
+statement of what the block-draft step computes, written in NumPy float64 from
+the FlashMap pages. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import or run it; the library
+(``include/flashmap.h`` and the CUDA sources) never does, and this module imports
+nothing from the library. The two share no code, tables or constants.
+
+Sources (each function cites the page and the section it follows):
+  * ``flashmap/modeling_flashmap.py`` -- the transformers reference model
+    (``rope_tables``, ``apply_rope``, ``FlashMapRMSNorm``, ``FlashMapTimeEmbedding``,
+    ``FlashMapAdaLayerNorm``, ``FlashMapAttention``, ``FlashMapLayer``,
+    ``FlashMapDraftModel.extend_context / mix_state / target_constants / draft``).
+  * ``flashmap/configuration_flashmap.py`` -- ``FlashMapConfig``, ``DEFAULT_JUMP_GRIDS``.
+  * ``flashmap/sglang/model.py`` -- the one-jump shortcut (``_draft_impl``), the
+    all-layer context K/V weight (``load_weights``), the fold (``_fold_lm_head``),
+    the anchor row (``forward``, ``_anchor_kv_impl``), the commit-masked write
+    (``write_target_hidden_kv``), FP8 copies (``_quantize_fp8``).
+  * ``flashmap/vllm/model.py`` -- position-keyed draft noise (module docstring,
+    ``_noise``), ``seqused_k = p + 1`` (``_prologue``), the modulation table
+    ``(layers, 9, dim)`` (``prepare``).
+  * ``flashmap/sglang/sampler.py`` -- whole-block sampling, Gumbel-max with
+    in-kernel Philox, the ``-inf`` full-vocabulary scatter (module docstring,
+    ``IdentityMarkov.sample_block``, ``_FullLogits``).
+  * tokenspeed ``dflash.py`` -- ``req_to_page`` / ``page_size`` slot addressing
+    (``DFlash._draft_native``, ``compute_out_cache_loc_uniform``).
+  * Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+    as 1, 2, 3" (SC'11), section 3 (the Philox round and key schedule).
+
+Readings where the pages are silent (listed with their reasons in the design doc):
+  R1 the noise of slot k of request b is keyed by (seed_b, position p_b+1+k);
+  R2 Philox4x32-10 with key (seed lo32, seed hi32); counter (j/4, position,
+     domain, step) with domain 0 = DiT noise (step 0), 1 = Gumbel noise;
+  R3 a word w maps to U = ((w >> 9) + 1/2) * 2^-23, exact in float32, in (0, 1);
+  R4 normals by Box-Muller on the word pairs (w0, w1) and (w2, w3);
+  R5 Gumbel-max: token = argmax_j (l_j / T + G_j), G = -ln(-ln U); lowest index
+     wins ties; T <= 0 or greedy -> argmax_j l_j;
+  R6 RoPE angle = float32(float32(p) * inv_freq), inv_freq = float32(theta^(-2i/hd)).
+
+Pinning (what fixes each function other than itself; see tests/test_oracle_pins.py):
+  philox4x32_10          published known-answer vectors (tests/golden/philox_kat.txt)
+  uniform/normals/gumbel exact word->U map; moments, KS and chi-square laws
+  rope                   closed-form rotation, norm, relative-position identity
+  rms_norm/layer_norm/   closed forms and library routines (scipy erf / norm.cdf)
+  gelu/silu/time_embed
+  attention              brute-force pure-Python softmax on tiny shapes
+  load_constants         L L^T = E^T E; fold identity; uniform constant closed form;
+                         cov(z L^T) vs E^T E and vs direct x0 @ E draws
+  slots/out_loc          brute-force page walk
+  sample_rows            greedy = argmax; Gumbel-max frequencies vs softmax(l/T);
+                         row independence; -inf outside the draft vocabulary
+  draft_request          parity unpinned beyond the composition of the pinned
+                         parts plus structural cases (zero gates, one-position
+                         context, seed independence at noise_scale 0)
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+from scipy.special import erf
+
+# ---------------------------------------------------------------------------------
+# Configuration and constants printed on the pages
+# ---------------------------------------------------------------------------------
+
+# configuration_flashmap.py, DEFAULT_JUMP_GRIDS: jump times per number of steps,
+# endpoints exactly 0 and 1. The one-jump step uses grid "1".
+DEFAULT_JUMP_GRIDS = {
+    "1": [0.0, 1.0],
+    "2": [0.0, 0.8172569274902344, 1.0],
+    "3": [0.0, 0.8010796308517456, 0.8310279846191406, 1.0],
+    "4": [0.0, 0.7906050682067871, 0.8172569274902344, 0.8379518389701843, 1.0],
+}
+
+
+@dataclass
+class Config:
+    """FlashMapConfig (configuration_flashmap.py) restricted to the fields the
+    one-jump draft step reads, plus the paging of the draft KV pool."""
+
+    target_hidden: int
+    num_target_layers: int
+    hidden: int
+    num_layers: int
+    num_heads: int
+    head_dim: int
+    intermediate: int
+    cond_dim: int
+    time_embed_dim: int
+    block_size: int
+    vocab_size: int
+    draft_vocab_size: int
+    page_size: int
+    rope_theta: float = 1e4
+    time_scale: float = 1000.0
+    rms_norm_eps: float = 1e-6
+    qk_norm_eps: float = 1e-5
+    layer_norm_eps: float = 1e-6
+    noise_gate_constant: bool = False  # False: "jump" gate, True: "constant"
+    num_steps: int = 1
+
+    @staticmethod
+    def from_dict(d: dict) -> "Config":
+        names = Config.__dataclass_fields__.keys()
+        return Config(**{k: d[k] for k in names if k in d})
+
+
+# ---------------------------------------------------------------------------------
+# Philox4x32-10 and the noise built from it (Salmon et al., SC'11, section 3)
+# ---------------------------------------------------------------------------------
+
+_MASK32 = np.uint64(0xFFFFFFFF)
+# The Philox4x32 round multipliers and the Weyl key increments of the paper.
+_PHILOX_M0 = np.uint64(0xD2511F53)
+_PHILOX_M1 = np.uint64(0xCD9E8D57)
+_PHILOX_W0 = np.uint64(0x9E3779B9)
+_PHILOX_W1 = np.uint64(0xBB67AE85)
+
+
+def philox4x32_10(counters, keys) -> np.ndarray:
+    """Philox4x32 with 10 rounds (Salmon et al., section 3).
+
+    counters: (n, 4) uint32 words (c0, c1, c2, c3); keys: (n, 2) uint32 (k0, k1).
+    A round multiplies c0 and c2 by the two multipliers into 64-bit products
+    (hi, lo) and outputs (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0); the key is
+    bumped by the Weyl constants between rounds. Returns (n, 4) uint32."""
+    c = np.asarray(counters, dtype=np.uint64).reshape(-1, 4).copy()
+    k = np.asarray(keys, dtype=np.uint64).reshape(-1, 2).copy()
+    c0, c1, c2, c3 = c[:, 0], c[:, 1], c[:, 2], c[:, 3]
+    k0, k1 = k[:, 0], k[:, 1]
+    for r in range(10):
+        if r:
+            k0 = (k0 + _PHILOX_W0) & _MASK32
+            k1 = (k1 + _PHILOX_W1) & _MASK32
+        p0 = _PHILOX_M0 * c0  # < 2^64: exact in uint64
+        p1 = _PHILOX_M1 * c2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _MASK32
+        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+    return np.stack([c0, c1, c2, c3], axis=1).astype(np.uint32)
+
+
+def seed_key(seed: int) -> tuple[int, int]:
+    """Reading R2: the Philox key of a request's 64-bit seed (lo32, hi32)."""
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    return seed & 0xFFFFFFFF, seed >> 32
+
+
+def word_to_uniform(w) -> np.ndarray:
+    """Reading R3: U = ((w >> 9) + 1/2) * 2^-23, in (0, 1); every value is exact
+    in float32 (23 significant bits plus the half)."""
+    w = np.asarray(w, dtype=np.uint64)
+    return ((w >> np.uint64(9)).astype(np.float64) + 0.5) * 2.0**-23
+
+
+def box_muller(wa, wb) -> tuple[np.ndarray, np.ndarray]:
+    """Reading R4: two standard normals from two words (textbook Box-Muller)."""
+    ua, ub = word_to_uniform(wa), word_to_uniform(wb)
+    r = np.sqrt(-2.0 * np.log(ua))
+    return r * np.cos(2.0 * np.pi * ub), r * np.sin(2.0 * np.pi * ub)
+
+
+def _philox_rows(seed: int, positions, ncols: int, domain: int, step: int) -> np.ndarray:
+    """Words for columns 0..ncols-1 of rows keyed by ``positions``: counter
+    (j/4, position, domain, step), word j mod 4 (reading R2).
+    Returns (len(positions), ceil(ncols/4), 4) uint32."""
+    pos = np.atleast_1d(np.asarray(positions, dtype=np.int64))
+    n4 = (ncols + 3) // 4
+    ctr = np.zeros((len(pos), n4, 4), dtype=np.uint64)
+    ctr[:, :, 0] = np.arange(n4, dtype=np.uint64)[None, :]
+    ctr[:, :, 1] = (pos.astype(np.uint64) & _MASK32)[:, None]
+    ctr[:, :, 2] = np.uint64(domain)
+    ctr[:, :, 3] = np.uint64(step & 0xFFFFFFFF)
+    k0, k1 = seed_key(seed)
+    keys = np.empty((len(pos) * n4, 2), dtype=np.uint64)
+    keys[:, 0], keys[:, 1] = k0, k1
+    return philox4x32_10(ctr.reshape(-1, 4), keys).reshape(len(pos), n4, 4)
+
+
+def draft_normals(seed: int, positions, ncols: int) -> np.ndarray:
+    """The starting noise z ~ N(0, I_H) of each slot (flashmap/vllm/model.py,
+    module docstring: noise keyed by the request's seed and the slot's position;
+    readings R1, R2, R4). Row i is keyed by positions[i]; returns (len, ncols):
+    column j is normal j mod 4 of counter j/4, the normals of a counter being the
+    Box-Muller pairs of its words (w0, w1) and (w2, w3)."""
+    w = _philox_rows(seed, positions, ncols, domain=0, step=0)
+    n0, n1 = box_muller(w[..., 0], w[..., 1])
+    n2, n3 = box_muller(w[..., 2], w[..., 3])
+    out = np.stack([n0, n1, n2, n3], axis=-1).reshape(w.shape[0], -1)
+    return out[:, :ncols]
+
+
+def gumbel_noise(seed: int, position: int, step: int, ncols: int) -> np.ndarray:
+    """Gumbel noise G = -ln(-ln U) for one block row (flashmap/sglang/sampler.py,
+    module docstring: Gumbel-max with in-kernel Philox noise; readings R2, R3, R5)."""
+    w = _philox_rows(seed, [int(position)], ncols, domain=1, step=step).reshape(-1)[:ncols]
+    return -np.log(-np.log(word_to_uniform(w)))
+
+
+# ---------------------------------------------------------------------------------
+# Elementwise and row operations (modeling_flashmap.py)
+# ---------------------------------------------------------------------------------
+
+
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """modeling_flashmap.py, rope_tables: inv_freq_i = theta^(-2i/hd), in float32
+    (reading R6: computed in float64, rounded once to float32)."""
+    i = np.arange(0, head_dim, 2, dtype=np.float64)
+    return (1.0 / theta ** (i / head_dim)).astype(np.float32)
+
+
+def rope_angles(positions, head_dim: int, theta: float) -> np.ndarray:
+    """modeling_flashmap.py, rope_tables: the float32 angles p * inv_freq
+    (one float32-rounded product per angle). Returns (n, hd/2) float32."""
+    p = np.asarray(positions, dtype=np.float32).reshape(-1, 1)
+    return p * rope_inv_freq(head_dim, theta)[None, :]  # float32 * float32 -> float32
+
+
+def apply_rope(x: np.ndarray, positions, theta: float) -> np.ndarray:
+    """modeling_flashmap.py, apply_rope: rotate the interleaved channel pairs
+    (x[2i], x[2i+1]) of x (n, heads, hd) by the angle of position n and pair i."""
+    hd = x.shape[-1]
+    ang = rope_angles(positions, hd, theta).astype(np.float64)  # (n, hd/2)
+    cos, sin = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x, dtype=np.float64)
+    out[..., 0::2] = x1 * cos - x2 * sin
+    out[..., 1::2] = x2 * cos + x1 * sin
+    return out
+
+
+def rms_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapRMSNorm: x * (w * rsqrt(mean(x^2) + eps)) over
+    the last axis (the dtype rounding of the scale is a no-op in float64)."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x * (np.asarray(weight, dtype=np.float64) / np.sqrt(ms + eps))
+
+
+def layer_norm(x: np.ndarray, eps: float) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapAdaLayerNorm: F.layer_norm with no affine:
+    (x - mean) / sqrt(biased var + eps) over the last axis."""
+    x = np.asarray(x, dtype=np.float64)
+    mu = np.mean(x, axis=-1, keepdims=True)
+    var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps)
+
+
+def gelu(x: np.ndarray) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapMLP: F.gelu (exact erf form)."""
+    return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def time_embedding(t: float, l1_w, l1_b, l2_w, l2_b, time_embed_dim: int, time_scale: float):
+    """modeling_flashmap.py, FlashMapTimeEmbedding: sinusoidal features of
+    t * time_scale with freqs exp(-ln(1e4) i / half), [cos, sin], then
+    linear_1 -> SiLU -> linear_2."""
+    half = time_embed_dim // 2
+    freqs = np.exp(-math.log(10000.0) * np.arange(half, dtype=np.float64) / half)
+    args = (t * time_scale) * freqs
+    emb = np.concatenate([np.cos(args), np.sin(args)])
+    h = silu(_f64(l1_w) @ emb + _f64(l1_b))
+    return _f64(l2_w) @ h + _f64(l2_b)
+
+
+def adaln_modulation(cond, w, b):
+    """modeling_flashmap.py, FlashMapAdaLayerNorm.modulation: linear(SiLU(cond))
+    chunked into (scale, shift, gate)."""
+    out = _f64(w) @ silu(cond) + _f64(b)
+    d = out.shape[0] // 3
+    return out[:d], out[d : 2 * d], out[2 * d :]
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """Non-causal softmax attention per head (F.scaled_dot_product_attention with
+    scale hd^-1/2). q (nq, heads, hd), k/v (nk, heads, hd) -> (nq, heads, hd)."""
+    hd = q.shape[-1]
+    s = np.einsum("qhd,khd->hqk", q, k) / math.sqrt(hd)
+    s = s - s.max(axis=-1, keepdims=True)
+    p = np.exp(s)
+    p /= p.sum(axis=-1, keepdims=True)
+    return np.einsum("hqk,khd->qhd", p, v)
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------------
+# Load-time constants
+# ---------------------------------------------------------------------------------
+
+
+@dataclass
+class Constants:
+    mods: np.ndarray  # (L, 9, D): (1+scale, shift, gate) x (self, cross, mlp)
+    final: np.ndarray  # (2, D): (1+scale, shift) of the final AdaLN
+    gate: float  # noise gate of the jump 0 -> 1
+    uniform: np.ndarray  # (H,): state_norm(mean row of E)
+    gram: np.ndarray  # (H, H) E^T E
+    chol: np.ndarray  # (H, H) lower L with L L^T = E^T E
+    hot: np.ndarray  # (Vd,) int64 sorted draft-vocabulary token ids
+    head_w: np.ndarray  # (Vd, D) folded head
+    head_b: np.ndarray  # (Vd,)
+    extra: dict = field(default_factory=dict)
+
+
+def jump_conditioning(cfg: Config, W: dict, s: float, t: float):
+    """modeling_flashmap.py, FlashMapDraftModel.time_conditioning:
+    cond = time_embed(s) + jump_embed(t); every AdaLN's (scale, shift, gate)."""
+    te = lambda name, x: time_embedding(  # noqa: E731
+        x, W[f"{name}.linear_1.weight"], W[f"{name}.linear_1.bias"],
+        W[f"{name}.linear_2.weight"], W[f"{name}.linear_2.bias"],
+        cfg.time_embed_dim, cfg.time_scale)
+    cond = te("time_embed", s) + te("jump_embed", t)
+    mods = np.zeros((cfg.num_layers, 9, cfg.hidden))
+    for l in range(cfg.num_layers):
+        for j, norm in enumerate(("self_attn_adaln", "cross_attn_adaln", "mlp_adaln")):
+            sc, sh, g = adaln_modulation(cond, W[f"layers.{l}.{norm}.linear.weight"],
+                                         W[f"layers.{l}.{norm}.linear.bias"])
+            # flashmap/vllm/model.py, prepare: stored as (1 + scale, shift, gate).
+            mods[l, 3 * j], mods[l, 3 * j + 1], mods[l, 3 * j + 2] = 1.0 + sc, sh, g
+    sc, sh, _ = adaln_modulation(cond, W["final_adaln.linear.weight"], W["final_adaln.linear.bias"])
+    return mods, np.stack([1.0 + sc, sh]), cond
+
+
+def draft_vocabulary(cfg: Config, ranking) -> np.ndarray:
+    """flashmap/sglang/model.py, prepare: hot ids = sort(ranking[:Vd]); a size
+    outside (0, V) (or no ranking) means the full vocabulary."""
+    vd, v = cfg.draft_vocab_size, cfg.vocab_size
+    if ranking is None or not (0 < vd < v):
+        return np.arange(v, dtype=np.int64)
+    return np.sort(np.asarray(ranking, dtype=np.int64)[:vd])
+
+
+def load_constants(cfg: Config, W: dict, E, LM, ranking, *, skip_gram: bool = False) -> Constants:
+    """Everything a one-jump draft reads that depends only on the weights:
+    modulations (modeling_flashmap.py, time_conditioning; flashmap/vllm/model.py,
+    prepare), the uniform-posterior constant and the Cholesky factor of E^T E
+    (modeling_flashmap.py, target_constants; flashmap/sglang/model.py,
+    _jump_constants / _embedding_gram), the draft vocabulary and the folded head
+    (flashmap/sglang/model.py, _fold_lm_head).
+
+    skip_gram=True replaces the gram and its factor by the identity: only for
+    timing runs, where the values of L do not change the work."""
+    s, t = DEFAULT_JUMP_GRIDS["1"]
+    mods, final, _ = jump_conditioning(cfg, W, s, t)
+    # modeling_flashmap.py, mix_state: noise_gate times the jump (t - s), or alone.
+    jump = 1.0 if cfg.noise_gate_constant else (t - s)
+    gate = float(np.asarray(W["noise_gate"], dtype=np.float64).reshape(-1)[0]) * jump
+    E64 = _f64(E)
+    # The uniform posterior (1/V each) embeds to the mean row of E, then state_norm.
+    uniform = rms_norm(E64.mean(axis=0), W["state_norm.weight"], cfg.rms_norm_eps)
+    H = E64.shape[1]
+    if skip_gram:
+        gram, chol = np.eye(H), np.eye(H)
+    else:
+        gram = E64.T @ E64
+        chol = np.linalg.cholesky(gram)  # lower, positive diagonal (unique)
+    hot = draft_vocabulary(cfg, ranking)
+    lm_hot = _f64(LM)[hot]
+    head_w = lm_hot @ _f64(W["head.weight"])  # (Vd, H) @ (H, D)
+    head_b = lm_hot @ _f64(W["head.bias"])
+    return Constants(mods=mods, final=final, gate=gate, uniform=uniform, gram=gram,
+                     chol=chol, hot=hot, head_w=head_w, head_b=head_b)
+
+
+# ---------------------------------------------------------------------------------
+# Context keys and values (the write and the anchor row)
+# ---------------------------------------------------------------------------------
+
+
+def _heads(x: np.ndarray, cfg: Config) -> np.ndarray:
+    return x.reshape(x.shape[0], cfg.num_heads, cfg.head_dim)
+
+
+def context_kv(cfg: Config, W: dict, ctx: np.ndarray, positions) -> tuple[np.ndarray, np.ndarray]:
+    """modeling_flashmap.py, FlashMapAttention.project_kv of every layer's
+    cross-attention: k = RoPE(k_norm(heads(k_proj ctx))), v = heads(v_proj ctx).
+    ctx (n, D) -> keys, values (L, n, heads, hd)."""
+    n = ctx.shape[0]
+    K = np.empty((cfg.num_layers, n, cfg.num_heads, cfg.head_dim))
+    V = np.empty_like(K)
+    for l in range(cfg.num_layers):
+        pre = f"layers.{l}.cross_attn"
+        k = _heads(ctx @ _f64(W[f"{pre}.k_proj.weight"]).T, cfg)
+        k = rms_norm(k, W[f"{pre}.k_norm.weight"], cfg.qk_norm_eps)
+        K[l] = apply_rope(k, positions, cfg.rope_theta)
+        V[l] = _heads(ctx @ _f64(W[f"{pre}.v_proj.weight"]).T, cfg)
+    return K, V
+
+
+def write_rows_kv(cfg: Config, W: dict, target_hidden: np.ndarray, positions):
+    """modeling_flashmap.py, extend_context (flashmap/sglang/model.py,
+    _write_context): ctx = hidden_norm(fc(target hidden)), then every layer's
+    context keys and values. target_hidden (n, Lt*H) -> (L, n, heads, hd) x 2."""
+    ctx = rms_norm(_f64(target_hidden) @ _f64(W["fc.weight"]).T, W["hidden_norm.weight"],
+                   cfg.rms_norm_eps)
+    return context_kv(cfg, W, ctx, positions)
+
+
+def anchor_kv(cfg: Config, W: dict, E, anchor_ids, positions):
+    """modeling_flashmap.py, draft (flashmap/sglang/model.py, _anchor_kv_impl):
+    the anchor's context row anchor_norm(anchor_proj(E[anchor])) projected by every
+    layer's cross-attention at the anchor's position."""
+    e = _f64(E)[np.asarray(anchor_ids, dtype=np.int64)]
+    a = rms_norm(e @ _f64(W["anchor_proj.weight"]).T + _f64(W["anchor_proj.bias"]),
+                 W["anchor_norm.weight"], cfg.rms_norm_eps)
+    return context_kv(cfg, W, a, positions)
+
+
+def slot_of(req_to_page: np.ndarray, req: int, pos: int, page_size: int) -> int:
+    """tokenspeed dflash.py, DFlash._draft_native (compute_out_cache_loc_uniform):
+    loc = req_to_page[req, pos / page] * page + pos % page."""
+    return int(req_to_page[req, pos // page_size]) * page_size + pos % page_size
+
+
+def write_locations(start_pos, commit_lens, window: int, req_pool_idx, req_to_page, page_size):
+    """flashmap/sglang/model.py, write_target_hidden_kv (verify windows): column c of
+    request b sits at position start_pos[b] + c and is written only if
+    c < commit_lens[b] (all columns without commit_lens). Returns (bs, W) int64
+    slots, -1 where skipped."""
+    bs = len(start_pos)
+    out = np.full((bs, window), -1, dtype=np.int64)
+    for b in range(bs):
+        n = window if commit_lens is None else int(commit_lens[b])
+        for c in range(min(n, window)):
+            out[b, c] = slot_of(req_to_page, int(req_pool_idx[b]), int(start_pos[b]) + c, page_size)
+    return out
+
+
+# ---------------------------------------------------------------------------------
+# The one-jump draft of one request
+# ---------------------------------------------------------------------------------
+
+
+def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, noise_scale: float):
+    """flashmap/sglang/model.py, _draft_impl (one jump from t = 0): the embedded
+    state u + gate * noise_norm(z L^T) with z keyed by the slot positions, then
+    x_embed. Returns (K, D)."""
+    z = noise_scale * draft_normals(seed, positions, cfg.target_hidden)
+    y = z @ C.chol.T
+    e = C.uniform + C.gate * rms_norm(y, W["noise_norm.weight"], cfg.rms_norm_eps)
+    return e @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
+
+
+def dit_layer(cfg: Config, W: dict, l: int, mods: np.ndarray, x: np.ndarray, positions,
+              ctx_k: np.ndarray, ctx_v: np.ndarray) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapLayer.forward on one request's block x (K, D):
+    self-attention across the block's slots, cross-attention onto the context
+    ctx_k/ctx_v (n, heads, hd) (positions 0..p), MLP; each behind a modulated
+    LayerNorm and a gated residual."""
+    eps = cfg.layer_norm_eps
+    pre = f"layers.{l}"
+    m = mods
+    # self-attention
+    h = layer_norm(x, eps) * m[0] + m[1]
+    sa = f"{pre}.self_attn"
+    q = rms_norm(_heads(h @ _f64(W[f"{sa}.q_proj.weight"]).T, cfg), W[f"{sa}.q_norm.weight"], cfg.qk_norm_eps)
+    k = rms_norm(_heads(h @ _f64(W[f"{sa}.k_proj.weight"]).T, cfg), W[f"{sa}.k_norm.weight"], cfg.qk_norm_eps)
+    v = _heads(h @ _f64(W[f"{sa}.v_proj.weight"]).T, cfg)
+    q, k = apply_rope(q, positions, cfg.rope_theta), apply_rope(k, positions, cfg.rope_theta)
+    att = attention(q, k, v).reshape(x.shape[0], -1)
+    x = x + m[2] * (att @ _f64(W[f"{sa}.o_proj.weight"]).T)
+    # cross-attention
+    h = layer_norm(x, eps) * m[3] + m[4]
+    ca = f"{pre}.cross_attn"
+    q = rms_norm(_heads(h @ _f64(W[f"{ca}.q_proj.weight"]).T, cfg), W[f"{ca}.q_norm.weight"], cfg.qk_norm_eps)
+    q = apply_rope(q, positions, cfg.rope_theta)
+    ctx = attention(q, ctx_k, ctx_v).reshape(x.shape[0], -1)
+    x = x + m[5] * (ctx @ _f64(W[f"{ca}.o_proj.weight"]).T)
+    # MLP
+    h = layer_norm(x, eps) * m[6] + m[7]
+    f1 = gelu(h @ _f64(W[f"{pre}.mlp.fc1.weight"]).T + _f64(W[f"{pre}.mlp.fc1.bias"]))
+    x = x + m[8] * (f1 @ _f64(W[f"{pre}.mlp.fc2.weight"]).T + _f64(W[f"{pre}.mlp.fc2.bias"]))
+    return x
+
+
+def draft_request(cfg: Config, W: dict, C: Constants, ctx_k: np.ndarray, ctx_v: np.ndarray,
+                  anchor_pos: int, seed: int, noise_scale: float = 1.0) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapDraftModel.draft with one step, for one request
+    whose cross-attention context (anchor included) is ctx_k/ctx_v (L, p+1, heads, hd):
+    slots at positions p+1 .. p+K; returns the final AdaLN output (K, D), which the
+    folded head maps to logits."""
+    K = cfg.block_size
+    positions = anchor_pos + 1 + np.arange(K)
+    assert ctx_k.shape[1] == anchor_pos + 1, "context is positions 0..p"
+    x = noise_embedding(cfg, W, C, seed, positions, noise_scale)
+    for l in range(cfg.num_layers):
+        x = dit_layer(cfg, W, l, C.mods[l], x, positions, ctx_k[l], ctx_v[l])
+    return layer_norm(x, cfg.layer_norm_eps) * C.final[0] + C.final[1]
+
+
+def head_logits(C: Constants, hidden: np.ndarray) -> np.ndarray:
+    """flashmap/sglang/model.py, head_logits: the folded head over the draft
+    vocabulary, (rows, D) -> (rows, Vd)."""
+    return _f64(hidden) @ C.head_w.T + C.head_b
+
+
+# ---------------------------------------------------------------------------------
+# Whole-block sampling
+# ---------------------------------------------------------------------------------
+
+
+def sample_rows(logits: np.ndarray, temperature, greedy, seeds, positions, step: int, hot):
+    """flashmap/sglang/sampler.py, FlashMapDraftSampler.__call__ (fused variant):
+    every row of the block at once; greedy rows (or T <= 0) take argmax_j l_j,
+    the others argmax_j (l_j / T + G_j) with G from the row's Philox stream
+    (readings R2, R3, R5); drafted index j -> token hot[j].
+
+    The decision is taken in float32 (the logits are rounded to float32 first),
+    as the library takes it. Returns (tokens int64 (rows,), index (rows,),
+    top-2 margin of the maximised quantity (rows,))."""
+    lg = np.asarray(logits, dtype=np.float64)
+    rows = lg.shape[0]
+    tokens = np.empty(rows, dtype=np.int64)
+    index = np.empty(rows, dtype=np.int64)
+    margin = np.empty(rows, dtype=np.float64)
+    for r in range(rows):
+        l32 = lg[r].astype(np.float32)
+        t = float(temperature[r])
+        if bool(greedy[r]) or t <= 0.0:
+            val = l32
+        else:
+            g = gumbel_noise(int(seeds[r]), int(positions[r]), step, lg.shape[1]).astype(np.float32)
+            val = (l32 / np.float32(t)).astype(np.float32) + g
+        j = int(np.argmax(val))  # first maximum: lowest index wins ties
+        index[r], tokens[r] = j, int(hot[j])
+        srt = np.sort(val.astype(np.float64))
+        margin[r] = srt[-1] - srt[-2] if len(srt) > 1 else np.inf
+    return tokens, index, margin
+
+
+def full_logits(logits: np.ndarray, hot, vocab_size: int) -> np.ndarray:
+    """flashmap/sglang/sampler.py, IdentityMarkov.sample_block / _FullLogits: the
+    draft-vocabulary logits scattered over the full vocabulary, -inf elsewhere."""
+    out = np.full((logits.shape[0], vocab_size), -np.inf)
+    out[:, np.asarray(hot)] = logits
+    return out
+
+
+# ---------------------------------------------------------------------------------
+# FP8 (e4m3) weight copies, per output channel
+# ---------------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x) -> np.ndarray:
+    """Round float32 values to the nearest e4m3fn value (ties to even),
+    saturating at +-448: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+    subnormal step 2^-9. Returns float64 holding exact e4m3 values."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    # exponent of the e4m3 binade of a (normals have e >= -6; below, step 2^-9)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))  # a = m 2^ex, m in [1/2, 1)
+    e = np.maximum(ex.astype(np.float64) - 1.0, -6.0)
+    step = 2.0 ** (e - 3)
+    q = np.round(a / step) * step  # np.round: ties to even; a/step exact (powers of 2)
+    q = np.minimum(q, E4M3_MAX)
+    return np.sign(x) * q
+
+
+def quantize_e4m3_per_channel(w) -> tuple[np.ndarray, np.ndarray]:
+    """flashmap/sglang/model.py, _quantize_fp8 (quantize_weight_fp8): per output
+    channel scale = max|w_row| / 448 in float32 (an all-zero row gets 1) and
+    q = e4m3(w / scale) with the division in float32. Returns (q, scale) with q
+    the exact e4m3 values (float64) and scale float32 (rows,)."""
+    w32 = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w32), axis=1)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    scale = np.where(amax > 0, scale, np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((w32 / scale[:, None]).astype(np.float32))
+    return q, scale
+
+
+def dequantize(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    return _f64(q) * _f64(scale)[:, None]

@@ -1,0 +1,392 @@
+"""Pins of the oracle to things other than itself: published vectors and printed
+constants, closed forms, library routines, brute force and statistical laws.
+
+Each test names what fixes the function; none re-types the oracle's formula."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.stats as st
+
+from oracle import flashmap_ref as ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+
+
+# --------------------------------------------------------------------- Philox
+
+
+def test_philox_known_answer_vectors():
+    """Random123's published Philox4x32-10 known-answer vectors."""
+    rows = _rows("philox_kat.txt")
+    ctr = np.array([[int(x, 16) for x in r[0:4]] for r in rows], dtype=np.uint64)
+    key = np.array([[int(x, 16) for x in r[4:6]] for r in rows], dtype=np.uint64)
+    want = np.array([[int(x, 16) for x in r[6:10]] for r in rows], dtype=np.uint32)
+    np.testing.assert_array_equal(ref.philox4x32_10(ctr, key), want)
+
+
+def test_uniform_map_exact_in_float32_and_open_interval():
+    w = np.array([0, 1, 511, 512, 0x7FFFFFFF, 0xFFFFFFFF], dtype=np.uint64)
+    u = ref.word_to_uniform(w)
+    assert u[0] == 2.0**-24 and u[-1] == 1.0 - 2.0**-24
+    assert np.all((u > 0) & (u < 1))
+    np.testing.assert_array_equal(u.astype(np.float32).astype(np.float64), u)
+
+
+def test_draft_normals_law():
+    """Box-Muller output is N(0, 1): KS test, moments, no column correlation."""
+    z = ref.draft_normals(12345, np.arange(4000), 64)
+    x = z.reshape(-1)
+    assert abs(x.mean()) < 0.01 and abs(x.var() - 1) < 0.01
+    assert st.kstest(x, "norm").pvalue > 1e-3
+    c = np.corrcoef(z[:, :8].T)
+    assert np.max(np.abs(c - np.eye(8))) < 0.06
+
+
+def test_draft_normals_keying():
+    """Rows depend only on (seed, position): the same slot position under the same
+    seed gives the same noise, another seed or position does not."""
+    a = ref.draft_normals(7, [10, 11, 12], 16)
+    b = ref.draft_normals(7, [12, 10], 16)
+    np.testing.assert_array_equal(a[2], b[0])
+    np.testing.assert_array_equal(a[0], b[1])
+    assert not np.allclose(ref.draft_normals(8, [10], 16), a[:1])
+
+
+def test_gumbel_law():
+    g = np.concatenate([ref.gumbel_noise(3, p, 5, 64) for p in range(1500)])
+    assert st.kstest(g, "gumbel_r").pvalue > 1e-3
+
+
+# --------------------------------------------------------------------- constants
+
+
+def test_jump_grids_printed_constants():
+    for r in _rows("jump_grids.txt"):
+        grid = [float(x) for x in r[1:]]
+        assert ref.DEFAULT_JUMP_GRIDS[r[0]] == grid
+        assert grid[0] == 0.0 and grid[-1] == 1.0
+        assert all(a < b for a, b in zip(grid, grid[1:]))
+
+
+def test_context_row_bytes_printed_value():
+    """The pages' 48 KB per committed row: every layer's key and value, D wide."""
+    for L, D, el, want in (map(int, r) for r in _rows("context_row_bytes.txt")):
+        k, v = np.zeros((L, 1, 1, D)), np.zeros((L, 1, 1, D))  # (L, n, heads, hd)
+        assert (k.size + v.size) * el == want
+
+
+# --------------------------------------------------------------------- RoPE
+
+
+def test_rope_closed_form_rotation_and_pairing():
+    hd, theta = 16, 1e4
+    for pos in (0, 1, 7, 1000):
+        ang = ref.rope_angles([pos], hd, theta)[0].astype(np.float64)
+        for i in range(hd // 2):
+            x = np.zeros((1, 1, hd))
+            x[0, 0, 2 * i] = 1.0
+            y = ref.apply_rope(x, [pos], theta)[0, 0]
+            want = np.zeros(hd)
+            want[2 * i], want[2 * i + 1] = math.cos(ang[i]), math.sin(ang[i])
+            np.testing.assert_allclose(y, want, atol=1e-15)
+    # the angle of pair i is p * theta^(-2i/hd) up to float32 rounding
+    ang = ref.rope_angles([3], 8, 10000.0)[0]
+    np.testing.assert_allclose(ang, [3 * 10000 ** (-2 * i / 8) for i in range(4)], rtol=1e-6)
+
+
+def test_rope_norm_and_relative_position():
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((1, 2, 32))
+    k = rng.standard_normal((1, 2, 32))
+    qr = ref.apply_rope(q, [5], 1e4)
+    np.testing.assert_allclose(np.linalg.norm(qr, axis=-1), np.linalg.norm(q, axis=-1), rtol=1e-13)
+    # <R_p q, R_p' k> depends on p - p' only (small positions: float32 angles exact enough)
+    d1 = np.sum(ref.apply_rope(q, [9], 1e4) * ref.apply_rope(k, [4], 1e4), axis=-1)
+    d2 = np.sum(ref.apply_rope(q, [25], 1e4) * ref.apply_rope(k, [20], 1e4), axis=-1)
+    np.testing.assert_allclose(d1, d2, rtol=1e-5)
+
+
+# --------------------------------------------------------------------- norms etc.
+
+
+def test_rms_norm_closed_forms():
+    w = np.array([1.0, 2.0, 3.0, 4.0])
+    x = np.full(4, -3.0)  # rms 3: scale 1/3 per unit weight (eps -> 0)
+    np.testing.assert_allclose(ref.rms_norm(x, w, 0.0), -w, rtol=1e-15)
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal(64)
+    # unit weights, eps 0: norm of the output is sqrt(n)
+    assert abs(np.linalg.norm(ref.rms_norm(y, np.ones(64), 0.0)) - 8.0) < 1e-12
+    # scale invariance (eps 0) and the eps limit at zero input
+    np.testing.assert_allclose(ref.rms_norm(5 * y, 1, 0.0), ref.rms_norm(y, 1, 0.0), rtol=1e-13)
+    assert np.all(ref.rms_norm(np.zeros(8), 1.0, 1e-6) == 0)
+
+
+def test_layer_norm_against_zscore():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((3, 50)) * 4 + 1
+    np.testing.assert_allclose(ref.layer_norm(x, 0.0), st.zscore(x, axis=-1), rtol=1e-12)
+
+
+def test_gelu_silu_library_forms():
+    x = np.linspace(-6, 6, 101)
+    np.testing.assert_allclose(ref.gelu(x), x * st.norm.cdf(x), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(ref.silu(x), x * (1 / (1 + np.exp(-x))), rtol=1e-15)
+
+
+def test_time_embedding_at_zero_and_one():
+    """t = 0: features cos(0) = 1 (first half), sin(0) = 0 (second half); with identity
+    linears and zero biases the output is SiLU of those features."""
+    Te = C = 8
+    I, z = np.eye(8), np.zeros(8)
+    out = ref.time_embedding(0.0, I, z, I, z, Te, 1000.0)
+    np.testing.assert_allclose(out, ref.silu(np.array([1.0] * 4 + [0.0] * 4)), rtol=1e-15)
+    out1 = ref.time_embedding(1.0, I, z, I, z, Te, 1000.0)
+    half = 4
+    a = 1000.0 * np.array([10000 ** (-i / half) for i in range(half)])
+    np.testing.assert_allclose(out1, ref.silu(np.concatenate([np.cos(a), np.sin(a)])), rtol=1e-12)
+
+
+# --------------------------------------------------------------------- attention
+
+
+def _attention_brute(q, k, v):
+    nq, nh, hd = q.shape
+    out = np.zeros_like(q)
+    for h in range(nh):
+        for i in range(nq):
+            s = [sum(q[i, h, d] * k[j, h, d] for d in range(hd)) / math.sqrt(hd) for j in range(k.shape[0])]
+            e = [math.exp(x) for x in s]
+            tot = sum(e)
+            for d in range(hd):
+                out[i, h, d] = sum(e[j] * v[j, h, d] for j in range(k.shape[0])) / tot
+    return out
+
+
+def test_attention_brute_force_tiny():
+    rng = np.random.default_rng(3)
+    q, k, v = rng.standard_normal((3, 2, 4)), rng.standard_normal((5, 2, 4)), rng.standard_normal((5, 2, 4))
+    np.testing.assert_allclose(ref.attention(q, k, v), _attention_brute(q, k, v), rtol=1e-12)
+
+
+def test_attention_degenerate_contexts():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((4, 2, 8))
+    k1, v1 = rng.standard_normal((1, 2, 8)), rng.standard_normal((1, 2, 8))
+    # one position: the output is that position's value whatever the query
+    np.testing.assert_allclose(ref.attention(q, k1, v1), np.broadcast_to(v1, (4, 2, 8)), rtol=1e-14)
+    # identical keys: the output is the mean value
+    k = np.broadcast_to(k1, (6, 2, 8))
+    v = rng.standard_normal((6, 2, 8))
+    np.testing.assert_allclose(ref.attention(q, k, v), np.broadcast_to(v.mean(0), (4, 2, 8)), rtol=1e-12)
+
+
+# --------------------------------------------------------------------- model-level
+
+
+def _tiny(**over):
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    d = syn.model_config("tiny_fp32")
+    d.update(over)
+    cfg = ref.Config.from_dict(d)
+    W, E, LM, rank = syn.make_model(d, "cpu")
+    W = {k: v.float().numpy() for k, v in W.items()}
+    return cfg, W, E.float().numpy(), LM.float().numpy(), rank.numpy()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    cfg, W, E, LM, rank = _tiny()
+    return cfg, W, E, LM, rank, ref.load_constants(cfg, W, E, LM, rank)
+
+
+def test_cholesky_identity(tiny):
+    cfg, W, E, LM, rank, C = tiny
+    G = E.astype(np.float64).T @ E.astype(np.float64)
+    assert np.linalg.norm(C.chol @ C.chol.T - G) / np.linalg.norm(G) < 1e-12
+    assert np.allclose(C.chol, np.tril(C.chol)) and np.all(np.diag(C.chol) > 0)
+
+
+def test_noise_law_matches_embedding_covariance():
+    """z L^T ~ N(0, E^T E) (modeling_flashmap.py, target_constants). A gram far from a
+    multiple of the identity makes a transposed factor (L^T L) fail."""
+    rng = np.random.default_rng(5)
+    V, H, N = 512, 24, 60000
+    E = rng.standard_normal((V, H)) @ (rng.standard_normal((H, H)) + 2 * np.eye(H)) * 0.05
+    L = np.linalg.cholesky(E.T @ E)
+    z = ref.draft_normals(99, np.arange(N), H)
+    y = z @ L.T
+    S = y.T @ y / N
+    G = E.T @ E
+    assert np.linalg.norm(S - G) / np.linalg.norm(G) < 0.05
+    assert np.linalg.norm(L.T @ L - G) / np.linalg.norm(G) > 0.2  # the test can tell
+    # the direct draw x0 @ E, x0 ~ N(0, I_V), has the same covariance
+    x0 = rng.standard_normal((N, V))
+    Y = x0 @ E
+    S2 = Y.T @ Y / N
+    assert np.linalg.norm(S - S2) / np.linalg.norm(G) < 0.07
+
+
+def test_fold_identity(tiny):
+    """flashmap/sglang/model.py, _fold_lm_head: no nonlinearity between the DiT head
+    and the LM head, so LM[hot] (W_head h + b_head) == W_f h + b_f."""
+    cfg, W, E, LM, rank, C = tiny
+    h = np.random.default_rng(6).standard_normal((3, cfg.hidden))
+    two_step = (h @ W["head.weight"].astype(np.float64).T + W["head.bias"]) @ LM[C.hot].astype(np.float64).T
+    np.testing.assert_allclose(ref.head_logits(C, h), two_step, rtol=1e-10, atol=1e-12)
+
+
+def test_uniform_constant_is_embedded_uniform_posterior(tiny):
+    """modeling_flashmap.py, target_constants: the uniform posterior (1/V each) times E,
+    through state_norm."""
+    cfg, W, E, LM, rank, C = tiny
+    post = np.full(cfg.vocab_size, 1.0 / cfg.vocab_size) @ E.astype(np.float64)
+    rms = np.sqrt(np.mean(post**2) + cfg.rms_norm_eps)
+    np.testing.assert_allclose(C.uniform, post / rms * W["state_norm.weight"], rtol=1e-12)
+
+
+def test_draft_vocabulary(tiny):
+    cfg, W, E, LM, rank, C = tiny
+    assert len(C.hot) == cfg.draft_vocab_size and np.all(np.diff(C.hot) > 0)
+    assert set(C.hot) == set(rank[: cfg.draft_vocab_size])
+    full = ref.draft_vocabulary(ref.Config.from_dict({**cfg.__dict__, "draft_vocab_size": 0}), rank)
+    np.testing.assert_array_equal(full, np.arange(cfg.vocab_size))
+
+
+def test_modulations_zero_adaln_gives_identity_modulation():
+    cfg, W, E, LM, rank = _tiny()
+    for k in W:
+        if "adaln.linear" in k:
+            W[k] = np.zeros_like(W[k])
+    mods, final, _ = ref.jump_conditioning(cfg, W, 0.0, 1.0)
+    assert np.all(mods[:, 0::3] == 1) and np.all(mods[:, 1::3] == 0) and np.all(mods[:, 2::3] == 0)
+    assert np.all(final[0] == 1) and np.all(final[1] == 0)
+
+
+def test_draft_zero_gates_reduces_to_embedding():
+    """With every AdaLN zeroed, each gated residual vanishes: the draft output is the
+    plain LayerNorm of the noise embedding (a dropped gate or residual fails)."""
+    cfg, W, E, LM, rank = _tiny()
+    for k in W:
+        if "adaln.linear" in k:
+            W[k] = np.zeros_like(W[k])
+    C = ref.load_constants(cfg, W, E, LM, rank)
+    p = 10
+    rng = np.random.default_rng(7)
+    kc = rng.standard_normal((cfg.num_layers, p + 1, cfg.num_heads, cfg.head_dim))
+    out = ref.draft_request(cfg, W, C, kc, kc, p, seed=42)
+    pos = p + 1 + np.arange(cfg.block_size)
+    x0 = ref.noise_embedding(cfg, W, C, 42, pos, 1.0)
+    np.testing.assert_allclose(out, ref.layer_norm(x0, cfg.layer_norm_eps), rtol=1e-12)
+
+
+def test_draft_noise_scale_zero_is_seed_independent(tiny):
+    cfg, W, E, LM, rank, C = tiny
+    p = 5
+    rng = np.random.default_rng(8)
+    kc = rng.standard_normal((cfg.num_layers, p + 1, cfg.num_heads, cfg.head_dim))
+    a = ref.draft_request(cfg, W, C, kc, kc, p, seed=1, noise_scale=0.0)
+    b = ref.draft_request(cfg, W, C, kc, kc, p, seed=2, noise_scale=0.0)
+    np.testing.assert_array_equal(a, b)
+    c = ref.draft_request(cfg, W, C, kc, kc, p, seed=1)
+    assert not np.allclose(a, c)
+
+
+# --------------------------------------------------------------------- slots
+
+
+def test_write_locations_brute_force_page_walk():
+    rng = np.random.default_rng(9)
+    P, rows, pages = 4, 5, 40
+    r2p = rng.permutation(pages)[: rows * 8].reshape(rows, 8)
+    start = np.array([0, 3, 13, 7])
+    commit = np.array([5, 0, 2, 5])
+    idx = np.array([2, 0, 4, 1])
+    out = ref.write_locations(start, commit, 5, idx, r2p, P)
+    for b in range(4):
+        # walk the request's pages one slot at a time
+        walk = [int(r2p[idx[b], q]) * P + o for q in range(8) for o in range(P)]
+        for c in range(5):
+            want = walk[start[b] + c] if c < commit[b] else -1
+            assert out[b, c] == want
+
+
+# --------------------------------------------------------------------- sampling
+
+
+def test_sampling_greedy_and_ties():
+    lg = np.array([[0.1, 0.5, 0.5, -1.0], [3.0, 3.0, 3.0, 3.0]])
+    hot = np.array([10, 20, 30, 40])
+    tok, idx, _ = ref.sample_rows(lg, [0, -1], [1, 0], [1, 2], [5, 6], 0, hot)
+    assert list(idx) == [1, 0] and list(tok) == [20, 10]
+
+
+def test_gumbel_max_law_chi_square():
+    """Gumbel-max draws are distributed as softmax(l / T)."""
+    l = np.array([0.3, -1.0, 1.2, 0.0, 0.7, -0.4])
+    T, n = 0.7, 20000
+    counts = np.zeros(len(l))
+    rows = np.tile(l, (n, 1))
+    seeds = np.arange(n) * 7919 + 3
+    _, idx, _ = ref.sample_rows(rows, [T] * n, [0] * n, seeds, np.arange(n) % 97, 11, np.arange(6))
+    for j in idx:
+        counts[j] += 1
+    p = np.exp(l / T) / np.exp(l / T).sum()
+    assert st.chisquare(counts, n * p).pvalue > 1e-3
+
+
+def test_sampling_row_independence():
+    rng = np.random.default_rng(10)
+    lg = rng.standard_normal((5, 50))
+    args = dict(temperature=[1.0] * 5, greedy=[0, 1, 0, 0, 1], seeds=[1, 2, 3, 4, 5],
+                positions=[9, 9, 10, 11, 12], step=4, hot=np.arange(50))
+    t1, _, _ = ref.sample_rows(lg, **args)
+    lg2 = lg.copy()
+    lg2[[0, 1, 3]] = rng.standard_normal((3, 50))
+    args2 = dict(args, seeds=[9, 2, 3, 8, 5])
+    t2, _, _ = ref.sample_rows(lg2, **args2)
+    assert t1[2] == t2[2] and t1[4] == t2[4]
+
+
+def test_full_logits_minus_inf_outside_draft_vocab():
+    lg = np.array([[1.0, 2.0, 3.0]])
+    full = ref.full_logits(lg, np.array([1, 4, 6]), 8)
+    assert np.all(np.isneginf(full[0, [0, 2, 3, 5, 7]]))
+    np.testing.assert_array_equal(full[0, [1, 4, 6]], lg[0])
+
+
+# --------------------------------------------------------------------- e4m3
+
+
+def test_e4m3_rounding_against_torch_and_tie_cases():
+    import torch
+
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(2000) * 1e-2,
+                        np.linspace(-448, 448, 4001)]).astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    np.testing.assert_array_equal(ref.e4m3_round(x), want)
+    # ties to even and saturation
+    cases = {1.0625: 1.0, 1.1875: 1.25, 2.0**-10: 0.0, 3 * 2.0**-10: 2.0**-8, 500.0: 448.0, -1e6: -448.0}
+    for a, b in cases.items():
+        assert ref.e4m3_round(np.float32(a)) == b
+
+
+def test_e4m3_per_channel_scale():
+    rng = np.random.default_rng(12)
+    w = rng.standard_normal((6, 40)).astype(np.float32)
+    w[3] = 0
+    q, s = ref.quantize_e4m3_per_channel(w)
+    assert s[3] == 1.0 and np.all(q[3] == 0)
+    assert np.all(np.max(np.abs(q[[0, 1, 2, 4, 5]]), axis=1) == 448.0)
+    deq = ref.dequantize(q, s)
+    assert np.max(np.abs(deq - w)) <= np.max(np.abs(w)) / 448 * 16  # half an e4m3 step at the top
