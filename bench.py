@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Benchmark of the FlashMap one-jump block-draft step on GB300.
+
+One step = the whole hot path for one batch: the context-KV write of the verify
+window's committed columns, the anchor row, the noise embedding and the DiT
+(flashmap_draft_block), and the folded head with whole-block sampling
+(flashmap_sample_block). Inputs are synthetic and resident in HBM; the step is
+captured once in a CUDA graph and replayed; the timed region is bracketed by a
+barrier and synchronizations and timed with CUDA events on the launch stream. Each
+step streams ~3 GB of weights, far above the 129 MB L2, so nothing survives in L2
+between steps.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_block_context_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "drafted tokens/sec (batch x block_size / s)"
+UNIT = "tokens/s"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        # samples are ~100 ms apart: keep those around the timed region
+        n = len(rows)
+        span = max(time.time() - self.t_start, 1e-3)
+        sel = [r for i, r in enumerate(rows) if t0 - 0.3 <= self.t_start + span * i / max(n, 1) <= t1 + 0.3] or rows
+        sm = [float(r[1]) for r in sel if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in sel if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in sel for j in range(4) if r[5 + j].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel)}
+
+
+# --------------------------------------------------------------------------- our arm
+
+
+def algorithmic_bytes(cfg: dict, req: dict) -> dict:
+    """Bytes the step must move (bf16 storage): every weight once, the context K/V of
+    positions 0..p of every request, the window and anchor rows written, the logits."""
+    H, Lt, D, L, F, Vd, V, K = (cfg[k] for k in ("target_hidden", "num_target_layers", "hidden", "num_layers",
+                                                 "intermediate", "draft_vocab_size", "vocab_size", "block_size"))
+    es = 4 if cfg["act_dtype"] == "f32" else 2
+    bs = req["bs"]
+    w_write = (D * Lt * H + 2 * L * D * D) * es if req["window"] else 0
+    w_draft = (D * H + 2 * L * D * D + H * H + D * H + L * (6 * D * D + 2 * D * F)) * es
+    w_head = Vd * D * es
+    kv_row = L * 2 * D * es
+    kv_read = sum((p + 1) * kv_row for p in req["anchor_pos"])
+    rows_written = (sum(req["commit"]) if req["window"] else 0) + bs
+    logits = bs * K * Vd * 4
+    x_in = (bs * (K + 1) * Lt * H * es) if req["window"] else 0
+    full = bs * K * V * 4 if req["full_scatter"] else 0
+    total = w_write + w_draft + w_head + kv_read + rows_written * kv_row + logits + x_in + full
+    return {"weights": w_write + w_draft + w_head, "kv_read": kv_read, "total": total}
+
+
+def setup_ours(workload: str, device: str):
+    from speculative_decoding_block_context_gb300 import _lib as F
+
+    cfg = syn.model_config(workload)
+    W, E, LM, rank = syn.make_model(cfg, device)
+    model = F.flashmap_load_weights(cfg, W, E, LM, rank)
+    torch.cuda.synchronize()
+    del W, LM
+    req = syn.make_requests(workload, device)
+    bs, K = req["bs"], cfg["block_size"]
+    dt = syn.torch_dtype(cfg["act_dtype"])
+    code = F.DTYPE_CODES[cfg["act_dtype"]]
+    pool_t = torch.empty(F.flashmap_pool_bytes(cfg, req["num_pages"]), dtype=torch.uint8, device=device)
+    pool = F.make_pool(pool_t, req["num_pages"], code)
+    max_rows = max(max(req["ctx"]) if req["prefill"] else 0, bs * (K + 1))
+    ws = torch.empty(F.flashmap_workspace_size(model, bs, min(max_rows, 4096)), dtype=torch.uint8, device=device)
+    i32 = dict(dtype=torch.int32, device=device)
+    if req["prefill"]:
+        for b in range(bs):
+            X = req["prefill_hidden"][b]
+            F.flashmap_write_context_kv(model, pool, X, 1, X.shape[0], req["req_pool_idx"][b : b + 1],
+                                        torch.zeros(1, **i32), None, req["req_to_page"], None, ws)
+        req.pop("prefill_hidden")
+    else:
+        syn.fill_pool_random(pool_t.view(dt), req["kv_generator_seed"])
+    Vd = cfg["draft_vocab_size"] if 0 < cfg["draft_vocab_size"] < cfg["vocab_size"] else cfg["vocab_size"]
+    st = dict(
+        F=F, cfg=cfg, model=model, E=E, req=req, pool_t=pool_t, pool=pool, ws=ws,
+        start=torch.tensor(req["ctx"], **i32), commit=torch.tensor(req["commit"], **i32),
+        anchor_pos=torch.tensor(req["anchor_pos"], **i32),
+        hidden=torch.empty((bs * K, cfg["hidden"]), dtype=dt, device=device),
+        tokens=torch.empty(bs * K, dtype=torch.int64, device=device),
+        logits=torch.empty((bs * K, Vd), dtype=torch.float32, device=device),
+        full=(torch.empty((bs * K, cfg["vocab_size"]), dtype=torch.float32, device=device)
+              if req["full_scatter"] else None),
+        window_loc=torch.empty(bs * (K + 1), dtype=torch.int64, device=device),
+    )
+    return st
+
+
+def run_step(st: dict, stream=None) -> None:
+    F, req, cfg = st["F"], st["req"], st["cfg"]
+    bs, K = req["bs"], cfg["block_size"]
+    if req["window"]:
+        F.flashmap_write_context_kv(st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"],
+                                    st["start"], st["commit"], req["req_to_page"], st["window_loc"], st["ws"], stream)
+    F.flashmap_draft_block(st["model"], st["pool"], bs, req["anchor_ids"], st["anchor_pos"], req["req_pool_idx"],
+                           req["req_to_page"], req["seeds"], 1.0, st["hidden"], None, st["ws"], stream)
+    F.flashmap_sample_block(st["model"], bs, st["hidden"], st["anchor_pos"], req["temperature"], req["greedy"],
+                            req["seeds"], req["step"], st["tokens"], st["logits"], st["full"], st["ws"], stream)
+
+
+def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: int = 3) -> dict:
+    """Event-timed launches of the tcgen05 GEMM over `steps` eager steps on the launch
+    stream: algorithmic bytes (weights + activations read, float32 outputs written)
+    per launch over the mean launch duration."""
+    F = st["F"]
+    es = 4 if st["cfg"]["act_dtype"] == "f32" else 2
+    with torch.cuda.stream(stream):
+        F.flashmap_profile_start(st["model"], 100000)
+        for _ in range(steps):
+            run_step(st)
+        recs = F.flashmap_profile_stop(st["model"], 100000)
+    gem = [r for r in recs if r[0] == "gemm"]
+    by_kind = {}
+    for r in recs:
+        by_kind[r[0]] = by_kind.get(r[0], 0.0) + r[5] / steps
+    byts = sum(n * k * es + rows * k * es + rows * n * 4 for _, _, rows, n, k, _ in gem) / len(gem)
+    ms = sum(r[5] for r in gem) / len(gem)
+    achieved = byts / (ms * 1e-3) / 1e9
+    return {"kernel": "tc_linear_kernel (tcgen05 GEMM, all launches of a step)", "bytes_per_launch": byts,
+            "ms_per_launch": ms, "launches_per_step": len(gem) // steps, "achieved_gbs": achieved,
+            "ms_by_kind_per_step": {k: round(v, 4) for k, v in sorted(by_kind.items())},
+            "launches_per_step_total": len(recs) // steps}
+
+
+def our_arm(args, rank: int, world: int) -> dict:
+    device = f"cuda:{int(os.environ.get('LOCAL_RANK', '0'))}"
+    torch.cuda.set_device(device)
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    st = setup_ours(args.workload, device)
+    F, cfg, req = st["F"], st["cfg"], st["req"]
+    bs, K = req["bs"], cfg["block_size"]
+    stream = torch.cuda.Stream(device=device)
+    # eager warm-up, then capture one step
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            run_step(st)
+    torch.cuda.synchronize()
+    err = F.flashmap_get_device_error(st["model"])
+    if err:
+        raise RuntimeError(f"device error word {err} during warm-up")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            run_step(st)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            graph.replay()
+    torch.cuda.synchronize()
+    t_ev0, t_ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        t_ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        t_ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t_ev0.elapsed_time(t_ev1) / args.steps
+    ms_t = torch.tensor([ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(ms_t.item())
+    clocks = sampler.stop(t0, t1)
+    tokens_per_step = bs * K * world
+    value = tokens_per_step / (ms * 1e-3)
+
+    # end to end through the public API with host buffers: pinned inputs copied in,
+    # the step, the sampled token ids copied out, every step
+    host_in = {k: req[k].cpu().pin_memory() for k in ("anchor_ids", "seeds", "temperature", "greedy")}
+    host_in["anchor_pos"] = st["anchor_pos"].cpu().pin_memory()
+    dev_in = {k: (req[k] if k in req else st[k]) for k in host_in}
+    if req["window"]:
+        host_in["window_hidden"] = req["window_hidden"].cpu().pin_memory()
+        dev_in["window_hidden"] = req["window_hidden"]
+    tok_host = torch.empty(st["tokens"].shape, dtype=torch.int64).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = tok_host.numel() * tok_host.element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            for k, t in host_in.items():
+                dev_in[k].copy_(t, non_blocking=True)
+            graph.replay()
+            tok_host.copy_(st["tokens"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_t = torch.tensor([e2e_ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = float(e2e_t.item())
+
+    roof = gemm_roofline(st, stream, hbm_peak)
+    ab = algorithmic_bytes(cfg, req)
+    launches = roof["launches_per_step_total"]
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "draft_step_us": round(ms * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg["act_dtype"],
+        "data": "synthetic (seeded random weights and inputs of the workload's shapes)",
+        "config": {"workload": args.workload, "batch": bs, "block_size": K,
+                   "context": {"min": min(req["ctx"]), "max": max(req["ctx"]),
+                               "mean": float(np.mean(req["ctx"]))},
+                   "window_write": bool(req["window"]), "full_vocab_scatter": bool(req["full_scatter"]),
+                   "parallelism": f"replicas x{world} (requests sharded, no collective)",
+                   "l2": "inputs larger than L2 (weights alone ~3 GB per step)", "cuda_graph": True},
+        "e2e": {"value": round(tokens_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(roof["achieved_gbs"] / hbm_peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs", "kernel": roof["kernel"],
+                     "bytes_per_launch": round(roof["bytes_per_launch"]), "us_per_launch": round(roof["ms_per_launch"] * 1e3, 2)},
+        "step_roofline": {"algorithmic_bytes": ab["total"], "achieved_gbs": round(ab["total"] / (ms * 1e-3) / 1e9, 1),
+                          "frac_of_measured_hbm": round(ab["total"] / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                          "frac_of_8tbs": round(ab["total"] / (ms * 1e-3) / 1e9 / 8000.0, 4)},
+        "breakdown_ms_per_step_eager": roof["ms_by_kind_per_step"],
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, st, budget_s=args.cpu_budget)
+    return line
+
+
+# --------------------------------------------------------------------------- the oracle arm
+
+
+def oracle_setup(workload: str, device: str, gen_model=None):
+    """Numpy inputs for the oracle: weights, constants (gram replaced by the identity:
+    the value of L does not change the work of a step), request inputs."""
+    from oracle import flashmap_ref as ref
+
+    cfg = syn.model_config(workload)
+    if gen_model is None:
+        W, E, LM, rank = syn.make_model(cfg, device)
+    else:
+        W, E, LM, rank = gen_model
+    Wnp = {k: v.double().cpu().numpy() for k, v in W.items()}
+    Enp = E.float().cpu().numpy()
+    ocfg = ref.Config.from_dict(cfg)
+    C = ref.load_constants(ocfg, Wnp, Enp, LM.float().cpu().numpy(), rank.cpu().numpy(), skip_gram=True)
+    return ocfg, Wnp, Enp, C
+
+
+def oracle_step(ref, ocfg, Wnp, Enp, C, req, b: int, ctx_kv, window_hidden) -> None:
+    """One request's whole step on the CPU oracle: window write, anchor row, draft,
+    folded head, sampling."""
+    K = ocfg.block_size
+    kc, vc = ctx_kv
+    if req["window"]:
+        m = req["commit"][b]
+        kw, vw = ref.write_rows_kv(ocfg, Wnp, window_hidden[:m], req["ctx"][b] + np.arange(m))
+        kc, vc = np.concatenate([kc, kw], 1), np.concatenate([vc, vw], 1)
+    p = req["anchor_pos"][b]
+    ka, va = ref.anchor_kv(ocfg, Wnp, Enp, [int(req["anchor_ids"][b])], [p])
+    kc, vc = np.concatenate([kc, ka], 1), np.concatenate([vc, va], 1)
+    seed = int(req["seeds"][b])
+    hid = ref.draft_requests(ocfg, Wnp, C, [(kc, vc)], [p], [seed])[0]
+    lg = ref.head_logits(C, hid)
+    ref.sample_rows(lg, [float(req["temperature"][b])] * K, [int(req["greedy"][b])] * K, [seed] * K,
+                    p + 1 + np.arange(K), req["step"], C.hot)
+
+
+def time_oracle(workload: str, device: str, n_steps: int, gen_model=None, req=None):
+    """Times n_steps oracle steps, each one request of the workload (requests are
+    independent; a step of bs requests costs bs times one). Returns seconds per
+    request-step and the sample description."""
+    from oracle import flashmap_ref as ref
+
+    ocfg, Wnp, Enp, C = oracle_setup(workload, device, gen_model)
+    req = req or syn.make_requests(workload, device)
+    rng = np.random.default_rng(0)
+    L, nh, hd = ocfg.num_layers, ocfg.num_heads, ocfg.head_dim
+    times = []
+    for i in range(n_steps):
+        b = i % req["bs"]
+        n = req["ctx"][b]
+        # context keys/values of positions 0..ctx-1 (their values do not change the work)
+        kc = rng.standard_normal((L, n, nh, hd)).astype(np.float32)
+        vc = rng.standard_normal((L, n, nh, hd)).astype(np.float32)
+        wh = req["window_hidden"][b].float().cpu().numpy() if req["window"] else None
+        t0 = time.perf_counter()
+        oracle_step(ref, ocfg, Wnp, Enp, C, req, b, (kc, vc), wh)
+        times.append(time.perf_counter() - t0)
+    return float(np.mean(times)), req
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(workload: str, st: dict | None, budget_s: float = 30.0) -> dict:
+    cfg = syn.model_config(workload)
+    K = cfg["block_size"]
+    n = 2
+    sec, req = time_oracle(workload, "cuda", n)
+    return {"value": round(K / sec, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+            "sample": f"{n} request-steps of {workload} (window write + anchor + draft + head + sampling of one "
+                      f"request, {K} tokens each) on the NumPy float64 oracle; {sec:.2f} s per request-step; "
+                      f"load-time constants untimed, E^T E factor replaced by the identity for timing"}
+
+
+def reference_arm(args) -> dict:
+    cfg = syn.model_config(args.workload)
+    K = cfg["block_size"]
+    n = max(1, args.steps)
+    for _ in range(args.warmup and 1):
+        pass
+    sec, req = time_oracle(args.workload, "cuda" if torch.cuda.is_available() else "cpu", n)
+    value = K / sec
+    sample = (f"{n} request-steps of {args.workload} on the NumPy float64 oracle (one request's window write, "
+              f"anchor, draft, head and sampling per step; requests are independent, so a batch costs bs steps)")
+    return {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0, "steps": n, "warmup": args.warmup,
+            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "impl": "reference",
+            "dtype": "f64", "data": "synthetic", "config": {"workload": args.workload},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3_8b_bs1", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(reference_arm(args)), flush=True)
+        return 0
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device(f"cuda:{os.environ.get('LOCAL_RANK', '0')}"))
+    line = our_arm(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -452,51 +452,71 @@ def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, no
     return e @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
 
 
+def _linear(x: np.ndarray, w) -> np.ndarray:
+    return x @ _f64(w).T
+
+
 def dit_layer(cfg: Config, W: dict, l: int, mods: np.ndarray, x: np.ndarray, positions,
-              ctx_k: np.ndarray, ctx_v: np.ndarray) -> np.ndarray:
-    """modeling_flashmap.py, FlashMapLayer.forward on one request's block x (K, D):
-    self-attention across the block's slots, cross-attention onto the context
-    ctx_k/ctx_v (n, heads, hd) (positions 0..p), MLP; each behind a modulated
-    LayerNorm and a gated residual."""
+              contexts) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapLayer.forward on the blocks of one or more requests,
+    x (n_req * K, D), row i * K + k being slot k of request i at positions[i*K + k]:
+    self-attention across each request's own K slots, cross-attention onto that
+    request's context contexts[i] = (keys, values) (n_i, heads, hd) (positions 0..p_i),
+    MLP; each behind a modulated LayerNorm and a gated residual. Requests never mix:
+    every linear acts row by row, every attention within one request."""
     eps = cfg.layer_norm_eps
+    K = cfg.block_size
     pre = f"layers.{l}"
     m = mods
+    nreq = x.shape[0] // K
     # self-attention
     h = layer_norm(x, eps) * m[0] + m[1]
     sa = f"{pre}.self_attn"
-    q = rms_norm(_heads(h @ _f64(W[f"{sa}.q_proj.weight"]).T, cfg), W[f"{sa}.q_norm.weight"], cfg.qk_norm_eps)
-    k = rms_norm(_heads(h @ _f64(W[f"{sa}.k_proj.weight"]).T, cfg), W[f"{sa}.k_norm.weight"], cfg.qk_norm_eps)
-    v = _heads(h @ _f64(W[f"{sa}.v_proj.weight"]).T, cfg)
+    q = rms_norm(_heads(_linear(h, W[f"{sa}.q_proj.weight"]), cfg), W[f"{sa}.q_norm.weight"], cfg.qk_norm_eps)
+    k = rms_norm(_heads(_linear(h, W[f"{sa}.k_proj.weight"]), cfg), W[f"{sa}.k_norm.weight"], cfg.qk_norm_eps)
+    v = _heads(_linear(h, W[f"{sa}.v_proj.weight"]), cfg)
     q, k = apply_rope(q, positions, cfg.rope_theta), apply_rope(k, positions, cfg.rope_theta)
-    att = attention(q, k, v).reshape(x.shape[0], -1)
-    x = x + m[2] * (att @ _f64(W[f"{sa}.o_proj.weight"]).T)
+    att = np.concatenate([attention(q[i * K:(i + 1) * K], k[i * K:(i + 1) * K], v[i * K:(i + 1) * K])
+                          for i in range(nreq)]).reshape(x.shape[0], -1)
+    x = x + m[2] * _linear(att, W[f"{sa}.o_proj.weight"])
     # cross-attention
     h = layer_norm(x, eps) * m[3] + m[4]
     ca = f"{pre}.cross_attn"
-    q = rms_norm(_heads(h @ _f64(W[f"{ca}.q_proj.weight"]).T, cfg), W[f"{ca}.q_norm.weight"], cfg.qk_norm_eps)
+    q = rms_norm(_heads(_linear(h, W[f"{ca}.q_proj.weight"]), cfg), W[f"{ca}.q_norm.weight"], cfg.qk_norm_eps)
     q = apply_rope(q, positions, cfg.rope_theta)
-    ctx = attention(q, ctx_k, ctx_v).reshape(x.shape[0], -1)
-    x = x + m[5] * (ctx @ _f64(W[f"{ca}.o_proj.weight"]).T)
+    ctx = np.concatenate([attention(q[i * K:(i + 1) * K], contexts[i][0], contexts[i][1])
+                          for i in range(nreq)]).reshape(x.shape[0], -1)
+    x = x + m[5] * _linear(ctx, W[f"{ca}.o_proj.weight"])
     # MLP
     h = layer_norm(x, eps) * m[6] + m[7]
-    f1 = gelu(h @ _f64(W[f"{pre}.mlp.fc1.weight"]).T + _f64(W[f"{pre}.mlp.fc1.bias"]))
-    x = x + m[8] * (f1 @ _f64(W[f"{pre}.mlp.fc2.weight"]).T + _f64(W[f"{pre}.mlp.fc2.bias"]))
+    f1 = gelu(_linear(h, W[f"{pre}.mlp.fc1.weight"]) + _f64(W[f"{pre}.mlp.fc1.bias"]))
+    x = x + m[8] * (_linear(f1, W[f"{pre}.mlp.fc2.weight"]) + _f64(W[f"{pre}.mlp.fc2.bias"]))
     return x
+
+
+def draft_requests(cfg: Config, W: dict, C: Constants, ctx_kv: list, anchor_pos: list, seeds: list,
+                   noise_scale: float = 1.0) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapDraftModel.draft with one step, for requests i whose
+    cross-attention context (anchor included) is ctx_kv[i] = (keys, values), each
+    (L, p_i + 1, heads, hd): slots at positions p_i+1 .. p_i+K; returns the final AdaLN
+    output (n_req, K, D), which the folded head maps to logits."""
+    K = cfg.block_size
+    nreq = len(anchor_pos)
+    positions = np.concatenate([p + 1 + np.arange(K) for p in anchor_pos])
+    for (kc, _), p in zip(ctx_kv, anchor_pos):
+        assert kc.shape[1] == p + 1, "context is positions 0..p"
+    x = np.concatenate([noise_embedding(cfg, W, C, s, p + 1 + np.arange(K), noise_scale)
+                        for s, p in zip(seeds, anchor_pos)])
+    for l in range(cfg.num_layers):
+        x = dit_layer(cfg, W, l, C.mods[l], x, positions, [(kc[l], vc[l]) for kc, vc in ctx_kv])
+    out = layer_norm(x, cfg.layer_norm_eps) * C.final[0] + C.final[1]
+    return out.reshape(nreq, K, -1)
 
 
 def draft_request(cfg: Config, W: dict, C: Constants, ctx_k: np.ndarray, ctx_v: np.ndarray,
                   anchor_pos: int, seed: int, noise_scale: float = 1.0) -> np.ndarray:
-    """modeling_flashmap.py, FlashMapDraftModel.draft with one step, for one request
-    whose cross-attention context (anchor included) is ctx_k/ctx_v (L, p+1, heads, hd):
-    slots at positions p+1 .. p+K; returns the final AdaLN output (K, D), which the
-    folded head maps to logits."""
-    K = cfg.block_size
-    positions = anchor_pos + 1 + np.arange(K)
-    assert ctx_k.shape[1] == anchor_pos + 1, "context is positions 0..p"
-    x = noise_embedding(cfg, W, C, seed, positions, noise_scale)
-    for l in range(cfg.num_layers):
-        x = dit_layer(cfg, W, l, C.mods[l], x, positions, ctx_k[l], ctx_v[l])
-    return layer_norm(x, cfg.layer_norm_eps) * C.final[0] + C.final[1]
+    """draft_requests for a single request: (K, D)."""
+    return draft_requests(cfg, W, C, [(ctx_k, ctx_v)], [anchor_pos], [seed], noise_scale)[0]
 
 
 def head_logits(C: Constants, hidden: np.ndarray) -> np.ndarray:

@@ -1,0 +1,77 @@
+"""Builds libflashmap.so in-tree from csrc/ for sm_103a (nvcc, one object per
+translation unit, compiled in parallel, then linked as a shared library)."""
+
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_PATH = os.path.join(HERE, "libflashmap.so")
+SOURCES = ["gemm.cu", "attention.cu", "rows.cu", "sample.cu", "loadtime.cu", "flashmap.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE] + ARCH
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libflashmap.so")
+
+
+def _deps_mtime() -> float:
+    t = os.path.getmtime(os.path.join(INCLUDE, "flashmap.h"))
+    for f in os.listdir(CSRC):
+        if f.endswith((".h", ".cuh")):
+            t = max(t, os.path.getmtime(os.path.join(CSRC, f)))
+    return t
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles what changed and links libflashmap.so; returns its path."""
+    nvcc = _nvcc()
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    deps = _deps_mtime()
+    jobs = []
+    for src in SOURCES:
+        s = os.path.join(CSRC, src)
+        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        stale = force or not os.path.exists(o) or os.path.getmtime(o) < max(os.path.getmtime(s), deps)
+        jobs.append((s, o, stale))
+
+    def compile_one(job):
+        s, o, stale = job
+        if not stale:
+            return None
+        cmd = [nvcc, *FLAGS, "-c", s, "-o", o]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            return f"{' '.join(cmd)}\n{r.stdout}\n{r.stderr}"
+        if verbose and (r.stdout or r.stderr):
+            print(r.stdout, r.stderr)
+        return None
+
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        errors = [e for e in ex.map(compile_one, jobs) if e]
+    if errors:
+        raise RuntimeError("nvcc failed:\n" + "\n".join(errors))
+    objs = [o for _, o, _ in jobs]
+    if force or not os.path.exists(LIB_PATH) or any(os.path.getmtime(o) > os.path.getmtime(LIB_PATH) for o in objs):
+        tmp = LIB_PATH + ".tmp"
+        cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

@@ -1,0 +1,833 @@
+// Host side of the FlashMap C ABI (include/flashmap.h): argument validation, the
+// load-time precompute, workspace carving and the launch sequence of each call.
+// Every call validates first and launches nothing on an invalid argument.
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using fm::Launch;
+using fm::Weight;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+flashmap_status fail(flashmap_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+#define FM_CUDA(call)                                                                          \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) return fail(FLASHMAP_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t dt_size(int dtype) { return dtype == FLASHMAP_F32 ? 4 : dtype == FLASHMAP_BF16 ? 2 : 1; }
+
+inline size_t align_up(size_t x, size_t a = 256) { return (x + a - 1) / a * a; }
+
+// Carves 256-byte aligned sub-buffers out of one allocation (or measures the total).
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  template <typename P>
+  P* take(size_t bytes) {
+    off = align_up(off);
+    P* p = base ? reinterpret_cast<P*>(base + off) : nullptr;
+    off += bytes;
+    return p;
+  }
+};
+
+struct LayerW {
+  Weight qkv, o, cq, co, fc1, fc2;
+  float *qn = nullptr, *kn = nullptr, *cqn = nullptr;
+  float* mods = nullptr;  // [9][D]: (1+scale, shift, gate) x (self, cross, mlp)
+  float *fc1_b = nullptr, *fc2_beta = nullptr;
+};
+
+}  // namespace
+
+struct flashmap_model {
+  flashmap_config cfg;
+  int device = 0, num_sms = 0;
+  int adt = FLASHMAP_F32, wdt = FLASHMAP_F32;
+  int H = 0, Lt = 0, D = 0, L = 0, nh = 0, hd = 0, F = 0, K = 0, V = 0, Vd = 0, P = 0, maxpos = 0;
+  void* arena = nullptr;
+  unsigned* dev_err = nullptr;
+  Weight fc, ap, ctx_kv, chol, xe, head;
+  std::vector<LayerW> layers;
+  float *hidden_norm_w = nullptr, *anchor_norm_w = nullptr, *noise_norm_w = nullptr;
+  float *ap_b = nullptr, *xe_b = nullptr, *head_b = nullptr, *ctx_knorm = nullptr;
+  float *final_mods = nullptr, *u = nullptr;
+  float gate = 1.f;
+  int64_t* hot = nullptr;
+  int32_t* inv_hot = nullptr;
+  float2* rope = nullptr;
+  const void* embedding = nullptr;
+  // launch timing (flashmap_profile_start / stop)
+  bool prof_on = false;
+  int prof_cap = 0;
+  std::vector<cudaEvent_t> prof_events;
+  std::vector<flashmap_launch_record> prof_recs;
+  Launch launch(cudaStream_t s) const { return Launch{s, num_sms, dev_err}; }
+};
+
+namespace {
+// Records an event pair around one launch while profiling is on.
+struct Prof {
+  flashmap_model* m;
+  cudaStream_t s;
+  bool on;
+  Prof(flashmap_model* m_, cudaStream_t s_, int kind, int layer, int rows = 0, int n = 0, int k = 0)
+      : m(m_), s(s_), on(m_->prof_on && static_cast<int>(m_->prof_recs.size()) < m_->prof_cap) {
+    if (!on) return;
+    const size_t i = m->prof_recs.size();
+    if (m->prof_events.size() < 2 * (i + 1)) {
+      cudaEvent_t a, b;
+      cudaEventCreate(&a);
+      cudaEventCreate(&b);
+      m->prof_events.push_back(a);
+      m->prof_events.push_back(b);
+    }
+    m->prof_recs.push_back(flashmap_launch_record{kind, layer, rows, n, k, 0.f});
+    cudaEventRecord(m->prof_events[2 * i], s);
+  }
+  ~Prof() {
+    if (on) cudaEventRecord(m->prof_events[2 * (m->prof_recs.size() - 1) + 1], s);
+  }
+};
+}  // namespace
+
+#define PROF(kind, layer, ...) Prof prof_##__LINE__(m, s, kind, layer, ##__VA_ARGS__)
+#define TIMED(kind, layer, call) \
+  do {                           \
+    PROF(kind, layer);           \
+    FM_CUDA(call);               \
+  } while (0)
+#define TIMED_GEMM(layer, W, rows, call)       \
+  do {                                         \
+    PROF(FLASHMAP_KIND_GEMM, layer, rows, (W).N, (W).K); \
+    FM_CUDA(call);                             \
+  } while (0)
+
+namespace {
+
+bool is_act(int d) { return d == FLASHMAP_F32 || d == FLASHMAP_BF16; }
+
+flashmap_status validate(const flashmap_config* c) {
+  if (!c) return fail(FLASHMAP_E_INVALID, "config is NULL");
+  const int dims[] = {c->target_hidden, c->num_target_layers, c->hidden, c->num_layers, c->num_heads, c->head_dim,
+                      c->intermediate, c->cond_dim, c->time_embed_dim, c->block_size, c->vocab_size,
+                      c->page_size, c->max_position};
+  for (int d : dims)
+    if (d <= 0) return fail(FLASHMAP_E_INVALID, "every size in the config must be positive");
+  if (c->draft_vocab_size < 0) return fail(FLASHMAP_E_INVALID, "draft_vocab_size must be >= 0");
+  if (c->num_steps != 1)
+    return fail(FLASHMAP_E_UNSUPPORTED, "only one-jump drafting (num_steps = 1) is built; got " +
+                                            std::to_string(c->num_steps));
+  if (c->hidden != c->num_heads * c->head_dim) return fail(FLASHMAP_E_INVALID, "hidden != num_heads * head_dim");
+  if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+    return fail(FLASHMAP_E_UNSUPPORTED, "head_dim must be 32, 64 or 128");
+  if (c->block_size > 16) return fail(FLASHMAP_E_UNSUPPORTED, "block_size must be <= 16");
+  if (c->page_size % 16) return fail(FLASHMAP_E_UNSUPPORTED, "page_size must be a multiple of 16");
+  if (c->time_embed_dim % 2) return fail(FLASHMAP_E_INVALID, "time_embed_dim must be even");
+  if (c->cond_dim > 8192 || c->time_embed_dim > 8192) return fail(FLASHMAP_E_UNSUPPORTED, "cond_dim too large");
+  if (!is_act(c->act_dtype)) return fail(FLASHMAP_E_INVALID, "act_dtype must be F32 or BF16");
+  if (c->weight_dtype != c->act_dtype) {
+    if (c->weight_dtype == FLASHMAP_E4M3 && c->act_dtype == FLASHMAP_BF16)
+      return fail(FLASHMAP_E_UNSUPPORTED, "E4M3 weights are not built yet");
+    return fail(FLASHMAP_E_INVALID, "weight_dtype must equal act_dtype (or E4M3 with BF16 activations)");
+  }
+  if (c->act_dtype == FLASHMAP_BF16) {
+    const int a[] = {c->target_hidden, c->hidden, c->intermediate};
+    for (int d : a)
+      if (d % 8) return fail(FLASHMAP_E_UNSUPPORTED, "bf16 GEMM widths must be multiples of 8");
+  }
+  if (!(c->rope_theta > 0) || !(c->time_scale >= 0) || !(c->rms_norm_eps >= 0) || !(c->qk_norm_eps >= 0) ||
+      !(c->layer_norm_eps >= 0))
+    return fail(FLASHMAP_E_INVALID, "rope_theta, time_scale and eps values must be non-negative");
+  return FLASHMAP_OK;
+}
+
+int draft_vocab(const flashmap_config* c) {
+  return (c->draft_vocab_size > 0 && c->draft_vocab_size < c->vocab_size) ? c->draft_vocab_size : c->vocab_size;
+}
+
+// The rotary table: inv_freq_i = float32(theta^(-2i/hd)) computed in float64; the
+// angle of position p is the float32 product float32(p) * inv_freq_i; cos and sin of
+// that angle are evaluated in float64 and stored as float32
+// (flashmap/modeling_flashmap.py, rope_tables: float32 angles).
+std::vector<float2> rope_table(int maxpos, int hd, double theta) {
+  std::vector<float> inv(hd / 2);
+  for (int i = 0; i < hd / 2; ++i) inv[i] = static_cast<float>(1.0 / std::pow(theta, (2.0 * i) / hd));
+  std::vector<float2> t(static_cast<size_t>(maxpos) * (hd / 2));
+  for (int p = 0; p < maxpos; ++p) {
+    for (int i = 0; i < hd / 2; ++i) {
+      volatile float a = static_cast<float>(p) * inv[i];
+      const double ad = static_cast<double>(a);
+      t[static_cast<size_t>(p) * (hd / 2) + i] = make_float2(static_cast<float>(std::cos(ad)), static_cast<float>(std::sin(ad)));
+    }
+  }
+  return t;
+}
+
+struct DraftWs {
+  float *x, *acc_big, *acc_d, *acc_a, *acc_kv;
+  void *act, *act2, *e_rows, *a_rows;
+  int* plan;
+  float *part_o, *part_ml;
+  size_t bytes;
+};
+
+DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
+  Carver c(base);
+  const size_t R = static_cast<size_t>(bs) * m->K, es = dt_size(m->adt);
+  const size_t big = std::max({3 * static_cast<size_t>(m->D), static_cast<size_t>(m->F), static_cast<size_t>(m->H)});
+  const size_t wide = std::max({static_cast<size_t>(m->D), static_cast<size_t>(m->F), static_cast<size_t>(m->H)});
+  DraftWs w;
+  w.x = c.take<float>(R * m->D * 4);
+  w.acc_big = c.take<float>(R * big * 4);
+  w.acc_d = c.take<float>(R * m->D * 4);
+  w.acc_a = c.take<float>(static_cast<size_t>(bs) * m->D * 4);
+  w.acc_kv = c.take<float>(static_cast<size_t>(bs) * 2 * m->L * m->D * 4);
+  w.act = c.take<void>(R * wide * es);
+  w.act2 = c.take<void>(R * m->D * es);
+  w.e_rows = c.take<void>(static_cast<size_t>(bs) * m->H * es);
+  w.a_rows = c.take<void>(static_cast<size_t>(bs) * m->D * es);
+  w.plan = c.take<int>(fm::xattn_plan_ints(m->num_sms, m->nh, bs) * 4);
+  const size_t chunks = fm::xattn_max_chunks(m->num_sms, m->nh, bs);
+  w.part_o = c.take<float>(chunks * m->nh * 16 * m->hd * 4);
+  w.part_ml = c.take<float>(chunks * m->nh * 32 * 4);
+  w.bytes = align_up(c.off);
+  return w;
+}
+
+struct WriteWs {
+  float *acc_fc, *acc_kv;
+  void* ctx;
+};
+size_t write_row_bytes(const flashmap_model* m) {
+  return static_cast<size_t>(m->D) * 4 + static_cast<size_t>(m->D) * dt_size(m->adt) +
+         static_cast<size_t>(2) * m->L * m->D * 4;
+}
+WriteWs carve_write(const flashmap_model* m, int rows, void* base, size_t* bytes) {
+  Carver c(base);
+  WriteWs w;
+  w.acc_fc = c.take<float>(static_cast<size_t>(rows) * m->D * 4);
+  w.ctx = c.take<void>(static_cast<size_t>(rows) * m->D * dt_size(m->adt));
+  w.acc_kv = c.take<float>(static_cast<size_t>(rows) * 2 * m->L * m->D * 4);
+  *bytes = align_up(c.off);
+  return w;
+}
+
+size_t sample_bytes(const flashmap_model* m, int bs) {
+  return align_up(static_cast<size_t>(bs) * m->K * m->Vd * 4);
+}
+
+flashmap_status check_weight_map(Weight& w, int dtype, std::string* err) {
+  w.dtype = dtype;
+  if (dtype == FLASHMAP_BF16) {
+    if (!fm::make_tmap_bf16(&w.map, w.ptr, w.N, w.K, w.K, 128, err)) return FLASHMAP_E_CUDA;
+    w.has_map = true;
+  }
+  return FLASHMAP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* flashmap_last_error(void) { return g_last_error.c_str(); }
+
+flashmap_status flashmap_validate_config(const flashmap_config* cfg) {
+  g_last_error.clear();
+  return validate(cfg);
+}
+
+flashmap_status flashmap_pool_bytes(const flashmap_config* cfg, int64_t num_pages, size_t* bytes) {
+  g_last_error.clear();
+  flashmap_status st = validate(cfg);
+  if (st != FLASHMAP_OK) return st;
+  if (!bytes || num_pages <= 0) return fail(FLASHMAP_E_INVALID, "num_pages must be positive and bytes non-NULL");
+  *bytes = static_cast<size_t>(cfg->num_layers) * 2 * static_cast<size_t>(num_pages) * cfg->num_heads *
+           cfg->page_size * cfg->head_dim * dt_size(cfg->act_dtype);
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_get_config(const flashmap_model* model, flashmap_config* cfg) {
+  if (!model || !cfg) return fail(FLASHMAP_E_INVALID, "NULL argument");
+  *cfg = model->cfg;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_free(flashmap_model* model) {
+  if (!model) return FLASHMAP_OK;
+  if (model->arena) cudaFree(model->arena);
+  for (cudaEvent_t e : model->prof_events) cudaEventDestroy(e);
+  delete model;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap_weights* w, const void* embedding,
+                                      const void* lm_head, const int64_t* vocab_ranking, flashmap_stream stream,
+                                      flashmap_model** out) {
+  g_last_error.clear();
+  flashmap_status st = validate(cfg);
+  if (st != FLASHMAP_OK) return st;
+  if (!w || !embedding || !lm_head || !out || !w->layers) return fail(FLASHMAP_E_INVALID, "NULL argument");
+  {
+    const void* req[] = {w->fc_w, w->hidden_norm_w, w->anchor_proj_w, w->anchor_proj_b, w->anchor_norm_w,
+                         w->state_norm_w, w->noise_norm_w, w->noise_gate, w->x_embed_w, w->x_embed_b,
+                         w->time_l1_w, w->time_l1_b, w->time_l2_w, w->time_l2_b, w->jump_l1_w, w->jump_l1_b,
+                         w->jump_l2_w, w->jump_l2_b, w->final_adaln_w, w->final_adaln_b, w->head_w, w->head_b};
+    for (const void* p : req)
+      if (!p) return fail(FLASHMAP_E_INVALID, "a weight pointer is NULL");
+    for (int l = 0; l < cfg->num_layers; ++l) {
+      const flashmap_layer_weights& lw = w->layers[l];
+      const void* lr[] = {lw.self_adaln_w, lw.self_adaln_b, lw.self_q_w, lw.self_k_w, lw.self_v_w, lw.self_o_w,
+                          lw.self_q_norm_w, lw.self_k_norm_w, lw.cross_adaln_w, lw.cross_adaln_b, lw.cross_q_w,
+                          lw.cross_k_w, lw.cross_v_w, lw.cross_o_w, lw.cross_q_norm_w, lw.cross_k_norm_w,
+                          lw.mlp_adaln_w, lw.mlp_adaln_b, lw.fc1_w, lw.fc1_b, lw.fc2_w, lw.fc2_b};
+      for (const void* p : lr)
+        if (!p) return fail(FLASHMAP_E_INVALID, "a layer weight pointer is NULL (layer " + std::to_string(l) + ")");
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto* m = new flashmap_model();
+  auto cleanup = [&](flashmap_status code) {
+    flashmap_free(m);
+    return code;
+  };
+  m->cfg = *cfg;
+  m->adt = cfg->act_dtype;
+  m->wdt = cfg->weight_dtype;
+  m->H = cfg->target_hidden;
+  m->Lt = cfg->num_target_layers;
+  m->D = cfg->hidden;
+  m->L = cfg->num_layers;
+  m->nh = cfg->num_heads;
+  m->hd = cfg->head_dim;
+  m->F = cfg->intermediate;
+  m->K = cfg->block_size;
+  m->V = cfg->vocab_size;
+  m->Vd = vocab_ranking ? draft_vocab(cfg) : cfg->vocab_size;  // no ranking: the full vocabulary
+  m->P = cfg->page_size;
+  m->maxpos = cfg->max_position;
+  m->embedding = embedding;
+  if (cudaGetDevice(&m->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
+    return cleanup(fail(FLASHMAP_E_CUDA, "no CUDA device"));
+  const int adt = m->adt;
+  const size_t es = dt_size(adt);
+  const int64_t H = m->H, D = m->D, L = m->L, F = m->F, Vd = m->Vd, V = m->V, hd = m->hd, C = cfg->cond_dim;
+
+  // ---- arena layout
+  auto layout = [&](Carver& c) {
+    m->fc.ptr = c.take<void>(D * m->Lt * H * es);
+    m->ap.ptr = c.take<void>(D * H * es);
+    m->ctx_kv.ptr = c.take<void>(2 * L * D * D * es);
+    m->chol.ptr = c.take<void>(H * H * es);
+    m->xe.ptr = c.take<void>(D * H * es);
+    m->head.ptr = c.take<void>(Vd * D * es);
+    m->layers.resize(L);
+    for (auto& lw : m->layers) {
+      lw.qkv.ptr = c.take<void>(3 * D * D * es);
+      lw.o.ptr = c.take<void>(D * D * es);
+      lw.cq.ptr = c.take<void>(D * D * es);
+      lw.co.ptr = c.take<void>(D * D * es);
+      lw.fc1.ptr = c.take<void>(F * D * es);
+      lw.fc2.ptr = c.take<void>(D * F * es);
+      lw.qn = c.take<float>(hd * 4);
+      lw.kn = c.take<float>(hd * 4);
+      lw.cqn = c.take<float>(hd * 4);
+      lw.mods = c.take<float>(9 * D * 4);
+      lw.fc1_b = c.take<float>(F * 4);
+      lw.fc2_beta = c.take<float>(D * 4);
+    }
+    m->hidden_norm_w = c.take<float>(D * 4);
+    m->anchor_norm_w = c.take<float>(D * 4);
+    m->noise_norm_w = c.take<float>(H * 4);
+    m->ap_b = c.take<float>(D * 4);
+    m->xe_b = c.take<float>(D * 4);
+    m->head_b = c.take<float>(Vd * 4);
+    m->ctx_knorm = c.take<float>(L * hd * 4);
+    m->final_mods = c.take<float>(2 * D * 4);
+    m->u = c.take<float>(H * 4);
+    m->hot = c.take<int64_t>(Vd * 8);
+    m->inv_hot = c.take<int32_t>(V * 4);
+    m->rope = c.take<float2>(static_cast<size_t>(m->maxpos) * (hd / 2) * 8);
+    m->dev_err = c.take<unsigned>(256);
+  };
+  Carver measure(nullptr);
+  layout(measure);
+  if (cudaMalloc(&m->arena, measure.off) != cudaSuccess) {
+    cudaGetLastError();
+    m->arena = nullptr;
+    return cleanup(fail(FLASHMAP_E_NOMEM, "cannot allocate " + std::to_string(measure.off) + " bytes of weights"));
+  }
+  Carver arena(m->arena);
+  layout(arena);
+
+  // Load-time scratch: gram (float64 H x H), column sums, conditioning, fc2 bias.
+  void* scratch = nullptr;
+  const size_t scratch_bytes = align_up(H * H * 8) + align_up(H * 8) + align_up(C * 8) + align_up(std::max(D, H) * 4);
+  if (cudaMalloc(&scratch, scratch_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return cleanup(fail(FLASHMAP_E_NOMEM, "cannot allocate load-time scratch"));
+  }
+  struct ScratchGuard {
+    void* p;
+    ~ScratchGuard() { cudaFree(p); }
+  } guard{scratch};
+  Carver sc(scratch);
+  double* gram = sc.take<double>(H * H * 8);
+  double* colsum = sc.take<double>(H * 8);
+  double* cond = sc.take<double>(C * 8);
+  float* tmp_d = sc.take<float>(std::max(D, H) * 4);  // D or H floats of scratch
+
+#define LCHK(call)                                                                                  \
+  do {                                                                                              \
+    cudaError_t e_ = (call);                                                                        \
+    if (e_ != cudaSuccess) return cleanup(fail(FLASHMAP_E_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_))); \
+  } while (0)
+
+  LCHK(fm::gemm_prepare());
+  LCHK(cudaMemsetAsync(m->dev_err, 0, 4, s));
+  auto copy = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
+  auto bytes_of = [&](int64_t rows, int64_t cols) { return static_cast<size_t>(rows) * cols * es; };
+  uint8_t* ck = static_cast<uint8_t*>(const_cast<void*>(m->ctx_kv.ptr));
+  // ---- copies: the all-layer context K/V weight [k_0; v_0; ...] and fused q/k/v
+  LCHK(copy(const_cast<void*>(m->fc.ptr), w->fc_w, bytes_of(D, m->Lt * H)));
+  LCHK(copy(const_cast<void*>(m->ap.ptr), w->anchor_proj_w, bytes_of(D, H)));
+  LCHK(copy(const_cast<void*>(m->xe.ptr), w->x_embed_w, bytes_of(D, H)));
+  for (int l = 0; l < L; ++l) {
+    const flashmap_layer_weights& lw = w->layers[l];
+    LayerW& d = m->layers[l];
+    LCHK(copy(ck + bytes_of(2 * l * D, D), lw.cross_k_w, bytes_of(D, D)));
+    LCHK(copy(ck + bytes_of((2 * l + 1) * D, D), lw.cross_v_w, bytes_of(D, D)));
+    uint8_t* q = static_cast<uint8_t*>(const_cast<void*>(d.qkv.ptr));
+    LCHK(copy(q, lw.self_q_w, bytes_of(D, D)));
+    LCHK(copy(q + bytes_of(D, D), lw.self_k_w, bytes_of(D, D)));
+    LCHK(copy(q + bytes_of(2 * D, D), lw.self_v_w, bytes_of(D, D)));
+    LCHK(copy(const_cast<void*>(d.o.ptr), lw.self_o_w, bytes_of(D, D)));
+    LCHK(copy(const_cast<void*>(d.cq.ptr), lw.cross_q_w, bytes_of(D, D)));
+    LCHK(copy(const_cast<void*>(d.co.ptr), lw.cross_o_w, bytes_of(D, D)));
+    LCHK(copy(const_cast<void*>(d.fc1.ptr), lw.fc1_w, bytes_of(F, D)));
+    LCHK(copy(const_cast<void*>(d.fc2.ptr), lw.fc2_w, bytes_of(D, F)));
+    LCHK(fm::to_f32(s, lw.self_q_norm_w, adt, hd, d.qn));
+    LCHK(fm::to_f32(s, lw.self_k_norm_w, adt, hd, d.kn));
+    LCHK(fm::to_f32(s, lw.cross_q_norm_w, adt, hd, d.cqn));
+    LCHK(fm::to_f32(s, lw.cross_k_norm_w, adt, hd, m->ctx_knorm + l * hd));
+    LCHK(fm::to_f32(s, lw.fc1_b, adt, F, d.fc1_b));
+  }
+  LCHK(fm::to_f32(s, w->hidden_norm_w, adt, D, m->hidden_norm_w));
+  LCHK(fm::to_f32(s, w->anchor_norm_w, adt, D, m->anchor_norm_w));
+  LCHK(fm::to_f32(s, w->noise_norm_w, adt, H, m->noise_norm_w));
+  LCHK(fm::to_f32(s, w->anchor_proj_b, adt, D, m->ap_b));
+  LCHK(fm::to_f32(s, w->x_embed_b, adt, D, m->xe_b));
+
+  // ---- AdaLN modulations of the jump 0 -> 1
+  fm::TimeCondArgs ta{w->time_l1_w, w->time_l1_b, w->time_l2_w, w->time_l2_b, w->jump_l1_w, w->jump_l1_b,
+                      w->jump_l2_w, w->jump_l2_b, adt, cfg->cond_dim, cfg->time_embed_dim, 0.0, 1.0,
+                      static_cast<double>(cfg->time_scale)};
+  LCHK(fm::time_cond(s, ta, cond));
+  for (int l = 0; l < L; ++l) {
+    const flashmap_layer_weights& lw = w->layers[l];
+    LayerW& d = m->layers[l];
+    const void* aw[3] = {lw.self_adaln_w, lw.cross_adaln_w, lw.mlp_adaln_w};
+    const void* ab[3] = {lw.self_adaln_b, lw.cross_adaln_b, lw.mlp_adaln_b};
+    for (int j = 0; j < 3; ++j)
+      LCHK(fm::adaln(s, aw[j], ab[j], adt, cfg->cond_dim, m->D, cond, d.mods + (3 * j) * D, d.mods + (3 * j + 1) * D,
+                     d.mods + (3 * j + 2) * D));
+    // fc2's bias enters the gated residual as gate * b2
+    LCHK(fm::to_f32(s, lw.fc2_b, adt, D, tmp_d));
+    LCHK(fm::mul_vec(s, d.mods + 8 * D, tmp_d, d.fc2_beta, m->D));
+  }
+  LCHK(fm::adaln(s, w->final_adaln_w, w->final_adaln_b, adt, cfg->cond_dim, m->D, cond, m->final_mods,
+                 m->final_mods + D, nullptr));
+
+  // ---- the uniform posterior's embedding and the Cholesky factor of E^T E
+  LCHK(fm::to_f32(s, w->state_norm_w, adt, H, tmp_d));
+  LCHK(fm::uniform_constant(s, embedding, adt, V, m->H, tmp_d, cfg->rms_norm_eps, colsum, m->u));
+  LCHK(cudaMemsetAsync(gram, 0, H * H * 8, s));
+  LCHK(fm::simt_gemm(s, m->H, m->H, m->V, embedding, adt, nullptr, 1, H, embedding, adt, H, 1, gram, FLASHMAP_F32, H, 2));
+  LCHK(fm::cholesky_f64(s, gram, m->H, m->dev_err));
+  LCHK(fm::chol_store(s, gram, m->H, adt, const_cast<void*>(m->chol.ptr)));
+
+  // ---- draft vocabulary and the folded head
+  {
+    std::vector<int64_t> hot(Vd);
+    if (Vd < V) {
+      std::vector<int64_t> rank(V);
+      LCHK(cudaMemcpyAsync(rank.data(), vocab_ranking, V * 8, cudaMemcpyDeviceToHost, s));
+      LCHK(cudaStreamSynchronize(s));
+      std::copy(rank.begin(), rank.begin() + Vd, hot.begin());
+      std::sort(hot.begin(), hot.end());
+      for (int64_t i = 0; i < Vd; ++i)
+        if (hot[i] < 0 || hot[i] >= V || (i && hot[i] == hot[i - 1]))
+          return cleanup(fail(FLASHMAP_E_INVALID, "vocab_ranking must hold distinct token ids in [0, V)"));
+    } else {
+      for (int64_t i = 0; i < V; ++i) hot[i] = i;
+    }
+    std::vector<int32_t> inv(V, -1);
+    for (int64_t i = 0; i < m->Vd; ++i) inv[hot[i]] = static_cast<int32_t>(i);
+    LCHK(cudaMemcpyAsync(m->hot, hot.data(), m->Vd * 8, cudaMemcpyHostToDevice, s));
+    LCHK(cudaMemcpyAsync(m->inv_hot, inv.data(), V * 4, cudaMemcpyHostToDevice, s));
+    // W_f = LM[hot] W_head (Vd x D), b_f = LM[hot] b_head, float32 accumulation
+    LCHK(fm::simt_gemm(s, m->Vd, m->D, m->H, lm_head, adt, m->hot, H, 1, w->head_w, adt, D, 1,
+                       const_cast<void*>(m->head.ptr), adt, D, 1));
+    LCHK(fm::simt_gemm(s, m->Vd, 1, m->H, lm_head, adt, m->hot, H, 1, w->head_b, adt, 1, 0, m->head_b,
+                       FLASHMAP_F32, 1, 0));
+    // rotary table
+    std::vector<float2> rt = rope_table(m->maxpos, m->hd, cfg->rope_theta);
+    LCHK(cudaMemcpyAsync(m->rope, rt.data(), rt.size() * sizeof(float2), cudaMemcpyHostToDevice, s));
+    // the noise gate of the jump 0 -> 1: noise_gate * (t - s) = noise_gate
+    float ng = 1.f;
+    if (adt == FLASHMAP_F32) {
+      LCHK(cudaMemcpyAsync(&ng, w->noise_gate, 4, cudaMemcpyDeviceToHost, s));
+      LCHK(cudaStreamSynchronize(s));
+    } else {
+      __nv_bfloat16 b;
+      LCHK(cudaMemcpyAsync(&b, w->noise_gate, 2, cudaMemcpyDeviceToHost, s));
+      LCHK(cudaStreamSynchronize(s));
+      ng = __bfloat162float(b);
+    }
+    m->gate = cfg->noise_gate_constant ? ng : ng * (1.0f - 0.0f);
+    LCHK(cudaStreamSynchronize(s));  // host vectors above must outlive their copies
+  }
+
+  // ---- GEMM descriptors
+  m->fc.N = m->D, m->fc.K = m->Lt * m->H;
+  m->ap.N = m->D, m->ap.K = m->H;
+  m->ctx_kv.N = 2 * m->L * m->D, m->ctx_kv.K = m->D;
+  m->chol.N = m->H, m->chol.K = m->H;
+  m->xe.N = m->D, m->xe.K = m->H;
+  m->head.N = m->Vd, m->head.K = m->D;
+  std::string err;
+  Weight* ws[] = {&m->fc, &m->ap, &m->ctx_kv, &m->chol, &m->xe, &m->head};
+  for (Weight* x : ws)
+    if (check_weight_map(*x, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  for (auto& d : m->layers) {
+    d.qkv.N = 3 * m->D, d.qkv.K = m->D;
+    d.o.N = m->D, d.o.K = m->D;
+    d.cq.N = m->D, d.cq.K = m->D;
+    d.co.N = m->D, d.co.K = m->D;
+    d.fc1.N = m->F, d.fc1.K = m->D;
+    d.fc2.N = m->D, d.fc2.K = m->F;
+    Weight* lws[] = {&d.qkv, &d.o, &d.cq, &d.co, &d.fc1, &d.fc2};
+    for (Weight* x : lws)
+      if (check_weight_map(*x, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  }
+  LCHK(cudaStreamSynchronize(s));
+  LCHK(cudaGetLastError());
+  unsigned derr = 0;
+  LCHK(cudaMemcpy(&derr, m->dev_err, 4, cudaMemcpyDeviceToHost));
+  if (derr) return cleanup(fail(FLASHMAP_E_DEVICE, "E^T E is not positive definite (Cholesky pivot <= 0)"));
+#undef LCHK
+  *out = m;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_workspace_size(const flashmap_model* m, int32_t max_bs, int32_t max_write_rows,
+                                        size_t* bytes) {
+  g_last_error.clear();
+  if (!m || !bytes || max_bs <= 0 || max_write_rows < 0) return fail(FLASHMAP_E_INVALID, "bad workspace query");
+  size_t wb = 0;
+  carve_write(m, std::max(max_write_rows, 1), nullptr, &wb);
+  *bytes = std::max({carve_draft(m, max_bs, nullptr).bytes, sample_bytes(m, max_bs), wb});
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_pool* pool, const void* target_hidden,
+                                          int32_t bs, int32_t W, const int32_t* req_pool_idx,
+                                          const int32_t* start_pos, const int32_t* commit_lens,
+                                          const int32_t* req_to_page, int32_t req_to_page_stride, int64_t* out_loc,
+                                          void* workspace, size_t workspace_bytes, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m || !pool || !target_hidden || !req_pool_idx || !start_pos || !req_to_page || !workspace)
+    return fail(FLASHMAP_E_INVALID, "NULL argument");
+  if (bs <= 0 || W <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs, W and the page-table stride must be positive");
+  if (pool->dtype != m->adt || !pool->base || pool->num_pages <= 0)
+    return fail(FLASHMAP_E_INVALID, "pool dtype must equal act_dtype, with pages");
+  if (m->adt == FLASHMAP_BF16 && (reinterpret_cast<uintptr_t>(target_hidden) & 15))
+    return fail(FLASHMAP_E_INVALID, "target_hidden must be 16-byte aligned");
+  const int64_t total = static_cast<int64_t>(bs) * W;
+  const size_t per_row = write_row_bytes(m) + 3 * 256;
+  int64_t chunk = static_cast<int64_t>(workspace_bytes / per_row);
+  chunk = std::min<int64_t>(chunk, total);
+  size_t need = 0;
+  while (chunk > 0) {
+    carve_write(m, static_cast<int>(chunk), nullptr, &need);
+    if (need <= workspace_bytes) break;
+    --chunk;
+  }
+  if (chunk <= 0) return fail(FLASHMAP_E_INVALID, "workspace too small for one write row");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Launch Lh = m->launch(s);
+  const size_t xrow = static_cast<size_t>(m->Lt) * m->H * dt_size(m->adt);
+  for (int64_t r0 = 0; r0 < total; r0 += chunk) {
+    const int rows = static_cast<int>(std::min<int64_t>(chunk, total - r0));
+    size_t b = 0;
+    WriteWs ws = carve_write(m, rows, workspace, &b);
+    TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_fc, 0, static_cast<size_t>(rows) * m->D * 4, s));
+    TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_kv, 0, static_cast<size_t>(rows) * 2 * m->L * m->D * 4, s));
+    const void* x = static_cast<const uint8_t*>(target_hidden) + r0 * xrow;
+    // ctx = RMSNorm_hidden(fc(x)); kv = W_ctx ctx
+    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, m->adt, ws.acc_fc, rows, m->D, m->hidden_norm_w, m->cfg.rms_norm_eps,
+                                               1.f, nullptr, 0.f, ws.ctx, m->D));
+    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr, nullptr));
+    fm::KvWriteArgs a;
+    a.acc = ws.acc_kv;
+    a.ld = 2LL * m->L * m->D;
+    a.rows = rows;
+    a.W = W;
+    a.row0 = r0;
+    a.start_pos = start_pos;
+    a.commit_lens = commit_lens;
+    a.req_pool_idx = req_pool_idx;
+    a.req_to_page = req_to_page;
+    a.r2p_stride = req_to_page_stride;
+    a.L = m->L;
+    a.nh = m->nh;
+    a.hd = m->hd;
+    a.P = m->P;
+    a.num_pages = pool->num_pages;
+    a.k_norm = m->ctx_knorm;
+    a.eps = m->cfg.qk_norm_eps;
+    a.rope = m->rope;
+    a.max_pos = m->maxpos;
+    a.pool = pool->base;
+    a.out_loc = out_loc;
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->adt, a));
+  }
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs,
+                                     const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                     const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                     int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
+                                     void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                     size_t workspace_bytes, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m || !pool || !anchor_ids || !anchor_pos || !req_pool_idx || !req_to_page || !seeds || !hidden_out || !workspace)
+    return fail(FLASHMAP_E_INVALID, "NULL argument");
+  if (bs <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs and the page-table stride must be positive");
+  if (pool->dtype != m->adt || !pool->base || pool->num_pages <= 0)
+    return fail(FLASHMAP_E_INVALID, "pool dtype must equal act_dtype, with pages");
+  if (!std::isfinite(noise_scale)) return fail(FLASHMAP_E_INVALID, "noise_scale must be finite");
+  const DraftWs need = carve_draft(m, bs, nullptr);
+  if (workspace_bytes < need.bytes)
+    return fail(FLASHMAP_E_INVALID, "workspace too small: need " + std::to_string(need.bytes) + " bytes");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Launch Lh = m->launch(s);
+  const DraftWs ws = carve_draft(m, bs, workspace);
+  const int R = bs * m->K, D = m->D, H = m->H, adt = m->adt;
+  const size_t big = std::max({3 * static_cast<size_t>(D), static_cast<size_t>(m->F), static_cast<size_t>(H)});
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.x, 0, static_cast<size_t>(R) * D * 4, s));
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_big, 0, static_cast<size_t>(R) * big * 4, s));
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_d, 0, static_cast<size_t>(R) * D * 4, s));
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_a, 0, static_cast<size_t>(bs) * D * 4, s));
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_kv, 0, static_cast<size_t>(bs) * 2 * m->L * D * 4, s));
+  // split-KV plan of the cross-attention, shared by every layer
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, anchor_pos, bs, m->nh, ws.plan));
+  // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(Lh, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
+  TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.a_rows, D));
+  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(Lh, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr));
+  {
+    fm::KvWriteArgs a;
+    a.acc = ws.acc_kv;
+    a.ld = 2LL * m->L * D;
+    a.rows = bs;
+    a.W = 1;
+    a.row0 = 0;
+    a.start_pos = anchor_pos;
+    a.req_pool_idx = req_pool_idx;
+    a.req_to_page = req_to_page;
+    a.r2p_stride = req_to_page_stride;
+    a.L = m->L;
+    a.nh = m->nh;
+    a.hd = m->hd;
+    a.P = m->P;
+    a.num_pages = pool->num_pages;
+    a.k_norm = m->ctx_knorm;
+    a.eps = m->cfg.qk_norm_eps;
+    a.rope = m->rope;
+    a.max_pos = m->maxpos;
+    a.pool = pool->base;
+    a.out_loc = anchor_loc_out;
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, adt, a));
+  }
+  // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act));
+  TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
+                       ws.act, H));
+  TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b));
+  // 3. the DiT blocks
+  const float eps_ln = m->cfg.layer_norm_eps, eps_qk = m->cfg.qk_norm_eps;
+  fm::XattnArgs xa;
+  xa.pool = pool->base;
+  xa.num_pages = pool->num_pages;
+  xa.bs = bs;
+  xa.K = m->K;
+  xa.nh = m->nh;
+  xa.hd = m->hd;
+  xa.P = m->P;
+  xa.anchor_pos = anchor_pos;
+  xa.req_pool_idx = req_pool_idx;
+  xa.req_to_page = req_to_page;
+  xa.r2p_stride = req_to_page_stride;
+  xa.plan = ws.plan;
+  xa.part_o = ws.part_o;
+  xa.part_ml = ws.part_ml;
+  xa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m->hd)));
+  xa.q = ws.act2;
+  for (int l = 0; l < m->L; ++l) {
+    const LayerW& lw = m->layers[l];
+    const float* md = lw.mods;
+    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
+    TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr));
+    TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bs, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
+                               anchor_pos, ws.act));
+    TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr));
+    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
+    TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr));
+    TIMED(FLASHMAP_KIND_ROWS, l, fm::qnorm_rope(Lh, adt, ws.acc_d, R, m->K, m->nh, m->hd, lw.cqn, eps_qk, m->rope, m->maxpos, anchor_pos,
+                           ws.act2));
+    xa.layer = l;
+    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, adt, xa));
+    TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
+    TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr));
+    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
+    TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b));
+    TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lh, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
+    TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, lw.fc2_beta));
+  }
+  // 4. final AdaLN
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, m->final_mods, m->final_mods + D, eps_ln, hidden_out));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void* hidden, const int32_t* anchor_pos,
+                                      const float* temperature, const uint8_t* greedy, const uint64_t* seeds,
+                                      uint64_t step, int64_t* tokens_out, float* draft_logits_out,
+                                      float* full_logits_out, void* workspace, size_t workspace_bytes,
+                                      flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m || !hidden || !anchor_pos || !temperature || !greedy || !seeds || !tokens_out)
+    return fail(FLASHMAP_E_INVALID, "NULL argument");
+  if (bs <= 0) return fail(FLASHMAP_E_INVALID, "bs must be positive");
+  if (m->adt == FLASHMAP_BF16 && (reinterpret_cast<uintptr_t>(hidden) & 15))
+    return fail(FLASHMAP_E_INVALID, "hidden must be 16-byte aligned");
+  float* logits = draft_logits_out;
+  if (!logits) {
+    if (!workspace || workspace_bytes < sample_bytes(m, bs))
+      return fail(FLASHMAP_E_INVALID, "workspace too small for the draft logits");
+    logits = static_cast<float*>(workspace);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Launch Lh = m->launch(s);
+  const int R = bs * m->K;
+  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(logits, 0, static_cast<size_t>(R) * m->Vd * 4, s));
+  TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b));
+  TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::sample_rows(Lh, logits, R, m->Vd, m->K, temperature, greedy, seeds, anchor_pos,
+                                                   static_cast<uint32_t>(step), m->hot, tokens_out));
+  if (full_logits_out)
+    TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::full_scatter(Lh, logits, R, m->Vd, m->inv_hot, m->V, full_logits_out));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_get_device_error(flashmap_model* m, flashmap_stream stream, uint32_t* code) {
+  g_last_error.clear();
+  if (!m || !code) return fail(FLASHMAP_E_INVALID, "NULL argument");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  FM_CUDA(cudaStreamSynchronize(s));
+  FM_CUDA(cudaMemcpy(&v, m->dev_err, 4, cudaMemcpyDeviceToHost));
+  FM_CUDA(cudaMemset(m->dev_err, 0, 4));
+  *code = v;
+  if (v) return fail(FLASHMAP_E_DEVICE, "device error bits " + std::to_string(v));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_profile_start(flashmap_model* m, int32_t capacity) {
+  g_last_error.clear();
+  if (!m || capacity < 0) return fail(FLASHMAP_E_INVALID, "bad argument");
+  m->prof_recs.clear();
+  m->prof_cap = capacity;
+  m->prof_on = true;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_profile_stop(flashmap_model* m, flashmap_launch_record* out, int32_t capacity,
+                                      int32_t* count) {
+  g_last_error.clear();
+  if (!m || !count) return fail(FLASHMAP_E_INVALID, "bad argument");
+  m->prof_on = false;
+  const int n = static_cast<int>(m->prof_recs.size());
+  for (int i = 0; i < n; ++i) {
+    FM_CUDA(cudaEventSynchronize(m->prof_events[2 * i + 1]));
+    float ms = 0.f;
+    FM_CUDA(cudaEventElapsedTime(&ms, m->prof_events[2 * i], m->prof_events[2 * i + 1]));
+    m->prof_recs[i].ms = ms;
+  }
+  if (out)
+    for (int i = 0; i < std::min(n, static_cast<int>(capacity)); ++i) out[i] = m->prof_recs[i];
+  *count = n;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_debug_philox(const uint64_t* seeds, const uint32_t* ctr, int64_t n, uint32_t* out,
+                                      float* normals, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!seeds || !ctr || !out || n < 0) return fail(FLASHMAP_E_INVALID, "bad argument");
+  FM_CUDA(fm::philox_export(reinterpret_cast<cudaStream_t>(stream), seeds, ctr, n, out, normals));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* w, int32_t rows, int32_t in_features,
+                                      int32_t out_features, float* out, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!x || !w || !out || rows <= 0 || in_features <= 0 || out_features <= 0 || !is_act(dtype))
+    return fail(FLASHMAP_E_INVALID, "bad argument");
+  if (dtype == FLASHMAP_BF16 && in_features % 8) return fail(FLASHMAP_E_INVALID, "in_features must be a multiple of 8");
+  int dev = 0, sms = 0;
+  FM_CUDA(cudaGetDevice(&dev));
+  FM_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  FM_CUDA(fm::gemm_prepare());
+  Weight W;
+  W.ptr = w;
+  W.N = out_features;
+  W.K = in_features;
+  std::string err;
+  if (check_weight_map(W, dtype, &err) != FLASHMAP_OK) return fail(FLASHMAP_E_CUDA, err);
+  Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr};
+  FM_CUDA(fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_debug_constants(const flashmap_model* m, float* chol, float* uniform, int64_t* hot_ids,
+                                         flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m) return fail(FLASHMAP_E_INVALID, "NULL model");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (chol) FM_CUDA(fm::to_f32(s, m->chol.ptr, m->adt, static_cast<int64_t>(m->H) * m->H, chol));
+  if (uniform) FM_CUDA(cudaMemcpyAsync(uniform, m->u, static_cast<size_t>(m->H) * 4, cudaMemcpyDeviceToDevice, s));
+  if (hot_ids) FM_CUDA(cudaMemcpyAsync(hot_ids, m->hot, static_cast<size_t>(m->Vd) * 8, cudaMemcpyDeviceToDevice, s));
+  return FLASHMAP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,450 @@
+// Dense contractions of the FlashMap step.
+//
+// bf16: a persistent, warp-specialized tcgen05 kernel. Every linear of the step is
+// "weights x activations" with few activation rows (16 at batch 1), so the weight
+// matrix W (N x K) is the MMA's A operand (M = 128 output channels per tile) and the
+// activation rows are the B operand (N = 16..256 rows): the tensor core's large M
+// dimension is spent on the weights and no row padding to 128 is needed. The
+// iteration space (output tile, 64-wide k block) is cut into equal contiguous ranges,
+// one per CTA (stream-K), so every SM streams the same number of weight bytes whatever
+// the shape; partial tiles are summed with float atomics into the caller's output.
+// Roles: warp 0 issues TMA loads (128B-swizzled, weights with an evict-first L2
+// policy), warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 drain the double-
+// buffered TMEM accumulator (tcgen05.ld) into global memory.
+//
+// float32: SIMT kernels (the float32 path must match a float64 reference to 1e-4,
+// which TF32 tensor cores cannot), and a general strided SIMT GEMM for load-time work.
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fm {
+namespace {
+
+constexpr int kTcThreads = 192;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = BN <= 32 ? 5 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  static constexpr int A_BYTES = 128 * 64 * 2;
+  static constexpr int B_BYTES = BN * 64 * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int PER_SM = 2 * (SMEM + 1024) <= 227 * 1024 ? 2 : 1;
+};
+
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_linear_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
+                     float* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
+                     const float* __restrict__ beta, unsigned* dev_err) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full_bar[C::STAGES], empty_bar[C::STAGES], acc_full[2], acc_empty[2], drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+  __shared__ int64_t issued, consumed;
+
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int mt = (N + 127) >> 7, rt = (R + BN - 1) / BN, KB = (K + 63) >> 6;
+  const int64_t T = static_cast<int64_t>(mt) * rt * KB;
+  const int64_t it0 = T * blockIdx.x / gridDim.x, it1 = T * (blockIdx.x + 1) / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(&drain_bar, 1);
+    abort_flag = 0;
+    issued = 0;
+    consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t it = it0; it < it1; ++it) {
+        const int64_t tile = it / KB;
+        const int kb = static_cast<int>(it - tile * KB);
+        const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) break;
+        uint8_t* sa = smem + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+        tma_load_2d(sa, &mapW, &full_bar[stage], kb * 64, m * 128, pol_w);
+        tma_load_2d(sa + C::A_BYTES, &mapX, &full_bar[stage], kb * 64, r * BN, pol_x);
+        ++issued;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int seg = 0;
+      int64_t it = it0;
+      bool ok = true;
+      while (ok && it < it1) {
+        const int64_t tile = it / KB;
+        const int64_t seg_end = min(it1, (tile + 1) * KB);
+        const int buf = seg & 1;
+        const uint32_t aph = (seg >> 1) & 1;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, &abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+        bool first = true;
+        for (; it < seg_end; ++it) {
+          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          ++consumed;
+          const uint32_t sa = base + stage * C::STAGE_BYTES;
+          const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // 4 x (K = 16) per 64-wide block; +32 B per step
+            umma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+          }
+          first = false;
+          umma_commit(&empty_bar[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[buf]);
+        ++seg;
+      }
+      umma_commit(&drain_bar);  // every MMA issued above has completed past this wait
+      if (!mbar_wait_timed(&drain_bar, 0)) abort_flag = 1;
+    }
+  } else {  // epilogue: warps 2..5, TMEM lane quadrant warp % 4
+    const int q = warp & 3;
+    int seg = 0;
+    int64_t it = it0;
+    while (it < it1) {
+      const int64_t tile = it / KB;
+      const int kb0 = static_cast<int>(it - tile * KB);
+      const int64_t seg_end = min(it1, (tile + 1) * KB);
+      const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+      const int buf = seg & 1;
+      const uint32_t aph = (seg >> 1) & 1;
+      if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
+      tc_fence_after();
+      const int n = m * 128 + q * 32 + lane;
+      // A tile whose whole k range is in this segment has no other writer: plain
+      // read-modify-write; partial tiles are summed with atomics.
+      const bool whole = kb0 == 0 && seg_end == (tile + 1) * KB;
+      float a = 1.f, b = 0.f;
+      if (n < N) {
+        if (alpha) a = alpha[n];
+        if (beta && kb0 == 0) b = beta[n];
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + c0), v);
+        const int row0 = r * BN + c0;
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (row0 + j < R) {
+              float* o = out + static_cast<int64_t>(row0 + j) * ldo + n;
+              if (whole)
+                *o += fmaf(a, v[j], b);
+              else
+                atomicAdd(o, fmaf(a, v[j], b));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      it = seg_end;
+      ++seg;
+    }
+  }
+
+  __syncthreads();
+  if (threadIdx.x == 0 && abort_flag) {
+    // Wait (bounded) for the TMA loads still in flight before the CTA exits.
+    for (int64_t i = consumed; i < issued; ++i) {
+      mbar_wait_timed(&full_bar[i % C::STAGES], static_cast<uint32_t>((i / C::STAGES) & 1));
+    }
+    set_dev_error(dev_err, FLASHMAP_DEVERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ SIMT linear (float32 path)
+
+template <typename T>
+__global__ void __launch_bounds__(256) linear_warp_kernel(const T* __restrict__ x, int R, int ldx,
+                                                          const T* __restrict__ w, int N, int K,
+                                                          float* __restrict__ out, int ldo,
+                                                          const float* __restrict__ alpha,
+                                                          const float* __restrict__ beta) {
+  constexpr int RB = 4;
+  const int n = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  const T* wr = w + static_cast<int64_t>(n) * K;
+  const float a = alpha ? alpha[n] : 1.f, b = beta ? beta[n] : 0.f;
+  for (int r0 = 0; r0 < R; r0 += RB) {
+    float acc[RB] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = lane; k < K; k += 32) {
+      const float wv = to_f32(wr[k]);
+#pragma unroll
+      for (int j = 0; j < RB; ++j)
+        if (r0 + j < R) acc[j] = fmaf(wv, to_f32(x[static_cast<int64_t>(r0 + j) * ldx + k]), acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const float s = warp_sum(acc[j]);
+      if (lane == 0 && r0 + j < R) atomicAdd(out + static_cast<int64_t>(r0 + j) * ldo + n, fmaf(a, s, b));
+    }
+  }
+}
+
+// ------------------------------------------------------------------ general strided SIMT GEMM (load time)
+
+__device__ __forceinline__ float ld_any(const void* p, int dt, int64_t i) {
+  return dt == FLASHMAP_F32 ? static_cast<const float*>(p)[i]
+                            : __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+__global__ void __launch_bounds__(256) simt_gemm_kernel(int M, int N, int K, int kchunk, const void* a, int adt,
+                                                        const int64_t* __restrict__ arows, int64_t sam,
+                                                        int64_t sak, const void* b, int bdt, int64_t sbk,
+                                                        int64_t sbn, void* c, int cdt, int64_t ldc, int mode) {
+  __shared__ float As[16][65], Bs[16][65];
+  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int kbeg = blockIdx.z * kchunk, kend = min(K, kbeg + kchunk);
+  float acc[4][4] = {};
+  for (int k0 = kbeg; k0 < kend; k0 += 16) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = tid + 256 * i;
+      int mm, kk;
+      if (sak == 1) {
+        kk = e & 15;
+        mm = e >> 4;
+      } else {
+        mm = e & 63;
+        kk = e >> 6;
+      }
+      const int gm = m0 + mm, gk = k0 + kk;
+      float v = 0.f;
+      if (gm < M && gk < kend) {
+        const int64_t row = arows ? arows[gm] : gm;
+        v = ld_any(a, adt, row * sam + static_cast<int64_t>(gk) * sak);
+      }
+      As[kk][mm] = v;
+      int nn;
+      if (sbn == 1) {
+        nn = e & 63;
+        kk = e >> 6;
+      } else {
+        kk = e & 15;
+        nn = e >> 4;
+      }
+      const int gn = n0 + nn, gk2 = k0 + kk;
+      float u = 0.f;
+      if (gn < N && gk2 < kend) u = ld_any(b, bdt, static_cast<int64_t>(gk2) * sbk + static_cast<int64_t>(gn) * sbn);
+      Bs[kk][nn] = u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][tm * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tn * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + tm * 4 + i;
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tn * 4 + j;
+      if (gn >= N) continue;
+      const int64_t idx = static_cast<int64_t>(gm) * ldc + gn;
+      if (mode == 0) {
+        static_cast<float*>(c)[idx] = acc[i][j];
+      } else if (mode == 1) {
+        if (cdt == FLASHMAP_F32)
+          static_cast<float*>(c)[idx] = acc[i][j];
+        else
+          static_cast<__nv_bfloat16*>(c)[idx] = __float2bfloat16_rn(acc[i][j]);
+      } else {
+        atomicAdd(static_cast<double*>(c) + idx, static_cast<double>(acc[i][j]));
+      }
+    }
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+template <int BN>
+cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, float* out, int ldo,
+                      const float* alpha, const float* beta) {
+  using C = TcCfg<BN>;
+  CUtensorMap mapX;
+  std::string err;
+  if (!make_tmap_bf16(&mapX, x, R, W.K, ldx, BN, &err)) return cudaErrorInvalidValue;
+  const int64_t mt = (W.N + 127) / 128, rt = (R + BN - 1) / BN, KB = (W.K + 63) / 64;
+  const int64_t T = mt * rt * KB;
+  const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * C::PER_SM));
+  tc_linear_kernel<BN><<<G, kTcThreads, C::SMEM, L.stream>>>(W.map, mapX, out, ldo, R, W.N, W.K, alpha, beta,
+                                                             L.dev_err);
+  return cudaGetLastError();
+}
+
+template <int BN>
+cudaError_t set_tc_attr() {
+  return cudaFuncSetAttribute(tc_linear_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
+}
+
+}  // namespace
+
+cudaError_t gemm_prepare() {
+  cudaError_t e;
+  if ((e = set_tc_attr<16>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<32>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<64>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<128>()) != cudaSuccess) return e;
+  return set_tc_attr<256>();
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows,
+                    std::string* err) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    if (err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || ((ld * 2) & 15) || cols <= 0 || rows <= 0) {
+    if (err) *err = "tensor map operand must be 16-byte aligned with a 16-byte multiple row pitch";
+    return false;
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) *err = "cuTensorMapEncodeTiled failed (" + std::to_string(static_cast<int>(r)) + ")";
+    return false;
+  }
+  return true;
+}
+
+cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
+                   const float* alpha, const float* beta) {
+  if (rows <= 0 || W.N <= 0) return cudaSuccess;
+  if (W.dtype == FLASHMAP_BF16) {
+    if (!W.has_map) return cudaErrorInvalidValue;
+    if (rows <= 16) return launch_tc<16>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+    if (rows <= 32) return launch_tc<32>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+    if (rows <= 64) return launch_tc<64>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+    if (rows <= 128) return launch_tc<128>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+    return launch_tc<256>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+  }
+  if (W.dtype == FLASHMAP_F32) {
+    const int64_t threads = static_cast<int64_t>(W.N) * 32;
+    const int blocks = static_cast<int>((threads + 255) / 256);
+    linear_warp_kernel<float><<<blocks, 256, 0, L.stream>>>(static_cast<const float*>(x), rows, ldx,
+                                                            static_cast<const float*>(W.ptr), W.N, W.K, out, ldo,
+                                                            alpha, beta);
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t simt_gemm(cudaStream_t s, int M, int N, int K, const void* a, int a_dtype, const int64_t* a_rows,
+                      int64_t sam, int64_t sak, const void* b, int b_dtype, int64_t sbk, int64_t sbn, void* c,
+                      int c_dtype, int64_t ldc, int mode) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  int kchunk = K, kz = 1;
+  if (mode == 2) {  // float32 partial sums over 1024-long k ranges, added in float64
+    kchunk = 1024;
+    kz = (K + kchunk - 1) / kchunk;
+  }
+  dim3 grid((N + 63) / 64, (M + 63) / 64, kz);
+  simt_gemm_kernel<<<grid, 256, 0, s>>>(M, N, K, kchunk, a, a_dtype, a_rows, sam, sak, b, b_dtype, sbk, sbn, c,
+                                        c_dtype, ldc, mode);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

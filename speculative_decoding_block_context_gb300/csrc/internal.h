@@ -1,0 +1,143 @@
+// Host-side interfaces shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "flashmap.h"
+
+namespace fm {
+
+struct Launch {
+  cudaStream_t stream;
+  int num_sms;
+  unsigned* dev_err;  // the model's device error word (may be null in debug calls)
+};
+
+// A GEMM weight W (N out, K in), row-major in device memory.
+struct Weight {
+  const void* ptr = nullptr;
+  int N = 0, K = 0;
+  int dtype = FLASHMAP_F32;      // F32 or BF16 (E4M3 copies are dequantized by the kernel)
+  const float* wscale = nullptr; // per-output-channel scale of an E4M3 weight
+  bool has_map = false;
+  CUtensorMap map;  // BF16: the A-operand tensor map (box 64 x 128, 128B swizzle)
+};
+
+// Encodes the tensor map of a row-major bf16 matrix (rows x cols, leading dim ld
+// elements) read in boxes of box_rows x 64 columns with 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                    int box_rows, std::string* err);
+
+// Sets the kernel attributes the tcgen05 GEMM needs on the current device (call once
+// per device before launching; not during stream capture).
+cudaError_t gemm_prepare();
+
+// out[r * ldo + n] += alpha[n] * sum_k x[r * ldx + k] * W[n][k] + beta[n]   (r < rows, n < N)
+// accumulated with float atomics (the output must hold its initial value, e.g. 0, or
+// the residual stream). alpha / beta may be null (1 / 0). x has W.dtype.
+cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
+                   const float* alpha, const float* beta);
+
+// General strided SIMT GEMM for load-time work, float32 accumulation:
+// C(m, n) = sum_k A(m, k) B(k, n), A(m, k) = a[arow(m) * sam + k * sak] with
+// arow(m) = a_rows ? a_rows[m] : m, B(k, n) = b[k * sbk + n * sbn]; types by dtype codes.
+// mode 0: c_f32[m * ldc + n] = acc;  mode 1: c (dtype c_dtype) = acc;  mode 2: atomic
+// double add into c_f64[m * ldc + n].
+cudaError_t simt_gemm(cudaStream_t s, int M, int N, int K, const void* a, int a_dtype, const int64_t* a_rows,
+                      int64_t sam, int64_t sak, const void* b, int b_dtype, int64_t sbk, int64_t sbn, void* c,
+                      int c_dtype, int64_t ldc, int mode);
+
+}  // namespace fm
+
+namespace fm {
+
+// ------------------------------------------------------------------ rows.cu
+struct KvWriteArgs {
+  float* acc = nullptr;  // [rows][ld] float32 projections: per layer [k (D) | v (D)]
+  int64_t ld = 0;
+  int rows = 0, W = 1;   // local row i is global row row0 + i = column % W of request / W
+  int64_t row0 = 0;
+  const int32_t* start_pos = nullptr;   // [bs] position of column 0
+  const int32_t* commit_lens = nullptr; // [bs] or null (all columns)
+  const int32_t* req_pool_idx = nullptr;
+  const int32_t* req_to_page = nullptr;
+  int r2p_stride = 0;
+  int L = 0, nh = 0, hd = 0, P = 0;
+  int64_t num_pages = 0;
+  const float* k_norm = nullptr;  // [L][hd]
+  float eps = 0.f;
+  const float2* rope = nullptr;   // [max_pos][hd / 2] (cos, sin)
+  int max_pos = 0;
+  void* pool = nullptr;
+  int64_t* out_loc = nullptr;
+  unsigned* dev_err = nullptr;
+};
+cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a);
+cudaError_t qnorm_rope(const Launch& L, int dtype, float* acc, int rows, int K, int nh, int hd, const float* w,
+                       float eps, const float2* rope, int max_pos, const int32_t* anchor_pos, void* out);
+cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
+                        const float* mh, float eps, void* out);
+cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
+                     float prescale, const float* add, float gate, void* out, int ldo);
+cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* out);
+cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
+                        int n, void* out);
+cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
+                        int H, void* out);
+cudaError_t philox_export(cudaStream_t s, const uint64_t* seeds, const uint32_t* ctr, int64_t n, uint32_t* out,
+                          float* normals);
+
+// ------------------------------------------------------------------ attention.cu
+struct XattnArgs {
+  const void* q = nullptr;      // [bs * K][D] normed, rotated queries
+  const void* pool = nullptr;
+  int64_t num_pages = 0;
+  int bs = 0, K = 0, nh = 0, hd = 0, P = 0, layer = 0;
+  const int32_t* anchor_pos = nullptr;
+  const int32_t* req_pool_idx = nullptr;
+  const int32_t* req_to_page = nullptr;
+  int r2p_stride = 0;
+  const int* plan = nullptr;
+  float* part_o = nullptr;   // [chunks * nh][16][hd]
+  float* part_ml = nullptr;  // [chunks * nh][16][2]
+  float scale_log2 = 0.f;    // hd^-1/2 * log2(e)
+  unsigned* dev_err = nullptr;
+};
+cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
+                           const float* kn, float eps, const float2* rope, int max_pos, const int32_t* anchor_pos,
+                           void* out);
+int xattn_max_chunks(int num_sms, int nh, int bs);
+size_t xattn_plan_ints(int num_sms, int nh, int bs);
+cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan);
+cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& a);
+cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& a, void* out);
+
+// ------------------------------------------------------------------ sample.cu
+cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
+                        const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
+                        const int64_t* hot, int64_t* tokens);
+cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
+                         float* full);
+
+// ------------------------------------------------------------------ loadtime.cu
+struct TimeCondArgs {
+  const void *te_l1_w, *te_l1_b, *te_l2_w, *te_l2_b, *je_l1_w, *je_l1_b, *je_l2_w, *je_l2_b;
+  int dtype, C, Te;
+  double s, t, time_scale;
+};
+cudaError_t to_f32(cudaStream_t s, const void* src, int dtype, int64_t n, float* dst);
+cudaError_t mul_vec(cudaStream_t s, const float* a, const float* b, float* out, int n);
+cudaError_t time_cond(cudaStream_t s, const TimeCondArgs& a, double* cond);
+cudaError_t adaln(cudaStream_t s, const void* w, const void* b, int dtype, int C, int D, const double* cond,
+                  float* s1, float* sh, float* gate);
+cudaError_t uniform_constant(cudaStream_t s, const void* E, int dtype, int64_t V, int H, const float* w, float eps,
+                             double* colsum, float* u);
+cudaError_t cholesky_f64(cudaStream_t s, double* A, int n, unsigned* err);
+cudaError_t chol_store(cudaStream_t s, const double* A, int n, int dtype, void* out);
+cudaError_t quantize_e4m3(cudaStream_t s, const void* w, int dtype, int rows, int cols, void* q, float* scale);
+
+}  // namespace fm

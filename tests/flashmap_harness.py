@@ -1,0 +1,253 @@
+"""Test harness: runs one draft step of a synthetic workload through the C ABI on the
+GPU and through the CPU oracle on the same seeded inputs, and compares them.
+
+The oracle never sees a value the CUDA path computed: its inputs are the seeded
+draws of ``synthetic`` (weights, hidden states, and, for prefilled workloads, the
+N(0, 1) context keys/values that torch wrote into the pool before any library call).
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from oracle import flashmap_ref as ref
+from speculative_decoding_block_context_gb300 import _lib as F
+from speculative_decoding_block_context_gb300 import synthetic as syn
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+TOKEN_MARGIN = 1e-2
+
+
+def max_rel(a, b) -> float:
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    den = max(float(np.max(np.abs(b))), 1e-30)
+    return float(np.max(np.abs(a - b))) / den
+
+
+@dataclass
+class ModelState:
+    cfg: dict
+    W: dict  # torch, device
+    E: torch.Tensor
+    LM: torch.Tensor
+    rank: torch.Tensor
+    handle: object = None
+    Wnp: dict = field(default_factory=dict)  # float32 numpy copies for the oracle
+    Enp: np.ndarray = None
+    consts: object = None
+
+    def oracle_cfg(self):
+        return ref.Config.from_dict(self.cfg)
+
+
+def load_model(workload: str, device="cuda", oracle: bool = True) -> ModelState:
+    cfg = syn.model_config(workload)
+    W, E, LM, rank = syn.make_model(cfg, device)
+    st = ModelState(cfg, W, E, LM, rank)
+    st.handle = F.flashmap_load_weights(cfg, W, E, LM, rank)
+    torch.cuda.synchronize()
+    if oracle:
+        st.Wnp = {k: v.float().cpu().numpy() for k, v in W.items()}
+        st.Enp = E.float().cpu().numpy()
+        st.consts = ref.load_constants(st.oracle_cfg(), st.Wnp, st.Enp, LM.float().cpu().numpy(),
+                                       rank.cpu().numpy())
+    return st
+
+
+def pool_view(cfg: dict, pool_t: torch.Tensor, num_pages: int) -> torch.Tensor:
+    dt = syn.torch_dtype(cfg["act_dtype"])
+    return pool_t.view(dt).view(cfg["num_layers"], 2, num_pages, cfg["num_heads"], cfg["page_size"], cfg["head_dim"])
+
+
+def gather_context(cfg: dict, pool6: torch.Tensor, req_to_page_row: torch.Tensor, n: int):
+    """Keys and values of positions 0..n-1 of one request, read through its page-table
+    row: numpy (L, n, heads, hd) x 2."""
+    P = cfg["page_size"]
+    npages = (n + P - 1) // P
+    pages = req_to_page_row[:npages].long()
+    g = pool6[:, :, pages]  # (L, 2, np, nh, P, hd)
+    g = g.permute(0, 1, 2, 4, 3, 5).reshape(cfg["num_layers"], 2, npages * P, cfg["num_heads"], cfg["head_dim"])
+    g = g[:, :, :n].float().cpu().numpy()
+    return g[:, 0], g[:, 1]
+
+
+@dataclass
+class LibRun:
+    req: dict
+    pool_t: torch.Tensor
+    pool6: torch.Tensor
+    prefill_loc: list
+    window_loc: torch.Tensor
+    anchor_loc: torch.Tensor
+    hidden: torch.Tensor
+    tokens: torch.Tensor
+    logits: torch.Tensor
+    full: torch.Tensor
+    prefilled_ctx: dict  # b -> (K, V) numpy of the drawn context (prefilled workloads)
+    dev_err: int
+
+
+def run_library(workload: str, st: ModelState, *, noise_scale: float = 1.0, check_subset=None,
+                req: dict | None = None) -> LibRun:
+    cfg, dev = st.cfg, "cuda"
+    req = req or syn.make_requests(workload, dev)
+    bs, K, D = req["bs"], cfg["block_size"], cfg["hidden"]
+    dt = syn.torch_dtype(cfg["act_dtype"])
+    code = F.DTYPE_CODES[cfg["act_dtype"]]
+    pool_t = torch.empty(F.flashmap_pool_bytes(cfg, req["num_pages"]), dtype=torch.uint8, device=dev)
+    pool6 = pool_view(cfg, pool_t, req["num_pages"])
+    prefilled = {}
+    if not req["prefill"]:
+        syn.fill_pool_random(pool_t.view(dt), req["kv_generator_seed"])
+        for b in (check_subset or []):
+            row = req["req_to_page"][int(req["req_pool_idx"][b])]
+            prefilled[b] = gather_context(cfg, pool6, row, req["ctx"][b])
+    pool = F.make_pool(pool_t, req["num_pages"], code)
+    max_rows = max(max(req["ctx"]) if req["prefill"] else 0, bs * (K + 1))
+    ws = torch.empty(F.flashmap_workspace_size(st.handle, bs, min(max_rows, 4096)), dtype=torch.uint8, device=dev)
+    prefill_loc = []
+    i32 = dict(dtype=torch.int32, device=dev)
+    if req["prefill"]:
+        for b in range(bs):
+            X = req["prefill_hidden"][b]
+            n = X.shape[0]
+            loc = torch.empty(n, dtype=torch.int64, device=dev)
+            F.flashmap_write_context_kv(st.handle, pool, X, 1, n, req["req_pool_idx"][b : b + 1],
+                                        torch.zeros(1, **i32), None, req["req_to_page"], loc, ws)
+            prefill_loc.append(loc)
+    window_loc = None
+    if req["window"]:
+        W = K + 1
+        window_loc = torch.empty(bs * W, dtype=torch.int64, device=dev)
+        F.flashmap_write_context_kv(st.handle, pool, req["window_hidden"], bs, W, req["req_pool_idx"],
+                                    torch.tensor(req["ctx"], **i32), torch.tensor(req["commit"], **i32),
+                                    req["req_to_page"], window_loc, ws)
+    anchor_pos = torch.tensor(req["anchor_pos"], **i32)
+    hidden = torch.empty((bs * K, D), dtype=dt, device=dev)
+    anchor_loc = torch.empty(bs, dtype=torch.int64, device=dev)
+    F.flashmap_draft_block(st.handle, pool, bs, req["anchor_ids"], anchor_pos, req["req_pool_idx"],
+                           req["req_to_page"], req["seeds"], noise_scale, hidden, anchor_loc, ws)
+    Vd = st.consts.hot.shape[0] if st.consts is not None else cfg["draft_vocab_size"] or cfg["vocab_size"]
+    tokens = torch.empty(bs * K, dtype=torch.int64, device=dev)
+    logits = torch.empty((bs * K, Vd), dtype=torch.float32, device=dev)
+    full = (torch.empty((bs * K, cfg["vocab_size"]), dtype=torch.float32, device=dev)
+            if req["full_scatter"] else None)
+    F.flashmap_sample_block(st.handle, bs, hidden, anchor_pos, req["temperature"], req["greedy"], req["seeds"],
+                            req["step"], tokens, logits, full, ws)
+    torch.cuda.synchronize()
+    err = F.flashmap_get_device_error(st.handle)
+    return LibRun(req, pool_t, pool6, prefill_loc, window_loc, anchor_loc, hidden, tokens, logits, full,
+                  prefilled, err)
+
+
+def oracle_batch(st: ModelState, run: LibRun, subset, noise_scale: float = 1.0) -> dict:
+    """The oracle's results for the requests in ``subset`` of the run's inputs."""
+    cfg, req = st.oracle_cfg(), run.req
+    W, C = st.Wnp, st.consts
+    K = cfg.block_size
+    outs, ctxs, ps, seeds = {}, [], [], []
+    for b in subset:
+        ctx = req["ctx"][b]
+        out = {}
+        if req["prefill"]:
+            X = req["prefill_hidden"][b].float().cpu().numpy()
+            kc, vc = ref.write_rows_kv(cfg, W, X, np.arange(ctx))
+            out["prefill_kv"] = (kc, vc)
+        else:
+            kc, vc = run.prefilled_ctx[b]
+        if req["window"]:
+            m = req["commit"][b]
+            X = req["window_hidden"][b, :m].float().cpu().numpy()
+            kw, vw = ref.write_rows_kv(cfg, W, X, ctx + np.arange(m))
+            out["window_kv"] = (kw, vw)
+            kc, vc = np.concatenate([kc, kw], axis=1), np.concatenate([vc, vw], axis=1)
+        p = req["anchor_pos"][b]
+        ka, va = ref.anchor_kv(cfg, W, st.Enp, [int(req["anchor_ids"][b])], [p])
+        out["anchor_kv"] = (ka, va)
+        ctxs.append((np.concatenate([kc, ka], axis=1), np.concatenate([vc, va], axis=1)))
+        ps.append(p)
+        seeds.append(int(req["seeds"][b]))
+        outs[b] = out
+    hidden = ref.draft_requests(cfg, W, C, ctxs, ps, seeds, noise_scale)
+    for i, b in enumerate(subset):
+        logits = ref.head_logits(C, hidden[i])
+        T = float(req["temperature"][b])
+        g = int(req["greedy"][b])
+        p = ps[i]
+        tok, _, margin = ref.sample_rows(logits, [T] * K, [g] * K, [seeds[i]] * K, p + 1 + np.arange(K),
+                                         req["step"], C.hot)
+        outs[b].update(hidden=hidden[i], logits=logits, tokens=tok, margin=margin)
+    return outs
+
+
+def oracle_request(st: ModelState, run: LibRun, b: int, noise_scale: float = 1.0) -> dict:
+    return oracle_batch(st, run, [b], noise_scale)[b]
+
+
+def slot_ids(req: dict, b: int, positions, P: int) -> np.ndarray:
+    r2p = req["req_to_page"].cpu().numpy()
+    row = int(req["req_pool_idx"][b])
+    return np.array([ref.slot_of(r2p, row, int(q), P) for q in positions], dtype=np.int64)
+
+
+def pool_rows(cfg: dict, pool6: torch.Tensor, slots) -> tuple:
+    """(L, n, heads, hd) keys and values stored at the given slots."""
+    P = cfg["page_size"]
+    s = torch.as_tensor(np.asarray(slots), device=pool6.device)
+    g = pool6.permute(2, 4, 0, 1, 3, 5)[s // P, s % P]  # (n, L, 2, nh, hd)
+    g = g.permute(1, 2, 0, 3, 4).float().cpu().numpy()
+    return g[:, 0], g[:, 1]
+
+
+def check_request(st: ModelState, run: LibRun, b: int, o: dict, tol: float, report: dict) -> None:
+    """Compares request b of a library run with the oracle's results ``o``; records the
+    worst errors in ``report`` and asserts the bars."""
+    cfg, req = st.cfg, run.req
+    K, P = cfg["block_size"], cfg["page_size"]
+    ctx, p = req["ctx"][b], req["anchor_pos"][b]
+
+    def bump(key, v):
+        report[key] = max(report.get(key, 0.0), v)
+
+    if "prefill_kv" in o:
+        want = slot_ids(req, b, np.arange(ctx), P)
+        got = run.prefill_loc[b].cpu().numpy()
+        assert np.array_equal(got, want), "prefill out_loc differs"
+        pick = np.unique(np.linspace(0, ctx - 1, min(ctx, 64)).astype(int))
+        k, v = pool_rows(cfg, run.pool6, want[pick])
+        e = max(max_rel(k, o["prefill_kv"][0][:, pick]), max_rel(v, o["prefill_kv"][1][:, pick]))
+        bump("write_kv", e)
+        assert e <= tol, f"prefill K/V max-rel {e}"
+    if "window_kv" in o:
+        m = req["commit"][b]
+        W = K + 1
+        got = run.window_loc.view(-1, W)[b].cpu().numpy()
+        want = np.full(W, -1, dtype=np.int64)
+        want[:m] = slot_ids(req, b, ctx + np.arange(m), P)
+        assert np.array_equal(got, want), "window out_loc differs"
+        k, v = pool_rows(cfg, run.pool6, want[:m])
+        e = max(max_rel(k, o["window_kv"][0]), max_rel(v, o["window_kv"][1]))
+        bump("write_kv", e)
+        assert e <= tol, f"window K/V max-rel {e}"
+    aslot = slot_ids(req, b, [p], P)
+    assert int(run.anchor_loc[b]) == int(aslot[0]), "anchor slot differs"
+    k, v = pool_rows(cfg, run.pool6, aslot)
+    e = max(max_rel(k, o["anchor_kv"][0]), max_rel(v, o["anchor_kv"][1]))
+    bump("anchor_kv", e)
+    assert e <= tol, f"anchor K/V max-rel {e}"
+    hid = run.hidden[b * K : (b + 1) * K].float().cpu().numpy()
+    e = max_rel(hid, o["hidden"])
+    bump("hidden", e)
+    assert e <= tol, f"draft hidden max-rel {e}"
+    lg = run.logits[b * K : (b + 1) * K].cpu().numpy()
+    e = max(max_rel(lg[r], o["logits"][r]) for r in range(K))
+    bump("logits", e)
+    assert e <= tol, f"logits max-rel {e}"
+    tok = run.tokens[b * K : (b + 1) * K].cpu().numpy()
+    sure = o["margin"] > TOKEN_MARGIN
+    report["tokens_checked"] = report.get("tokens_checked", 0) + int(sure.sum())
+    report["tokens_total"] = report.get("tokens_total", 0) + K
+    assert np.array_equal(tok[sure], o["tokens"][sure]), f"tokens differ: {tok} vs {o['tokens']}"

@@ -1,0 +1,177 @@
+"""Parity of the CUDA path with the oracle on the same seeded inputs (needs a GPU).
+
+Bars (element by element): page-table slots and Philox words bit-exact; keys/values,
+hidden states and logits within max-relative-error 2e-2 (bf16) / 1e-4 (float32),
+logits per row; token ids identical wherever the oracle's top-2 margin exceeds 1e-2.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import flashmap_ref as ref
+from speculative_decoding_block_context_gb300 import _lib as F
+from speculative_decoding_block_context_gb300 import synthetic as syn
+
+from .flashmap_harness import TOL, check_request, load_model, max_rel, oracle_batch, oracle_request, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built():
+    from speculative_decoding_block_context_gb300 import build
+
+    build.build()
+    F.lib()
+
+
+# ---------------------------------------------------------------------- kernels in isolation
+
+
+def test_philox_words_bit_exact():
+    g = torch.Generator().manual_seed(0)
+    n = 1 << 20
+    seeds = torch.randint(0, 2**63 - 1, (n,), generator=g, dtype=torch.int64)
+    ctr = torch.randint(0, 2**32, (n, 4), generator=g, dtype=torch.int64)
+    ctr[:4] = torch.tensor([[0, 0, 0, 0], [2**32 - 1] * 4, [1, 2, 3, 4], [5, 6, 7, 8]])
+    out = torch.empty((n, 4), dtype=torch.int32, device="cuda")
+    normals = torch.empty((n, 4), dtype=torch.float32, device="cuda")
+    F.flashmap_debug_philox(seeds.cuda(), ctr.to(torch.int32).cuda(), out, normals)
+    torch.cuda.synchronize()
+    s = seeds.numpy().astype(np.uint64)
+    keys = np.stack([s & np.uint64(0xFFFFFFFF), s >> np.uint64(32)], axis=1)
+    want = ref.philox4x32_10(ctr.numpy().astype(np.uint64), keys)
+    np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), want)
+    # the Box-Muller normals of the draft noise, within float32 evaluation error
+    w = want[:4096].astype(np.uint64)
+    n0, n1 = ref.box_muller(w[:, 0], w[:, 1])
+    n2, n3 = ref.box_muller(w[:, 2], w[:, 3])
+    np.testing.assert_allclose(normals[:4096].cpu().numpy(), np.stack([n0, n1, n2, n3], 1), rtol=2e-5, atol=2e-5)
+
+
+@pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 200, 300), (16, 4096, 4096), (37, 384, 1234),
+                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512)])
+def test_linear_bf16_tcgen05(rows, k, n):
+    g = torch.Generator(device="cuda").manual_seed(rows * 7 + k)
+    x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((n, k), generator=g, device="cuda") / k**0.5).to(torch.bfloat16)
+    out = torch.zeros((rows, n), dtype=torch.float32, device="cuda")
+    F.flashmap_debug_linear(F.BF16, x, w, out)
+    torch.cuda.synchronize()
+    want = x.double().cpu().numpy() @ w.double().cpu().numpy().T
+    assert max_rel(out.cpu().numpy(), want) < 1e-5
+
+
+def test_linear_f32_simt():
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn((7, 300), generator=g, device="cuda")
+    w = torch.randn((129, 300), generator=g, device="cuda")
+    out = torch.zeros((7, 129), dtype=torch.float32, device="cuda")
+    F.flashmap_debug_linear(F.F32, x, w, out)
+    torch.cuda.synchronize()
+    want = x.double().cpu().numpy() @ w.double().cpu().numpy().T
+    assert max_rel(out.cpu().numpy(), want) < 1e-6
+
+
+# ---------------------------------------------------------------------- whole step
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return load_model("tiny_fp32")
+
+
+@pytest.fixture(scope="module")
+def small():
+    return load_model("small_bf16")
+
+
+def _check_all(st, run, subset, tol):
+    report = {}
+    outs = oracle_batch(st, run, list(subset))
+    for b in subset:
+        check_request(st, run, b, outs[b], tol, report)
+    return report
+
+
+def _check_constants(st, tol):
+    H = st.cfg["target_hidden"]
+    chol = torch.empty((H, H), dtype=torch.float32, device="cuda")
+    u = torch.empty(H, dtype=torch.float32, device="cuda")
+    hot = torch.empty(st.consts.hot.shape[0], dtype=torch.int64, device="cuda")
+    F.flashmap_debug_constants(st.handle, chol, u, hot)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(hot.cpu().numpy(), st.consts.hot)
+    assert max_rel(u.cpu().numpy(), st.consts.uniform) < tol
+    assert max_rel(chol.cpu().numpy(), st.consts.chol) < tol
+
+
+def test_tiny_fp32_end_to_end(tiny):
+    _check_constants(tiny, 1e-5)
+    run = run_library("tiny_fp32", tiny)
+    assert run.dev_err == 0
+    rep = _check_all(tiny, run, range(run.req["bs"]), TOL["f32"])
+    assert rep["tokens_checked"] > 0
+
+
+def test_small_bf16_end_to_end(small):
+    _check_constants(small, 1e-2)
+    run = run_library("small_bf16", small)
+    assert run.dev_err == 0
+    _check_all(small, run, range(run.req["bs"]), TOL["bf16"])
+    # full-vocabulary logits: the draft logits at their token ids, -inf elsewhere (exact)
+    hot = torch.as_tensor(small.consts.hot, device="cuda")
+    mask = torch.ones(small.cfg["vocab_size"], dtype=torch.bool, device="cuda")
+    mask[hot] = False
+    assert torch.isneginf(run.full[:, mask]).all()
+    assert torch.equal(run.full[:, hot], run.logits)
+
+
+def test_noise_scale_zero_is_seed_independent(small):
+    req = syn.make_requests("small_bf16", "cuda")
+    a = run_library("small_bf16", small, noise_scale=0.0, req=req)
+    req2 = dict(req, seeds=req["seeds"] + 12345)
+    b = run_library("small_bf16", small, noise_scale=0.0, req=req2)
+    assert torch.equal(a.hidden, b.hidden)
+    o = oracle_request(small, a, 1, noise_scale=0.0)
+    K = small.cfg["block_size"]
+    assert max_rel(a.hidden[K : 2 * K].float().cpu().numpy(), o["hidden"]) <= TOL["bf16"]
+
+
+def test_out_of_range_page_sets_device_error(small):
+    """A page id outside the pool is skipped and reported, not dereferenced."""
+    req = syn.make_requests("small_bf16", "cuda")
+    row = int(req["req_pool_idx"][0])
+    req["req_to_page"][row, 0] = req["num_pages"] + 5
+    run = run_library("small_bf16", small, req=req)
+    assert run.dev_err & F.DEVERR["PAGE"]
+    assert int(run.prefill_loc[0][0]) == -1
+
+
+def test_graph_capture_replays_draft_and_sample(small):
+    """The per-step calls allocate nothing and never sync: they capture into a CUDA
+    graph whose replay reproduces the eager results."""
+    st = small
+    cfg = st.cfg
+    req = syn.make_requests("small_bf16", "cuda")
+    eager = run_library("small_bf16", st, req=req)
+    bs, K = req["bs"], cfg["block_size"]
+    pool = F.make_pool(eager.pool_t, req["num_pages"], F.BF16)
+    ws = torch.empty(F.flashmap_workspace_size(st.handle, bs, 64), dtype=torch.uint8, device="cuda")
+    anchor_pos = torch.tensor(req["anchor_pos"], dtype=torch.int32, device="cuda")
+    hidden = torch.empty_like(eager.hidden)
+    tokens = torch.empty_like(eager.tokens)
+    logits = torch.empty_like(eager.logits)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            F.flashmap_draft_block(st.handle, pool, bs, req["anchor_ids"], anchor_pos, req["req_pool_idx"],
+                                   req["req_to_page"], req["seeds"], 1.0, hidden, None, ws)
+            F.flashmap_sample_block(st.handle, bs, hidden, anchor_pos, req["temperature"], req["greedy"],
+                                    req["seeds"], req["step"], tokens, logits, None, ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(tokens, eager.tokens)
+    assert max_rel(hidden.float().cpu().numpy(), eager.hidden.float().cpu().numpy()) < 1e-3

@@ -1,0 +1,80 @@
+"""Parity at the full Qwen3-8B-shaped sizes (target_hidden 4096 x 3 layers, DiT 5 x 4096,
+32 x 128 heads, MLP 12288, vocabulary 151936, draft vocabulary 32768), in the launch
+configuration the benchmark times. Requests are independent, so the oracle checks a
+fixed subset exactly: the shortest and longest contexts and six seeded others."""
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_block_context_gb300 import _lib as F
+
+from .flashmap_harness import TOL, check_request, load_model, max_rel, oracle_batch, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qwen():
+    from speculative_decoding_block_context_gb300 import build
+
+    build.build()
+    return load_model("qwen3_8b_bs1")
+
+
+def subset_of(req, n_random=6, seed=0):
+    ctx = np.asarray(req["ctx"])
+    picks = {int(np.argmin(ctx)), int(np.argmax(ctx))}
+    rng = np.random.default_rng(seed)
+    for b in rng.permutation(len(ctx)):
+        if len(picks) >= 2 + n_random:
+            break
+        picks.add(int(b))
+    return sorted(picks)
+
+
+def _run_and_check(qwen, workload):
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    req = syn.make_requests(workload, "cuda")
+    subset = list(range(req["bs"])) if req["bs"] == 1 else subset_of(req)
+    run = run_library(workload, qwen, req=req, check_subset=subset)
+    assert run.dev_err == 0
+    report = {}
+    outs = oracle_batch(qwen, run, subset)
+    for b in subset:
+        check_request(qwen, run, b, outs[b], TOL["bf16"], report)
+    print(workload, report)
+    assert report["tokens_checked"] >= report["tokens_total"] // 2
+    return run, report
+
+
+def test_qwen3_constants(qwen):
+    H = qwen.cfg["target_hidden"]
+    chol = torch.empty((H, H), dtype=torch.float32, device="cuda")
+    u = torch.empty(H, dtype=torch.float32, device="cuda")
+    hot = torch.empty(qwen.consts.hot.shape[0], dtype=torch.int64, device="cuda")
+    F.flashmap_debug_constants(qwen.handle, chol, u, hot)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(hot.cpu().numpy(), qwen.consts.hot)
+    assert max_rel(u.cpu().numpy(), qwen.consts.uniform) < 1e-4
+    assert max_rel(chol.cpu().numpy(), qwen.consts.chol) < 1e-2  # L is stored in bf16
+
+
+def test_qwen3_bs1_prefill_window_draft_sample(qwen):
+    _run_and_check(qwen, "qwen3_8b_bs1")
+
+
+def test_qwen3_bs32_ragged_contexts(qwen):
+    _run_and_check(qwen, "qwen3_8b_bs32")
+
+
+def test_qwen3_bs128_window_and_full_vocab_scatter(qwen):
+    run, _ = _run_and_check(qwen, "qwen3_8b_bs128")
+    hot = torch.as_tensor(qwen.consts.hot, device="cuda")
+    mask = torch.ones(qwen.cfg["vocab_size"], dtype=torch.bool, device="cuda")
+    mask[hot] = False
+    for r0 in range(0, run.full.shape[0], 256):
+        blk = run.full[r0 : r0 + 256]
+        assert torch.isneginf(blk[:, mask]).all()
+        assert torch.equal(blk[:, hot], run.logits[r0 : r0 + 256])
