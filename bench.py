@@ -248,7 +248,8 @@ def our_arm(args, rank: int, world: int) -> dict:
     # the step, the sampled token ids copied out, every step
     host_in = {k: req[k].cpu().pin_memory() for k in ("anchor_ids", "seeds", "temperature", "greedy")}
     host_in["anchor_pos"] = st["anchor_pos"].cpu().pin_memory()
-    dev_in = {k: (req[k] if k in req else st[k]) for k in host_in}
+    dev_in = {k: req[k] for k in ("anchor_ids", "seeds", "temperature", "greedy")}
+    dev_in["anchor_pos"] = st["anchor_pos"]
     if req["window"]:
         host_in["window_hidden"] = req["window_hidden"].cpu().pin_memory()
         dev_in["window_hidden"] = req["window_hidden"]
