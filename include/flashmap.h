@@ -239,6 +239,8 @@ flashmap_status flashmap_draft_block(flashmap_model* model, const flashmap_kv_po
  *   draft_logits_out (device) float32 [bs * K][Vd], or NULL
  *   full_logits_out  (device) float32 [bs * K][V]: the draft logits at their token ids,
  *                    -inf elsewhere (flashmap/sglang/sampler.py, _FullLogits), or NULL
+ *   workspace    (device) per-row merge slots of the split sampler, plus the logits
+ *                when draft_logits_out is NULL (flashmap_workspace_size covers both)
  */
 flashmap_status flashmap_sample_block(flashmap_model* model, int32_t bs, const void* hidden,
                                       const int32_t* anchor_pos, const float* temperature,

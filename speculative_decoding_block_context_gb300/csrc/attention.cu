@@ -34,6 +34,8 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   float* sq = sm;                  // [K][HD + 1]
   float* sk = sq + K * (HD + 1);   // [K][HD + 1]
   float* sv = sk + K * (HD + 1);   // [K][HD]
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D = nh * HD;
@@ -46,38 +48,16 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   }
   const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
   float* base = qkv + static_cast<int64_t>(row) * 3 * D + h * HD;
-  float v[EPL];
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
     float* src = base + part * D;
+    float v[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       v[e] = src[lane * EPL + e];
       src[lane * EPL + e] = 0.f;
     }
-    if (part < 2) {  // q or k: RMSNorm then rotation (the pair partner may be another lane)
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) ss = fmaf(v[e], v[e], ss);
-      ss = warp_sum(ss);
-      const float r = rsqrtf(ss * (1.f / HD) + eps);
-      const float* w = part == 0 ? qn : kn;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) v[e] *= r * w[lane * EPL + e];
-      if constexpr (EPL >= 2) {
-#pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-          const float2 cs = rope[(lane * EPL + e) >> 1];
-          const float x1 = v[e], x2 = v[e + 1];
-          v[e] = x1 * cs.x - x2 * cs.y;
-          v[e + 1] = x2 * cs.x + x1 * cs.y;
-        }
-      } else {
-        const float other = __shfl_xor_sync(0xffffffffu, v[0], 1);
-        const float2 cs = rope[lane >> 1];
-        v[0] = (lane & 1) ? (v[0] * cs.x + other * cs.y) : (v[0] * cs.x - other * cs.y);
-      }
-    }
+    if (part < 2) head_norm_rope<EPL>(v, part == 0 ? qn : kn, eps, rope, lane);
     float* dst = part == 0 ? sq + k * (HD + 1) : part == 1 ? sk + k * (HD + 1) : sv + k * HD;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = v[e];
@@ -114,6 +94,8 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
                                                           unsigned* dev_err) {
   __shared__ float red[32];
   __shared__ int carry;
+  pdl_trigger();
+  pdl_wait();
   float t16 = 0.f;
   for (int b = threadIdx.x; b < bs; b += blockDim.x) t16 += static_cast<float>((max(anchor_pos[b] + 1, 1) + 15) / 16);
   const float total16 = block_sum(t16, red);
@@ -167,17 +149,51 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
   }
 }
 
+// ------------------------------------------------------------------ cross-attention queries
+
+// The layer's cross-attention queries of request b, head h, in float32 sq[16][HD]
+// (rows >= K zero): q = RoPE(RMSNorm_{q_norm}(W_q n)) at the slot positions
+// p + 1 + k (flashmap/modeling_flashmap.py, FlashMapAttention.forward). Every item of a
+// (request, head) derives them from the projection accumulator; 128 threads.
+template <int HD>
+__device__ __forceinline__ void load_queries(const XattnArgs& a, int b, int h, float* sq) {
+  constexpr int EPL = HD / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int D = a.nh * HD;
+  for (int q = warp; q < 16; q += 4) {
+    float v[EPL];
+    if (q < a.K) {  // warp-uniform
+      const float* src = a.qacc + static_cast<int64_t>(b * a.K + q) * D + h * HD;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[e] = src[lane * EPL + e];
+      int pos = a.anchor_pos[b] + 1 + q;
+      if (pos < 0 || pos >= a.max_pos) {
+        if (lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
+        pos = 0;
+      }
+      head_norm_rope<EPL>(v, a.q_norm, a.eps, a.rope + static_cast<int64_t>(pos) * (HD / 2), lane);
+    } else {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) sq[q * HD + lane * EPL + e] = v[e];
+  }
+}
+
 // ------------------------------------------------------------------ paged cross-attention items (SIMT)
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sq[16][HD];
   __shared__ float sk[16][HD + 1];
   __shared__ float sv[16][HD];
   __shared__ float ss[16][17];
   __shared__ float sm[16], sl[16], scorr[16];
   const int tid = threadIdx.x;
-  const int K = a.K, nh = a.nh, D = nh * HD;
+  const int nh = a.nh;
   const int items = a.plan[0], chunk_len = a.plan[1];
   const int* pairs = a.plan + 4 + a.bs;
   const T* pool = static_cast<const T*>(a.pool);
@@ -187,12 +203,8 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
     const int n = a.anchor_pos[b] + 1;
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
     const int rrow = a.req_pool_idx ? a.req_pool_idx[b] : b;
-    const T* qb = static_cast<const T*>(a.q) + static_cast<int64_t>(b) * K * D + h * HD;
     __syncthreads();
-    for (int i = tid; i < 16 * HD; i += blockDim.x) {
-      const int qi = i / HD, d = i - qi * HD;
-      sq[qi][d] = qi < K ? to_f32(qb[static_cast<int64_t>(qi) * D + d]) * a.scale_log2 : 0.f;
-    }
+    load_queries<HD>(a, b, h, &sq[0][0]);
     if (tid < 16) {
       sm[tid] = -INFINITY;
       sl[tid] = 0.f;
@@ -222,7 +234,7 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
         float acc = 0.f;
 #pragma unroll 8
         for (int d = 0; d < HD; ++d) acc = fmaf(sq[qi][d], sk[j][d], acc);
-        ss[qi][j] = (blk + j < p1 && ok) ? acc : -INFINITY;
+        ss[qi][j] = (blk + j < p1 && ok) ? acc * a.scale_log2 : -INFINITY;
       }
       __syncthreads();
       if (tid < 16) {
@@ -264,15 +276,256 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ paged cross-attention items (tensor cores)
+//
+// bf16 path. The 16 queries of a (request, head) are exactly the M = 16 of
+// mma.sync.m16n8k16, so S = Q K^T and O += P V run on the tensor cores without
+// padding (tcgen05's smallest tile would waste 3/4 of its rows here). Each warp
+// streams its own 16-position blocks of K and V (4 KB each at hd 128: one page
+// slice) through a 3-deep cp.async ring in XOR-swizzled shared memory (16-byte
+// chunk c of row r stored at c ^ (r & 7): conflict-free ldmatrix), keeps the running
+// max / sum / O of its blocks in registers (base-2 exponents), and the CTA merges its
+// four warps before writing the item's partial.
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+constexpr int kXStages = 3;
+
+template <int HD>
+struct XCfg {
+  static constexpr int ROWB = HD * 2;     // bytes of one position row
+  static constexpr int BLK = 16 * ROWB;   // one 16-position block of K (or V)
+  static constexpr int CH = HD / 8;       // 16-byte chunks per row
+  static constexpr int RING = kXStages * 2 * BLK;  // per warp
+  static constexpr int SMEM_RING = 4 * RING;
+  static constexpr int SMEM_MERGE = 4 * 16 * (HD + 2) * 4;
+  static constexpr int SMEM = SMEM_RING > SMEM_MERGE ? SMEM_RING : SMEM_MERGE;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
+  using C = XCfg<HD>;
+  extern __shared__ __align__(128) uint8_t xsm[];
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int nh = a.nh;
+  const int items = a.plan[0], chunk_len = a.plan[1];
+  const int* pairs = a.plan + 4 + a.bs;
+  const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(a.pool);
+  const uint32_t ring = smem_u32(xsm) + warp * C::RING;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int g = item / nh, h = item - g * nh;
+    const int b = pairs[2 * g], c = pairs[2 * g + 1];
+    const int n = a.anchor_pos[b] + 1;
+    const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
+    const int nblk = (p1 - p0 + 15) >> 4;
+    const int rrow = a.req_pool_idx ? a.req_pool_idx[b] : b;
+    // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
+    float* sq = reinterpret_cast<float*>(xsm);  // aliases the ring until the first loads
+    load_queries<HD>(a, b, h, sq);
+    __syncthreads();
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = g8 + ((j & 1) << 3);
+        const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
+        qa[kk][j] = pack_bf16(sq[row * HD + col], sq[row * HD + col + 1]);
+      }
+    }
+    __syncthreads();
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const int nj = warp < nblk ? (nblk - warp + 3) >> 2 : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const int blk = p0 + ((warp + 4 * j) << 4);
+        const int pi = blk / a.P;
+        const int page = pi < a.r2p_stride ? a.req_to_page[static_cast<int64_t>(rrow) * a.r2p_stride + pi] : -1;
+        const bool ok = page >= 0 && page < a.num_pages;
+        if (!ok && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
+        const int off = blk - pi * a.P;
+        const int64_t kb = ((((static_cast<int64_t>(a.layer) * 2 + 0) * a.num_pages + (ok ? page : 0)) * nh + h) * a.P + off) * HD;
+        const int64_t vb = kb + static_cast<int64_t>(a.num_pages) * nh * a.P * HD;
+        const uint32_t st = ring + (j % kXStages) * 2 * C::BLK;
+#pragma unroll
+        for (int i = lane; i < 16 * C::CH; i += 32) {
+          const int r = i / C::CH, ch = i - r * C::CH;
+          const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
+          const uint32_t dst = st + r * C::ROWB + ((ch ^ (r & 7)) << 4);
+          cp_async16(dst, pool + kb + r * HD + ch * 8, bytes);
+          cp_async16(dst + C::BLK, pool + vb + r * HD + ch * 8, bytes);
+        }
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kXStages - 1; ++j) issue(j);
+    for (int j = 0; j < nj; ++j) {
+      issue(j + kXStages - 1);
+      cp_async_wait<kXStages - 1>();
+      __syncwarp();
+      const int blk = p0 + ((warp + 4 * j) << 4);
+      const uint32_t kst = ring + (j % kXStages) * 2 * C::BLK, vst = kst + C::BLK;
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const int r = (lane & 7) + ((lane >> 4) << 3);
+        const int ch = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qa[kk], b0, b1);
+        mma_bf16_16816(s[1], qa[kk], b2, b3);
+      }
+      // scale to base 2 and mask positions past the chunk
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
+          s[nt][e] = pos < p1 ? s[nt][e] * a.scale_log2 : -INFINITY;
+        }
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+      const float c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = n0 == -INFINITY ? 0.f : exp2f(s[nt][0] - n0);
+        p[nt][1] = n0 == -INFINITY ? 0.f : exp2f(s[nt][1] - n0);
+        p[nt][2] = n1 == -INFINITY ? 0.f : exp2f(s[nt][2] - n1);
+        p[nt][3] = n1 == -INFINITY ? 0.f : exp2f(s[nt][3] - n1);
+      }
+      l0 = l0 * c0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
+      l1 = l1 * c1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
+      m0 = n0;
+      m1 = n1;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        o[i][0] *= c0;
+        o[i][1] *= c0;
+        o[i][2] *= c1;
+        o[i][3] *= c1;
+      }
+      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]), pack_bf16(p[1][0], p[1][1]),
+                              pack_bf16(p[1][2], p[1][3])};
+#pragma unroll
+      for (int dn = 0; dn < HD / 16; ++dn) {
+        const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int ch = dn * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dn], pa, b0, b1);
+        mma_bf16_16816(o[2 * dn + 1], pa, b2, b3);
+      }
+      __syncwarp();
+    }
+    cp_async_wait<0>();
+    // row sums over the quad
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();  // every warp is done with its ring: reuse it for the merge
+    float* mm = reinterpret_cast<float*>(xsm);        // [4][16] max
+    float* ll = mm + 64;                               // [4][16] sum
+    float* oo = ll + 64;                               // [4][16][HD]
+    if (t4 == 0) {
+      mm[warp * 16 + g8] = m0;
+      mm[warp * 16 + g8 + 8] = m1;
+      ll[warp * 16 + g8] = l0;
+      ll[warp * 16 + g8 + 8] = l1;
+    }
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) {
+      float* r0 = oo + (warp * 16 + g8) * HD + i * 8 + 2 * t4;
+      float* r1 = oo + (warp * 16 + g8 + 8) * HD + i * 8 + 2 * t4;
+      r0[0] = o[i][0];
+      r0[1] = o[i][1];
+      r1[0] = o[i][2];
+      r1[1] = o[i][3];
+    }
+    __syncthreads();
+    const int64_t pidx = static_cast<int64_t>(g) * nh + h;
+    {
+      const int q = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * (HD / 8);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 16 + q]);
+      float wgt[4], L = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = mm[w * 16 + q];
+        wgt[w] = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L = fmaf(wgt[w], ll[w * 16 + q], L);
+      }
+      float* po = a.part_o + pidx * 16 * HD + q * HD;
+      for (int d = d0; d < d0 + HD / 8; ++d) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc = fmaf(wgt[w], oo[(w * 16 + q) * HD + d], acc);
+        po[d] = acc;
+      }
+      if ((threadIdx.x & 7) == 0) {
+        a.part_ml[pidx * 32 + 2 * q] = M;
+        a.part_ml[pidx * 32 + 2 * q + 1] = L;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // ------------------------------------------------------------------ combine
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(HD) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
   const int* first = a.plan + 3;
   const int g0 = first[b], g1 = first[b + 1];
-  for (int qi = 0; qi < a.K; ++qi) {
+  {
+    const int qi = blockIdx.z;
     float M = -INFINITY;
     for (int g = g0; g < g1; ++g) M = fmaxf(M, a.part_ml[(static_cast<int64_t>(g) * nh + h) * 32 + 2 * qi]);
     float L = 0.f, acc = 0.f;
@@ -285,6 +538,7 @@ __global__ void __launch_bounds__(HD) xattn_combine_kernel(XattnArgs a, T* __res
       acc = fmaf(a.part_o[pidx * 16 * HD + qi * HD + d], w, acc);
     }
     out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
+    a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
   }
 }
 
@@ -321,17 +575,19 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
   if (bs <= 0) return cudaSuccess;
   dim3 grid(bs, nh);
   const size_t smem = static_cast<size_t>(K) * ((hd + 1) * 2 + hd) * sizeof(float);
+  cudaError_t e = cudaSuccess;
+  const dim3 block(32 * K);
   if (hd == 32) {
-    FM_DISPATCH_T2(dtype, (self_attn_kernel<T, 1><<<grid, 32 * K, smem, L.stream>>>(
-                              qkv, K, nh, qn, kn, eps, rope, max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 1>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
+                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
   } else if (hd == 64) {
-    FM_DISPATCH_T2(dtype, (self_attn_kernel<T, 2><<<grid, 32 * K, smem, L.stream>>>(
-                              qkv, K, nh, qn, kn, eps, rope, max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 2>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
+                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
   } else {
-    FM_DISPATCH_T2(dtype, (self_attn_kernel<T, 4><<<grid, 32 * K, smem, L.stream>>>(
-                              qkv, K, nh, qn, kn, eps, rope, max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 4>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
+                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
   }
-  return cudaGetLastError();
+  return e;
 }
 
 int xattn_target_items(int num_sms) { return num_sms * 8; }
@@ -339,26 +595,40 @@ int xattn_max_chunks(int num_sms, int nh, int bs) { return xattn_target_items(nu
 size_t xattn_plan_ints(int num_sms, int nh, int bs) { return 4 + bs + 2 * static_cast<size_t>(xattn_max_chunks(num_sms, nh, bs)); }
 
 cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan) {
-  xattn_plan_kernel<<<1, 1024, 0, L.stream>>>(anchor_pos, bs, nh, xattn_target_items(L.num_sms),
-                                              xattn_max_chunks(L.num_sms, nh, bs), plan, L.dev_err);
-  return cudaGetLastError();
+  return launch_k(L, xattn_plan_kernel, dim3(1), dim3(1024), 0, anchor_pos, bs, nh, xattn_target_items(L.num_sms),
+                  xattn_max_chunks(L.num_sms, nh, bs), plan, L.dev_err);
 }
 
 cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args) {
   XattnArgs a = args;
   a.dev_err = L.dev_err;
-  const int grid = L.num_sms * 4;
-  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (xattn_items_simt_kernel<T, HD><<<grid, 128, 0, L.stream>>>(a))));
-  return cudaGetLastError();
+  const int grid = L.num_sms * 2;
+  cudaError_t e = cudaSuccess;
+  if (dtype == FLASHMAP_BF16) {
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD>, dim3(grid), dim3(128), XCfg<HD>::SMEM, a)));
+  } else {
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_simt_kernel<float, HD>, dim3(grid), dim3(128), 0, a)));
+  }
+  return e;
+}
+
+cudaError_t xattn_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(xattn_items_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       XCfg<128>::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(xattn_items_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<64>::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(xattn_items_mma_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<32>::SMEM);
 }
 
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& args, void* out) {
   XattnArgs a = args;
   a.dev_err = L.dev_err;
-  dim3 cgrid(a.bs, a.nh);
-  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (xattn_combine_kernel<T, HD><<<cgrid, HD, 0, L.stream>>>(
-                                                 a, static_cast<T*>(out)))));
-  return cudaGetLastError();
+  dim3 cgrid(a.bs, a.nh, a.K);
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_kernel<T, HD>, cgrid, dim3(HD), 0, a,
+                                                           static_cast<T*>(out)))));
+  return e;
 }
 
 }  // namespace fm

@@ -47,6 +47,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Every pipeline wait gives up after this long and reports FLASHMAP_DEVERR_TIMEOUT.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of a call is launched with programmatic stream serialization: it lets
+// its dependents launch at once (their prologue, and a GEMM's weight prefetch,
+// overlap its tail) and waits for its predecessors' completion before touching data
+// they produce. Without a programmatic predecessor both are no-ops.
+
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -70,6 +79,37 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   float t = lane < nw ? red[lane] : 0.f;
   t = warp_sum(t);
   return t;
+}
+
+// RMSNorm of one head vector held EPL-per-lane by a warp (lane owns channels
+// lane*EPL .. lane*EPL+EPL-1), then the interleaved-pair rotation of the pairs
+// (2i, 2i+1) by angle row `rope` (cos, sin per pair), if given
+// (flashmap/modeling_flashmap.py, FlashMapRMSNorm and apply_rope).
+template <int EPL>
+__device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __restrict__ w, float eps,
+                                               const float2* __restrict__ rope, int lane) {
+  constexpr int HD = EPL * 32;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(v[e], v[e], ss);
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss * (1.f / HD) + eps);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) v[e] *= r * w[lane * EPL + e];
+  if (rope == nullptr) return;
+  if constexpr (EPL >= 2) {
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) {
+      const float2 cs = rope[(lane * EPL + e) >> 1];
+      const float x1 = v[e], x2 = v[e + 1];
+      v[e] = x1 * cs.x - x2 * cs.y;
+      v[e + 1] = x2 * cs.x + x1 * cs.y;
+    }
+  } else {
+    const float other = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    const float2 cs = rope[lane >> 1];
+    v[0] = (lane & 1) ? (v[0] * cs.x + other * cs.y) : (v[0] * cs.x - other * cs.y);
+  }
 }
 
 // ------------------------------------------------------------------ shared memory / mbarrier

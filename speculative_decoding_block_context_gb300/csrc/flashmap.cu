@@ -182,7 +182,7 @@ std::vector<float2> rope_table(int maxpos, int hd, double theta) {
 
 struct DraftWs {
   float *x, *acc_big, *acc_d, *acc_a, *acc_kv;
-  void *act, *act2, *e_rows, *a_rows;
+  void *act, *e_rows, *a_rows;
   int* plan;
   float *part_o, *part_ml;
   size_t bytes;
@@ -200,7 +200,6 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   w.acc_a = c.take<float>(static_cast<size_t>(bs) * m->D * 4);
   w.acc_kv = c.take<float>(static_cast<size_t>(bs) * 2 * m->L * m->D * 4);
   w.act = c.take<void>(R * wide * es);
-  w.act2 = c.take<void>(R * m->D * es);
   w.e_rows = c.take<void>(static_cast<size_t>(bs) * m->H * es);
   w.a_rows = c.take<void>(static_cast<size_t>(bs) * m->D * es);
   w.plan = c.take<int>(fm::xattn_plan_ints(m->num_sms, m->nh, bs) * 4);
@@ -229,8 +228,23 @@ WriteWs carve_write(const flashmap_model* m, int rows, void* base, size_t* bytes
   return w;
 }
 
-size_t sample_bytes(const flashmap_model* m, int bs) {
-  return align_up(static_cast<size_t>(bs) * m->K * m->Vd * 4);
+// sample workspace: the row keys and counters of the split sampler, then the draft
+// logits unless the caller takes them
+struct SampleWs {
+  unsigned long long* keys;
+  unsigned* counters;
+  float* logits;
+  size_t bytes;
+};
+SampleWs carve_sample(const flashmap_model* m, int bs, bool own_logits, void* base) {
+  Carver c(base);
+  const size_t R = static_cast<size_t>(bs) * m->K;
+  SampleWs w;
+  w.keys = c.take<unsigned long long>(R * 8);
+  w.counters = c.take<unsigned>(R * 4);
+  w.logits = own_logits ? c.take<float>(R * m->Vd * 4) : nullptr;
+  w.bytes = align_up(c.off);
+  return w;
 }
 
 flashmap_status check_weight_map(Weight& w, int dtype, std::string* err) {
@@ -401,6 +415,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   } while (0)
 
   LCHK(fm::gemm_prepare());
+  LCHK(fm::xattn_prepare());
   LCHK(cudaMemsetAsync(m->dev_err, 0, 4, s));
   auto copy = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto bytes_of = [&](int64_t rows, int64_t cols) { return static_cast<size_t>(rows) * cols * es; };
@@ -543,7 +558,7 @@ flashmap_status flashmap_workspace_size(const flashmap_model* m, int32_t max_bs,
   if (!m || !bytes || max_bs <= 0 || max_write_rows < 0) return fail(FLASHMAP_E_INVALID, "bad workspace query");
   size_t wb = 0;
   carve_write(m, std::max(max_write_rows, 1), nullptr, &wb);
-  *bytes = std::max({carve_draft(m, max_bs, nullptr).bytes, sample_bytes(m, max_bs), wb});
+  *bytes = std::max({carve_draft(m, max_bs, nullptr).bytes, carve_sample(m, max_bs, true, nullptr).bytes, wb});
   return FLASHMAP_OK;
 }
 
@@ -578,8 +593,10 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     const int rows = static_cast<int>(std::min<int64_t>(chunk, total - r0));
     size_t b = 0;
     WriteWs ws = carve_write(m, rows, workspace, &b);
-    TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_fc, 0, static_cast<size_t>(rows) * m->D * 4, s));
-    TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_kv, 0, static_cast<size_t>(rows) * 2 * m->L * m->D * 4, s));
+    fm::ZeroList z;
+    z.add(ws.acc_fc, static_cast<int64_t>(rows) * m->D);
+    z.add(ws.acc_kv, static_cast<int64_t>(rows) * 2 * m->L * m->D);
+    TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
     const void* x = static_cast<const uint8_t*>(target_hidden) + r0 * xrow;
     // ctx = RMSNorm_hidden(fc(x)); kv = W_ctx ctx
     TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr));
@@ -634,11 +651,15 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   const DraftWs ws = carve_draft(m, bs, workspace);
   const int R = bs * m->K, D = m->D, H = m->H, adt = m->adt;
   const size_t big = std::max({3 * static_cast<size_t>(D), static_cast<size_t>(m->F), static_cast<size_t>(H)});
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.x, 0, static_cast<size_t>(R) * D * 4, s));
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_big, 0, static_cast<size_t>(R) * big * 4, s));
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_d, 0, static_cast<size_t>(R) * D * 4, s));
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_a, 0, static_cast<size_t>(bs) * D * 4, s));
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(ws.acc_kv, 0, static_cast<size_t>(bs) * 2 * m->L * D * 4, s));
+  {
+    fm::ZeroList z;
+    z.add(ws.x, static_cast<int64_t>(R) * D);
+    z.add(ws.acc_big, static_cast<int64_t>(R) * static_cast<int64_t>(big));
+    z.add(ws.acc_d, static_cast<int64_t>(R) * D);
+    z.add(ws.acc_a, static_cast<int64_t>(bs) * D);
+    z.add(ws.acc_kv, static_cast<int64_t>(bs) * 2 * m->L * D);
+    TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
+  }
   // split-KV plan of the cross-attention, shared by every layer
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, anchor_pos, bs, m->nh, ws.plan));
   // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
@@ -694,7 +715,10 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   xa.part_o = ws.part_o;
   xa.part_ml = ws.part_ml;
   xa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(m->hd)));
-  xa.q = ws.act2;
+  xa.qacc = ws.acc_d;
+  xa.eps = eps_qk;
+  xa.rope = m->rope;
+  xa.max_pos = m->maxpos;
   for (int l = 0; l < m->L; ++l) {
     const LayerW& lw = m->layers[l];
     const float* md = lw.mods;
@@ -705,9 +729,8 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
     TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr));
-    TIMED(FLASHMAP_KIND_ROWS, l, fm::qnorm_rope(Lh, adt, ws.acc_d, R, m->K, m->nh, m->hd, lw.cqn, eps_qk, m->rope, m->maxpos, anchor_pos,
-                           ws.act2));
     xa.layer = l;
+    xa.q_norm = lw.cqn;
     TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, adt, xa));
     TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
     TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr));
@@ -732,19 +755,25 @@ flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void*
   if (bs <= 0) return fail(FLASHMAP_E_INVALID, "bs must be positive");
   if (m->adt == FLASHMAP_BF16 && (reinterpret_cast<uintptr_t>(hidden) & 15))
     return fail(FLASHMAP_E_INVALID, "hidden must be 16-byte aligned");
-  float* logits = draft_logits_out;
-  if (!logits) {
-    if (!workspace || workspace_bytes < sample_bytes(m, bs))
-      return fail(FLASHMAP_E_INVALID, "workspace too small for the draft logits");
-    logits = static_cast<float*>(workspace);
-  }
+  const SampleWs need = carve_sample(m, bs, draft_logits_out == nullptr, nullptr);
+  if (!workspace || workspace_bytes < need.bytes)
+    return fail(FLASHMAP_E_INVALID, "workspace too small: need " + std::to_string(need.bytes) + " bytes");
+  const SampleWs ws = carve_sample(m, bs, draft_logits_out == nullptr, workspace);
+  float* logits = draft_logits_out ? draft_logits_out : ws.logits;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Launch Lh = m->launch(s);
   const int R = bs * m->K;
-  TIMED(FLASHMAP_KIND_MEMSET, -1, cudaMemsetAsync(logits, 0, static_cast<size_t>(R) * m->Vd * 4, s));
+  {
+    fm::ZeroList z;
+    z.add(logits, static_cast<int64_t>(R) * m->Vd);
+    z.add(reinterpret_cast<float*>(ws.keys), 2LL * R);
+    z.add(reinterpret_cast<float*>(ws.counters), R);
+    TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
+  }
   TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b));
   TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::sample_rows(Lh, logits, R, m->Vd, m->K, temperature, greedy, seeds, anchor_pos,
-                                                   static_cast<uint32_t>(step), m->hot, tokens_out));
+                                                   static_cast<uint32_t>(step), m->hot, tokens_out, ws.keys,
+                                                   ws.counters));
   if (full_logits_out)
     TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::full_scatter(Lh, logits, R, m->Vd, m->inv_hot, m->V, full_logits_out));
   return FLASHMAP_OK;
@@ -814,7 +843,7 @@ flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* 
   W.K = in_features;
   std::string err;
   if (check_weight_map(W, dtype, &err) != FLASHMAP_OK) return fail(FLASHMAP_E_CUDA, err);
-  Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr};
+  Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr, true};
   FM_CUDA(fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr));
   return FLASHMAP_OK;
 }

@@ -27,15 +27,24 @@ namespace {
 
 constexpr int kTcThreads = 192;
 
+// Pipeline depth of the narrow (<= 32 activation rows) GEMMs, and CTAs launched per SM.
+#ifndef FM_TC_STAGES_NARROW
+#define FM_TC_STAGES_NARROW 5
+#endif
+#ifndef FM_TC_CTAS_PER_SM
+#define FM_TC_CTAS_PER_SM 2
+#endif
+
 template <int BN>
 struct TcCfg {
-  static constexpr int STAGES = BN <= 32 ? 5 : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  static constexpr int STAGES = BN <= 32 ? FM_TC_STAGES_NARROW : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
   static constexpr int A_BYTES = 128 * 64 * 2;
   static constexpr int B_BYTES = BN * 64 * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int PER_SM = 2 * (SMEM + 1024) <= 227 * 1024 ? 2 : 1;
+  static constexpr int FIT = (228 * 1024) / (SMEM + 1024);
+  static constexpr int PER_SM = FIT < FM_TC_CTAS_PER_SM ? (FIT < 1 ? 1 : FIT) : FM_TC_CTAS_PER_SM;
 };
 
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
@@ -91,12 +100,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
+  pdl_trigger();
   if (warp == 0) {
     if (lane == 0) {  // TMA producer
       const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int64_t it = it0; it < it1; ++it) {
+      // The weights depend on no earlier kernel: the first stages' weight tiles are
+      // requested before waiting for the kernel that produced the activations.
+      const int pre = static_cast<int>(min(static_cast<int64_t>(C::STAGES), it1 - it0));
+      for (int i = 0; i < pre; ++i) {
+        const int64_t tile = (it0 + i) / KB;
+        const int kb = static_cast<int>(it0 + i - tile * KB);
+        const int m = static_cast<int>(tile / rt);
+        mbar_arrive_expect_tx(&full_bar[i], C::STAGE_BYTES);
+        tma_load_2d(smem + i * C::STAGE_BYTES, &mapW, &full_bar[i], kb * 64, m * 128, pol_w);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        const int64_t tile = (it0 + i) / KB;
+        const int kb = static_cast<int>(it0 + i - tile * KB);
+        const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+        tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &mapX, &full_bar[i], kb * 64, r * BN, pol_x);
+      }
+      issued = pre;
+      int stage = pre % C::STAGES;
+      uint32_t phase = pre == C::STAGES ? 1u : 0u;
+      for (int64_t it = it0 + pre; it < it1; ++it) {
         const int64_t tile = it / KB;
         const int kb = static_cast<int>(it - tile * KB);
         const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
@@ -157,6 +185,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mbar_wait_timed(&drain_bar, 0)) abort_flag = 1;
     }
   } else {  // epilogue: warps 2..5, TMEM lane quadrant warp % 4
+    pdl_wait();
     const int q = warp & 3;
     int seg = 0;
     int64_t it = it0;
@@ -229,6 +258,8 @@ __global__ void __launch_bounds__(256) linear_warp_kernel(const T* __restrict__ 
                                                           const float* __restrict__ alpha,
                                                           const float* __restrict__ beta) {
   constexpr int RB = 4;
+  pdl_trigger();
+  pdl_wait();
   const int n = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (n >= N) return;
@@ -364,9 +395,8 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   const int64_t mt = (W.N + 127) / 128, rt = (R + BN - 1) / BN, KB = (W.K + 63) / 64;
   const int64_t T = mt * rt * KB;
   const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * C::PER_SM));
-  tc_linear_kernel<BN><<<G, kTcThreads, C::SMEM, L.stream>>>(W.map, mapX, out, ldo, R, W.N, W.K, alpha, beta,
-                                                             L.dev_err);
-  return cudaGetLastError();
+  return launch_k(L, tc_linear_kernel<BN>, dim3(G), dim3(kTcThreads), C::SMEM, W.map, mapX, out, ldo, R, W.N, W.K,
+                  alpha, beta, L.dev_err);
 }
 
 template <int BN>
@@ -424,10 +454,8 @@ cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, in
   if (W.dtype == FLASHMAP_F32) {
     const int64_t threads = static_cast<int64_t>(W.N) * 32;
     const int blocks = static_cast<int>((threads + 255) / 256);
-    linear_warp_kernel<float><<<blocks, 256, 0, L.stream>>>(static_cast<const float*>(x), rows, ldx,
-                                                            static_cast<const float*>(W.ptr), W.N, W.K, out, ldo,
-                                                            alpha, beta);
-    return cudaGetLastError();
+    return launch_k(L, linear_warp_kernel<float>, dim3(blocks), dim3(256), 0, static_cast<const float*>(x), rows,
+                    ldx, static_cast<const float*>(W.ptr), W.N, W.K, out, ldo, alpha, beta);
   }
   return cudaErrorInvalidValue;
 }

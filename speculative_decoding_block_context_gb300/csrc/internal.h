@@ -15,7 +15,40 @@ struct Launch {
   cudaStream_t stream;
   int num_sms;
   unsigned* dev_err;  // the model's device error word (may be null in debug calls)
+  bool pdl = true;    // launch with programmatic stream serialization
 };
+
+// Launches `kernel` on L.stream, with programmatic stream serialization when L.pdl.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Zeroes up to 8 float32 ranges in one launch (accumulators a call sums into).
+struct ZeroList {
+  float* ptr[8];
+  int64_t n[8];
+  int count = 0;
+  void add(float* p, int64_t len) {
+    if (len > 0) {
+      ptr[count] = p;
+      n[count] = len;
+      ++count;
+    }
+  }
+};
+cudaError_t zero_ranges(const Launch& L, const ZeroList& z);
 
 // A GEMM weight W (N out, K in), row-major in device memory.
 struct Weight {
@@ -77,8 +110,6 @@ struct KvWriteArgs {
   unsigned* dev_err = nullptr;
 };
 cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a);
-cudaError_t qnorm_rope(const Launch& L, int dtype, float* acc, int rows, int K, int nh, int hd, const float* w,
-                       float eps, const float2* rope, int max_pos, const int32_t* anchor_pos, void* out);
 cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
                         const float* mh, float eps, void* out);
 cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
@@ -93,7 +124,11 @@ cudaError_t philox_export(cudaStream_t s, const uint64_t* seeds, const uint32_t*
 
 // ------------------------------------------------------------------ attention.cu
 struct XattnArgs {
-  const void* q = nullptr;      // [bs * K][D] normed, rotated queries
+  float* qacc = nullptr;        // [bs * K][D] float32 query projections (cleared by the combine)
+  const float* q_norm = nullptr;  // [hd] the layer's cross-attention q_norm weight
+  float eps = 0.f;
+  const float2* rope = nullptr;   // [max_pos][hd / 2]
+  int max_pos = 0;
   const void* pool = nullptr;
   int64_t num_pages = 0;
   int bs = 0, K = 0, nh = 0, hd = 0, P = 0, layer = 0;
@@ -114,12 +149,16 @@ int xattn_max_chunks(int num_sms, int nh, int bs);
 size_t xattn_plan_ints(int num_sms, int nh, int bs);
 cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan);
 cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& a);
+cudaError_t xattn_prepare();  // kernel attributes, once per device (not during capture)
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& a, void* out);
 
 // ------------------------------------------------------------------ sample.cu
+// keys: [rows] uint64 + counters [rows] uint32, zero before the first call; the
+// sampler leaves them zero again.
+int sample_splits(int Vd);
 cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
-                        const int64_t* hot, int64_t* tokens);
+                        const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters);
 cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
                          float* full);
 

@@ -13,37 +13,6 @@
 namespace fm {
 namespace {
 
-// RMSNorm of one head vector held EPL-per-lane by a warp (lane owns channels
-// lane*EPL .. lane*EPL+EPL-1), then the interleaved-pair rotation of the pairs
-// (2i, 2i+1) by angle row `rope` (cos, sin per pair), if given
-// (flashmap/modeling_flashmap.py, FlashMapRMSNorm and apply_rope).
-template <int EPL>
-__device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __restrict__ w, float eps,
-                                               const float2* __restrict__ rope, int lane) {
-  constexpr int HD = EPL * 32;
-  float ss = 0.f;
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) ss = fmaf(v[e], v[e], ss);
-  ss = warp_sum(ss);
-  const float r = rsqrtf(ss * (1.f / HD) + eps);
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) v[e] *= r * w[lane * EPL + e];
-  if (rope == nullptr) return;
-  if constexpr (EPL >= 2) {
-#pragma unroll
-    for (int e = 0; e < EPL; e += 2) {
-      const float2 cs = rope[(lane * EPL + e) >> 1];
-      const float x1 = v[e], x2 = v[e + 1];
-      v[e] = x1 * cs.x - x2 * cs.y;
-      v[e + 1] = x2 * cs.x + x1 * cs.y;
-    }
-  } else {
-    const float other = __shfl_xor_sync(0xffffffffu, v[0], 1);
-    const float2 cs = rope[lane >> 1];
-    v[0] = (lane & 1) ? (v[0] * cs.x + other * cs.y) : (v[0] * cs.x - other * cs.y);
-  }
-}
-
 template <typename T, int EPL>
 __device__ __forceinline__ void store_head(T* dst, const float (&v)[EPL], int lane) {
 #pragma unroll
@@ -64,6 +33,8 @@ __device__ __forceinline__ void load_clear_head(float* src, float (&v)[EPL], int
 template <typename T, int EPL>
 __global__ void __launch_bounds__(128) kv_write_kernel(KvWriteArgs a) {
   constexpr int HD = EPL * 32;
+  pdl_trigger();
+  pdl_wait();
   const int il = blockIdx.x, l = blockIdx.y;
   const int64_t i = a.row0 + il;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,32 +78,6 @@ __global__ void __launch_bounds__(128) kv_write_kernel(KvWriteArgs a) {
   }
 }
 
-// ------------------------------------------------------------------ cross-attention queries
-
-template <typename T, int EPL>
-__global__ void __launch_bounds__(128) qnorm_rope_kernel(float* __restrict__ acc, int K, int nh,
-                                                         const float* __restrict__ w, float eps,
-                                                         const float2* __restrict__ rope_tab, int max_pos,
-                                                         const int32_t* __restrict__ anchor_pos,
-                                                         T* __restrict__ out, unsigned* dev_err) {
-  constexpr int HD = EPL * 32;
-  const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = row / K, k = row - b * K;
-  int pos = anchor_pos[b] + 1 + k;
-  if (pos < 0 || pos >= max_pos) {
-    if (threadIdx.x == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
-    pos = 0;
-  }
-  const int D = nh * HD;
-  const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
-  for (int h = warp; h < nh; h += 4) {
-    float v[EPL];
-    load_clear_head<EPL>(acc + static_cast<int64_t>(row) * D + h * HD, v, lane);
-    head_norm_rope<EPL>(v, w, eps, rope, lane);
-    store_head<T, EPL>(out + static_cast<int64_t>(row) * D + h * HD, v, lane);
-  }
-}
-
 // ------------------------------------------------------------------ row norms
 
 // out = LayerNorm(x) * mscale + mshift   (no affine; biased variance)
@@ -141,6 +86,8 @@ __global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x
                                                      const float* __restrict__ ms, const float* __restrict__ mh,
                                                      float eps, T* __restrict__ out) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   const float* xr = x + static_cast<int64_t>(blockIdx.x) * width;
   float s = 0.f;
   for (int i = threadIdx.x; i < width; i += blockDim.x) s += xr[i];
@@ -162,6 +109,8 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(float* __restrict__ acc, 
                                                        const float* __restrict__ add, float gate,
                                                        T* __restrict__ out, int ldo) {
   __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
   float* ar = acc + static_cast<int64_t>(blockIdx.x) * width;
   float s = 0.f;
   for (int i = threadIdx.x; i < width; i += blockDim.x) {
@@ -180,6 +129,8 @@ __global__ void __launch_bounds__(256) rms_rows_kernel(float* __restrict__ acc, 
 
 template <typename T>
 __global__ void gelu_kernel(float* __restrict__ acc, int64_t n, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float x = acc[i];
@@ -191,6 +142,8 @@ __global__ void gelu_kernel(float* __restrict__ acc, int64_t n, T* __restrict__ 
 template <typename T>
 __global__ void gather_rows_kernel(const T* __restrict__ table, int64_t nrows, int width,
                                    const int64_t* __restrict__ ids, T* __restrict__ out, unsigned* dev_err) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x;
   int64_t id = ids[b];
   const bool ok = id >= 0 && id < nrows;
@@ -205,6 +158,8 @@ __global__ void gather_rows_kernel(const T* __restrict__ table, int64_t nrows, i
 template <typename T>
 __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int32_t* __restrict__ anchor_pos,
                                    int K, int H, int64_t total, T* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int n4 = (H + 3) >> 2;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -221,9 +176,32 @@ __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int
   }
 }
 
+__global__ void zero_kernel(ZeroList z) {
+  pdl_trigger();
+  pdl_wait();
+  for (int r = 0; r < z.count; ++r) {
+    float4* p = reinterpret_cast<float4*>(z.ptr[r]);
+    const int64_t n4 = (reinterpret_cast<uintptr_t>(z.ptr[r]) & 15) ? 0 : z.n[r] >> 2;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = (n4 << 2) + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < z.n[r];
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      z.ptr[r][i] = 0.f;
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+
+cudaError_t zero_ranges(const Launch& L, const ZeroList& z) {
+  int64_t total = 0;
+  for (int r = 0; r < z.count; ++r) total += z.n[r];
+  if (total <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<int64_t>((total / 4 + 255) / 256 + 1, static_cast<int64_t>(L.num_sms) * 8));
+  return launch_k(L, zero_kernel, dim3(blocks), dim3(256), 0, z);
+}
 
 #define FM_DISPATCH_T(dtype, ...)                 \
   do {                                            \
@@ -255,47 +233,44 @@ cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a) {
   KvWriteArgs b = a;
   b.dev_err = L.dev_err;
   dim3 grid(a.rows, a.L);
-  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (kv_write_kernel<T, EPL><<<grid, 128, 0, L.stream>>>(b))));
-  return cudaGetLastError();
-}
-
-cudaError_t qnorm_rope(const Launch& L, int dtype, float* acc, int rows, int K, int nh, int hd, const float* w,
-                       float eps, const float2* rope, int max_pos, const int32_t* anchor_pos, void* out) {
-  if (rows <= 0) return cudaSuccess;
-  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(hd, (qnorm_rope_kernel<T, EPL><<<rows, 128, 0, L.stream>>>(
-                                               acc, K, nh, w, eps, rope, max_pos, anchor_pos,
-                                               static_cast<T*>(out), L.dev_err))));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, dim3(128), 0, b))));
+  return e;
 }
 
 cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
                         const float* mh, float eps, void* out) {
   if (rows <= 0) return cudaSuccess;
-  FM_DISPATCH_T(dtype, (ln_mod_kernel<T><<<rows, 256, 0, L.stream>>>(x, width, ms, mh, eps, static_cast<T*>(out))));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, ln_mod_kernel<T>, dim3(rows), dim3(256), 0, x, width, ms, mh, eps,
+                                     static_cast<T*>(out))));
+  return e;
 }
 
 cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
                      float prescale, const float* add, float gate, void* out, int ldo) {
   if (rows <= 0) return cudaSuccess;
-  FM_DISPATCH_T(dtype, (rms_rows_kernel<T><<<rows, 256, 0, L.stream>>>(acc, width, w, eps, prescale, add, gate,
-                                                                     static_cast<T*>(out), ldo)));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, rms_rows_kernel<T>, dim3(rows), dim3(256), 0, acc, width, w, eps, prescale,
+                                     add, gate, static_cast<T*>(out), ldo)));
+  return e;
 }
 
 cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* out) {
   if (n <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(L.num_sms) * 16));
-  FM_DISPATCH_T(dtype, (gelu_kernel<T><<<blocks, 256, 0, L.stream>>>(acc, n, static_cast<T*>(out))));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, gelu_kernel<T>, dim3(blocks), dim3(256), 0, acc, n, static_cast<T*>(out))));
+  return e;
 }
 
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out) {
   if (n <= 0) return cudaSuccess;
-  FM_DISPATCH_T(dtype, (gather_rows_kernel<T><<<n, 256, 0, L.stream>>>(static_cast<const T*>(table), nrows, width,
-                                                                     ids, static_cast<T*>(out), L.dev_err)));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, gather_rows_kernel<T>, dim3(n), dim3(256), 0, static_cast<const T*>(table),
+                                     nrows, width, ids, static_cast<T*>(out), L.dev_err)));
+  return e;
 }
 
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
@@ -303,9 +278,10 @@ cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const
   const int64_t total = static_cast<int64_t>(bs) * K * ((H + 3) / 4);
   if (total <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(L.num_sms) * 16));
-  FM_DISPATCH_T(dtype, (draft_noise_kernel<T><<<blocks, 256, 0, L.stream>>>(seeds, anchor_pos, K, H, total,
-                                                                          static_cast<T*>(out))));
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, draft_noise_kernel<T>, dim3(blocks), dim3(256), 0, seeds, anchor_pos, K, H,
+                                     total, static_cast<T*>(out))));
+  return e;
 }
 
 // ------------------------------------------------------------------ Philox export

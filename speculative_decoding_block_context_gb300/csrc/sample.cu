@@ -1,9 +1,10 @@
 // Whole-block sampling (flashmap/sglang/sampler.py, FlashMapDraftSampler, fused
-// variant): one CTA per block row takes the row's argmax (greedy rows) or its
+// variant): a few CTAs per block row take the row's argmax (greedy rows) or its
 // Gumbel-max at the request's temperature with Philox noise drawn in the kernel, and
-// maps the drafted index to a token id; and the optional full-vocabulary logits with
+// map the drafted index to a token id; and the optional full-vocabulary logits with
 // -inf outside the draft vocabulary (flashmap/sglang/sampler.py, _FullLogits).
 
+#include <algorithm>
 #include <climits>
 
 #include "common.cuh"
@@ -15,15 +16,30 @@ namespace {
 
 __device__ __forceinline__ bool better(float v, int j, float bv, int bj) { return v > bv || (v == bv && j < bj); }
 
+// A float's bits mapped so that unsigned order is float order.
+__device__ __forceinline__ uint32_t orderable(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Row r is scanned by `splits` CTAs (blockIdx.y), each over a contiguous slice of the
+// draft vocabulary. Each slice's best (value, lowest index) is merged into keys[r] by
+// one 64-bit atomicMax on (orderable(value) << 32 | ~index), so larger values win and
+// equal values go to the lowest index. The CTA that finishes a row last (a counter,
+// no waiting) writes the token and clears the row's key and counter for the next call.
 __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ logits, int Vd, int K,
                                                      const float* __restrict__ temps,
                                                      const uint8_t* __restrict__ greedy,
                                                      const uint64_t* __restrict__ seeds,
                                                      const int32_t* __restrict__ anchor_pos, uint32_t step,
-                                                     const int64_t* __restrict__ hot, int64_t* __restrict__ tokens) {
+                                                     const int64_t* __restrict__ hot, int64_t* __restrict__ tokens,
+                                                     unsigned long long* keys, unsigned* counters) {
   __shared__ float rv[32];
   __shared__ int rj[32];
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x, b = row / K, k = row - b * K;
+  const int splits = gridDim.y, sp = blockIdx.y;
   const float T = temps[b];
   const bool argmax_only = greedy[b] != 0 || !(T > 0.f);
   const uint64_t seed = seeds[b];
@@ -32,7 +48,9 @@ __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ l
   float bv = -INFINITY;
   int bj = INT_MAX;
   const int n4 = (Vd + 3) >> 2;
-  for (int j4 = threadIdx.x; j4 < n4; j4 += blockDim.x) {
+  const int j4_0 = static_cast<int>(static_cast<int64_t>(n4) * sp / splits);
+  const int j4_1 = static_cast<int>(static_cast<int64_t>(n4) * (sp + 1) / splits);
+  for (int j4 = j4_0 + threadIdx.x; j4 < j4_1; j4 += blockDim.x) {
     uint4 w = make_uint4(0, 0, 0, 0);
     if (!argmax_only) w = philox_seeded(seed, static_cast<uint32_t>(j4), pos, kDomainGumbel, step);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -63,28 +81,38 @@ __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ l
     rj[warp] = bj;
   }
   __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    bv = lane < nw ? rv[lane] : -INFINITY;
-    bj = lane < nw ? rj[lane] : INT_MAX;
+  if (warp != 0) return;
+  const int nw = blockDim.x >> 5;
+  bv = lane < nw ? rv[lane] : -INFINITY;
+  bj = lane < nw ? rj[lane] : INT_MAX;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
-      if (better(ov, oj, bv, bj)) {
-        bv = ov;
-        bj = oj;
-      }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oj = __shfl_xor_sync(0xffffffffu, bj, o);
+    if (better(ov, oj, bv, bj)) {
+      bv = ov;
+      bj = oj;
     }
-    if (lane == 0) {
-      if (bj == INT_MAX) bj = 0;  // every value NaN
-      tokens[row] = hot ? hot[bj] : bj;
-    }
+  }
+  if (lane != 0) return;
+  const unsigned long long key = (static_cast<unsigned long long>(orderable(bv)) << 32) |
+                                 static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(bj));
+  atomicMax(keys + row, key);
+  __threadfence();
+  if (atomicAdd(counters + row, 1u) == static_cast<unsigned>(splits - 1)) {
+    __threadfence();
+    const unsigned long long best = atomicExch(keys + row, 0ull);
+    counters[row] = 0;
+    uint32_t j = 0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFull);
+    if (j >= static_cast<uint32_t>(Vd)) j = 0;  // every value NaN
+    tokens[row] = hot ? hot[j] : static_cast<int64_t>(j);
   }
 }
 
 __global__ void full_scatter_kernel(const float* __restrict__ logits, int Vd, const int32_t* __restrict__ inv,
                                     int V, float* __restrict__ full) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.y;
   const float* lr = logits + static_cast<int64_t>(row) * Vd;
   float* fr = full + static_cast<int64_t>(row) * V;
@@ -96,20 +124,21 @@ __global__ void full_scatter_kernel(const float* __restrict__ logits, int Vd, co
 
 }  // namespace
 
+int sample_splits(int Vd) { return std::max(1, std::min(32, (Vd + 2047) / 2048)); }
+
 cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
-                        const int64_t* hot, int64_t* tokens) {
+                        const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters) {
   if (rows <= 0) return cudaSuccess;
-  sample_kernel<<<rows, 256, 0, L.stream>>>(logits, Vd, K, temps, greedy, seeds, anchor_pos, step, hot, tokens);
-  return cudaGetLastError();
+  return launch_k(L, sample_kernel, dim3(rows, sample_splits(Vd)), dim3(256), 0, logits, Vd, K, temps, greedy, seeds,
+                  anchor_pos, step, hot, tokens, keys, counters);
 }
 
 cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
                          float* full) {
   if (rows <= 0) return cudaSuccess;
   dim3 grid(std::min((V + 255) / 256, 64), rows);
-  full_scatter_kernel<<<grid, 256, 0, L.stream>>>(logits, Vd, inv, V, full);
-  return cudaGetLastError();
+  return launch_k(L, full_scatter_kernel, grid, dim3(256), 0, logits, Vd, inv, V, full);
 }
 
 }  // namespace fm
