@@ -41,7 +41,7 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   const int D = nh * HD;
   const int k = warp;  // one warp per slot
   const int row = b * K + k;
-  int pos = anchor_pos[b] + 1 + k;
+  int pos = LDCG(anchor_pos + b) + 1 + k;
   if (pos < 0 || pos >= max_pos) {
     if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
     pos = 0;
@@ -54,7 +54,7 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
     float v[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-      v[e] = src[lane * EPL + e];
+      v[e] = LDCG(src + lane * EPL + e);
       src[lane * EPL + e] = 0.f;
     }
     if (part < 2) head_norm_rope<EPL>(v, part == 0 ? qn : kn, eps, rope, lane);
@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
   pdl_trigger();
   pdl_wait();
   float t16 = 0.f;
-  for (int b = threadIdx.x; b < bs; b += blockDim.x) t16 += static_cast<float>((max(anchor_pos[b] + 1, 1) + 15) / 16);
+  for (int b = threadIdx.x; b < bs; b += blockDim.x) t16 += static_cast<float>((max(LDCG(anchor_pos + b) + 1, 1) + 15) / 16);
   const float total16 = block_sum(t16, red);
   const int64_t need = static_cast<int64_t>(total16) * nh;
   int bpc = static_cast<int>((need + target_items - 1) / target_items);
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
   __shared__ int scan[1024];
   for (int b0 = 0; b0 < bs; b0 += blockDim.x) {
     const int b = b0 + threadIdx.x;
-    const int n = b < bs ? max(anchor_pos[b] + 1, 1) : 0;
+    const int n = b < bs ? max(LDCG(anchor_pos + b) + 1, 1) : 0;
     const int cnt = b < bs ? (n + chunk_len - 1) / chunk_len : 0;
     scan[threadIdx.x] = cnt;
     __syncthreads();
@@ -160,24 +160,28 @@ __device__ __forceinline__ void load_queries(const XattnArgs& a, int b, int h, f
   constexpr int EPL = HD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D = a.nh * HD;
-  for (int q = warp; q < 16; q += 4) {
-    float v[EPL];
-    if (q < a.K) {  // warp-uniform
-      const float* src = a.qacc + static_cast<int64_t>(b * a.K + q) * D + h * HD;
+  float v[4][EPL];
+  // every load of the warp's four rows first, then the reductions
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) v[e] = src[lane * EPL + e];
-      int pos = a.anchor_pos[b] + 1 + q;
+  for (int i = 0; i < 4; ++i) {
+    const int q = warp + 4 * i;
+    const float* src = a.qacc + static_cast<int64_t>(b * a.K + q) * D + h * HD + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[i][e] = q < a.K ? LDCG(src + e) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = warp + 4 * i;
+    if (q < a.K) {  // warp-uniform
+      int pos = LDCG(a.anchor_pos + b) + 1 + q;
       if (pos < 0 || pos >= a.max_pos) {
         if (lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
         pos = 0;
       }
-      head_norm_rope<EPL>(v, a.q_norm, a.eps, a.rope + static_cast<int64_t>(pos) * (HD / 2), lane);
-    } else {
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) v[e] = 0.f;
+      head_norm_rope<EPL>(v[i], a.q_norm, a.eps, a.rope + static_cast<int64_t>(pos) * (HD / 2), lane);
     }
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) sq[q * HD + lane * EPL + e] = v[e];
+    for (int e = 0; e < EPL; ++e) sq[q * HD + lane * EPL + e] = v[i][e];
   }
 }
 
@@ -194,15 +198,15 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
   __shared__ float sm[16], sl[16], scorr[16];
   const int tid = threadIdx.x;
   const int nh = a.nh;
-  const int items = a.plan[0], chunk_len = a.plan[1];
+  const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
   const int* pairs = a.plan + 4 + a.bs;
   const T* pool = static_cast<const T*>(a.pool);
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int g = item / nh, h = item - g * nh;
-    const int b = pairs[2 * g], c = pairs[2 * g + 1];
-    const int n = a.anchor_pos[b] + 1;
+    const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
+    const int n = LDCG(a.anchor_pos + b) + 1;
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
-    const int rrow = a.req_pool_idx ? a.req_pool_idx[b] : b;
+    const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
     __syncthreads();
     load_queries<HD>(a, b, h, &sq[0][0]);
     if (tid < 16) {
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
     for (int blk = p0; blk < p1; blk += 16) {
       // the 16 positions blk..blk+15 lie in one page (page_size is a multiple of 16)
       const int pi = blk / a.P;
-      int page = pi < a.r2p_stride ? a.req_to_page[static_cast<int64_t>(rrow) * a.r2p_stride + pi] : -1;
+      int page = pi < a.r2p_stride ? LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi) : -1;
       const bool ok = page >= 0 && page < a.num_pages;
       if (!ok && tid == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
       const int off = blk - pi * a.P;
@@ -225,8 +229,8 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
       for (int i = tid; i < 16 * HD; i += blockDim.x) {
         const int j = i / HD, d = i - j * HD;
         const bool valid = ok && blk + j < p1;
-        sk[j][d] = valid ? to_f32(pool[kb + i]) : 0.f;
-        sv[j][d] = valid ? to_f32(pool[vb + i]) : 0.f;
+        sk[j][d] = valid ? to_f32(LDCG(pool + kb + i)) : 0.f;
+        sv[j][d] = valid ? to_f32(LDCG(pool + vb + i)) : 0.f;
       }
       __syncthreads();
       for (int i = tid; i < 256; i += blockDim.x) {
@@ -339,17 +343,17 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, t4 = lane & 3;
   const int nh = a.nh;
-  const int items = a.plan[0], chunk_len = a.plan[1];
+  const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
   const int* pairs = a.plan + 4 + a.bs;
   const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(a.pool);
   const uint32_t ring = smem_u32(xsm) + warp * C::RING;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int g = item / nh, h = item - g * nh;
-    const int b = pairs[2 * g], c = pairs[2 * g + 1];
-    const int n = a.anchor_pos[b] + 1;
+    const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
+    const int n = LDCG(a.anchor_pos + b) + 1;
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
     const int nblk = (p1 - p0 + 15) >> 4;
-    const int rrow = a.req_pool_idx ? a.req_pool_idx[b] : b;
+    const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
     // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
     float* sq = reinterpret_cast<float*>(xsm);  // aliases the ring until the first loads
     load_queries<HD>(a, b, h, sq);
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
       if (j < nj) {
         const int blk = p0 + ((warp + 4 * j) << 4);
         const int pi = blk / a.P;
-        const int page = pi < a.r2p_stride ? a.req_to_page[static_cast<int64_t>(rrow) * a.r2p_stride + pi] : -1;
+        const int page = pi < a.r2p_stride ? LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi) : -1;
         const bool ok = page >= 0 && page < a.num_pages;
         if (!ok && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
         const int off = blk - pi * a.P;
@@ -516,30 +520,47 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 
 // ------------------------------------------------------------------ combine
 
+// One CTA per (request, head, query row): the chunks' (max, sum) are read in parallel
+// into shared memory, then each thread sums its channel over the chunks.
+constexpr int kMaxChunksPerRequest = 1024;  // max_position <= 262144, chunks >= 256 positions
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(HD) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
+  __shared__ float sw[kMaxChunksPerRequest];
+  __shared__ float red[32];
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  const int b = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
   const int* first = a.plan + 3;
-  const int g0 = first[b], g1 = first[b + 1];
-  {
-    const int qi = blockIdx.z;
-    float M = -INFINITY;
-    for (int g = g0; g < g1; ++g) M = fmaxf(M, a.part_ml[(static_cast<int64_t>(g) * nh + h) * 32 + 2 * qi]);
-    float L = 0.f, acc = 0.f;
-    for (int g = g0; g < g1; ++g) {
-      const int64_t pidx = static_cast<int64_t>(g) * nh + h;
-      const float m = a.part_ml[pidx * 32 + 2 * qi];
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
-      L = fmaf(a.part_ml[pidx * 32 + 2 * qi + 1], w, L);
-      acc = fmaf(a.part_o[pidx * 16 * HD + qi * HD + d], w, acc);
-    }
-    out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
-    a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
+  const int g0 = LDCG(first + b), nc = min(LDCG(first + b + 1) - g0, kMaxChunksPerRequest);
+  float mloc = -INFINITY;
+  for (int c = d; c < nc; c += HD) {
+    const float m = LDCG(a.part_ml + ((static_cast<int64_t>(g0 + c)) * nh + h) * 32 + 2 * qi);
+    sw[c] = m;
+    mloc = fmaxf(mloc, m);
   }
+  // block max
+  mloc = warp_max(mloc);
+  if ((d & 31) == 0) red[d >> 5] = mloc;
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < HD / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float lloc = 0.f;
+  for (int c = d; c < nc; c += HD) {
+    const int64_t pidx = static_cast<int64_t>(g0 + c) * nh + h;
+    const float wgt = sw[c] == -INFINITY ? 0.f : exp2f(sw[c] - M);
+    sw[c] = wgt;
+    lloc = fmaf(wgt, LDCG(a.part_ml + pidx * 32 + 2 * qi + 1), lloc);
+  }
+  const float L = block_sum(lloc, red);  // synchronizes: sw complete
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nc; ++c)
+    acc = fmaf(sw[c], LDCG(a.part_o + (static_cast<int64_t>(g0 + c) * nh + h) * 16 * HD + qi * HD + d), acc);
+  out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
+  a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
 }
 
 }  // namespace

@@ -53,6 +53,12 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 // overlap its tail) and waits for its predecessors' completion before touching data
 // they produce. Without a programmatic predecessor both are no-ops.
 
+// Loads of data written earlier in the same chain of launches (accumulators, the
+// residual stream, plans, partial results) and of per-call inputs go to L2
+// (ld.global.cg): under programmatic dependent launch a CTA's L1 may still hold a
+// line that other SMs have since changed in L2.
+#define LDCG(p) __ldcg(p)
+
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -147,11 +147,14 @@ flashmap_status validate(const flashmap_config* c) {
       return fail(FLASHMAP_E_UNSUPPORTED, "E4M3 weights are not built yet");
     return fail(FLASHMAP_E_INVALID, "weight_dtype must equal act_dtype (or E4M3 with BF16 activations)");
   }
-  if (c->act_dtype == FLASHMAP_BF16) {
+  {
     const int a[] = {c->target_hidden, c->hidden, c->intermediate};
     for (int d : a)
-      if (d % 8) return fail(FLASHMAP_E_UNSUPPORTED, "bf16 GEMM widths must be multiples of 8");
+      if (d % 8) return fail(FLASHMAP_E_UNSUPPORTED, "target_hidden, hidden and intermediate must be multiples of 8");
+    if (c->target_hidden > 16384 || c->hidden > 16384)
+      return fail(FLASHMAP_E_UNSUPPORTED, "target_hidden and hidden must be <= 16384");
   }
+  if (c->max_position > (1 << 18)) return fail(FLASHMAP_E_UNSUPPORTED, "max_position must be <= 262144");
   if (!(c->rope_theta > 0) || !(c->time_scale >= 0) || !(c->rms_norm_eps >= 0) || !(c->qk_norm_eps >= 0) ||
       !(c->layer_norm_eps >= 0))
     return fail(FLASHMAP_E_INVALID, "rope_theta, time_scale and eps values must be non-negative");

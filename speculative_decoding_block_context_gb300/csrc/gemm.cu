@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (row0 + j < R) {
               float* o = out + static_cast<int64_t>(row0 + j) * ldo + n;
               if (whole)
-                *o += fmaf(a, v[j], b);
+                *o = LDCG(o) + fmaf(a, v[j], b);
               else
                 atomicAdd(o, fmaf(a, v[j], b));
             }
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(256) linear_warp_kernel(const T* __restrict__ 
       const float wv = to_f32(wr[k]);
 #pragma unroll
       for (int j = 0; j < RB; ++j)
-        if (r0 + j < R) acc[j] = fmaf(wv, to_f32(x[static_cast<int64_t>(r0 + j) * ldx + k]), acc[j]);
+        if (r0 + j < R) acc[j] = fmaf(wv, to_f32(LDCG(x + static_cast<int64_t>(r0 + j) * ldx + k)), acc[j]);
     }
 #pragma unroll
     for (int j = 0; j < RB; ++j) {

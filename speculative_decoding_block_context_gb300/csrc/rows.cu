@@ -13,43 +13,64 @@
 namespace fm {
 namespace {
 
-template <typename T, int EPL>
-__device__ __forceinline__ void store_head(T* dst, const float (&v)[EPL], int lane) {
-#pragma unroll
-  for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = from_f32<T>(v[e]);
-}
-
+// Loads (and clears) the EPL channels lane*EPL.. of one head vector in one go.
 template <int EPL>
 __device__ __forceinline__ void load_clear_head(float* src, float (&v)[EPL], int lane) {
+  float* p = src + lane * EPL;
+  if constexpr (EPL == 4) {
+    const float4 t = LDCG(reinterpret_cast<const float4*>(p));
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if constexpr (EPL == 2) {
+    const float2 t = LDCG(reinterpret_cast<const float2*>(p));
+    v[0] = t.x, v[1] = t.y;
+    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
+  } else {
+    v[0] = LDCG(p);
+    p[0] = 0.f;
+  }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void store_vec(T* dst, const float* v) {
+  if constexpr (sizeof(T) == 2 && N == 4) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = u;
+  } else if constexpr (sizeof(T) == 4 && N == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    v[e] = src[lane * EPL + e];
-    src[lane * EPL + e] = 0.f;
+    for (int e = 0; e < N; ++e) dst[e] = from_f32<T>(v[e]);
   }
 }
 
 // ------------------------------------------------------------------ context-KV write
 
+// One CTA per (row, layer), one warp per head: the key and value of a head are read
+// in a single vector load per lane, the key k-normed and rotated, both stored.
 template <typename T, int EPL>
-__global__ void __launch_bounds__(128) kv_write_kernel(KvWriteArgs a) {
+__global__ void __launch_bounds__(1024) kv_write_kernel(KvWriteArgs a) {
   constexpr int HD = EPL * 32;
   pdl_trigger();
   pdl_wait();
   const int il = blockIdx.x, l = blockIdx.y;
   const int64_t i = a.row0 + il;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int b = static_cast<int>(i / a.W), c = static_cast<int>(i - static_cast<int64_t>(b) * a.W);
-  const int pos = a.start_pos[b] + c;
-  bool write = a.commit_lens == nullptr || c < a.commit_lens[b];
+  const int pos = LDCG(a.start_pos + b) + c;
+  bool write = a.commit_lens == nullptr || c < LDCG(a.commit_lens + b);
   int64_t slot = -1;
   if (write) {
-    const int rrow = a.req_pool_idx ? a.req_pool_idx[b] : b;
+    const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
     const int pi = pos >= 0 ? pos / a.P : -1;
     if (pos < 0 || pos >= a.max_pos || pi >= a.r2p_stride || rrow < 0) {
       if (threadIdx.x == 0 && l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
       write = false;
     } else {
-      const int page = a.req_to_page[static_cast<int64_t>(rrow) * a.r2p_stride + pi];
+      const int page = LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi);
       if (page < 0 || page >= a.num_pages) {
         if (threadIdx.x == 0 && l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
         write = false;
@@ -65,7 +86,7 @@ __global__ void __launch_bounds__(128) kv_write_kernel(KvWriteArgs a) {
   const float2* rope = write ? a.rope + static_cast<int64_t>(pos) * (HD / 2) : nullptr;
   T* pool = static_cast<T*>(a.pool);
   const int64_t page = write ? slot / a.P : 0, off = write ? slot - page * a.P : 0;
-  for (int h = warp; h < a.nh; h += 4) {
+  for (int h = warp; h < a.nh; h += nw) {
     float k[EPL], v[EPL];
     load_clear_head<EPL>(row + h * HD, k, lane);
     load_clear_head<EPL>(row + D + h * HD, v, lane);
@@ -73,57 +94,107 @@ __global__ void __launch_bounds__(128) kv_write_kernel(KvWriteArgs a) {
     head_norm_rope<EPL>(k, kw, a.eps, rope, lane);
     const int64_t kbase = (((static_cast<int64_t>(l) * 2 + 0) * a.num_pages + page) * a.nh + h) * a.P;
     const int64_t vbase = (((static_cast<int64_t>(l) * 2 + 1) * a.num_pages + page) * a.nh + h) * a.P;
-    store_head<T, EPL>(pool + (kbase + off) * HD, k, lane);
-    store_head<T, EPL>(pool + (vbase + off) * HD, v, lane);
+    store_vec<T, EPL>(pool + (kbase + off) * HD + lane * EPL, k);
+    store_vec<T, EPL>(pool + (vbase + off) * HD + lane * EPL, v);
   }
 }
 
 // ------------------------------------------------------------------ row norms
+//
+// One CTA of 256 threads per row; thread t holds the float4 groups t, t + 256, ...
+// (NV of them) in registers: the row is read once, both statistics come from the
+// registers, and the result is written once.
+
+constexpr int kRowThreads = 256;
+
+// constants (weights, modulations) may use any load; rows produced in the step use L2
+template <int NV, bool kCoherent>
+__device__ __forceinline__ void load_row4(const float* src, int w4, float4 (&v)[NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int f = threadIdx.x + i * kRowThreads;
+    const float4* p = reinterpret_cast<const float4*>(src) + f;
+    v[i] = f < w4 ? (kCoherent ? LDCG(p) : *p) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
 
 // out = LayerNorm(x) * mscale + mshift   (no affine; biased variance)
-template <typename T>
-__global__ void __launch_bounds__(256) ln_mod_kernel(const float* __restrict__ x, int width,
-                                                     const float* __restrict__ ms, const float* __restrict__ mh,
-                                                     float eps, T* __restrict__ out) {
+template <typename T, int NV>
+__global__ void __launch_bounds__(kRowThreads) ln_mod_kernel(const float* __restrict__ x, int width,
+                                                             const float* __restrict__ ms,
+                                                             const float* __restrict__ mh, float eps,
+                                                             T* __restrict__ out) {
   __shared__ float red[32];
   pdl_trigger();
+  const int w4 = width >> 2;
+  float4 m1[NV], m2[NV], v[NV];
+  load_row4<NV, false>(ms, w4, m1);  // constants: read before waiting
+  load_row4<NV, false>(mh, w4, m2);
   pdl_wait();
-  const float* xr = x + static_cast<int64_t>(blockIdx.x) * width;
+  load_row4<NV, true>(x + static_cast<int64_t>(blockIdx.x) * width, w4, v);
   float s = 0.f;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) s += xr[i];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
   const float mean = block_sum(s, red) / width;
   float s2 = 0.f;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) {
-    const float d = xr[i] - mean;
-    s2 = fmaf(d, d, s2);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    if (threadIdx.x + i * kRowThreads < w4) {
+      const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
+      s2 += (a * a + b * b) + (c * c + d * d);
+    }
   }
   const float rstd = rsqrtf(block_sum(s2, red) / width + eps);
   T* o = out + static_cast<int64_t>(blockIdx.x) * width;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) o[i] = from_f32<T>(fmaf((xr[i] - mean) * rstd, ms[i], mh[i]));
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int f = threadIdx.x + i * kRowThreads;
+    if (f < w4) {
+      const float r[4] = {fmaf((v[i].x - mean) * rstd, m1[i].x, m2[i].x), fmaf((v[i].y - mean) * rstd, m1[i].y, m2[i].y),
+                          fmaf((v[i].z - mean) * rstd, m1[i].z, m2[i].z), fmaf((v[i].w - mean) * rstd, m1[i].w, m2[i].w)};
+      store_vec<T, 4>(o + 4 * f, r);
+    }
+  }
 }
 
-// y = prescale * acc; v = y * w * rsqrt(mean(y^2) + eps); out = add ? add + gate * v : v
-template <typename T>
-__global__ void __launch_bounds__(256) rms_rows_kernel(float* __restrict__ acc, int width,
-                                                       const float* __restrict__ w, float eps, float prescale,
-                                                       const float* __restrict__ add, float gate,
-                                                       T* __restrict__ out, int ldo) {
+// y = prescale * acc; v = y * w * rsqrt(mean(y^2) + eps); out = add ? add + gate * v : v;
+// the accumulator row is cleared.
+template <typename T, int NV>
+__global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict__ acc, int width,
+                                                               const float* __restrict__ w, float eps,
+                                                               float prescale, const float* __restrict__ add,
+                                                               float gate, T* __restrict__ out, int ldo) {
   __shared__ float red[32];
   pdl_trigger();
+  const int w4 = width >> 2;
+  float4 wv[NV], av[NV], v[NV];
+  load_row4<NV, false>(w, w4, wv);
+  if (add) load_row4<NV, false>(add, w4, av);
   pdl_wait();
   float* ar = acc + static_cast<int64_t>(blockIdx.x) * width;
+  load_row4<NV, true>(ar, w4, v);
   float s = 0.f;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) {
-    const float y = prescale * ar[i];
-    s = fmaf(y, y, s);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i].x *= prescale, v[i].y *= prescale, v[i].z *= prescale, v[i].w *= prescale;
+    s += (v[i].x * v[i].x + v[i].y * v[i].y) + (v[i].z * v[i].z + v[i].w * v[i].w);
   }
   const float r = rsqrtf(block_sum(s, red) / width + eps);
   T* o = out + static_cast<int64_t>(blockIdx.x) * ldo;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) {
-    float v = prescale * ar[i] * r * w[i];
-    if (add) v = fmaf(gate, v, add[i]);
-    o[i] = from_f32<T>(v);
-    ar[i] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int f = threadIdx.x + i * kRowThreads;
+    if (f < w4) {
+      float q[4] = {v[i].x * r * wv[i].x, v[i].y * r * wv[i].y, v[i].z * r * wv[i].z, v[i].w * r * wv[i].w};
+      if (add) {
+        q[0] = fmaf(gate, q[0], av[i].x);
+        q[1] = fmaf(gate, q[1], av[i].y);
+        q[2] = fmaf(gate, q[2], av[i].z);
+        q[3] = fmaf(gate, q[3], av[i].w);
+      }
+      store_vec<T, 4>(o + 4 * f, q);
+      reinterpret_cast<float4*>(ar)[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -133,24 +204,23 @@ __global__ void gelu_kernel(float* __restrict__ acc, int64_t n, T* __restrict__ 
   pdl_wait();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float x = acc[i];
+    const float x = LDCG(acc + i);
     out[i] = from_f32<T>(0.5f * x * (1.f + erff(x * 0.70710678118654752f)));
     acc[i] = 0.f;
   }
 }
 
-template <typename T>
-__global__ void gather_rows_kernel(const T* __restrict__ table, int64_t nrows, int width,
-                                   const int64_t* __restrict__ ids, T* __restrict__ out, unsigned* dev_err) {
+// Row copies in 16-byte chunks: grid (rows, chunk blocks).
+__global__ void gather_rows_kernel(const uint4* __restrict__ table, int64_t nrows, int chunks,
+                                   const int64_t* __restrict__ ids, uint4* __restrict__ out, unsigned* dev_err) {
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x;
-  int64_t id = ids[b];
+  const int64_t id = LDCG(ids + b);
   const bool ok = id >= 0 && id < nrows;
-  if (!ok && threadIdx.x == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_TOKEN);
-  const T* src = table + (ok ? id : 0) * width;
-  T* dst = out + static_cast<int64_t>(b) * width;
-  for (int i = threadIdx.x; i < width; i += blockDim.x) dst[i] = ok ? src[i] : from_f32<T>(0.f);
+  if (!ok && threadIdx.x == 0 && blockIdx.y == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_TOKEN);
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c < chunks) out[static_cast<int64_t>(b) * chunks + c] = ok ? table[id * chunks + c] : make_uint4(0, 0, 0, 0);
 }
 
 // z[b*K + k][j] ~ N(0, 1) keyed by (seeds[b], position anchor_pos[b] + 1 + k): counter
@@ -165,8 +235,8 @@ __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int row = static_cast<int>(t / n4), j4 = static_cast<int>(t - static_cast<int64_t>(row) * n4);
     const int b = row / K, k = row - b * K;
-    const uint32_t pos = static_cast<uint32_t>(anchor_pos[b] + 1 + k);
-    const uint4 w = philox_seeded(seeds[b], static_cast<uint32_t>(j4), pos, kDomainDraftNoise, 0u);
+    const uint32_t pos = static_cast<uint32_t>(LDCG(anchor_pos + b) + 1 + k);
+    const uint4 w = philox_seeded(LDCG(seeds + b), static_cast<uint32_t>(j4), pos, kDomainDraftNoise, 0u);
     const float2 n01 = box_muller(w.x, w.y), n23 = box_muller(w.z, w.w);
     const float v[4] = {n01.x, n01.y, n23.x, n23.y};
     T* o = out + static_cast<int64_t>(row) * H + 4 * j4;
@@ -234,16 +304,39 @@ cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a) {
   b.dev_err = L.dev_err;
   dim3 grid(a.rows, a.L);
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, dim3(128), 0, b))));
+  const dim3 block(32 * std::min(a.nh, 32));
+  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, block, 0, b))));
   return e;
 }
 
+#define FM_DISPATCH_NV(width, ...)                                          \
+  do {                                                                      \
+    const int nv_ = ((width) / 4 + kRowThreads - 1) / kRowThreads;          \
+    if (nv_ <= 1) {                                                         \
+      constexpr int NV = 1;                                                 \
+      __VA_ARGS__;                                                          \
+    } else if (nv_ <= 2) {                                                  \
+      constexpr int NV = 2;                                                 \
+      __VA_ARGS__;                                                          \
+    } else if (nv_ <= 4) {                                                  \
+      constexpr int NV = 4;                                                 \
+      __VA_ARGS__;                                                          \
+    } else if (nv_ <= 8) {                                                  \
+      constexpr int NV = 8;                                                 \
+      __VA_ARGS__;                                                          \
+    } else {                                                                \
+      constexpr int NV = 16;                                                \
+      __VA_ARGS__;                                                          \
+    }                                                                       \
+  } while (0)
+
+// width % 4 == 0 and width <= 16384 (checked at load)
 cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
                         const float* mh, float eps, void* out) {
   if (rows <= 0) return cudaSuccess;
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, (e = launch_k(L, ln_mod_kernel<T>, dim3(rows), dim3(256), 0, x, width, ms, mh, eps,
-                                     static_cast<T*>(out))));
+  FM_DISPATCH_T(dtype, FM_DISPATCH_NV(width, (e = launch_k(L, ln_mod_kernel<T, NV>, dim3(rows), dim3(kRowThreads), 0,
+                                                          x, width, ms, mh, eps, static_cast<T*>(out)))));
   return e;
 }
 
@@ -251,8 +344,9 @@ cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width
                      float prescale, const float* add, float gate, void* out, int ldo) {
   if (rows <= 0) return cudaSuccess;
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, (e = launch_k(L, rms_rows_kernel<T>, dim3(rows), dim3(256), 0, acc, width, w, eps, prescale,
-                                     add, gate, static_cast<T*>(out), ldo)));
+  FM_DISPATCH_T(dtype, FM_DISPATCH_NV(width, (e = launch_k(L, rms_rows_kernel<T, NV>, dim3(rows), dim3(kRowThreads),
+                                                          0, acc, width, w, eps, prescale, add, gate,
+                                                          static_cast<T*>(out), ldo))));
   return e;
 }
 
@@ -264,13 +358,13 @@ cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* o
   return e;
 }
 
+// width * element size must be a multiple of 16 bytes (checked at load)
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out) {
   if (n <= 0) return cudaSuccess;
-  cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, (e = launch_k(L, gather_rows_kernel<T>, dim3(n), dim3(256), 0, static_cast<const T*>(table),
-                                     nrows, width, ids, static_cast<T*>(out), L.dev_err)));
-  return e;
+  const int chunks = width * (dtype == FLASHMAP_F32 ? 4 : 2) / 16;
+  return launch_k(L, gather_rows_kernel, dim3(n, (chunks + 255) / 256), dim3(256), 0,
+                  static_cast<const uint4*>(table), nrows, chunks, ids, static_cast<uint4*>(out), L.dev_err);
 }
 
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,

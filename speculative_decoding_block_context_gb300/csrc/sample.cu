@@ -40,10 +40,10 @@ __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ l
   pdl_wait();
   const int row = blockIdx.x, b = row / K, k = row - b * K;
   const int splits = gridDim.y, sp = blockIdx.y;
-  const float T = temps[b];
-  const bool argmax_only = greedy[b] != 0 || !(T > 0.f);
-  const uint64_t seed = seeds[b];
-  const uint32_t pos = static_cast<uint32_t>(anchor_pos[b] + 1 + k);
+  const float T = LDCG(temps + b);
+  const bool argmax_only = LDCG(greedy + b) != 0 || !(T > 0.f);
+  const uint64_t seed = LDCG(seeds + b);
+  const uint32_t pos = static_cast<uint32_t>(LDCG(anchor_pos + b) + 1 + k);
   const float* lr = logits + static_cast<int64_t>(row) * Vd;
   float bv = -INFINITY;
   int bj = INT_MAX;
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ l
     for (int e = 0; e < 4; ++e) {
       const int j = 4 * j4 + e;
       if (j >= Vd) break;
-      const float l = lr[j];
+      const float l = LDCG(lr + j);
       const float v = argmax_only ? l : __fdiv_rn(l, T) + gumbel_of_word(ws[e]);
       if (better(v, j, bv, bj)) {
         bv = v;
@@ -118,7 +118,7 @@ __global__ void full_scatter_kernel(const float* __restrict__ logits, int Vd, co
   float* fr = full + static_cast<int64_t>(row) * V;
   for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) {
     const int j = inv[v];
-    fr[v] = j >= 0 ? lr[j] : -INFINITY;
+    fr[v] = j >= 0 ? LDCG(lr + j) : -INFINITY;
   }
 }
 
