@@ -249,6 +249,27 @@ flashmap_status flashmap_sample_block(flashmap_model* model, int32_t bs, const v
                                       float* full_logits_out, void* workspace,
                                       size_t workspace_bytes, flashmap_stream stream);
 
+/*
+ * flashmap_sample_block's sampling step for callers that cannot allocate device
+ * memory: for example a host runtime that owns every device allocation and hands a
+ * plugin only its input and output buffers, or code running where a device
+ * allocation would not be allowed. The paper has no counterpart; this is a
+ * library-level addition. The caller passes the draft-vocabulary logits (device,
+ * float32 [bs * K][Vd], e.g. flashmap_sample_block's draft_logits_out) and the same
+ * per-request inputs as flashmap_sample_block; tokens_out (device, int64 [bs * K])
+ * receives the same token ids flashmap_sample_block draws from those logits. The
+ * per-row merge slots live in a fixed array inside the library (96 KB on every GPU
+ * that loads it, kept until the process exits), so bs * block_size may not exceed
+ * 8192 rows (E_INVALID otherwise). The first call on a device looks up that array's
+ * device address; make it before any stream capture on that device. The array is
+ * shared by every call and keeps the last call's contents (the call clears what it
+ * uses): calls that overlap on the GPU, on any stream, race and give wrong tokens.
+ */
+flashmap_status flashmap_sample_logits_static(flashmap_model* model, int32_t bs, const float* logits,
+                                             const int32_t* anchor_pos, const float* temperature,
+                                             const uint8_t* greedy, const uint64_t* seeds, uint64_t step,
+                                             int64_t* tokens_out, flashmap_stream stream);
+
 /* The device error word (FLASHMAP_DEVERR_* bits), then clears it. Synchronizes
  * `stream`. Returns E_DEVICE when the word was non-zero. */
 flashmap_status flashmap_get_device_error(flashmap_model* model, flashmap_stream stream,

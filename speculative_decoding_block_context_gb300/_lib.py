@@ -115,6 +115,7 @@ def lib():
         L.flashmap_debug_philox.argtypes = [_vp, _vp, _c.c_int64, _vp, _vp, _vp]
         L.flashmap_debug_linear.argtypes = [_c.c_int32, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp]
         L.flashmap_debug_constants.argtypes = [_vp, _vp, _vp, _vp, _vp]
+        L.flashmap_sample_logits_static.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp]
         L.flashmap_profile_start.argtypes = [_vp, _c.c_int32]
         L.flashmap_profile_stop.argtypes = [_vp, P(flashmap_launch_record), _c.c_int32, P(_c.c_int32)]
         for name in header_functions():
@@ -243,6 +244,15 @@ def flashmap_sample_block(model: Model, bs: int, hidden, anchor_pos, temperature
         model.handle, int(bs), _ptr(hidden), _ptr(anchor_pos), _ptr(temperature), _ptr(greedy), _ptr(seeds),
         int(step), _ptr(tokens_out), _ptr(draft_logits_out), _ptr(full_logits_out), _ptr(workspace), ws_bytes,
         _stream(stream)))
+
+
+def flashmap_sample_logits_static(model: Model, bs: int, logits, anchor_pos, temperature, greedy, seeds, step: int,
+                                  tokens_out, stream=None) -> None:
+    """Sampling from caller-provided logits with the library's static scratch (no
+    device allocation; at most 8192 rows; overlapping calls race)."""
+    _check(lib().flashmap_sample_logits_static(model.handle, int(bs), _ptr(logits), _ptr(anchor_pos),
+                                               _ptr(temperature), _ptr(greedy), _ptr(seeds), int(step),
+                                               _ptr(tokens_out), _stream(stream)))
 
 
 def flashmap_get_device_error(model: Model, stream=None) -> int:

@@ -782,6 +782,33 @@ flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void*
   return FLASHMAP_OK;
 }
 
+flashmap_status flashmap_sample_logits_static(flashmap_model* m, int32_t bs, const float* logits,
+                                             const int32_t* anchor_pos, const float* temperature,
+                                             const uint8_t* greedy, const uint64_t* seeds, uint64_t step,
+                                             int64_t* tokens_out, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m || !logits || !anchor_pos || !temperature || !greedy || !seeds || !tokens_out)
+    return fail(FLASHMAP_E_INVALID, "NULL argument");
+  if (bs <= 0) return fail(FLASHMAP_E_INVALID, "bs must be positive");
+  const int64_t rows = static_cast<int64_t>(bs) * m->K;
+  if (rows > fm::kStaticSampleRows)
+    return fail(FLASHMAP_E_INVALID, "bs * block_size = " + std::to_string(rows) + " rows exceeds the " +
+                                        std::to_string(fm::kStaticSampleRows) + " rows of the static sampler scratch");
+  void* scratch = nullptr;
+  FM_CUDA(fm::static_sample_scratch(&scratch));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Launch Lh = m->launch(s);
+  auto* keys = static_cast<unsigned long long*>(scratch);
+  auto* counters = reinterpret_cast<unsigned*>(static_cast<unsigned char*>(scratch) + rows * 8);
+  fm::ZeroList z;  // the array keeps the last call's contents
+  z.add(reinterpret_cast<float*>(keys), 2 * rows);
+  z.add(reinterpret_cast<float*>(counters), rows);
+  FM_CUDA(fm::zero_ranges(Lh, z));
+  FM_CUDA(fm::sample_rows(Lh, logits, static_cast<int>(rows), m->Vd, m->K, temperature, greedy, seeds, anchor_pos,
+                          static_cast<uint32_t>(step), m->hot, tokens_out, keys, counters));
+  return FLASHMAP_OK;
+}
+
 flashmap_status flashmap_get_device_error(flashmap_model* m, flashmap_stream stream, uint32_t* code) {
   g_last_error.clear();
   if (!m || !code) return fail(FLASHMAP_E_INVALID, "NULL argument");

@@ -156,6 +156,9 @@ cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& a, void* 
 // keys: [rows] uint64 + counters [rows] uint32, zero before the first call; the
 // sampler leaves them zero again.
 int sample_splits(int Vd);
+// Sampler merge slots in a static device array (no allocation): rows <= kStaticSampleRows.
+constexpr int kStaticSampleRows = 8192;
+cudaError_t static_sample_scratch(void** out);
 cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
                         const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters);

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -123,6 +124,32 @@ __global__ void full_scatter_kernel(const float* __restrict__ logits, int Vd, co
 }
 
 }  // namespace
+
+// Merge slots of the sampler for callers that cannot allocate device memory: one
+// 8-byte key and one 4-byte counter per row, kStaticSampleRows rows, in a file-scope
+// array that every GPU loading the library holds until the process exits.
+static __device__ __align__(256) unsigned char g_sample_scratch[kStaticSampleRows * 12];
+
+// The device address of g_sample_scratch on the current device. The host-side name
+// of the array is only a stand-in: the address comes from cudaGetSymbolAddress,
+// looked up once per device (with that device current) and cached.
+cudaError_t static_sample_scratch(void** out) {
+  static std::mutex mu;
+  static void* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sample_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = p;
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
 
 int sample_splits(int Vd) { return std::max(1, std::min(32, (Vd + 2047) / 2048)); }
 
