@@ -602,10 +602,10 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
     const void* x = static_cast<const uint8_t*>(target_hidden) + r0 * xrow;
     // ctx = RMSNorm_hidden(fc(x)); kv = W_ctx ctx
-    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr));
+    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr, true));
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, m->adt, ws.acc_fc, rows, m->D, m->hidden_norm_w, m->cfg.rms_norm_eps,
                                                1.f, nullptr, 0.f, ws.ctx, m->D));
-    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr, nullptr));
+    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr, nullptr, true));
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
     a.ld = 2LL * m->L * m->D;
@@ -667,9 +667,9 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, anchor_pos, bs, m->nh, ws.plan));
   // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(Lh, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
-  TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b));
+  TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.a_rows, D));
-  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(Lh, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr));
+  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(Lh, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, true));
   {
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
@@ -696,10 +696,10 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   }
   // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act));
-  TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr));
+  TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
                        ws.act, H));
-  TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b));
+  TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
   // 3. the DiT blocks
   const float eps_ln = m->cfg.layer_norm_eps, eps_qk = m->cfg.qk_norm_eps;
   fm::XattnArgs xa;
@@ -726,21 +726,21 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     const LayerW& lw = m->layers[l];
     const float* md = lw.mods;
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr));
+    TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
     TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bs, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
                                anchor_pos, ws.act));
-    TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr));
+    TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr));
+    TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
     xa.layer = l;
     xa.q_norm = lw.cqn;
     TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, adt, xa));
     TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
-    TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr));
+    TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b));
+    TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lh, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
-    TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, lw.fc2_beta));
+    TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, lw.fc2_beta, false));
   }
   // 4. final AdaLN
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, m->final_mods, m->final_mods + D, eps_ln, hidden_out));
@@ -773,7 +773,7 @@ flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void*
     z.add(reinterpret_cast<float*>(ws.counters), R);
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
   }
-  TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b));
+  TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b, true));
   TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::sample_rows(Lh, logits, R, m->Vd, m->K, temperature, greedy, seeds, anchor_pos,
                                                    static_cast<uint32_t>(step), m->hot, tokens_out, ws.keys,
                                                    ws.counters));
@@ -874,7 +874,7 @@ flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* 
   std::string err;
   if (check_weight_map(W, dtype, &err) != FLASHMAP_OK) return fail(FLASHMAP_E_CUDA, err);
   Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr, true};
-  FM_CUDA(fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr));
+  FM_CUDA(fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, false));
   return FLASHMAP_OK;
 }
 

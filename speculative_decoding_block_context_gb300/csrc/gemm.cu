@@ -59,7 +59,7 @@ template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                      float* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
-                     const float* __restrict__ beta, unsigned* dev_err) {
+                     const float* __restrict__ beta, int out_zeroed, unsigned* dev_err) {
   using C = TcCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[C::STAGES], empty_bar[C::STAGES], acc_full[2], acc_empty[2], drain_bar;
@@ -199,9 +199,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
       tc_fence_after();
       const int n = m * 128 + q * 32 + lane;
-      // A tile whose whole k range is in this segment has no other writer: plain
-      // read-modify-write; partial tiles are summed with atomics.
-      const bool whole = kb0 == 0 && seg_end == (tile + 1) * KB;
+      // No loads here (a load per chunk would stall the drain behind the next tile's
+      // MMAs): a tile whose whole k range is in this segment and whose output starts at
+      // zero is stored; everything else is added with fire-and-forget reductions.
+      const bool store = out_zeroed && kb0 == 0 && seg_end == (tile + 1) * KB;
       float a = 1.f, b = 0.f;
       if (n < N) {
         if (alpha) a = alpha[n];
@@ -217,8 +218,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (row0 + j < R) {
               float* o = out + static_cast<int64_t>(row0 + j) * ldo + n;
-              if (whole)
-                *o = LDCG(o) + fmaf(a, v[j], b);
+              if (store)
+                *o = fmaf(a, v[j], b);
               else
                 atomicAdd(o, fmaf(a, v[j], b));
             }
@@ -387,7 +388,7 @@ EncodeTiledFn encode_fn() {
 
 template <int BN>
 cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, float* out, int ldo,
-                      const float* alpha, const float* beta) {
+                      const float* alpha, const float* beta, bool zeroed) {
   using C = TcCfg<BN>;
   CUtensorMap mapX;
   std::string err;
@@ -396,7 +397,7 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   const int64_t T = mt * rt * KB;
   const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * C::PER_SM));
   return launch_k(L, tc_linear_kernel<BN>, dim3(G), dim3(kTcThreads), C::SMEM, W.map, mapX, out, ldo, R, W.N, W.K,
-                  alpha, beta, L.dev_err);
+                  alpha, beta, zeroed ? 1 : 0, L.dev_err);
 }
 
 template <int BN>
@@ -441,15 +442,15 @@ bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
 }
 
 cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta) {
+                   const float* alpha, const float* beta, bool zeroed) {
   if (rows <= 0 || W.N <= 0) return cudaSuccess;
   if (W.dtype == FLASHMAP_BF16) {
     if (!W.has_map) return cudaErrorInvalidValue;
-    if (rows <= 16) return launch_tc<16>(L, W, x, rows, ldx, out, ldo, alpha, beta);
-    if (rows <= 32) return launch_tc<32>(L, W, x, rows, ldx, out, ldo, alpha, beta);
-    if (rows <= 64) return launch_tc<64>(L, W, x, rows, ldx, out, ldo, alpha, beta);
-    if (rows <= 128) return launch_tc<128>(L, W, x, rows, ldx, out, ldo, alpha, beta);
-    return launch_tc<256>(L, W, x, rows, ldx, out, ldo, alpha, beta);
+    if (rows <= 16) return launch_tc<16>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    if (rows <= 32) return launch_tc<32>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    if (rows <= 64) return launch_tc<64>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    if (rows <= 128) return launch_tc<128>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    return launch_tc<256>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
   }
   if (W.dtype == FLASHMAP_F32) {
     const int64_t threads = static_cast<int64_t>(W.N) * 32;

@@ -70,10 +70,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
 cudaError_t gemm_prepare();
 
 // out[r * ldo + n] += alpha[n] * sum_k x[r * ldx + k] * W[n][k] + beta[n]   (r < rows, n < N)
-// accumulated with float atomics (the output must hold its initial value, e.g. 0, or
-// the residual stream). alpha / beta may be null (1 / 0). x has W.dtype.
+// accumulated with float reductions (the output must hold its initial value, e.g. 0,
+// or the residual stream); zeroed = the output is known to be zero, so tiles one CTA
+// covers entirely may be stored instead. alpha / beta may be null (1 / 0). x has W.dtype.
 cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta);
+                   const float* alpha, const float* beta, bool zeroed);
 
 // General strided SIMT GEMM for load-time work, float32 accumulation:
 // C(m, n) = sum_k A(m, k) B(k, n), A(m, k) = a[arow(m) * sam + k * sak] with

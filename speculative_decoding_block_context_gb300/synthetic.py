@@ -35,6 +35,12 @@ MODELS = {
                   head_dim=64, intermediate=704, cond_dim=96, time_embed_dim=64, block_size=16,
                   vocab_size=5000, draft_vocab_size=1234, page_size=16, rope_theta=1e6,
                   act_dtype="bf16", weight_dtype="bf16", max_position=4096),
+    # one DiT layer at the Qwen3-8B width with a small vocabulary: a case for profiling
+    # the cross-attention on ~1 GB of context without the full model's weights
+    "probe": dict(target_hidden=1024, num_target_layers=1, hidden=4096, num_layers=1, num_heads=32,
+                  head_dim=128, intermediate=1024, cond_dim=64, time_embed_dim=64, block_size=16,
+                  vocab_size=2048, draft_vocab_size=0, page_size=16, rope_theta=1e6,
+                  act_dtype="bf16", weight_dtype="bf16", max_position=8192),
     "qwen3_8b": dict(target_hidden=4096, num_target_layers=3, hidden=4096, num_layers=5,
                      num_heads=32, head_dim=128, intermediate=12288, cond_dim=256,
                      time_embed_dim=256, block_size=16, vocab_size=151936,
@@ -54,6 +60,8 @@ WORKLOADS = {
                       temps=("greedy",), full_scatter=False, seed=0),
     "small_bf16": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
                        window=True, temps=("mix", 0.5, 1.2), full_scatter=True, seed=11),
+    "attn_probe": dict(model="probe", bs=16, ctx=("fixed", 4096), prefill=False, window=False,
+                       temps=("greedy",), full_scatter=False, seed=6),
     "qwen3_8b_bs1": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
                          temps=("all", 1.0), full_scatter=False, seed=2),
     "qwen3_8b_bs32": dict(model="qwen3_8b", bs=32, ctx=("uniform", 512, 8192), prefill=False,
