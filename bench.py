@@ -196,6 +196,21 @@ def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: i
             "launches_per_step_total": len(recs) // steps}
 
 
+def world_max(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest rank's step time); identity at N=1."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step: int, world: int, ms_max: float) -> float:
+    """Whole-job drafted tokens/s: every rank drafts its own batch (requests are
+    sharded across ranks, weak scaling) and the job takes the slowest rank's time."""
+    return tokens_per_rank_step * world / (ms_max * 1e-3)
+
+
 def our_arm(args, rank: int, world: int) -> dict:
     device = f"cuda:{int(os.environ.get('LOCAL_RANK', '0'))}"
     torch.cuda.set_device(device)
@@ -236,14 +251,10 @@ def our_arm(args, rank: int, world: int) -> dict:
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-    ms = t_ev0.elapsed_time(t_ev1) / args.steps
-    ms_t = torch.tensor([ms], device=device)
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(ms_t.item())
+    ms = world_max(t_ev0.elapsed_time(t_ev1) / args.steps, world, device)
     clocks = sampler.stop(t0, t1)
     tokens_per_step = bs * K * world
-    value = tokens_per_step / (ms * 1e-3)
+    value = job_throughput(bs * K, world, ms)
 
     # end to end through the public API with host buffers: pinned inputs copied in,
     # the step, the sampled token ids copied out, every step
@@ -267,11 +278,7 @@ def our_arm(args, rank: int, world: int) -> dict:
             tok_host.copy_(st["tokens"], non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    e2e_t = torch.tensor([e2e_ms], device=device)
-    if world > 1:
-        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(e2e_t.item())
+    e2e_ms = world_max(e0.elapsed_time(e1) / args.steps, world, device)
 
     roof = gemm_roofline(st, stream, hbm_peak)
     ab = algorithmic_bytes(cfg, req)
@@ -301,7 +308,7 @@ def our_arm(args, rank: int, world: int) -> dict:
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, st, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
     return line
 
 
@@ -344,10 +351,11 @@ def oracle_step(ref, ocfg, Wnp, Enp, C, req, b: int, ctx_kv, window_hidden) -> N
                     p + 1 + np.arange(K), req["step"], C.hot)
 
 
-def time_oracle(workload: str, device: str, n_steps: int, gen_model=None, req=None):
-    """Times n_steps oracle steps, each one request of the workload (requests are
-    independent; a step of bs requests costs bs times one). Returns seconds per
-    request-step and the sample description."""
+def time_oracle(workload: str, device: str, n_steps: int, budget_s: float = 90.0, warmup: int = 1,
+                gen_model=None, req=None):
+    """Times up to n_steps oracle steps (stopping once budget_s is spent, at least one),
+    each one request of the workload: requests are independent, so a step of bs
+    requests costs bs of these. Returns (seconds per request-step, steps timed)."""
     from oracle import flashmap_ref as ref
 
     ocfg, Wnp, Enp, C = oracle_setup(workload, device, gen_model)
@@ -355,7 +363,8 @@ def time_oracle(workload: str, device: str, n_steps: int, gen_model=None, req=No
     rng = np.random.default_rng(0)
     L, nh, hd = ocfg.num_layers, ocfg.num_heads, ocfg.head_dim
     times = []
-    for i in range(n_steps):
+    spent = 0.0
+    for i in range(warmup + n_steps):
         b = i % req["bs"]
         n = req["ctx"][b]
         # context keys/values of positions 0..ctx-1 (their values do not change the work)
@@ -364,8 +373,13 @@ def time_oracle(workload: str, device: str, n_steps: int, gen_model=None, req=No
         wh = req["window_hidden"][b].float().cpu().numpy() if req["window"] else None
         t0 = time.perf_counter()
         oracle_step(ref, ocfg, Wnp, Enp, C, req, b, (kc, vc), wh)
-        times.append(time.perf_counter() - t0)
-    return float(np.mean(times)), req
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dt)
+            spent += dt
+            if spent > budget_s:
+                break
+    return float(np.mean(times)), len(times)
 
 
 def cores_used() -> int:
@@ -375,65 +389,30 @@ def cores_used() -> int:
         return os.cpu_count() or 1
 
 
-def cpu_baseline(workload: str, st: dict | None, budget_s: float = 30.0) -> dict:
-    cfg = syn.model_config(workload)
-    K = cfg["block_size"]
-    n = 2
-    sec, req = time_oracle(workload, "cuda", n)
+def cpu_baseline(workload: str, budget_s: float = 30.0) -> dict:
+    K = syn.model_config(workload)["block_size"]
+    sec, n = time_oracle(workload, "cuda", 3, budget_s=budget_s)
     return {"value": round(K / sec, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
             "sample": f"{n} request-steps of {workload} (window write + anchor + draft + head + sampling of one "
-                      f"request, {K} tokens each) on the NumPy float64 oracle; {sec:.2f} s per request-step; "
-                      f"load-time constants untimed, E^T E factor replaced by the identity for timing"}
+                      f"request, {K} tokens each) on the NumPy float64 oracle, {sec:.2f} s each; load-time "
+                      f"constants untimed, the E^T E factor replaced by the identity for timing"}
 
 
 def reference_arm(args) -> dict:
-    cfg = syn.model_config(args.workload)
-    K = cfg["block_size"]
-    n = max(1, args.steps)
-    for _ in range(args.warmup and 1):
-        pass
-    sec, req = time_oracle(args.workload, "cuda" if torch.cuda.is_available() else "cpu", n)
+    K = syn.model_config(args.workload)["block_size"]
+    sec, n = time_oracle(args.workload, "cuda" if torch.cuda.is_available() else "cpu", max(1, args.steps),
+                         budget_s=90.0, warmup=min(args.warmup, 1))
     value = K / sec
-    sample = (f"{n} request-steps of {args.workload} on the NumPy float64 oracle (one request's window write, "
-              f"anchor, draft, head and sampling per step; requests are independent, so a batch costs bs steps)")
-    return {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0, "steps": n, "warmup": args.warmup,
-            "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "impl": "reference",
-            "dtype": "f64", "data": "synthetic", "config": {"workload": args.workload},
+    sample = (f"{n} request-steps of {args.workload} on the NumPy float64 oracle, each one request's window "
+              f"write, anchor row, draft, head and sampling ({K} tokens); requests are independent, so a batch "
+              f"costs bs request-steps; stopped after 90 s of timed work")
+    return {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 0, "steps": n,
+            "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+            "higher_is_better": True, "impl": "reference", "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-
-
-def kernel_case(args) -> dict:
-    """One tcgen05 GEMM timed alone over --steps launches: "gemm" is the batch-1 shape
-    (16 activation rows x the all-layer context K/V weight, 40960 x 4096 bf16 = 335 MB,
-    above L2; HBM-bound), "gemm2048" the batch-128 MLP shape (2048 rows x 12288 x 4096;
-    tensor-bound)."""
-    from speculative_decoding_block_context_gb300 import _lib as F
-
-    hbm_peak, tf_peak, src = load_peaks()
-    rows, n, k = (16, 40960, 4096) if args.kernel_case == "gemm" else (2048, 12288, 4096)
-    g = torch.Generator(device="cuda").manual_seed(0)
-    x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
-    w = (torch.randn((n, k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
-    out = torch.zeros((rows, n), dtype=torch.float32, device="cuda")
-    for _ in range(max(args.warmup, 3)):
-        F.flashmap_debug_linear(F.BF16, x, w, out)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        F.flashmap_debug_linear(F.BF16, x, w, out)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    byts = n * k * 2 + rows * k * 2 + rows * n * 4
-    flops = 2.0 * rows * n * k
-    return {"kernel_case": args.kernel_case, "shape": [rows, n, k], "us_per_launch": round(ms * 1e3, 2),
-            "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm_peak, "peak_source": src,
-            "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4),
-            "achieved_tflops": round(flops / (ms * 1e-3) / 1e12, 1), "peak_tflops": tf_peak,
-            "frac_tensor": round(flops / (ms * 1e-3) / 1e12 / tf_peak, 4)}
 
 
 def main() -> int:
