@@ -415,6 +415,38 @@ def reference_arm(args) -> dict:
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def kernel_case(args) -> dict:
+    """One tcgen05 GEMM timed alone over --steps launches: "gemm" is the batch-1 shape
+    (16 activation rows x the all-layer context K/V weight, 40960 x 4096 bf16 = 335 MB,
+    above L2; HBM-bound), "gemm2048" the batch-128 MLP shape (2048 rows x 12288 x 4096;
+    tensor-bound)."""
+    from speculative_decoding_block_context_gb300 import _lib as F
+
+    hbm_peak, tf_peak, src = load_peaks()
+    rows, n, k = (16, 40960, 4096) if args.kernel_case == "gemm" else (2048, 12288, 4096)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((n, k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    out = torch.zeros((rows, n), dtype=torch.float32, device="cuda")
+    for _ in range(max(args.warmup, 3)):
+        F.flashmap_debug_linear(F.BF16, x, w, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        F.flashmap_debug_linear(F.BF16, x, w, out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    byts = n * k * 2 + rows * k * 2 + rows * n * 4
+    flops = 2.0 * rows * n * k
+    return {"kernel_case": args.kernel_case, "shape": [rows, n, k], "us_per_launch": round(ms * 1e3, 2),
+            "achieved_gbs": round(byts / (ms * 1e-3) / 1e9, 1), "peak_gbs": hbm_peak, "peak_source": src,
+            "frac_hbm": round(byts / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "achieved_tflops": round(flops / (ms * 1e-3) / 1e12, 1), "peak_tflops": tf_peak,
+            "frac_tensor": round(flops / (ms * 1e-3) / 1e12 / tf_peak, 4)}
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
