@@ -41,7 +41,10 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   const int D = nh * HD;
   const int k = warp;  // one warp per slot
   const int row = b * K + k;
-  int pos = LDCG(anchor_pos + b) + 1 + k;
+  __shared__ int s_anchor;
+  if (threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);  // once per CTA
+  __syncthreads();
+  int pos = s_anchor + 1 + k;
   if (pos < 0 || pos >= max_pos) {
     if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
     pos = 0;
@@ -528,12 +531,15 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(HD) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
   __shared__ float sw[kMaxChunksPerRequest];
   __shared__ float red[32];
+  __shared__ int s_g[2];
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
-  const int* first = a.plan + 3;
-  const int g0 = LDCG(first + b), nc = min(LDCG(first + b + 1) - g0, kMaxChunksPerRequest);
+  // the request's chunk range, loaded once per CTA
+  if (d < 2) s_g[d] = LDCG(a.plan + 3 + b + d);
+  __syncthreads();
+  const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
   float mloc = -INFINITY;
   for (int c = d; c < nc; c += HD) {
     const float m = LDCG(a.part_ml + ((static_cast<int64_t>(g0 + c)) * nh + h) * 32 + 2 * qi);

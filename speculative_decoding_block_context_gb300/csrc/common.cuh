@@ -92,8 +92,8 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // (2i, 2i+1) by angle row `rope` (cos, sin per pair), if given
 // (flashmap/modeling_flashmap.py, FlashMapRMSNorm and apply_rope).
 template <int EPL>
-__device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __restrict__ w, float eps,
-                                               const float2* __restrict__ rope, int lane) {
+__device__ __forceinline__ void head_norm_rope_w(float (&v)[EPL], const float (&w)[EPL], float eps,
+                                                 const float2* __restrict__ rope, int lane) {
   constexpr int HD = EPL * 32;
   float ss = 0.f;
 #pragma unroll
@@ -101,7 +101,7 @@ __device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __r
   ss = warp_sum(ss);
   const float r = rsqrtf(ss * (1.f / HD) + eps);
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) v[e] *= r * w[lane * EPL + e];
+  for (int e = 0; e < EPL; ++e) v[e] *= r * w[e];
   if (rope == nullptr) return;
   if constexpr (EPL >= 2) {
 #pragma unroll
@@ -116,6 +116,16 @@ __device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __r
     const float2 cs = rope[lane >> 1];
     v[0] = (lane & 1) ? (v[0] * cs.x + other * cs.y) : (v[0] * cs.x - other * cs.y);
   }
+}
+
+// The same with the norm weight read from memory (channels lane*EPL..).
+template <int EPL>
+__device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __restrict__ w, float eps,
+                                               const float2* __restrict__ rope, int lane) {
+  float wr[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) wr[e] = w[lane * EPL + e];
+  head_norm_rope_w<EPL>(v, wr, eps, rope, lane);
 }
 
 // ------------------------------------------------------------------ shared memory / mbarrier

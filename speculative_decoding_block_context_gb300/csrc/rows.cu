@@ -2,9 +2,11 @@
 // (context, anchor, noise embedding), GELU, the seeded draft noise, per-head q/k
 // RMSNorm + interleaved RoPE, and the paged context-KV write. Every kernel that
 // reads a GEMM's float32 accumulator also clears it, so the next GEMM into the same
-// buffer starts from zero.
+// buffer starts from zero; the KV write is the exception (its accumulator is zeroed
+// by the caller before each all-layer KV GEMM).
 
 #include <algorithm>
+#include <climits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -31,6 +33,21 @@ __device__ __forceinline__ void load_clear_head(float* src, float (&v)[EPL], int
   }
 }
 
+// Loads the EPL channels lane*EPL.. of one head vector (L2, no clearing).
+template <int EPL>
+__device__ __forceinline__ void load_head(const float* src, float (&v)[EPL], int lane) {
+  const float* p = src + lane * EPL;
+  if constexpr (EPL == 4) {
+    const float4 t = LDCG(reinterpret_cast<const float4*>(p));
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else if constexpr (EPL == 2) {
+    const float2 t = LDCG(reinterpret_cast<const float2*>(p));
+    v[0] = t.x, v[1] = t.y;
+  } else {
+    v[0] = LDCG(p);
+  }
+}
+
 template <typename T, int N>
 __device__ __forceinline__ void store_vec(T* dst, const float* v) {
   if constexpr (sizeof(T) == 2 && N == 4) {
@@ -49,53 +66,75 @@ __device__ __forceinline__ void store_vec(T* dst, const float* v) {
 
 // ------------------------------------------------------------------ context-KV write
 
-// One CTA per (row, layer), one warp per head: the key and value of a head are read
-// in a single vector load per lane, the key k-normed and rotated, both stored.
+// One CTA per (row, layer), one warp per head. Thread 0 resolves the row's slot (the
+// request's start position, commit length, page-table row and page: four dependent
+// loads of per-request scalars) and hands it to the CTA through shared memory, while
+// every warp already streams its head's key and value from the accumulator. Loading
+// the scalars once per CTA instead of once per warp keeps thousands of CTAs from
+// queueing on the same few L2 sectors. The accumulator is left as it is: the caller
+// zeroes it before the GEMM that fills it.
 template <typename T, int EPL>
-__global__ void __launch_bounds__(1024) kv_write_kernel(KvWriteArgs a) {
+__global__ void __launch_bounds__(1024, 2) kv_write_kernel(KvWriteArgs a) {
   constexpr int HD = EPL * 32;
+  __shared__ int64_t s_slot;
+  __shared__ int s_pos;
   pdl_trigger();
   pdl_wait();
   const int il = blockIdx.x, l = blockIdx.y;
   const int64_t i = a.row0 + il;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int b = static_cast<int>(i / a.W), c = static_cast<int>(i - static_cast<int64_t>(b) * a.W);
-  const int pos = LDCG(a.start_pos + b) + c;
-  bool write = a.commit_lens == nullptr || c < LDCG(a.commit_lens + b);
-  int64_t slot = -1;
-  if (write) {
+  const int D = a.nh * HD;
+  const float* row = a.acc + static_cast<int64_t>(il) * a.ld + static_cast<int64_t>(l) * 2 * D;
+  // this warp's first head, loaded before the slot is known
+  float k[EPL], v[EPL], kw[EPL];
+  if (warp < a.nh) {
+    load_head<EPL>(row + warp * HD, k, lane);
+    load_head<EPL>(row + D + warp * HD, v, lane);
+  }
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) kw[e] = a.k_norm[static_cast<int64_t>(l) * HD + lane * EPL + e];
+  if (threadIdx.x == 0) {
+    const int b = static_cast<int>(i / a.W), c = static_cast<int>(i - static_cast<int64_t>(b) * a.W);
+    // the three per-request scalars in one round trip, then the page
+    const int start = LDCG(a.start_pos + b);
+    const int clen = a.commit_lens ? LDCG(a.commit_lens + b) : INT_MAX;
     const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
-    const int pi = pos >= 0 ? pos / a.P : -1;
-    if (pos < 0 || pos >= a.max_pos || pi >= a.r2p_stride || rrow < 0) {
-      if (threadIdx.x == 0 && l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
-      write = false;
-    } else {
-      const int page = LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi);
-      if (page < 0 || page >= a.num_pages) {
-        if (threadIdx.x == 0 && l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
-        write = false;
+    const int pos = start + c;
+    int64_t slot = -1;
+    if (c < clen) {
+      const int pi = pos >= 0 ? pos / a.P : -1;
+      if (pos < 0 || pos >= a.max_pos || pi >= a.r2p_stride || rrow < 0) {
+        if (l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
       } else {
-        slot = static_cast<int64_t>(page) * a.P + (pos - pi * a.P);
+        const int page = LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi);
+        if (page < 0 || page >= a.num_pages) {
+          if (l == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
+        } else {
+          slot = static_cast<int64_t>(page) * a.P + (pos - pi * a.P);
+        }
       }
     }
+    if (a.out_loc && l == 0) a.out_loc[i] = slot;
+    s_slot = slot;
+    s_pos = pos;
   }
-  if (a.out_loc && l == 0 && threadIdx.x == 0) a.out_loc[i] = write ? slot : -1;
-  const int D = a.nh * HD;
-  float* row = a.acc + static_cast<int64_t>(il) * a.ld + static_cast<int64_t>(l) * 2 * D;
-  const float* kw = a.k_norm + static_cast<int64_t>(l) * HD;
-  const float2* rope = write ? a.rope + static_cast<int64_t>(pos) * (HD / 2) : nullptr;
+  __syncthreads();
+  const int64_t slot = s_slot;
+  if (slot < 0) return;
+  const float2* rope = a.rope + static_cast<int64_t>(s_pos) * (HD / 2);
   T* pool = static_cast<T*>(a.pool);
-  const int64_t page = write ? slot / a.P : 0, off = write ? slot - page * a.P : 0;
+  const int64_t page = slot / a.P, off = slot - page * a.P;
+  const int64_t kv_stride = a.num_pages * a.nh * a.P;  // pool rows between a layer's keys and values
+  const int64_t kbase = (static_cast<int64_t>(l) * 2 * a.num_pages + page) * a.nh * a.P + off;
   for (int h = warp; h < a.nh; h += nw) {
-    float k[EPL], v[EPL];
-    load_clear_head<EPL>(row + h * HD, k, lane);
-    load_clear_head<EPL>(row + D + h * HD, v, lane);
-    if (!write) continue;
-    head_norm_rope<EPL>(k, kw, a.eps, rope, lane);
-    const int64_t kbase = (((static_cast<int64_t>(l) * 2 + 0) * a.num_pages + page) * a.nh + h) * a.P;
-    const int64_t vbase = (((static_cast<int64_t>(l) * 2 + 1) * a.num_pages + page) * a.nh + h) * a.P;
-    store_vec<T, EPL>(pool + (kbase + off) * HD + lane * EPL, k);
-    store_vec<T, EPL>(pool + (vbase + off) * HD + lane * EPL, v);
+    if (h != warp) {  // more heads than warps
+      load_head<EPL>(row + h * HD, k, lane);
+      load_head<EPL>(row + D + h * HD, v, lane);
+    }
+    head_norm_rope_w<EPL>(k, kw, a.eps, rope, lane);
+    const int64_t r = kbase + static_cast<int64_t>(h) * a.P;
+    store_vec<T, EPL>(pool + r * HD + lane * EPL, k);
+    store_vec<T, EPL>(pool + (r + kv_stride) * HD + lane * EPL, v);
   }
 }
 

@@ -28,6 +28,7 @@ __device__ __forceinline__ uint32_t orderable(float v) {
 // one 64-bit atomicMax on (orderable(value) << 32 | ~index), so larger values win and
 // equal values go to the lowest index. The CTA that finishes a row last (a counter,
 // no waiting) writes the token and clears the row's key and counter for the next call.
+template <bool kVec>
 __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ logits, int Vd, int K,
                                                      const float* __restrict__ temps,
                                                      const uint8_t* __restrict__ greedy,
@@ -37,29 +38,53 @@ __global__ void __launch_bounds__(256) sample_kernel(const float* __restrict__ l
                                                      unsigned long long* keys, unsigned* counters) {
   __shared__ float rv[32];
   __shared__ int rj[32];
+  __shared__ float s_T;
+  __shared__ int s_pos, s_greedy;
+  __shared__ uint64_t s_seed;
   pdl_trigger();
   pdl_wait();
   const int row = blockIdx.x, b = row / K, k = row - b * K;
   const int splits = gridDim.y, sp = blockIdx.y;
-  const float T = LDCG(temps + b);
-  const bool argmax_only = LDCG(greedy + b) != 0 || !(T > 0.f);
-  const uint64_t seed = LDCG(seeds + b);
-  const uint32_t pos = static_cast<uint32_t>(LDCG(anchor_pos + b) + 1 + k);
+  // the request's scalars, loaded once per CTA (every CTA of a request reads the same
+  // few bytes; per-warp loads would queue on one L2 sector)
+  if (threadIdx.x == 0) {
+    s_T = LDCG(temps + b);
+    s_greedy = LDCG(greedy + b);
+    s_seed = LDCG(seeds + b);
+    s_pos = LDCG(anchor_pos + b);
+  }
   const float* lr = logits + static_cast<int64_t>(row) * Vd;
-  float bv = -INFINITY;
-  int bj = INT_MAX;
   const int n4 = (Vd + 3) >> 2;
   const int j4_0 = static_cast<int>(static_cast<int64_t>(n4) * sp / splits);
   const int j4_1 = static_cast<int>(static_cast<int64_t>(n4) * (sp + 1) / splits);
+  // kVec: every row starts 16-byte aligned and holds whole float4 groups
+  float4 lv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (kVec && j4_0 + static_cast<int>(threadIdx.x) < j4_1)
+    lv = LDCG(reinterpret_cast<const float4*>(lr) + j4_0 + threadIdx.x);
+  __syncthreads();
+  const float T = s_T;
+  const bool argmax_only = s_greedy != 0 || !(T > 0.f);
+  const uint64_t seed = s_seed;
+  const uint32_t pos = static_cast<uint32_t>(s_pos + 1 + k);
+  float bv = -INFINITY;
+  int bj = INT_MAX;
   for (int j4 = j4_0 + threadIdx.x; j4 < j4_1; j4 += blockDim.x) {
+    float ls[4];
+    if constexpr (kVec) {
+      ls[0] = lv.x, ls[1] = lv.y, ls[2] = lv.z, ls[3] = lv.w;
+      if (j4 + static_cast<int>(blockDim.x) < j4_1) lv = LDCG(reinterpret_cast<const float4*>(lr) + j4 + blockDim.x);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ls[e] = 4 * j4 + e < Vd ? LDCG(lr + 4 * j4 + e) : -INFINITY;
+    }
     uint4 w = make_uint4(0, 0, 0, 0);
     if (!argmax_only) w = philox_seeded(seed, static_cast<uint32_t>(j4), pos, kDomainGumbel, step);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = 4 * j4 + e;
-      if (j >= Vd) break;
-      const float l = LDCG(lr + j);
+      if (!kVec && j >= Vd) break;
+      const float l = ls[e];
       const float v = argmax_only ? l : __fdiv_rn(l, T) + gumbel_of_word(ws[e]);
       if (better(v, j, bv, bj)) {
         bv = v;
@@ -157,8 +182,9 @@ cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, 
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
                         const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters) {
   if (rows <= 0) return cudaSuccess;
-  return launch_k(L, sample_kernel, dim3(rows, sample_splits(Vd)), dim3(256), 0, logits, Vd, K, temps, greedy, seeds,
-                  anchor_pos, step, hot, tokens, keys, counters);
+  const bool vec = Vd % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  return launch_k(L, vec ? sample_kernel<true> : sample_kernel<false>, dim3(rows, sample_splits(Vd)), dim3(256), 0,
+                  logits, Vd, K, temps, greedy, seeds, anchor_pos, step, hot, tokens, keys, counters);
 }
 
 cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
