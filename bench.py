@@ -100,16 +100,19 @@ class ClockSampler:
 
 
 def algorithmic_bytes(cfg: dict, req: dict) -> dict:
-    """Bytes the step must move (bf16 storage): every weight once, the context K/V of
-    positions 0..p of every request, the window and anchor rows written, the logits."""
+    """Bytes the step must move: every weight once (bf16, or e4m3 plus one float32
+    scale per output channel), the context K/V of positions 0..p of every request, the
+    window and anchor rows written, the logits."""
     H, Lt, D, L, F, Vd, V, K = (cfg[k] for k in ("target_hidden", "num_target_layers", "hidden", "num_layers",
                                                  "intermediate", "draft_vocab_size", "vocab_size", "block_size"))
     es = 4 if cfg["act_dtype"] == "f32" else 2
+    wes = 1 if cfg.get("weight_dtype") == "e4m3" else es  # e4m3 weights: one byte (+ a scale per row)
     Vd = Vd if 0 < Vd < V else V
     bs = req["bs"]
-    w_write = (D * Lt * H + 2 * L * D * D) * es if req["window"] else 0
-    w_draft = (D * H + 2 * L * D * D + H * H + D * H + L * (6 * D * D + 2 * D * F)) * es
-    w_head = Vd * D * es
+    w_write = ((D * Lt * H + 2 * L * D * D) * wes + (D + 2 * L * D) * 4 * (wes == 1)) if req["window"] else 0
+    w_draft = ((D * H + 2 * L * D * D + D * H + L * (6 * D * D + 2 * D * F)) * wes + H * H * es
+               + (D + 2 * L * D + D + L * (6 * D + D + F)) * 4 * (wes == 1))
+    w_head = Vd * D * wes + Vd * 4 * (wes == 1)
     kv_row = L * 2 * D * es
     kv_read = sum((p + 1) * kv_row for p in req["anchor_pos"])
     rows_written = (sum(req["commit"]) if req["window"] else 0) + bs

@@ -77,10 +77,17 @@ typedef enum { FLASHMAP_F32 = 0, FLASHMAP_BF16 = 1, FLASHMAP_E4M3 = 2 } flashmap
  *   max_position         positions are < max_position (sizes the RoPE table)
  *   rope_theta, rms_norm_eps, qk_norm_eps, layer_norm_eps   as in FlashMapConfig
  *   act_dtype            F32 or BF16: activations, raw weights and the KV pool
- *   weight_dtype         act_dtype, or E4M3 (bf16 activations only): the large GEMM
- *                        weights are quantized at load to e4m3 with one float32
- *                        scale per output channel (flashmap/sglang/model.py,
- *                        _quantize_fp8); activations stay bf16 (W8A16).
+ *   weight_dtype         act_dtype, or E4M3 (bf16 activations only): at load, every
+ *                        large GEMM weight (fc, anchor_proj, x_embed, the all-layer
+ *                        context K/V, each block's q/k/v, o, cross q and o, fc1, fc2,
+ *                        and the folded head after folding) is quantized to e4m3fn
+ *                        with one float32 scale per output channel, scale = max|w|/448
+ *                        (1 for an all-zero row), q = w / scale rounded to nearest
+ *                        even and saturated (flashmap/sglang/model.py, _quantize_fp8).
+ *                        The noise factor L stays bf16. Activations stay bf16 and
+ *                        accumulation float32 (W8A16): the GEMM expands each e4m3 tile
+ *                        to bf16 on chip and applies the scale to its output. Needs
+ *                        target_hidden, hidden and intermediate multiples of 16.
  */
 typedef struct {
   int32_t target_hidden, num_target_layers, hidden, num_layers, num_heads, head_dim;
@@ -318,7 +325,10 @@ flashmap_status flashmap_debug_philox(const uint64_t* seeds, const uint32_t* ctr
 
 /* out[r][n] += sum_k x[r][k] w[n][k] for r < rows, n < out_features, through the same
  * GEMM the draft uses for dtype (F32: SIMT; BF16: tcgen05). x (device) [rows][in]
- * and w (device) [out][in] in dtype; out (device) float32 [rows][out_features]. */
+ * and w (device) [out][in] in dtype; out (device) float32 [rows][out_features].
+ * dtype E4M3: x and w are bf16; w is first quantized per output channel exactly as
+ * flashmap_load_weights does for E4M3 weights, and the e4m3 tcgen05 GEMM computes
+ * out += x (q * scale)^T (stream-ordered temporary allocation for q and scale). */
 flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* w, int32_t rows,
                                       int32_t in_features, int32_t out_features, float* out,
                                       flashmap_stream stream);

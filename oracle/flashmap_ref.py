@@ -604,3 +604,37 @@ def quantize_e4m3_per_channel(w) -> tuple[np.ndarray, np.ndarray]:
 
 def dequantize(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return _f64(q) * _f64(scale)[:, None]
+
+
+def e4m3_linear_names(cfg: Config) -> list:
+    """flashmap/sglang/model.py, _quantize_fp8: the weights with e4m3 copies, by their
+    module names: x_embed, fc, anchor_proj, every block's self q/k/v (the fused qkv)
+    and o, cross q and o, the cross k/v (the all-layer context K/V weight), fc1 and
+    fc2. The folded head is quantized too (e4m3_constants); the noise factor L, the
+    norms and the AdaLN weights stay in the activation dtype."""
+    names = ["x_embed.weight", "fc.weight", "anchor_proj.weight"]
+    for l in range(cfg.num_layers):
+        p = f"layers.{l}"
+        names += [f"{p}.self_attn.{x}_proj.weight" for x in ("q", "k", "v", "o")]
+        names += [f"{p}.cross_attn.{x}_proj.weight" for x in ("q", "k", "v", "o")]
+        names += [f"{p}.mlp.fc1.weight", f"{p}.mlp.fc2.weight"]
+    return names
+
+
+def e4m3_weights(cfg: Config, W: dict) -> dict:
+    """The weights an e4m3 drafter computes with: each quantized weight replaced by
+    its dequantized copy q * scale (per output channel). Quantizing q, k and v (or
+    each layer's cross k and v) separately equals quantizing their row concatenation,
+    as the scales are per row."""
+    out = dict(W)
+    for name in e4m3_linear_names(cfg):
+        out[name] = dequantize(*quantize_e4m3_per_channel(W[name]))
+    return out
+
+
+def e4m3_constants(consts: Constants) -> Constants:
+    """The folded head of an e4m3 drafter: W_f quantized per output channel after
+    folding (flashmap/sglang/model.py, _quantize_fp8, "head": the folded head)."""
+    from dataclasses import replace
+
+    return replace(consts, head_w=dequantize(*quantize_e4m3_per_channel(consts.head_w)))

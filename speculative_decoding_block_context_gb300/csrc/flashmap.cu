@@ -142,11 +142,10 @@ flashmap_status validate(const flashmap_config* c) {
   if (c->time_embed_dim % 2) return fail(FLASHMAP_E_INVALID, "time_embed_dim must be even");
   if (c->cond_dim > 8192 || c->time_embed_dim > 8192) return fail(FLASHMAP_E_UNSUPPORTED, "cond_dim too large");
   if (!is_act(c->act_dtype)) return fail(FLASHMAP_E_INVALID, "act_dtype must be F32 or BF16");
-  if (c->weight_dtype != c->act_dtype) {
-    if (c->weight_dtype == FLASHMAP_E4M3 && c->act_dtype == FLASHMAP_BF16)
-      return fail(FLASHMAP_E_UNSUPPORTED, "E4M3 weights are not built yet");
+  if (c->weight_dtype != c->act_dtype && !(c->weight_dtype == FLASHMAP_E4M3 && c->act_dtype == FLASHMAP_BF16))
     return fail(FLASHMAP_E_INVALID, "weight_dtype must equal act_dtype (or E4M3 with BF16 activations)");
-  }
+  if (c->weight_dtype == FLASHMAP_E4M3 && (c->target_hidden % 16 || c->hidden % 16 || c->intermediate % 16))
+    return fail(FLASHMAP_E_UNSUPPORTED, "E4M3 weights need target_hidden, hidden and intermediate multiples of 16");
   {
     const int a[] = {c->target_hidden, c->hidden, c->intermediate};
     for (int d : a)
@@ -255,6 +254,9 @@ flashmap_status check_weight_map(Weight& w, int dtype, std::string* err) {
   if (dtype == FLASHMAP_BF16) {
     if (!fm::make_tmap_bf16(&w.map, w.ptr, w.N, w.K, w.K, 128, err)) return FLASHMAP_E_CUDA;
     w.has_map = true;
+  } else if (dtype == FLASHMAP_E4M3) {
+    if (!fm::make_tmap_e4m3(&w.map, w.ptr, w.N, w.K, err)) return FLASHMAP_E_CUDA;
+    w.has_map = true;
   }
   return FLASHMAP_OK;
 }
@@ -344,25 +346,32 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return cleanup(fail(FLASHMAP_E_CUDA, "no CUDA device"));
   const int adt = m->adt;
+  const bool e4m3 = m->wdt == FLASHMAP_E4M3;
   const size_t es = dt_size(adt);
   const int64_t H = m->H, D = m->D, L = m->L, F = m->F, Vd = m->Vd, V = m->V, hd = m->hd, C = cfg->cond_dim;
 
-  // ---- arena layout
+  // ---- arena layout. With e4m3 weights every large GEMM weight (all but the noise
+  // factor L) is stored as e4m3 plus one float32 scale per output channel
+  // (flashmap/sglang/model.py, _quantize_fp8).
   auto layout = [&](Carver& c) {
-    m->fc.ptr = c.take<void>(D * m->Lt * H * es);
-    m->ap.ptr = c.take<void>(D * H * es);
-    m->ctx_kv.ptr = c.take<void>(2 * L * D * D * es);
+    auto big = [&](Weight& W, int64_t rows, int64_t cols) {
+      W.ptr = c.take<void>(rows * cols * (e4m3 ? 1 : es));
+      W.wscale = e4m3 ? c.take<float>(rows * 4) : nullptr;
+    };
+    big(m->fc, D, m->Lt * H);
+    big(m->ap, D, H);
+    big(m->ctx_kv, 2 * L * D, D);
     m->chol.ptr = c.take<void>(H * H * es);
-    m->xe.ptr = c.take<void>(D * H * es);
-    m->head.ptr = c.take<void>(Vd * D * es);
+    big(m->xe, D, H);
+    big(m->head, Vd, D);
     m->layers.resize(L);
     for (auto& lw : m->layers) {
-      lw.qkv.ptr = c.take<void>(3 * D * D * es);
-      lw.o.ptr = c.take<void>(D * D * es);
-      lw.cq.ptr = c.take<void>(D * D * es);
-      lw.co.ptr = c.take<void>(D * D * es);
-      lw.fc1.ptr = c.take<void>(F * D * es);
-      lw.fc2.ptr = c.take<void>(D * F * es);
+      big(lw.qkv, 3 * D, D);
+      big(lw.o, D, D);
+      big(lw.cq, D, D);
+      big(lw.co, D, D);
+      big(lw.fc1, F, D);
+      big(lw.fc2, D, F);
       lw.qn = c.take<float>(hd * 4);
       lw.kn = c.take<float>(hd * 4);
       lw.cqn = c.take<float>(hd * 4);
@@ -410,6 +419,24 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   double* colsum = sc.take<double>(H * 8);
   double* cond = sc.take<double>(C * 8);
   float* tmp_d = sc.take<float>(std::max(D, H) * 4);  // D or H floats of scratch
+  // e4m3: each weight is assembled in act_dtype (the folded head in float32) in one
+  // staging buffer, then quantized into the arena; stream order serializes the reuse.
+  void* stage = nullptr;
+  if (e4m3) {
+    const size_t stage_bytes = std::max({static_cast<size_t>(D * m->Lt * H) * es, static_cast<size_t>(2 * L * D * D) * es,
+                                         static_cast<size_t>(3 * D * D) * es, static_cast<size_t>(F * D) * es,
+                                         static_cast<size_t>(D * H) * es, static_cast<size_t>(Vd * D) * 4});
+    if (cudaMalloc(&stage, stage_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return cleanup(fail(FLASHMAP_E_NOMEM, "cannot allocate the e4m3 staging buffer"));
+    }
+  }
+  struct StageGuard {
+    void* p;
+    ~StageGuard() {
+      if (p) cudaFree(p);
+    }
+  } stage_guard{stage};
 
 #define LCHK(call)                                                                                  \
   do {                                                                                              \
@@ -422,25 +449,47 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   LCHK(cudaMemsetAsync(m->dev_err, 0, 4, s));
   auto copy = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto bytes_of = [&](int64_t rows, int64_t cols) { return static_cast<size_t>(rows) * cols * es; };
-  uint8_t* ck = static_cast<uint8_t*>(const_cast<void*>(m->ctx_kv.ptr));
+  // where a weight's raw values go: its arena slot, or the staging buffer (e4m3)
+  auto dst = [&](Weight& W) { return static_cast<uint8_t*>(e4m3 ? stage : const_cast<void*>(W.ptr)); };
+  // e4m3: quantize the staged weight (rows x cols, src_dtype) into its arena slot
+  auto finish = [&](Weight& W, int64_t rows, int64_t cols, int src_dtype) -> cudaError_t {
+    if (!e4m3) return cudaSuccess;
+    return fm::quantize_e4m3(s, stage, src_dtype, static_cast<int>(rows), static_cast<int>(cols),
+                             const_cast<void*>(W.ptr), const_cast<float*>(W.wscale));
+  };
   // ---- copies: the all-layer context K/V weight [k_0; v_0; ...] and fused q/k/v
-  LCHK(copy(const_cast<void*>(m->fc.ptr), w->fc_w, bytes_of(D, m->Lt * H)));
-  LCHK(copy(const_cast<void*>(m->ap.ptr), w->anchor_proj_w, bytes_of(D, H)));
-  LCHK(copy(const_cast<void*>(m->xe.ptr), w->x_embed_w, bytes_of(D, H)));
+  LCHK(copy(dst(m->fc), w->fc_w, bytes_of(D, m->Lt * H)));
+  LCHK(finish(m->fc, D, m->Lt * H, adt));
+  LCHK(copy(dst(m->ap), w->anchor_proj_w, bytes_of(D, H)));
+  LCHK(finish(m->ap, D, H, adt));
+  LCHK(copy(dst(m->xe), w->x_embed_w, bytes_of(D, H)));
+  LCHK(finish(m->xe, D, H, adt));
+  {
+    uint8_t* ck = dst(m->ctx_kv);
+    for (int l = 0; l < L; ++l) {
+      LCHK(copy(ck + bytes_of(2 * l * D, D), w->layers[l].cross_k_w, bytes_of(D, D)));
+      LCHK(copy(ck + bytes_of((2 * l + 1) * D, D), w->layers[l].cross_v_w, bytes_of(D, D)));
+    }
+    LCHK(finish(m->ctx_kv, 2 * L * D, D, adt));
+  }
   for (int l = 0; l < L; ++l) {
     const flashmap_layer_weights& lw = w->layers[l];
     LayerW& d = m->layers[l];
-    LCHK(copy(ck + bytes_of(2 * l * D, D), lw.cross_k_w, bytes_of(D, D)));
-    LCHK(copy(ck + bytes_of((2 * l + 1) * D, D), lw.cross_v_w, bytes_of(D, D)));
-    uint8_t* q = static_cast<uint8_t*>(const_cast<void*>(d.qkv.ptr));
+    uint8_t* q = dst(d.qkv);
     LCHK(copy(q, lw.self_q_w, bytes_of(D, D)));
     LCHK(copy(q + bytes_of(D, D), lw.self_k_w, bytes_of(D, D)));
     LCHK(copy(q + bytes_of(2 * D, D), lw.self_v_w, bytes_of(D, D)));
-    LCHK(copy(const_cast<void*>(d.o.ptr), lw.self_o_w, bytes_of(D, D)));
-    LCHK(copy(const_cast<void*>(d.cq.ptr), lw.cross_q_w, bytes_of(D, D)));
-    LCHK(copy(const_cast<void*>(d.co.ptr), lw.cross_o_w, bytes_of(D, D)));
-    LCHK(copy(const_cast<void*>(d.fc1.ptr), lw.fc1_w, bytes_of(F, D)));
-    LCHK(copy(const_cast<void*>(d.fc2.ptr), lw.fc2_w, bytes_of(D, F)));
+    LCHK(finish(d.qkv, 3 * D, D, adt));
+    LCHK(copy(dst(d.o), lw.self_o_w, bytes_of(D, D)));
+    LCHK(finish(d.o, D, D, adt));
+    LCHK(copy(dst(d.cq), lw.cross_q_w, bytes_of(D, D)));
+    LCHK(finish(d.cq, D, D, adt));
+    LCHK(copy(dst(d.co), lw.cross_o_w, bytes_of(D, D)));
+    LCHK(finish(d.co, D, D, adt));
+    LCHK(copy(dst(d.fc1), lw.fc1_w, bytes_of(F, D)));
+    LCHK(finish(d.fc1, F, D, adt));
+    LCHK(copy(dst(d.fc2), lw.fc2_w, bytes_of(D, F)));
+    LCHK(finish(d.fc2, D, F, adt));
     LCHK(fm::to_f32(s, lw.self_q_norm_w, adt, hd, d.qn));
     LCHK(fm::to_f32(s, lw.self_k_norm_w, adt, hd, d.kn));
     LCHK(fm::to_f32(s, lw.cross_q_norm_w, adt, hd, d.cqn));
@@ -501,8 +550,9 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
     LCHK(cudaMemcpyAsync(m->hot, hot.data(), m->Vd * 8, cudaMemcpyHostToDevice, s));
     LCHK(cudaMemcpyAsync(m->inv_hot, inv.data(), V * 4, cudaMemcpyHostToDevice, s));
     // W_f = LM[hot] W_head (Vd x D), b_f = LM[hot] b_head, float32 accumulation
-    LCHK(fm::simt_gemm(s, m->Vd, m->D, m->H, lm_head, adt, m->hot, H, 1, w->head_w, adt, D, 1,
-                       const_cast<void*>(m->head.ptr), adt, D, 1));
+    LCHK(fm::simt_gemm(s, m->Vd, m->D, m->H, lm_head, adt, m->hot, H, 1, w->head_w, adt, D, 1, dst(m->head),
+                       e4m3 ? FLASHMAP_F32 : adt, D, 1));
+    LCHK(finish(m->head, Vd, D, FLASHMAP_F32));
     LCHK(fm::simt_gemm(s, m->Vd, 1, m->H, lm_head, adt, m->hot, H, 1, w->head_b, adt, 1, 0, m->head_b,
                        FLASHMAP_F32, 1, 0));
     // rotary table
@@ -531,9 +581,10 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   m->xe.N = m->D, m->xe.K = m->H;
   m->head.N = m->Vd, m->head.K = m->D;
   std::string err;
-  Weight* ws[] = {&m->fc, &m->ap, &m->ctx_kv, &m->chol, &m->xe, &m->head};
+  Weight* ws[] = {&m->fc, &m->ap, &m->ctx_kv, &m->xe, &m->head};
   for (Weight* x : ws)
-    if (check_weight_map(*x, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+    if (check_weight_map(*x, m->wdt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  if (check_weight_map(m->chol, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
   for (auto& d : m->layers) {
     d.qkv.N = 3 * m->D, d.qkv.K = m->D;
     d.o.N = m->D, d.o.K = m->D;
@@ -543,7 +594,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
     d.fc2.N = m->D, d.fc2.K = m->F;
     Weight* lws[] = {&d.qkv, &d.o, &d.cq, &d.co, &d.fc1, &d.fc2};
     for (Weight* x : lws)
-      if (check_weight_map(*x, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+      if (check_weight_map(*x, m->wdt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
   }
   LCHK(cudaStreamSynchronize(s));
   LCHK(cudaGetLastError());
@@ -860,21 +911,38 @@ flashmap_status flashmap_debug_philox(const uint64_t* seeds, const uint32_t* ctr
 flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* w, int32_t rows, int32_t in_features,
                                       int32_t out_features, float* out, flashmap_stream stream) {
   g_last_error.clear();
-  if (!x || !w || !out || rows <= 0 || in_features <= 0 || out_features <= 0 || !is_act(dtype))
+  if (!x || !w || !out || rows <= 0 || in_features <= 0 || out_features <= 0 ||
+      !(is_act(dtype) || dtype == FLASHMAP_E4M3))
     return fail(FLASHMAP_E_INVALID, "bad argument");
-  if (dtype == FLASHMAP_BF16 && in_features % 8) return fail(FLASHMAP_E_INVALID, "in_features must be a multiple of 8");
+  if (dtype != FLASHMAP_F32 && in_features % (dtype == FLASHMAP_E4M3 ? 16 : 8))
+    return fail(FLASHMAP_E_INVALID, "in_features must be a multiple of 8 (16 for E4M3)");
   int dev = 0, sms = 0;
   FM_CUDA(cudaGetDevice(&dev));
   FM_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   FM_CUDA(fm::gemm_prepare());
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Weight W;
   W.ptr = w;
   W.N = out_features;
   W.K = in_features;
+  void* q = nullptr;
+  if (dtype == FLASHMAP_E4M3) {  // w is bf16: quantize it as flashmap_load_weights does
+    const size_t qbytes = align_up(static_cast<size_t>(out_features) * in_features);
+    FM_CUDA(cudaMallocAsync(&q, qbytes + static_cast<size_t>(out_features) * 4, s));
+    float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(q) + qbytes);
+    FM_CUDA(fm::quantize_e4m3(s, w, FLASHMAP_BF16, out_features, in_features, q, scale));
+    W.ptr = q;
+    W.wscale = scale;
+  }
   std::string err;
-  if (check_weight_map(W, dtype, &err) != FLASHMAP_OK) return fail(FLASHMAP_E_CUDA, err);
-  Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr, true};
-  FM_CUDA(fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, false));
+  if (check_weight_map(W, dtype, &err) != FLASHMAP_OK) {
+    if (q) cudaFreeAsync(q, s);
+    return fail(FLASHMAP_E_CUDA, err);
+  }
+  Launch Lh{s, sms, nullptr, true};
+  const cudaError_t e = fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, false);
+  if (q) cudaFreeAsync(q, s);
+  FM_CUDA(e);
   return FLASHMAP_OK;
 }
 

@@ -25,7 +25,10 @@
 namespace fm {
 namespace {
 
+// Warps: 0 TMA producer, 1 MMA issuer, 2-5 epilogue, and for e4m3 weights 6-9
+// converters (e4m3 weight tile -> bf16 tile in the MMA's swizzled layout).
 constexpr int kTcThreads = 192;
+constexpr int kTcThreadsF8 = 320;
 
 // Pipeline depth of the narrow (<= 32 activation rows) GEMMs, and CTAs launched per SM.
 #ifndef FM_TC_STAGES_NARROW
@@ -35,17 +38,45 @@ constexpr int kTcThreads = 192;
 #define FM_TC_CTAS_PER_SM 2
 #endif
 
-template <int BN>
+// One pipeline stage: the bf16 weight tile (A, 128 x 64, 128B-swizzled), the
+// activation tile (B, BN x 64, 128B-swizzled) and, for e4m3 weights, the raw e4m3
+// weight tile as TMA wrote it (128 rows x 64 bytes, unswizzled) that the converter
+// warps expand into A.
+template <int BN, bool F8>
 struct TcCfg {
-  static constexpr int STAGES = BN <= 32 ? FM_TC_STAGES_NARROW : BN <= 64 ? 4 : BN <= 128 ? 6 : 4;
+  static constexpr int STAGES = F8 ? (BN <= 32 ? 4 : BN <= 64 ? 3 : BN <= 128 ? 5 : 4)
+                                   : (BN <= 32 ? FM_TC_STAGES_NARROW : BN <= 64 ? 4 : BN <= 128 ? 6 : 4);
   static constexpr int A_BYTES = 128 * 64 * 2;
   static constexpr int B_BYTES = BN * 64 * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int A8_BYTES = F8 ? 128 * 64 : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + A8_BYTES;
+  static constexpr uint32_t TX_BYTES = (F8 ? A8_BYTES : A_BYTES) + B_BYTES;  // bytes TMA writes per stage
   static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int THREADS = F8 ? kTcThreadsF8 : kTcThreads;
   static constexpr int FIT = (228 * 1024) / (SMEM + 1024);
   static constexpr int PER_SM = FIT < FM_TC_CTAS_PER_SM ? (FIT < 1 ? 1 : FIT) : FM_TC_CTAS_PER_SM;
 };
+
+// e4m3 x 16 (one 16-byte chunk of a weight row) -> bf16 x 16 (two 16-byte chunks).
+// Every e4m3 value is exact in half and in bf16.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 u, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      const float2 f = __half22float2(__half2(hr));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
 
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -55,14 +86,18 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int BN, bool F8>
+__global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                      float* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
-                     const float* __restrict__ beta, int out_zeroed, unsigned* dev_err) {
-  using C = TcCfg<BN>;
+                     const float* __restrict__ beta, const float* __restrict__ wscale, int out_zeroed,
+                     unsigned* dev_err) {
+  using C = TcCfg<BN, F8>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[C::STAGES], empty_bar[C::STAGES], acc_full[2], acc_empty[2], drain_bar;
+  // full: TMA bytes landed; conv (e4m3 only): the bf16 weight tile is written;
+  // empty: the MMAs reading the stage completed
+  __shared__ uint64_t full_bar[C::STAGES], conv_bar[C::STAGES], empty_bar[C::STAGES], acc_full[2], acc_empty[2],
+      drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ int64_t issued, consumed;
@@ -79,6 +114,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
+      mbar_init(&conv_bar[s], 4);
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -111,8 +147,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int64_t tile = (it0 + i) / KB;
         const int kb = static_cast<int>(it0 + i - tile * KB);
         const int m = static_cast<int>(tile / rt);
-        mbar_arrive_expect_tx(&full_bar[i], C::STAGE_BYTES);
-        tma_load_2d(smem + i * C::STAGE_BYTES, &mapW, &full_bar[i], kb * 64, m * 128, pol_w);
+        mbar_arrive_expect_tx(&full_bar[i], C::TX_BYTES);
+        tma_load_2d(smem + i * C::STAGE_BYTES + (F8 ? C::A_BYTES + C::B_BYTES : 0), &mapW, &full_bar[i], kb * 64,
+                    m * 128, pol_w);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
@@ -130,8 +167,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) break;
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-        tma_load_2d(sa, &mapW, &full_bar[stage], kb * 64, m * 128, pol_w);
+        mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
+        tma_load_2d(sa + (F8 ? C::A_BYTES + C::B_BYTES : 0), &mapW, &full_bar[stage], kb * 64, m * 128, pol_w);
         tma_load_2d(sa + C::A_BYTES, &mapX, &full_bar[stage], kb * 64, r * BN, pol_x);
         ++issued;
         if (++stage == C::STAGES) {
@@ -158,7 +195,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
         bool first = true;
         for (; it < seg_end; ++it) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+          if (!mbar_wait(F8 ? &conv_bar[stage] : &full_bar[stage], phase, &abort_flag)) {
             ok = false;
             break;
           }
@@ -184,6 +221,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit(&drain_bar);  // every MMA issued above has completed past this wait
       if (!mbar_wait_timed(&drain_bar, 0)) abort_flag = 1;
     }
+  } else if (F8 && warp >= 6) {  // converters: warps 6..9, 128 threads
+    const int t = threadIdx.x - 192;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t it = it0; it < it1; ++it) {
+      if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) break;
+      const uint8_t* a8 = smem + stage * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+      uint8_t* a16 = smem + stage * C::STAGE_BYTES;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {  // 512 chunks of 16 e4m3: row = chunk / 4, 16-byte column c = chunk % 4
+        const int chunk = t + 128 * j, row = chunk >> 2, c = chunk & 3;
+        uint4 lo, hi;
+        e4m3x16_to_bf16(*reinterpret_cast<const uint4*>(a8 + row * 64 + c * 16), lo, hi);
+        // 128B swizzle: 16-byte chunk q of row `row` sits at q ^ (row % 8)
+        *reinterpret_cast<uint4*>(a16 + row * 128 + (((2 * c) ^ (row & 7)) << 4)) = lo;
+        *reinterpret_cast<uint4*>(a16 + row * 128 + (((2 * c + 1) ^ (row & 7)) << 4)) = hi;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&conv_bar[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
   } else {  // epilogue: warps 2..5, TMEM lane quadrant warp % 4
     pdl_wait();
     const int q = warp & 3;
@@ -206,6 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float a = 1.f, b = 0.f;
       if (n < N) {
         if (alpha) a = alpha[n];
+        if (F8) a *= wscale[n];  // the weight's per-output-channel scale
         if (beta && kb0 == 0) b = beta[n];
       }
 #pragma unroll 1
@@ -386,34 +449,51 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <int BN>
+template <int BN, bool F8>
 cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, float* out, int ldo,
                       const float* alpha, const float* beta, bool zeroed) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, F8>;
   CUtensorMap mapX;
   std::string err;
   if (!make_tmap_bf16(&mapX, x, R, W.K, ldx, BN, &err)) return cudaErrorInvalidValue;
   const int64_t mt = (W.N + 127) / 128, rt = (R + BN - 1) / BN, KB = (W.K + 63) / 64;
   const int64_t T = mt * rt * KB;
   const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * C::PER_SM));
-  return launch_k(L, tc_linear_kernel<BN>, dim3(G), dim3(kTcThreads), C::SMEM, W.map, mapX, out, ldo, R, W.N, W.K,
-                  alpha, beta, zeroed ? 1 : 0, L.dev_err);
+  return launch_k(L, tc_linear_kernel<BN, F8>, dim3(G), dim3(C::THREADS), C::SMEM, W.map, mapX, out, ldo, R, W.N,
+                  W.K, alpha, beta, W.wscale, zeroed ? 1 : 0, L.dev_err);
 }
 
-template <int BN>
+template <bool F8>
+cudaError_t launch_tc_rows(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
+                           const float* alpha, const float* beta, bool zeroed) {
+  if (rows <= 16) return launch_tc<16, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+  if (rows <= 32) return launch_tc<32, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+  if (rows <= 64) return launch_tc<64, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+  if (rows <= 128) return launch_tc<128, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+  return launch_tc<256, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+}
+
+template <int BN, bool F8>
 cudaError_t set_tc_attr() {
-  return cudaFuncSetAttribute(tc_linear_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg<BN>::SMEM);
+  return cudaFuncSetAttribute(tc_linear_kernel<BN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              TcCfg<BN, F8>::SMEM);
+}
+
+template <bool F8>
+cudaError_t set_tc_attrs() {
+  cudaError_t e;
+  if ((e = set_tc_attr<16, F8>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<32, F8>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<64, F8>()) != cudaSuccess) return e;
+  if ((e = set_tc_attr<128, F8>()) != cudaSuccess) return e;
+  return set_tc_attr<256, F8>();
 }
 
 }  // namespace
 
 cudaError_t gemm_prepare() {
-  cudaError_t e;
-  if ((e = set_tc_attr<16>()) != cudaSuccess) return e;
-  if ((e = set_tc_attr<32>()) != cudaSuccess) return e;
-  if ((e = set_tc_attr<64>()) != cudaSuccess) return e;
-  if ((e = set_tc_attr<128>()) != cudaSuccess) return e;
-  return set_tc_attr<256>();
+  cudaError_t e = set_tc_attrs<false>();
+  return e != cudaSuccess ? e : set_tc_attrs<true>();
 }
 
 bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows,
@@ -441,16 +521,40 @@ bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
   return true;
 }
 
+bool make_tmap_e4m3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, std::string* err) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    if (err) *err = "cuTensorMapEncodeTiled is not available from the driver";
+    return false;
+  }
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols & 15) || cols <= 0 || rows <= 0) {
+    if (err) *err = "an e4m3 weight must be 16-byte aligned with a multiple of 16 columns";
+    return false;
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  const cuuint32_t box[2] = {64, 128};  // 64 bytes x 128 rows, unswizzled
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) *err = "cuTensorMapEncodeTiled failed (" + std::to_string(static_cast<int>(r)) + ")";
+    return false;
+  }
+  return true;
+}
+
 cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
                    const float* alpha, const float* beta, bool zeroed) {
   if (rows <= 0 || W.N <= 0) return cudaSuccess;
   if (W.dtype == FLASHMAP_BF16) {
     if (!W.has_map) return cudaErrorInvalidValue;
-    if (rows <= 16) return launch_tc<16>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-    if (rows <= 32) return launch_tc<32>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-    if (rows <= 64) return launch_tc<64>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-    if (rows <= 128) return launch_tc<128>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-    return launch_tc<256>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    return launch_tc_rows<false>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+  }
+  if (W.dtype == FLASHMAP_E4M3) {  // e4m3 weights, bf16 activations
+    if (!W.has_map || !W.wscale) return cudaErrorInvalidValue;
+    return launch_tc_rows<true>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
   }
   if (W.dtype == FLASHMAP_F32) {
     const int64_t threads = static_cast<int64_t>(W.N) * 32;

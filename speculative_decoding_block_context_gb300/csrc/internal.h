@@ -54,16 +54,18 @@ cudaError_t zero_ranges(const Launch& L, const ZeroList& z);
 struct Weight {
   const void* ptr = nullptr;
   int N = 0, K = 0;
-  int dtype = FLASHMAP_F32;      // F32 or BF16 (E4M3 copies are dequantized by the kernel)
+  int dtype = FLASHMAP_F32;      // F32, BF16, or E4M3 (expanded to bf16 in shared memory by the GEMM)
   const float* wscale = nullptr; // per-output-channel scale of an E4M3 weight
   bool has_map = false;
-  CUtensorMap map;  // BF16: the A-operand tensor map (box 64 x 128, 128B swizzle)
+  CUtensorMap map;  // BF16: box 64 x 128, 128B swizzle; E4M3: box 64 bytes x 128 rows, no swizzle
 };
 
 // Encodes the tensor map of a row-major bf16 matrix (rows x cols, leading dim ld
 // elements) read in boxes of box_rows x 64 columns with 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
                     int box_rows, std::string* err);
+// The same for a dense row-major e4m3 matrix (cols a multiple of 16), box 64 x 128.
+bool make_tmap_e4m3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, std::string* err);
 
 // Sets the kernel attributes the tcgen05 GEMM needs on the current device (call once
 // per device before launching; not during stream capture).

@@ -52,8 +52,12 @@ def load_model(workload: str, device="cuda", oracle: bool = True) -> ModelState:
     if oracle:
         st.Wnp = {k: v.float().cpu().numpy() for k, v in W.items()}
         st.Enp = E.float().cpu().numpy()
+        if cfg["weight_dtype"] == "e4m3":  # the oracle runs on the dequantized weights
+            st.Wnp = ref.e4m3_weights(st.oracle_cfg(), st.Wnp)
         st.consts = ref.load_constants(st.oracle_cfg(), st.Wnp, st.Enp, LM.float().cpu().numpy(),
                                        rank.cpu().numpy())
+        if cfg["weight_dtype"] == "e4m3":
+            st.consts = ref.e4m3_constants(st.consts)
     return st
 
 

@@ -31,10 +31,7 @@ def test_validate_configs_of_every_workload(lib):
     for wl in syn.WORKLOADS:
         cfg = syn.model_config(wl)
         st = F.flashmap_validate_config(cfg)
-        if cfg["weight_dtype"] == "e4m3":
-            assert st in (0, 2)
-        else:
-            assert st == 0, (wl, F.flashmap_last_error())
+        assert st == 0, (wl, F.flashmap_last_error())
 
 
 @pytest.mark.parametrize(
@@ -47,6 +44,8 @@ def test_validate_configs_of_every_workload(lib):
         (dict(block_size=32), 2),
         (dict(vocab_size=0), 1),
         (dict(act_dtype="f32", weight_dtype="bf16"), 1),
+        (dict(act_dtype="f32", weight_dtype="e4m3"), 1),  # e4m3 weights need bf16 activations
+        (dict(act_dtype="bf16", weight_dtype="e4m3", intermediate=392), 2),  # not a multiple of 16
         (dict(time_embed_dim=63), 1),
         (dict(rope_theta=-1.0), 1),
     ],

@@ -63,6 +63,22 @@ def test_linear_bf16_tcgen05(rows, k, n):
     assert max_rel(out.cpu().numpy(), want) < 1e-5
 
 
+@pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 208, 300), (16, 4096, 4096), (37, 384, 1234),
+                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512)])
+def test_linear_e4m3_tcgen05(rows, k, n):
+    """W8A16: w quantized per output channel at call time, expanded to bf16 on chip."""
+    g = torch.Generator(device="cuda").manual_seed(rows * 11 + k)
+    x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((n, k), generator=g, device="cuda") / k**0.5).to(torch.bfloat16)
+    w[min(3, n - 1)] = 0  # an all-zero channel takes scale 1
+    out = torch.zeros((rows, n), dtype=torch.float32, device="cuda")
+    F.flashmap_debug_linear(F.E4M3, x, w, out)
+    torch.cuda.synchronize()
+    wq = ref.dequantize(*ref.quantize_e4m3_per_channel(w.float().cpu().numpy()))
+    want = x.double().cpu().numpy() @ wq.T
+    assert max_rel(out.cpu().numpy(), want) < 1e-5
+
+
 def test_linear_f32_simt():
     g = torch.Generator(device="cuda").manual_seed(3)
     x = torch.randn((7, 300), generator=g, device="cuda")

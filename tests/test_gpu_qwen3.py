@@ -69,6 +69,15 @@ def test_qwen3_bs32_ragged_contexts(qwen):
     _run_and_check(qwen, "qwen3_8b_bs32")
 
 
+def test_qwen3_fp8_weights_bs64_greedy(qwen):
+    """Config 5: e4m3 DiT weights with per-channel scales, bf16 activations; the oracle
+    runs on the dequantized weights. The bf16 model of the other tests stays loaded."""
+    fp8 = load_model("qwen3_8b_fp8_bs64")
+    run, _ = _run_and_check(fp8, "qwen3_8b_fp8_bs64")
+    del run, fp8  # the handle frees the model's arena
+    torch.cuda.empty_cache()
+
+
 def test_qwen3_bs128_window_and_full_vocab_scatter(qwen):
     run, _ = _run_and_check(qwen, "qwen3_8b_bs128")
     hot = torch.as_tensor(qwen.consts.hot, device="cuda")

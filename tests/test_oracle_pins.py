@@ -11,6 +11,7 @@ import pytest
 import scipy.stats as st
 
 from oracle import flashmap_ref as ref
+from speculative_decoding_block_context_gb300 import synthetic as syn
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -390,3 +391,54 @@ def test_e4m3_per_channel_scale():
     assert np.all(np.max(np.abs(q[[0, 1, 2, 4, 5]]), axis=1) == 448.0)
     deq = ref.dequantize(q, s)
     assert np.max(np.abs(deq - w)) <= np.max(np.abs(w)) / 448 * 16  # half an e4m3 step at the top
+
+
+def test_e4m3_weight_set_matches_the_pages_list():
+    """flashmap/sglang/model.py, _quantize_fp8 lists x_embed, fc, the context/anchor
+    projections, the folded head and every block's linears; norms, AdaLN weights and
+    the noise factor stay unquantized. The set is fixed by name here, independently of
+    the oracle's list."""
+    cfg = ref.Config.from_dict(syn.model_config("small_bf16"))
+    names = set(ref.e4m3_linear_names(cfg))
+    shapes = syn.weight_shapes(syn.model_config("small_bf16"))
+    want = {"x_embed.weight", "fc.weight", "anchor_proj.weight"}
+    for l in range(cfg.num_layers):
+        for att in ("self_attn", "cross_attn"):
+            want |= {f"layers.{l}.{att}.{p}_proj.weight" for p in "qkvo"}
+        want |= {f"layers.{l}.mlp.fc1.weight", f"layers.{l}.mlp.fc2.weight"}
+    assert names == want
+    assert names <= set(shapes)
+    assert not any("norm" in n or "adaln" in n or "embed." in n.replace("x_embed", "") for n in names)
+
+
+def test_e4m3_weights_quantize_only_the_set_and_stay_within_half_a_step():
+    cfg = ref.Config.from_dict(syn.model_config("tiny_fp32"))
+    rng = np.random.default_rng(5)
+    W = {n: rng.standard_normal(s).astype(np.float32) for n, s in syn.weight_shapes(syn.model_config("tiny_fp32")).items()}
+    Wq = ref.e4m3_weights(cfg, W)
+    qset = set(ref.e4m3_linear_names(cfg))
+    for n, w in W.items():
+        if n not in qset:
+            assert Wq[n] is w
+            continue
+        amax = np.max(np.abs(w), axis=1, keepdims=True)
+        scale = amax / 448.0
+        # every dequantized value is an e4m3 value times its row's scale ...
+        q = Wq[n] / scale.astype(np.float32).astype(np.float64)
+        np.testing.assert_array_equal(ref.e4m3_round(q.astype(np.float32)), q)
+        # ... within half an e4m3 step (relative 2^-4) of the original, or 2^-10 scale absolute
+        err = np.abs(Wq[n] - w)
+        assert np.all(err <= np.maximum(np.abs(w) * 2.0**-4, scale * 2.0**-10) * (1 + 1e-6))
+        # the row maximum maps to exactly 448 * scale
+        np.testing.assert_allclose(np.max(np.abs(Wq[n]), axis=1), amax[:, 0], rtol=1e-6)
+
+
+def test_e4m3_constants_quantize_the_folded_head_only():
+    cfg = ref.Config.from_dict(syn.model_config("tiny_fp32"))
+    rng = np.random.default_rng(6)
+    C = ref.Constants(mods=None, final=None, gate=1.0, uniform=None, gram=None, chol=None,
+                      hot=np.arange(8), head_w=rng.standard_normal((8, 16)), head_b=rng.standard_normal(8))
+    Cq = ref.e4m3_constants(C)
+    assert Cq.head_b is C.head_b and Cq.hot is C.hot
+    assert not np.array_equal(Cq.head_w, C.head_w)
+    assert np.max(np.abs(Cq.head_w - C.head_w)) <= np.max(np.abs(C.head_w)) / 448 * 16
