@@ -120,7 +120,8 @@ def algorithmic_bytes(cfg: dict, req: dict) -> dict:
     x_in = (bs * (K + 1) * Lt * H * es) if req["window"] else 0
     full = bs * K * V * 4 if req["full_scatter"] else 0
     total = w_write + w_draft + w_head + kv_read + rows_written * kv_row + logits + x_in + full
-    return {"weights": w_write + w_draft + w_head, "kv_read": kv_read, "total": total}
+    draft_sample = w_draft + w_head + kv_read + bs * kv_row + logits + full
+    return {"weights": w_write + w_draft + w_head, "kv_read": kv_read, "total": total, "draft_sample": draft_sample}
 
 
 def setup_ours(workload: str, device: str):
@@ -181,6 +182,7 @@ def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: i
     per launch over the mean launch duration."""
     F = st["F"]
     es = 4 if st["cfg"]["act_dtype"] == "f32" else 2
+    e4m3 = st["cfg"].get("weight_dtype") == "e4m3"
     with torch.cuda.stream(stream):
         F.flashmap_profile_start(st["model"], 100000)
         for _ in range(steps):
@@ -190,13 +192,79 @@ def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: i
     by_kind = {}
     for r in recs:
         by_kind[r[0]] = by_kind.get(r[0], 0.0) + r[5] / steps
-    byts = sum(n * k * es + rows * k * es + rows * n * 4 for _, _, rows, n, k, _ in gem) / len(gem)
+    # e4m3 weights: one byte per element plus a float32 scale per channel, except the
+    # noise factor L (square H x H), which stays bf16
+    H = st["cfg"]["target_hidden"]
+
+    def wbytes(n, k):
+        return n * k * es if not e4m3 or (n == H and k == H) else n * k + n * 4
+
+    byts = sum(wbytes(n, k) + rows * k * es + rows * n * 4 for _, _, rows, n, k, _ in gem) / len(gem)
     ms = sum(r[5] for r in gem) / len(gem)
     achieved = byts / (ms * 1e-3) / 1e9
     return {"kernel": "tc_linear_kernel (tcgen05 GEMM, all launches of a step)", "bytes_per_launch": byts,
             "ms_per_launch": ms, "launches_per_step": len(gem) // steps, "achieved_gbs": achieved,
             "ms_by_kind_per_step": {k: round(v, 4) for k, v in sorted(by_kind.items())},
             "launches_per_step_total": len(recs) // steps}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu summary of this workload, or
+    None when there is none or csrc/gemm.cu changed since the counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"tc_linear_step_{workload}.md")
+    src = os.path.join(ROOT, "speculative_decoding_block_context_gb300", "csrc", "gemm.cu")
+    try:
+        kv = {}
+        with open(path) as f:
+            for ln in f:
+                if ":" in ln and ln.split(":")[0] in ("traffic_bytes_per_launch", "kernel_source_sha256"):
+                    k, v = ln.split(":", 1)
+                    kv[k] = v.strip()
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        return int(kv["traffic_bytes_per_launch"]) if kv.get("kernel_source_sha256") == sha else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def phase_times(st: dict, stream: torch.cuda.Stream, n: int = 60) -> dict:
+    """The step's three calls captured as separate graphs and replayed n times each,
+    every replay timed with its own event pair on the launch stream: median and p90 in
+    microseconds (write only when the workload writes a verify window)."""
+    F, req, cfg = st["F"], st["req"], st["cfg"]
+    bs, K = req["bs"], cfg["block_size"]
+    calls = {}
+    if req["window"]:
+        calls["write"] = lambda: F.flashmap_write_context_kv(
+            st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"], st["start"],
+            st["commit"], req["req_to_page"], st["window_loc"], st["ws"])
+    calls["draft"] = lambda: F.flashmap_draft_block(
+        st["model"], st["pool"], bs, req["anchor_ids"], st["anchor_pos"], req["req_pool_idx"], req["req_to_page"],
+        req["seeds"], 1.0, st["hidden"], None, st["ws"])
+    calls["sample"] = lambda: F.flashmap_sample_block(
+        st["model"], bs, st["hidden"], st["anchor_pos"], req["temperature"], req["greedy"], req["seeds"],
+        req["step"], st["tokens"], st["logits"], st["full"], st["ws"])
+    out = {}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            for _ in range(3):
+                g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        us = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+        out[name] = {"median_us": round(float(np.median(us)), 1), "p90_us": round(float(np.percentile(us, 90)), 1)}
+    return out
 
 
 def world_max(value: float, world: int, device) -> float:
@@ -284,7 +352,9 @@ def our_arm(args, rank: int, world: int) -> dict:
     e2e_ms = world_max(e0.elapsed_time(e1) / args.steps, world, device)
 
     roof = gemm_roofline(st, stream, hbm_peak)
+    phases = phase_times(st, stream)
     ab = algorithmic_bytes(cfg, req)
+    t_ds = (phases["draft"]["median_us"] + phases["sample"]["median_us"]) * 1e-6
     launches = roof["launches_per_step_total"]
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -301,12 +371,19 @@ def our_arm(args, rank: int, world: int) -> dict:
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(roof["achieved_gbs"] / hbm_peak, 4), "traffic": None,
+                     "frac": round(roof["achieved_gbs"] / hbm_peak, 4), "traffic": profiled_traffic(args.workload),
                      "peak_source": f"{peak_src} hbm_gbs", "kernel": roof["kernel"],
                      "bytes_per_launch": round(roof["bytes_per_launch"]), "us_per_launch": round(roof["ms_per_launch"] * 1e3, 2)},
         "step_roofline": {"algorithmic_bytes": ab["total"], "achieved_gbs": round(ab["total"] / (ms * 1e-3) / 1e9, 1),
                           "frac_of_measured_hbm": round(ab["total"] / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                           "frac_of_8tbs": round(ab["total"] / (ms * 1e-3) / 1e9 / 8000.0, 4)},
+        # the draft step proper (draft + sample calls, each its own graph), against the
+        # bytes it must move (the window write's weights and rows excluded)
+        "phases": phases,
+        "draft_sample_roofline": {"algorithmic_bytes": ab["draft_sample"],
+                                  "us": round(t_ds * 1e6, 1),
+                                  "frac_of_measured_hbm": round(ab["draft_sample"] / t_ds / 1e9 / hbm_peak, 4),
+                                  "frac_of_8tbs": round(ab["draft_sample"] / t_ds / 1e9 / 8000.0, 4)},
         "breakdown_ms_per_step_eager": roof["ms_by_kind_per_step"],
         "clocks": clocks,
     }
