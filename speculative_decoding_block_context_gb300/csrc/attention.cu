@@ -377,11 +377,25 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     const int nj = warp < nblk ? (nblk - warp + 3) >> 2 : 0;
+    // The page ids of this warp's blocks, 32 blocks at a time, one per lane: loaded
+    // ahead so that no page-table load sits between a block's issue and the next.
+    const int32_t* r2p = a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride;
+    auto page_ids = [&](int j0) {
+      const int j = j0 + lane;
+      if (j >= nj) return -1;
+      const int pi = (p0 + ((warp + 4 * j) << 4)) / a.P;
+      return pi < a.r2p_stride ? LDCG(r2p + pi) : -1;
+    };
+    int pg = page_ids(0), pg_group = 0;
     auto issue = [&](int j) {
       if (j < nj) {
+        if ((j >> 5) != pg_group) {  // warp-uniform: more than 32 blocks per warp
+          pg_group = j >> 5;
+          pg = page_ids(j & ~31);
+        }
         const int blk = p0 + ((warp + 4 * j) << 4);
         const int pi = blk / a.P;
-        const int page = pi < a.r2p_stride ? LDCG(a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride + pi) : -1;
+        const int page = __shfl_sync(0xffffffffu, pg, j & 31);
         const bool ok = page >= 0 && page < a.num_pages;
         if (!ok && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
         const int off = blk - pi * a.P;
