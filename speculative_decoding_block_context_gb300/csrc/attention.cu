@@ -22,6 +22,32 @@
 namespace fm {
 namespace {
 
+// One head vector (channels lane*EPL..) of a step-produced float32 row: one L2 load.
+template <int EPL>
+__device__ __forceinline__ void load_head_vec(const float* src, float (&v)[EPL], int lane) {
+  const float* p = src + lane * EPL;
+  if constexpr (EPL == 4) {
+    const float4 t = LDCG(reinterpret_cast<const float4*>(p));
+    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+  } else if constexpr (EPL == 2) {
+    const float2 t = LDCG(reinterpret_cast<const float2*>(p));
+    v[0] = t.x, v[1] = t.y;
+  } else {
+    v[0] = LDCG(p);
+  }
+}
+template <int EPL>
+__device__ __forceinline__ void clear_head_vec(float* dst, int lane) {
+  float* p = dst + lane * EPL;
+  if constexpr (EPL == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if constexpr (EPL == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
+  } else {
+    p[0] = 0.f;
+  }
+}
+
 // ------------------------------------------------------------------ block self-attention
 
 template <typename T, int EPL>
@@ -31,9 +57,10 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
                                  unsigned* dev_err) {
   constexpr int HD = EPL * 32;
   extern __shared__ float sm[];
-  float* sq = sm;                  // [K][HD + 1]
-  float* sk = sq + K * (HD + 1);   // [K][HD + 1]
-  float* sv = sk + K * (HD + 1);   // [K][HD]
+  constexpr int LDQ = HD + 4;      // 16-byte rows, 4 banks apart: conflict-free float4 reads
+  float* sq = sm;                  // [K][LDQ]
+  float* sk = sq + K * LDQ;        // [K][LDQ]
+  float* sv = sk + K * LDQ;        // [K][HD]
   pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y;
@@ -41,29 +68,31 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   const int D = nh * HD;
   const int k = warp;  // one warp per slot
   const int row = b * K + k;
+  float* base = qkv + static_cast<int64_t>(row) * 3 * D + h * HD;
+  // q, k and v of this slot and head: all loads first (one vector per lane and part),
+  // then the request's position (once per CTA), the clears and the norms, so the
+  // L2 round trips overlap
+  float v[3][EPL];
+#pragma unroll
+  for (int part = 0; part < 3; ++part) load_head_vec<EPL>(base + part * D, v[part], lane);
   __shared__ int s_anchor;
-  if (threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);  // once per CTA
+  if (threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
   __syncthreads();
+#pragma unroll
+  for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
   int pos = s_anchor + 1 + k;
   if (pos < 0 || pos >= max_pos) {
     if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
     pos = 0;
   }
   const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
-  float* base = qkv + static_cast<int64_t>(row) * 3 * D + h * HD;
+  head_norm_rope<EPL>(v[0], qn, eps, rope, lane);
+  head_norm_rope<EPL>(v[1], kn, eps, rope, lane);
 #pragma unroll
-  for (int part = 0; part < 3; ++part) {
-    float* src = base + part * D;
-    float v[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      v[e] = LDCG(src + lane * EPL + e);
-      src[lane * EPL + e] = 0.f;
-    }
-    if (part < 2) head_norm_rope<EPL>(v, part == 0 ? qn : kn, eps, rope, lane);
-    float* dst = part == 0 ? sq + k * (HD + 1) : part == 1 ? sk + k * (HD + 1) : sv + k * HD;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) dst[lane * EPL + e] = v[e];
+  for (int e = 0; e < EPL; ++e) {
+    sq[k * LDQ + lane * EPL + e] = v[0][e];
+    sk[k * LDQ + lane * EPL + e] = v[1][e];
+    sv[k * HD + lane * EPL + e] = v[2][e];
   }
   __syncthreads();
   // scores of slot k against slot j = lane
@@ -71,9 +100,16 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   float s = -INFINITY;
   if (lane < K) {
     float acc = 0.f;
-    const float* qr = sq + k * (HD + 1);
-    const float* kr = sk + lane * (HD + 1);
-    for (int d = 0; d < HD; ++d) acc = fmaf(qr[d], kr[d], acc);
+    const float4* qr = reinterpret_cast<const float4*>(sq + k * LDQ);
+    const float4* kr = reinterpret_cast<const float4*>(sk + lane * LDQ);
+#pragma unroll 8
+    for (int d4 = 0; d4 < HD / 4; ++d4) {
+      const float4 a4 = qr[d4], b4 = kr[d4];
+      acc = fmaf(a4.x, b4.x, acc);
+      acc = fmaf(a4.y, b4.y, acc);
+      acc = fmaf(a4.z, b4.z, acc);
+      acc = fmaf(a4.w, b4.w, acc);
+    }
     s = acc * scale;
   }
   const float m = warp_max(s);
@@ -333,8 +369,10 @@ struct XCfg {
   static constexpr int CH = HD / 8;       // 16-byte chunks per row
   static constexpr int RING = kXStages * 2 * BLK;  // per warp
   static constexpr int SMEM_RING = 4 * RING;
+  static constexpr int SQ_OFF = SMEM_RING;          // the item's queries, beside the rings
+  static constexpr int SMEM_Q = SQ_OFF + 16 * HD * 4;
   static constexpr int SMEM_MERGE = 4 * 16 * (HD + 2) * 4;
-  static constexpr int SMEM = SMEM_RING > SMEM_MERGE ? SMEM_RING : SMEM_MERGE;
+  static constexpr int SMEM = SMEM_Q > SMEM_MERGE ? SMEM_Q : SMEM_MERGE;
 };
 
 template <int HD>
@@ -357,25 +395,8 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
     const int nblk = (p1 - p0 + 15) >> 4;
     const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
-    // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
-    float* sq = reinterpret_cast<float*>(xsm);  // aliases the ring until the first loads
-    load_queries<HD>(a, b, h, sq);
-    __syncthreads();
-    uint32_t qa[HD / 16][4];
-#pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int row = g8 + ((j & 1) << 3);
-        const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
-        qa[kk][j] = pack_bf16(sq[row * HD + col], sq[row * HD + col + 1]);
-      }
-    }
-    __syncthreads();
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[HD / 8][4];
-#pragma unroll
-    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    // The first blocks of keys and values are requested before the queries are
+    // prepared (the two do not depend on each other).
     const int nj = warp < nblk ? (nblk - warp + 3) >> 2 : 0;
     // The page ids of this warp's blocks, 32 blocks at a time, one per lane: loaded
     // ahead so that no page-table load sits between a block's issue and the next.
@@ -415,6 +436,24 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
     };
 #pragma unroll
     for (int j = 0; j < kXStages - 1; ++j) issue(j);
+    // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
+    float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
+    load_queries<HD>(a, b, h, sq);
+    __syncthreads();
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = g8 + ((j & 1) << 3);
+        const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
+        qa[kk][j] = pack_bf16(sq[row * HD + col], sq[row * HD + col + 1]);
+      }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     for (int j = 0; j < nj; ++j) {
       issue(j + kXStages - 1);
       cp_async_wait<kXStages - 1>();
@@ -537,50 +576,57 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 
 // ------------------------------------------------------------------ combine
 
-// One CTA per (request, head, query row): the chunks' (max, sum) are read in parallel
-// into shared memory, then each thread sums its channel over the chunks.
+// One CTA of 256 threads per (request, head): the chunks' running maxima and sums are
+// reduced per query row (16 threads per row), then each thread sums HD / 16 channels
+// of its row over the chunks with the chunk weights 2^(m_c - M) / L.
 constexpr int kMaxChunksPerRequest = 1024;  // max_position <= 262144, chunks >= 256 positions
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(HD) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
-  __shared__ float sw[kMaxChunksPerRequest];
-  __shared__ float red[32];
+__global__ void __launch_bounds__(256) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
   __shared__ int s_g[2];
   pdl_trigger();
   pdl_wait();
-  const int b = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x;
+  const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
-  // the request's chunk range, loaded once per CTA
-  if (d < 2) s_g[d] = LDCG(a.plan + 3 + b + d);
+  if (t < 2) s_g[t] = LDCG(a.plan + 3 + b + t);  // the request's chunk range
   __syncthreads();
   const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
-  float mloc = -INFINITY;
-  for (int c = d; c < nc; c += HD) {
-    const float m = LDCG(a.part_ml + ((static_cast<int64_t>(g0 + c)) * nh + h) * 32 + 2 * qi);
-    sw[c] = m;
-    mloc = fmaxf(mloc, m);
-  }
-  // block max
-  mloc = warp_max(mloc);
-  if ((d & 31) == 0) red[d >> 5] = mloc;
-  __syncthreads();
+  const int q = t >> 4, j = t & 15;  // query row, lane within the row's 16 threads
+  const float* ml = a.part_ml + (static_cast<int64_t>(g0) * nh + h) * 32 + 2 * q;
+  const int64_t mls = static_cast<int64_t>(nh) * 32;  // between chunks
   float M = -INFINITY;
-  for (int w = 0; w < HD / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float lloc = 0.f;
-  for (int c = d; c < nc; c += HD) {
-    const int64_t pidx = static_cast<int64_t>(g0 + c) * nh + h;
-    const float wgt = sw[c] == -INFINITY ? 0.f : exp2f(sw[c] - M);
-    sw[c] = wgt;
-    lloc = fmaf(wgt, LDCG(a.part_ml + pidx * 32 + 2 * qi + 1), lloc);
+  for (int c = j; c < nc; c += 16) M = fmaxf(M, LDCG(ml + c * mls));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));  // the row's 16 lanes
+  float L = 0.f;
+  for (int c = j; c < nc; c += 16) {
+    const float m = LDCG(ml + c * mls);
+    if (m != -INFINITY) L = fmaf(exp2f(m - M), LDCG(ml + c * mls + 1), L);
   }
-  const float L = block_sum(lloc, red);  // synchronizes: sw complete
-  float acc = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < nc; ++c)
-    acc = fmaf(sw[c], LDCG(a.part_o + (static_cast<int64_t>(g0 + c) * nh + h) * 16 * HD + qi * HD + d), acc);
-  out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
-  a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  // channels d = j, j + 16, ...
+  constexpr int NV = HD / 16;
+  float acc[NV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+  const float* po = a.part_o + (static_cast<int64_t>(g0) * nh + h) * 16 * HD + q * HD + j;
+  const int64_t pos_ = static_cast<int64_t>(nh) * 16 * HD;  // between chunks
+  for (int c = 0; c < nc; ++c) {
+    const float m = LDCG(ml + c * mls);
+    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = fmaf(w, LDCG(po + c * pos_ + 16 * v), acc[v]);
+  }
+  if (q < a.K) {
+    const int64_t r = (static_cast<int64_t>(b) * a.K + q) * D + h * HD + j;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      out[r + 16 * v] = from_f32<T>(L > 0.f ? acc[v] * inv : 0.f);
+      a.qacc[r + 16 * v] = 0.f;  // every item has read it
+    }
+  }
 }
 
 }  // namespace
@@ -615,7 +661,7 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
                            void* out) {
   if (bs <= 0) return cudaSuccess;
   dim3 grid(bs, nh);
-  const size_t smem = static_cast<size_t>(K) * ((hd + 1) * 2 + hd) * sizeof(float);
+  const size_t smem = static_cast<size_t>(K) * ((hd + 4) * 2 + hd) * sizeof(float);
   cudaError_t e = cudaSuccess;
   const dim3 block(32 * K);
   if (hd == 32) {
@@ -665,9 +711,9 @@ cudaError_t xattn_prepare() {
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& args, void* out) {
   XattnArgs a = args;
   a.dev_err = L.dev_err;
-  dim3 cgrid(a.bs, a.nh, a.K);
+  dim3 cgrid(a.bs, a.nh);
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_kernel<T, HD>, cgrid, dim3(HD), 0, a,
+  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_kernel<T, HD>, cgrid, dim3(256), 0, a,
                                                            static_cast<T*>(out)))));
   return e;
 }
