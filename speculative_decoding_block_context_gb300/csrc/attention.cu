@@ -576,13 +576,15 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 
 // ------------------------------------------------------------------ combine
 
-// One CTA of 256 threads per (request, head): the chunks' running maxima and sums are
-// reduced per query row (16 threads per row), then each thread sums HD / 16 channels
-// of its row over the chunks with the chunk weights 2^(m_c - M) / L.
+// One CTA of 64 threads per (request, head, 4 query rows): the chunks' running maxima
+// and sums are reduced per query row (16 threads per row), then each thread sums
+// HD / 16 channels of its row over the chunks with the chunk weights 2^(m_c - M) / L.
 constexpr int kMaxChunksPerRequest = 1024;  // max_position <= 262144, chunks >= 256 positions
+constexpr int kCombineRowsMaxBatch = 4;     // up to this batch the one-row-per-CTA combine is faster
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(256) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
+__global__ void __launch_bounds__(64) xattn_combine_kernel(XattnArgs a, T* __restrict__ out) {
+  __shared__ float sw[4][kMaxChunksPerRequest];  // per row: the chunks' maxima, then weights
   __shared__ int s_g[2];
   pdl_trigger();
   pdl_wait();
@@ -591,32 +593,40 @@ __global__ void __launch_bounds__(256) xattn_combine_kernel(XattnArgs a, T* __re
   if (t < 2) s_g[t] = LDCG(a.plan + 3 + b + t);  // the request's chunk range
   __syncthreads();
   const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
-  const int q = t >> 4, j = t & 15;  // query row, lane within the row's 16 threads
+  const int ql = t >> 4, q = blockIdx.z * 4 + ql, j = t & 15;  // query row, lane within its 16 threads
+  float* w = sw[ql];
   const float* ml = a.part_ml + (static_cast<int64_t>(g0) * nh + h) * 32 + 2 * q;
   const int64_t mls = static_cast<int64_t>(nh) * 32;  // between chunks
   float M = -INFINITY;
-  for (int c = j; c < nc; c += 16) M = fmaxf(M, LDCG(ml + c * mls));
+  for (int c = j; c < nc; c += 16) {
+    const float m = LDCG(ml + c * mls);
+    w[c] = m;
+    M = fmaxf(M, m);
+  }
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));  // the row's 16 lanes
   float L = 0.f;
   for (int c = j; c < nc; c += 16) {
-    const float m = LDCG(ml + c * mls);
-    if (m != -INFINITY) L = fmaf(exp2f(m - M), LDCG(ml + c * mls + 1), L);
+    const float m = w[c];
+    const float wc = m == -INFINITY ? 0.f : exp2f(m - M);
+    w[c] = wc;
+    L = fmaf(wc, LDCG(ml + c * mls + 1), L);
   }
 #pragma unroll
   for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  // channels d = j, j + 16, ...
+  __syncwarp();  // the row's weights are written by its own 16 lanes
+  // channels d = j, j + 16, ...: independent loads over the chunks
   constexpr int NV = HD / 16;
   float acc[NV];
 #pragma unroll
   for (int v = 0; v < NV; ++v) acc[v] = 0.f;
   const float* po = a.part_o + (static_cast<int64_t>(g0) * nh + h) * 16 * HD + q * HD + j;
   const int64_t pos_ = static_cast<int64_t>(nh) * 16 * HD;  // between chunks
+#pragma unroll 2
   for (int c = 0; c < nc; ++c) {
-    const float m = LDCG(ml + c * mls);
-    const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+    const float wc = w[c];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) acc[v] = fmaf(w, LDCG(po + c * pos_ + 16 * v), acc[v]);
+    for (int v = 0; v < NV; ++v) acc[v] = fmaf(wc, LDCG(po + c * pos_ + 16 * v), acc[v]);
   }
   if (q < a.K) {
     const int64_t r = (static_cast<int64_t>(b) * a.K + q) * D + h * HD + j;
@@ -627,6 +637,50 @@ __global__ void __launch_bounds__(256) xattn_combine_kernel(XattnArgs a, T* __re
       a.qacc[r + 16 * v] = 0.f;  // every item has read it
     }
   }
+}
+
+// Small batches: one CTA of HD threads per (request, head, query row), one thread per
+// channel, for more CTAs in flight when there are few requests.
+template <typename T, int HD>
+__global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* __restrict__ out) {
+  __shared__ float sw[kMaxChunksPerRequest];
+  __shared__ float red[32];
+  __shared__ int s_g[2];
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x;
+  const int nh = a.nh, D = nh * HD;
+  // the request's chunk range, loaded once per CTA
+  if (d < 2) s_g[d] = LDCG(a.plan + 3 + b + d);
+  __syncthreads();
+  const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
+  float mloc = -INFINITY;
+  for (int c = d; c < nc; c += HD) {
+    const float m = LDCG(a.part_ml + ((static_cast<int64_t>(g0 + c)) * nh + h) * 32 + 2 * qi);
+    sw[c] = m;
+    mloc = fmaxf(mloc, m);
+  }
+  // block max
+  mloc = warp_max(mloc);
+  if ((d & 31) == 0) red[d >> 5] = mloc;
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < HD / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float lloc = 0.f;
+  for (int c = d; c < nc; c += HD) {
+    const int64_t pidx = static_cast<int64_t>(g0 + c) * nh + h;
+    const float wgt = sw[c] == -INFINITY ? 0.f : exp2f(sw[c] - M);
+    sw[c] = wgt;
+    lloc = fmaf(wgt, LDCG(a.part_ml + pidx * 32 + 2 * qi + 1), lloc);
+  }
+  const float L = block_sum(lloc, red);  // synchronizes: sw complete
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < nc; ++c)
+    acc = fmaf(sw[c], LDCG(a.part_o + (static_cast<int64_t>(g0 + c) * nh + h) * 16 * HD + qi * HD + d), acc);
+  out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
+  a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
 }
 
 }  // namespace
@@ -711,10 +765,15 @@ cudaError_t xattn_prepare() {
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& args, void* out) {
   XattnArgs a = args;
   a.dev_err = L.dev_err;
-  dim3 cgrid(a.bs, a.nh);
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_kernel<T, HD>, cgrid, dim3(256), 0, a,
-                                                           static_cast<T*>(out)))));
+  if (a.bs <= kCombineRowsMaxBatch) {
+    FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_rows_kernel<T, HD>,
+                                                             dim3(a.bs, a.nh, a.K), dim3(HD), 0, a,
+                                                             static_cast<T*>(out)))));
+    return e;
+  }
+  FM_DISPATCH_T2(dtype, FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_combine_kernel<T, HD>, dim3(a.bs, a.nh, 4),
+                                                           dim3(64), 0, a, static_cast<T*>(out)))));
   return e;
 }
 

@@ -148,6 +148,32 @@ __global__ void full_scatter_kernel(const float* __restrict__ logits, int Vd, co
   }
 }
 
+// The same with V a multiple of 4 and 16-byte aligned rows: each thread maps 4
+// consecutive vocabulary entries (one int4 of the inverse map, read once) for
+// kScatterRows rows (one float4 streaming store per row: the full logits are written
+// once and not re-read here).
+constexpr int kScatterRows = 8;
+__global__ void __launch_bounds__(256) full_scatter4_kernel(const float* __restrict__ logits, int Vd,
+                                                            const int32_t* __restrict__ inv, int V, int rows,
+                                                            float* __restrict__ full) {
+  pdl_trigger();
+  const int v4 = blockIdx.x * blockDim.x + threadIdx.x;  // group of 4 entries
+  const bool live = v4 * 4 < V;
+  const int4 j = live ? *reinterpret_cast<const int4*>(inv + 4 * v4) : make_int4(-1, -1, -1, -1);
+  pdl_wait();
+  if (!live) return;
+  const int r0 = blockIdx.y * kScatterRows, r1 = min(rows, r0 + kScatterRows);
+  for (int r = r0; r < r1; ++r) {
+    const float* lr = logits + static_cast<int64_t>(r) * Vd;
+    float4 o;
+    o.x = j.x >= 0 ? LDCG(lr + j.x) : -INFINITY;
+    o.y = j.y >= 0 ? LDCG(lr + j.y) : -INFINITY;
+    o.z = j.z >= 0 ? LDCG(lr + j.z) : -INFINITY;
+    o.w = j.w >= 0 ? LDCG(lr + j.w) : -INFINITY;
+    __stcs(reinterpret_cast<float4*>(full + static_cast<int64_t>(r) * V) + v4, o);
+  }
+}
+
 }  // namespace
 
 // Merge slots of the sampler for callers that cannot allocate device memory: one
@@ -190,6 +216,10 @@ cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, 
 cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
                          float* full) {
   if (rows <= 0) return cudaSuccess;
+  if (V % 4 == 0 && (reinterpret_cast<uintptr_t>(full) & 15) == 0 && (reinterpret_cast<uintptr_t>(inv) & 15) == 0) {
+    dim3 grid((V / 4 + 255) / 256, (rows + kScatterRows - 1) / kScatterRows);
+    return launch_k(L, full_scatter4_kernel, grid, dim3(256), 0, logits, Vd, inv, V, rows, full);
+  }
   dim3 grid(std::min((V + 255) / 256, 64), rows);
   return launch_k(L, full_scatter_kernel, grid, dim3(256), 0, logits, Vd, inv, V, full);
 }
