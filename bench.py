@@ -113,7 +113,7 @@ def algorithmic_bytes(cfg: dict, req: dict) -> dict:
     w_draft = ((D * H + 2 * L * D * D + D * H + L * (6 * D * D + 2 * D * F)) * wes + H * H * es
                + (D + 2 * L * D + D + L * (6 * D + D + F)) * 4 * (wes == 1))
     w_head = Vd * D * wes + Vd * 4 * (wes == 1)
-    kv_row = L * 2 * D * es
+    kv_row = L * 2 * D * (1 if cfg.get("kv_dtype") == "e4m3" else es)
     kv_read = sum((p + 1) * kv_row for p in req["anchor_pos"])
     rows_written = (sum(req["commit"]) if req["window"] else 0) + bs
     logits = bs * K * Vd * 4
@@ -135,7 +135,7 @@ def setup_ours(workload: str, device: str):
     req = syn.make_requests(workload, device)
     bs, K = req["bs"], cfg["block_size"]
     dt = syn.torch_dtype(cfg["act_dtype"])
-    code = F.DTYPE_CODES[cfg["act_dtype"]]
+    code = F.DTYPE_CODES[cfg["kv_dtype"]]
     pool_t = torch.empty(F.flashmap_pool_bytes(cfg, req["num_pages"]), dtype=torch.uint8, device=device)
     pool = F.make_pool(pool_t, req["num_pages"], code)
     max_rows = max(max(req["ctx"]) if req["prefill"] else 0, bs * (K + 1))
@@ -148,7 +148,7 @@ def setup_ours(workload: str, device: str):
                                         torch.zeros(1, **i32), None, req["req_to_page"], None, ws)
         req.pop("prefill_hidden")
     else:
-        syn.fill_pool_random(pool_t.view(dt), req["kv_generator_seed"])
+        syn.fill_pool_random(pool_t.view(syn.torch_dtype(cfg["kv_dtype"])), req["kv_generator_seed"])
     Vd = cfg["draft_vocab_size"] if 0 < cfg["draft_vocab_size"] < cfg["vocab_size"] else cfg["vocab_size"]
     st = dict(
         F=F, cfg=cfg, model=model, E=E, req=req, pool_t=pool_t, pool=pool, ws=ws,

@@ -88,13 +88,21 @@ typedef enum { FLASHMAP_F32 = 0, FLASHMAP_BF16 = 1, FLASHMAP_E4M3 = 2 } flashmap
  *                        accumulation float32 (W8A16): the GEMM expands each e4m3 tile
  *                        to bf16 on chip and applies the scale to its output. Needs
  *                        target_hidden, hidden and intermediate multiples of 16.
+ *   kv_dtype             the draft KV pool's element type: act_dtype, or E4M3 (bf16
+ *                        activations only): keys (after k-norm and RoPE) and values
+ *                        are stored as e4m3fn with scale 1, rounded to nearest even
+ *                        and saturated at +-448, and the cross-attention quantizes each
+ *                        request's queries per head to e4m3 with scale
+ *                        max(max|q|, 1e-12) / 448 over the block's slots and channels,
+ *                        descaling the scores by it (flashmap/sglang/model.py,
+ *                        _paged_cross_attention_fp8). Halves the pool's bytes.
  */
 typedef struct {
   int32_t target_hidden, num_target_layers, hidden, num_layers, num_heads, head_dim;
   int32_t intermediate, cond_dim, time_embed_dim, block_size, vocab_size, draft_vocab_size;
   int32_t num_steps, noise_gate_constant, page_size, max_position;
   float time_scale, rope_theta, rms_norm_eps, qk_norm_eps, layer_norm_eps;
-  int32_t act_dtype, weight_dtype;
+  int32_t act_dtype, weight_dtype, kv_dtype;
 } flashmap_config;
 
 /* One DiT block's raw weights (flashmap/modeling_flashmap.py, FlashMapLayer), all
@@ -127,7 +135,7 @@ typedef struct {
 /*
  * The paged draft KV pool (flashmap/sglang/model.py, _fused_write_args: per layer
  * keys and values; tokenspeed dflash.py: req_to_page / page_size addressing).
- * Layout (device, act_dtype): [num_layers][2 (key, value)][num_pages][num_heads]
+ * Layout (device, kv_dtype): [num_layers][2 (key, value)][num_pages][num_heads]
  * [page_size][head_dim]; the slot of position pos of the request in page-table row
  * r is req_to_page[r][pos / P] * P + pos % P. Caller-owned; size it with
  * flashmap_pool_bytes.
@@ -135,7 +143,7 @@ typedef struct {
 typedef struct {
   void* base;
   int64_t num_pages;
-  int32_t dtype; /* must equal act_dtype */
+  int32_t dtype; /* must equal kv_dtype */
 } flashmap_kv_pool;
 
 typedef struct flashmap_model flashmap_model;

@@ -102,6 +102,7 @@ class Config:
     layer_norm_eps: float = 1e-6
     noise_gate_constant: bool = False  # False: "jump" gate, True: "constant"
     num_steps: int = 1
+    kv_dtype: str = ""  # "e4m3": the draft KV pool stores e4m3 keys/values (else act dtype)
 
     @staticmethod
     def from_dict(d: dict) -> "Config":
@@ -484,7 +485,10 @@ def dit_layer(cfg: Config, W: dict, l: int, mods: np.ndarray, x: np.ndarray, pos
     ca = f"{pre}.cross_attn"
     q = rms_norm(_heads(_linear(h, W[f"{ca}.q_proj.weight"]), cfg), W[f"{ca}.q_norm.weight"], cfg.qk_norm_eps)
     q = apply_rope(q, positions, cfg.rope_theta)
-    ctx = np.concatenate([attention(q[i * K:(i + 1) * K], contexts[i][0], contexts[i][1])
+    qs = [q[i * K:(i + 1) * K] for i in range(nreq)]
+    if cfg.kv_dtype == "e4m3":  # e4m3 pool: the queries are quantized per (request, head)
+        qs = [quantize_query_e4m3(qi) for qi in qs]
+    ctx = np.concatenate([attention(qs[i], contexts[i][0], contexts[i][1])
                           for i in range(nreq)]).reshape(x.shape[0], -1)
     x = x + m[5] * _linear(ctx, W[f"{ca}.o_proj.weight"])
     # MLP
@@ -638,3 +642,28 @@ def e4m3_constants(consts: Constants) -> Constants:
     from dataclasses import replace
 
     return replace(consts, head_w=dequantize(*quantize_e4m3_per_channel(consts.head_w)))
+
+
+# ---------------------------------------------------------------------------------
+# e4m3 draft KV pool (flashmap/sglang/model.py, _paged_cross_attention_fp8)
+# ---------------------------------------------------------------------------------
+
+
+def store_kv(cfg: Config, k: np.ndarray, v: np.ndarray) -> tuple:
+    """The values a pool of cfg's kv dtype holds for keys/values k, v: e4m3 with scale
+    1 (nearest even, saturated at +-448) for an e4m3 pool, else k, v themselves."""
+    if cfg.kv_dtype != "e4m3":
+        return k, v
+    return e4m3_round(np.asarray(k, dtype=np.float32)), e4m3_round(np.asarray(v, dtype=np.float32))
+
+
+def quantize_query_e4m3(q: np.ndarray) -> np.ndarray:
+    """One request's queries (slots, heads, hd) as the fp8 cross-attention sees them:
+    per head, scale = max(max|q| over slots and channels, 1e-12) / 448 in float32,
+    q8 = e4m3(q / scale) with the division in float32; returns q8 * scale (float64),
+    so that attention(q8 * scale, K, V) equals the descaled fp8 product."""
+    q32 = np.asarray(q, dtype=np.float32)
+    amax = np.max(np.abs(q32), axis=(0, 2))
+    scale = (np.maximum(amax, np.float32(1e-12)) / np.float32(E4M3_MAX)).astype(np.float32)
+    q8 = e4m3_round((q32 / scale[None, :, None]).astype(np.float32))
+    return q8 * _f64(scale)[None, :, None]

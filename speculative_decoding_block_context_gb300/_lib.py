@@ -31,7 +31,7 @@ class flashmap_config(_c.Structure):
         "intermediate", "cond_dim", "time_embed_dim", "block_size", "vocab_size", "draft_vocab_size",
         "num_steps", "noise_gate_constant", "page_size", "max_position")] + \
         [(n, _c.c_float) for n in ("time_scale", "rope_theta", "rms_norm_eps", "qk_norm_eps", "layer_norm_eps")] + \
-        [("act_dtype", _c.c_int32), ("weight_dtype", _c.c_int32)]
+        [("act_dtype", _c.c_int32), ("weight_dtype", _c.c_int32), ("kv_dtype", _c.c_int32)]
 
 
 LAYER_FIELDS = {
@@ -151,8 +151,9 @@ def _stream(stream):
 def make_config(d: dict) -> flashmap_config:
     c = flashmap_config()
     for name, ctype in flashmap_config._fields_:
-        if name in ("act_dtype", "weight_dtype"):
-            setattr(c, name, DTYPE_CODES[d[name]] if isinstance(d[name], str) else int(d[name]))
+        if name in ("act_dtype", "weight_dtype", "kv_dtype"):
+            v = d.get(name, d["act_dtype"])  # the pool defaults to the activation dtype
+            setattr(c, name, DTYPE_CODES[v] if isinstance(v, str) else int(v))
         elif ctype is _c.c_float:
             setattr(c, name, float(d[name]))
         else:

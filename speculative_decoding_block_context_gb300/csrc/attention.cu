@@ -194,8 +194,8 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
 // (rows >= K zero): q = RoPE(RMSNorm_{q_norm}(W_q n)) at the slot positions
 // p + 1 + k (flashmap/modeling_flashmap.py, FlashMapAttention.forward). Every item of a
 // (request, head) derives them from the projection accumulator; 128 threads.
-template <int HD>
-__device__ __forceinline__ void load_queries(const XattnArgs& a, int b, int h, float* sq) {
+template <int HD, bool kQuant = false>
+__device__ __forceinline__ float load_queries(const XattnArgs& a, int b, int h, float* sq) {
   constexpr int EPL = HD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D = a.nh * HD;
@@ -219,9 +219,37 @@ __device__ __forceinline__ void load_queries(const XattnArgs& a, int b, int h, f
       }
       head_norm_rope<EPL>(v[i], a.q_norm, a.eps, a.rope + static_cast<int64_t>(pos) * (HD / 2), lane);
     }
+  }
+  float qscale = 1.f;
+  if constexpr (kQuant) {
+    // e4m3 queries for an e4m3 pool: one scale per (request, head), max|q| / 448 over
+    // the block's slots and channels (flashmap/sglang/model.py, _paged_cross_attention_fp8)
+    __shared__ float red[4];
+    float mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) mx = fmaxf(mx, fabsf(v[i][e]));
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    qscale = __fdiv_rn(fmaxf(mx, 1e-12f), 448.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const __nv_fp8_storage_t q8 = __nv_cvt_float_to_fp8(__fdiv_rn(v[i][e], qscale), __NV_SATFINITE, __NV_E4M3);
+        v[i][e] = __half2float(__half(__nv_cvt_fp8_to_halfraw(q8, __NV_E4M3)));
+      }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int q = warp + 4 * i;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) sq[q * HD + lane * EPL + e] = v[i][e];
   }
+  return qscale;
 }
 
 // ------------------------------------------------------------------ paged cross-attention items (SIMT)
@@ -359,15 +387,49 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// bf16 operands for a bf16 pool; half for an e4m3 pool (e4m3 widens to half in one
+// conversion per pair, and the e4m3 queries and the probabilities are exact or finer
+// in half)
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  return F16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16)
+    mma_f16_16816(d, a, b0, b1);
+  else
+    mma_bf16_16816(d, a, b0, b1);
+}
 
-constexpr int kXStages = 3;
+constexpr int kXStages = 3;   // bf16 pool: cp.async stages per warp
+constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage)
 
-template <int HD>
+// Per warp: a ring of K/V blocks as they arrive and, for an e4m3 pool, one half block
+// pair (the converted current block) in the swizzled layout the ldmatrix reads use.
+template <int HD, bool F8 = false>
 struct XCfg {
-  static constexpr int ROWB = HD * 2;     // bytes of one position row
-  static constexpr int BLK = 16 * ROWB;   // one 16-position block of K (or V)
-  static constexpr int CH = HD / 8;       // 16-byte chunks per row
-  static constexpr int RING = kXStages * 2 * BLK;  // per warp
+  static constexpr int ROWB = HD * 2;     // bytes of one bf16 position row
+  static constexpr int BLK = 16 * ROWB;   // one 16-position block of K (or V), bf16
+  static constexpr int CH = HD / 8;       // 16-byte chunks per bf16 row
+  static constexpr int ROWB8 = HD;        // bytes of one e4m3 row
+  static constexpr int BLK8 = 16 * ROWB8;
+  static constexpr int CH8 = HD / 16;     // 16-byte chunks per e4m3 row
+  static constexpr int STAGES = F8 ? kXStages8 : kXStages;
+  static constexpr int STAGE = F8 ? 2 * BLK8 : 2 * BLK;
+  static constexpr int WORK = F8 ? 2 * BLK : 0;     // converted block pair (e4m3 only)
+  static constexpr int RING = STAGES * STAGE + WORK;  // per warp
   static constexpr int SMEM_RING = 4 * RING;
   static constexpr int SQ_OFF = SMEM_RING;          // the item's queries, beside the rings
   static constexpr int SMEM_Q = SQ_OFF + 16 * HD * 4;
@@ -375,9 +437,9 @@ struct XCfg {
   static constexpr int SMEM = SMEM_Q > SMEM_MERGE ? SMEM_Q : SMEM_MERGE;
 };
 
-template <int HD>
+template <int HD, bool F8>
 __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
-  using C = XCfg<HD>;
+  using C = XCfg<HD, F8>;
   extern __shared__ __align__(128) uint8_t xsm[];
   pdl_trigger();
   pdl_wait();
@@ -386,8 +448,11 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
   const int nh = a.nh;
   const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
   const int* pairs = a.plan + 4 + a.bs;
-  const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(a.pool);
+  const uint8_t* pool = static_cast<const uint8_t*>(a.pool);  // element e at byte e * (F8 ? 1 : 2)
+  constexpr int ES = F8 ? 1 : 2;
   const uint32_t ring = smem_u32(xsm) + warp * C::RING;
+  const uint32_t work = ring + C::STAGES * C::STAGE;  // e4m3: the converted block pair
+  uint8_t* work_ptr = xsm + warp * C::RING + C::STAGES * C::STAGE;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int g = item / nh, h = item - g * nh;
     const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
@@ -422,23 +487,35 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
         const int off = blk - pi * a.P;
         const int64_t kb = ((((static_cast<int64_t>(a.layer) * 2 + 0) * a.num_pages + (ok ? page : 0)) * nh + h) * a.P + off) * HD;
         const int64_t vb = kb + static_cast<int64_t>(a.num_pages) * nh * a.P * HD;
-        const uint32_t st = ring + (j % kXStages) * 2 * C::BLK;
+        const uint32_t st = ring + (j % C::STAGES) * C::STAGE;
+        if constexpr (F8) {  // rows of 16-byte chunks as stored; converted after arrival
 #pragma unroll
-        for (int i = lane; i < 16 * C::CH; i += 32) {
-          const int r = i / C::CH, ch = i - r * C::CH;
-          const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
-          const uint32_t dst = st + r * C::ROWB + ((ch ^ (r & 7)) << 4);
-          cp_async16(dst, pool + kb + r * HD + ch * 8, bytes);
-          cp_async16(dst + C::BLK, pool + vb + r * HD + ch * 8, bytes);
+          for (int i = lane; i < 16 * C::CH8; i += 32) {
+            const int r = i / C::CH8, ch = i - r * C::CH8;
+            const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
+            const uint32_t dst = st + r * C::ROWB8 + (ch << 4);
+            cp_async16(dst, pool + (kb + r * HD) * ES + ch * 16, bytes);
+            cp_async16(dst + C::BLK8, pool + (vb + r * HD) * ES + ch * 16, bytes);
+          }
+        } else {
+#pragma unroll
+          for (int i = lane; i < 16 * C::CH; i += 32) {
+            const int r = i / C::CH, ch = i - r * C::CH;
+            const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
+            const uint32_t dst = st + r * C::ROWB + ((ch ^ (r & 7)) << 4);
+            cp_async16(dst, pool + (kb + r * HD) * ES + ch * 16, bytes);
+            cp_async16(dst + C::BLK, pool + (vb + r * HD) * ES + ch * 16, bytes);
+          }
         }
       }
       cp_async_commit();
     };
 #pragma unroll
-    for (int j = 0; j < kXStages - 1; ++j) issue(j);
+    for (int j = 0; j < C::STAGES - 1; ++j) issue(j);
     // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
-    load_queries<HD>(a, b, h, sq);
+    const float qscale = load_queries<HD, F8>(a, b, h, sq);  // 1 unless e4m3 queries
+    const float s_scale = a.scale_log2 * qscale;
     __syncthreads();
     uint32_t qa[HD / 16][4];
 #pragma unroll
@@ -447,7 +524,7 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int row = g8 + ((j & 1) << 3);
         const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
-        qa[kk][j] = pack_bf16(sq[row * HD + col], sq[row * HD + col + 1]);
+        qa[kk][j] = pack2<F8>(sq[row * HD + col], sq[row * HD + col + 1]);
       }
     }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -455,11 +532,29 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     for (int j = 0; j < nj; ++j) {
-      issue(j + kXStages - 1);
-      cp_async_wait<kXStages - 1>();
+      issue(j + C::STAGES - 1);
+      cp_async_wait<C::STAGES - 1>();
       __syncwarp();
       const int blk = p0 + ((warp + 4 * j) << 4);
-      const uint32_t kst = ring + (j % kXStages) * 2 * C::BLK, vst = kst + C::BLK;
+      uint32_t kst = ring + (j % C::STAGES) * C::STAGE, vst = kst + C::BLK;
+      if constexpr (F8) {
+        // e4m3 K and V rows -> half (exact) in the swizzled layout: 16-byte chunk c of
+        // a row holds channels 16c..16c+15 and becomes half chunks 2c and 2c+1
+        const uint8_t* st8 = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
+#pragma unroll
+        for (int i = lane; i < 2 * 16 * C::CH8; i += 32) {
+          const int kv = i / (16 * C::CH8), rem = i - kv * 16 * C::CH8;
+          const int r = rem / C::CH8, c = rem - r * C::CH8;
+          uint4 lo, hi;
+          e4m3x16_to_f16(*reinterpret_cast<const uint4*>(st8 + kv * C::BLK8 + r * C::ROWB8 + c * 16), lo, hi);
+          uint8_t* row = work_ptr + kv * C::BLK + r * C::ROWB;
+          *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        __syncwarp();
+        kst = work;
+        vst = work + C::BLK;
+      }
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk) {
@@ -467,8 +562,8 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
         const int ch = kk * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(s[0], qa[kk], b0, b1);
-        mma_bf16_16816(s[1], qa[kk], b2, b3);
+        mma16816<F8>(s[0], qa[kk], b0, b1);
+        mma16816<F8>(s[1], qa[kk], b2, b3);
       }
       // scale to base 2 and mask positions past the chunk
 #pragma unroll
@@ -476,7 +571,7 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
-          s[nt][e] = pos < p1 ? s[nt][e] * a.scale_log2 : -INFINITY;
+          s[nt][e] = pos < p1 ? s[nt][e] * s_scale : -INFINITY;
         }
       float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
       float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
@@ -506,16 +601,16 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
         o[i][2] *= c1;
         o[i][3] *= c1;
       }
-      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]), pack_bf16(p[1][0], p[1][1]),
-                              pack_bf16(p[1][2], p[1][3])};
+      const uint32_t pa[4] = {pack2<F8>(p[0][0], p[0][1]), pack2<F8>(p[0][2], p[0][3]), pack2<F8>(p[1][0], p[1][1]),
+                              pack2<F8>(p[1][2], p[1][3])};
 #pragma unroll
       for (int dn = 0; dn < HD / 16; ++dn) {
         const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
         const int ch = dn * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dn], pa, b0, b1);
-        mma_bf16_16816(o[2 * dn + 1], pa, b2, b3);
+        mma16816<F8>(o[2 * dn], pa, b0, b1);
+        mma16816<F8>(o[2 * dn + 1], pa, b2, b3);
       }
       __syncwarp();
     }
@@ -746,7 +841,11 @@ cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args) {
   const int grid = L.num_sms * 2;
   cudaError_t e = cudaSuccess;
   if (dtype == FLASHMAP_BF16) {
-    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD>, dim3(grid), dim3(128), XCfg<HD>::SMEM, a)));
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false>, dim3(grid), dim3(128),
+                                       XCfg<HD, false>::SMEM, a)));
+  } else if (dtype == FLASHMAP_E4M3) {
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true>, dim3(grid), dim3(128),
+                                       XCfg<HD, true>::SMEM, a)));
   } else {
     FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_simt_kernel<float, HD>, dim3(grid), dim3(128), 0, a)));
   }
@@ -754,12 +853,15 @@ cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args) {
 }
 
 cudaError_t xattn_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(xattn_items_mma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       XCfg<128>::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(xattn_items_mma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<64>::SMEM);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(xattn_items_mma_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, XCfg<32>::SMEM);
+  cudaError_t e = cudaSuccess;
+#define FM_XATTR(HD_, F8_)                                                                                      \
+  if (e == cudaSuccess)                                                                                         \
+    e = cudaFuncSetAttribute(xattn_items_mma_kernel<HD_, F8_>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             XCfg<HD_, F8_>::SMEM);
+  FM_XATTR(128, false) FM_XATTR(64, false) FM_XATTR(32, false) FM_XATTR(128, true) FM_XATTR(64, true)
+  FM_XATTR(32, true)
+#undef FM_XATTR
+  return e;
 }
 
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& args, void* out) {

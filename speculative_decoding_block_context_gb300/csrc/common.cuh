@@ -128,6 +128,43 @@ __device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __r
   head_norm_rope_w<EPL>(v, wr, eps, rope, lane);
 }
 
+// e4m3 x 16 (one 16-byte chunk) -> bf16 x 16 (two 16-byte chunks).
+// Every e4m3 value is exact in half and in bf16.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 u, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      const float2 f = __half22float2(__half2(hr));
+      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// e4m3 x 16 -> half x 16 (one conversion per pair; every e4m3 value is exact in half).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 u, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const __half2_raw hr =
+          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+      o[2 * i + h] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // ------------------------------------------------------------------ shared memory / mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -59,7 +59,7 @@ struct LayerW {
 struct flashmap_model {
   flashmap_config cfg;
   int device = 0, num_sms = 0;
-  int adt = FLASHMAP_F32, wdt = FLASHMAP_F32;
+  int adt = FLASHMAP_F32, wdt = FLASHMAP_F32, kdt = FLASHMAP_F32;  // activations, GEMM weights, KV pool
   int H = 0, Lt = 0, D = 0, L = 0, nh = 0, hd = 0, F = 0, K = 0, V = 0, Vd = 0, P = 0, maxpos = 0;
   void* arena = nullptr;
   unsigned* dev_err = nullptr;
@@ -144,6 +144,8 @@ flashmap_status validate(const flashmap_config* c) {
   if (!is_act(c->act_dtype)) return fail(FLASHMAP_E_INVALID, "act_dtype must be F32 or BF16");
   if (c->weight_dtype != c->act_dtype && !(c->weight_dtype == FLASHMAP_E4M3 && c->act_dtype == FLASHMAP_BF16))
     return fail(FLASHMAP_E_INVALID, "weight_dtype must equal act_dtype (or E4M3 with BF16 activations)");
+  if (c->kv_dtype != c->act_dtype && !(c->kv_dtype == FLASHMAP_E4M3 && c->act_dtype == FLASHMAP_BF16))
+    return fail(FLASHMAP_E_INVALID, "kv_dtype must equal act_dtype (or E4M3 with BF16 activations)");
   if (c->weight_dtype == FLASHMAP_E4M3 && (c->target_hidden % 16 || c->hidden % 16 || c->intermediate % 16))
     return fail(FLASHMAP_E_UNSUPPORTED, "E4M3 weights need target_hidden, hidden and intermediate multiples of 16");
   {
@@ -278,7 +280,7 @@ flashmap_status flashmap_pool_bytes(const flashmap_config* cfg, int64_t num_page
   if (st != FLASHMAP_OK) return st;
   if (!bytes || num_pages <= 0) return fail(FLASHMAP_E_INVALID, "num_pages must be positive and bytes non-NULL");
   *bytes = static_cast<size_t>(cfg->num_layers) * 2 * static_cast<size_t>(num_pages) * cfg->num_heads *
-           cfg->page_size * cfg->head_dim * dt_size(cfg->act_dtype);
+           cfg->page_size * cfg->head_dim * dt_size(cfg->kv_dtype);
   return FLASHMAP_OK;
 }
 
@@ -329,6 +331,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   m->cfg = *cfg;
   m->adt = cfg->act_dtype;
   m->wdt = cfg->weight_dtype;
+  m->kdt = cfg->kv_dtype;
   m->H = cfg->target_hidden;
   m->Lt = cfg->num_target_layers;
   m->D = cfg->hidden;
@@ -625,8 +628,8 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
   if (!m || !pool || !target_hidden || !req_pool_idx || !start_pos || !req_to_page || !workspace)
     return fail(FLASHMAP_E_INVALID, "NULL argument");
   if (bs <= 0 || W <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs, W and the page-table stride must be positive");
-  if (pool->dtype != m->adt || !pool->base || pool->num_pages <= 0)
-    return fail(FLASHMAP_E_INVALID, "pool dtype must equal act_dtype, with pages");
+  if (pool->dtype != m->kdt || !pool->base || pool->num_pages <= 0)
+    return fail(FLASHMAP_E_INVALID, "pool dtype must equal kv_dtype, with pages");
   if (m->adt == FLASHMAP_BF16 && (reinterpret_cast<uintptr_t>(target_hidden) & 15))
     return fail(FLASHMAP_E_INVALID, "target_hidden must be 16-byte aligned");
   const int64_t total = static_cast<int64_t>(bs) * W;
@@ -679,7 +682,7 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     a.max_pos = m->maxpos;
     a.pool = pool->base;
     a.out_loc = out_loc;
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->adt, a));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
   }
   return FLASHMAP_OK;
 }
@@ -694,8 +697,8 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   if (!m || !pool || !anchor_ids || !anchor_pos || !req_pool_idx || !req_to_page || !seeds || !hidden_out || !workspace)
     return fail(FLASHMAP_E_INVALID, "NULL argument");
   if (bs <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs and the page-table stride must be positive");
-  if (pool->dtype != m->adt || !pool->base || pool->num_pages <= 0)
-    return fail(FLASHMAP_E_INVALID, "pool dtype must equal act_dtype, with pages");
+  if (pool->dtype != m->kdt || !pool->base || pool->num_pages <= 0)
+    return fail(FLASHMAP_E_INVALID, "pool dtype must equal kv_dtype, with pages");
   if (!std::isfinite(noise_scale)) return fail(FLASHMAP_E_INVALID, "noise_scale must be finite");
   const DraftWs need = carve_draft(m, bs, nullptr);
   if (workspace_bytes < need.bytes)
@@ -743,7 +746,7 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     a.max_pos = m->maxpos;
     a.pool = pool->base;
     a.out_loc = anchor_loc_out;
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, adt, a));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
   }
   // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act));
@@ -785,7 +788,7 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
     xa.layer = l;
     xa.q_norm = lw.cqn;
-    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, adt, xa));
+    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa));
     TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
     TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));

@@ -58,25 +58,6 @@ struct TcCfg {
   static constexpr int PER_SM = FIT < FM_TC_CTAS_PER_SM ? (FIT < 1 ? 1 : FIT) : FM_TC_CTAS_PER_SM;
 };
 
-// e4m3 x 16 (one 16-byte chunk of a weight row) -> bf16 x 16 (two 16-byte chunks).
-// Every e4m3 value is exact in half and in bf16.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 u, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __half2_raw hr =
-          __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
-      const float2 f = __half22float2(__half2(hr));
-      const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-      o[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
-}
 
 __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();

@@ -58,6 +58,17 @@ __device__ __forceinline__ void store_vec(T* dst, const float* v) {
     *reinterpret_cast<uint2*>(dst) = u;
   } else if constexpr (sizeof(T) == 4 && N == 4) {
     *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  } else if constexpr (sizeof(T) == 1) {  // e4m3 pool: scale 1, nearest even, saturated at +-448
+    uint32_t u = 0;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+      u |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(v[e], __NV_SATFINITE, __NV_E4M3)) << (8 * (e & 3));
+    if constexpr (N == 4)
+      *reinterpret_cast<uint32_t*>(dst) = u;
+    else if constexpr (N == 2)
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(u);
+    else
+      dst[0] = static_cast<T>(u);
   } else {
 #pragma unroll
     for (int e = 0; e < N; ++e) dst[e] = from_f32<T>(v[e]);
@@ -344,7 +355,12 @@ cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a) {
   dim3 grid(a.rows, a.L);
   cudaError_t e = cudaSuccess;
   const dim3 block(32 * std::min(a.nh, 32));
-  FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, block, 0, b))));
+  if (dtype == FLASHMAP_E4M3) {
+    using T = uint8_t;
+    FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, block, 0, b)));
+  } else {
+    FM_DISPATCH_T(dtype, FM_DISPATCH_EPL(a.hd, (e = launch_k(L, kv_write_kernel<T, EPL>, grid, block, 0, b))));
+  }
   return e;
 }
 

@@ -62,6 +62,8 @@ WORKLOADS = {
                        window=True, temps=("mix", 0.5, 1.2), full_scatter=True, seed=11),
     "attn_probe": dict(model="probe", bs=16, ctx=("fixed", 4096), prefill=False, window=False,
                        temps=("greedy",), full_scatter=False, seed=6),
+    "attn_probe_kv8": dict(model="probe", bs=16, ctx=("fixed", 4096), prefill=False, window=False,
+                           temps=("greedy",), full_scatter=False, seed=6, kv_dtype="e4m3"),
     "qwen3_8b_bs1": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
                          temps=("all", 1.0), full_scatter=False, seed=2),
     "qwen3_8b_bs32": dict(model="qwen3_8b", bs=32, ctx=("uniform", 512, 8192), prefill=False,
@@ -72,6 +74,16 @@ WORKLOADS = {
     "qwen3_8b_fp8_bs64": dict(model="qwen3_8b", bs=64, ctx=("uniform", 1024, 16384),
                               prefill=False, window=False, temps=("greedy",),
                               full_scatter=False, seed=5, weight_dtype="e4m3"),
+    # e4m3 draft KV pool (keys and values stored with scale 1, fp8 queries per head)
+    "small_bf16_kv8": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
+                           window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=12,
+                           kv_dtype="e4m3"),
+    "qwen3_8b_bs32_kv8": dict(model="qwen3_8b", bs=32, ctx=("uniform", 512, 8192), prefill=False,
+                              window=False, temps=("mix", 0.5, 1.2), full_scatter=False, seed=3,
+                              kv_dtype="e4m3"),
+    "qwen3_8b_bs128_kv8": dict(model="qwen3_8b", bs=128, ctx=("loguniform", 16, 32768),
+                               prefill=False, window=True, temps=("mix", 0.5, 1.2),
+                               full_scatter=True, seed=4, kv_dtype="e4m3"),
 }
 
 MODEL_SEED = 1234  # one weight draw per model shape, shared by its workloads
@@ -83,11 +95,12 @@ def model_config(workload: str) -> dict:
     cfg.update(COMMON)
     if "weight_dtype" in wl:
         cfg["weight_dtype"] = wl["weight_dtype"]
+    cfg["kv_dtype"] = wl.get("kv_dtype", cfg["act_dtype"])
     return cfg
 
 
 def torch_dtype(name: str):
-    return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[name]
 
 
 def weight_shapes(cfg: dict) -> dict:
@@ -241,4 +254,7 @@ def fill_pool_random(pool: torch.Tensor, seed: int) -> None:
     chunk = 1 << 28
     for s in range(0, flat.numel(), chunk):
         n = min(chunk, flat.numel() - s)
-        flat[s : s + n] = torch.randn((n,), generator=g, device=pool.device, dtype=pool.dtype)
+        if pool.dtype == torch.float8_e4m3fn:  # drawn in float32, stored as e4m3
+            flat[s : s + n] = torch.randn((n,), generator=g, device=pool.device).to(pool.dtype)
+        else:
+            flat[s : s + n] = torch.randn((n,), generator=g, device=pool.device, dtype=pool.dtype)

@@ -45,7 +45,9 @@ def test_validate_configs_of_every_workload(lib):
         (dict(vocab_size=0), 1),
         (dict(act_dtype="f32", weight_dtype="bf16"), 1),
         (dict(act_dtype="f32", weight_dtype="e4m3"), 1),  # e4m3 weights need bf16 activations
-        (dict(act_dtype="bf16", weight_dtype="e4m3", intermediate=392), 2),  # not a multiple of 16
+        (dict(act_dtype="bf16", weight_dtype="e4m3", kv_dtype="bf16", intermediate=392), 2),  # not a multiple of 16
+        (dict(act_dtype="f32", weight_dtype="f32", kv_dtype="e4m3"), 1),  # an e4m3 pool needs bf16 activations
+        (dict(act_dtype="bf16", weight_dtype="bf16", kv_dtype="f32"), 1),
         (dict(time_embed_dim=63), 1),
         (dict(rope_theta=-1.0), 1),
     ],
@@ -85,3 +87,12 @@ def test_null_model_calls_fail_cleanly(lib):
     assert lib.flashmap_free(None) == 0
     assert lib.flashmap_draft_block(None, None, 1, None, None, None, None, 1, None, 1.0, None, None, None, 0,
                                     None) == 1
+
+
+def test_e4m3_pool_is_half_the_bf16_pool(lib):
+    cfg = syn.model_config("qwen3_8b_bs32_kv8")
+    assert cfg["kv_dtype"] == "e4m3"
+    n8 = F.flashmap_pool_bytes(cfg, 7)
+    assert n8 * 2 == F.flashmap_pool_bytes(dict(cfg, kv_dtype="bf16"), 7)
+    L, nh, P, hd = (cfg[k] for k in ("num_layers", "num_heads", "page_size", "head_dim"))
+    assert n8 == L * 2 * 7 * nh * P * hd

@@ -144,6 +144,21 @@ def test_small_bf16_end_to_end(small):
     assert torch.equal(run.full[:, hot], run.logits)
 
 
+@pytest.fixture(scope="module")
+def small_kv8():
+    return load_model("small_bf16_kv8")
+
+
+def test_small_e4m3_kv_pool_end_to_end(small_kv8):
+    """e4m3 draft KV pool: the written rows are the e4m3 rounding (scale 1) of the
+    oracle's keys/values, and the draft with fp8 queries per (request, head) matches
+    the oracle run on the stored values."""
+    run = run_library("small_bf16_kv8", small_kv8)
+    assert run.dev_err == 0
+    assert run.pool_t.numel() * 2 == F.flashmap_pool_bytes(dict(small_kv8.cfg, kv_dtype="bf16"), run.req["num_pages"])
+    _check_all(small_kv8, run, range(run.req["bs"]), TOL["bf16"])
+
+
 def test_noise_scale_zero_is_seed_independent(small):
     """noise_scale 0 makes the draft a fixed function of the context: other seeds give
     the same hidden states, up to the run-to-run order of the GEMMs' float32 atomic

@@ -69,6 +69,21 @@ def test_qwen3_bs32_ragged_contexts(qwen):
     _run_and_check(qwen, "qwen3_8b_bs32")
 
 
+def test_qwen3_e4m3_kv_pool_bs32(qwen):
+    """The batch-32 workload over an e4m3 draft KV pool: the same weights loaded with
+    kv_dtype e4m3 (the oracle reads the pool's e4m3 values and quantizes its queries
+    per (request, head) as the fp8 cross-attention does)."""
+    import dataclasses
+
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    cfg8 = syn.model_config("qwen3_8b_bs32_kv8")
+    st8 = dataclasses.replace(qwen, cfg=cfg8, handle=F.flashmap_load_weights(cfg8, qwen.W, qwen.E, qwen.LM, qwen.rank))
+    run, _ = _run_and_check(st8, "qwen3_8b_bs32_kv8")
+    del run, st8
+    torch.cuda.empty_cache()
+
+
 def test_qwen3_fp8_weights_bs64_greedy(qwen):
     """Config 5: e4m3 DiT weights with per-channel scales, bf16 activations; the oracle
     runs on the dequantized weights. The bf16 model of the other tests stays loaded."""
