@@ -669,6 +669,277 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
   }
 }
 
+// ------------------------------------------------------------------ paged cross-attention items (TMA-fed)
+//
+// bf16 pool, head_dim 64 or 128. The same items and arithmetic as the cp.async kernel
+// above, but each warp's 16-position blocks of K and V are fetched by one lane with
+// TMA tensor copies (the pool viewed as rows of head_dim channels; one 64-channel box
+// of 16 rows per copy, 128-byte swizzled for conflict-free ldmatrix) into a per-warp
+// ring completed on mbarriers: a block costs the warp 2 * HD / 64 copy instructions
+// instead of 16 per-lane cp.async with their address arithmetic. Rows past the chunk
+// (or of an invalid page) arrive as whatever the pool holds there: their scores are
+// masked and, in partial blocks, their value rows are zeroed before use.
+
+constexpr int kXattnTmaMaxBatch = 8;
+
+template <int HD>
+struct XTCfg {
+  static constexpr int BOX = 16 * 128;         // 16 rows x 64 bf16 channels, 128B-swizzled
+  static constexpr int NB = HD / 64;           // boxes per block of K (or V)
+  static constexpr int BLK = NB * BOX;
+  static constexpr int STAGES = 3;
+  static constexpr int STAGE = 2 * BLK;        // K then V
+  static constexpr int RING = STAGES * STAGE;  // per warp
+  static constexpr int SMEM_RING = 4 * RING;
+  static constexpr int SQ_OFF = SMEM_RING;
+  static constexpr int SMEM_Q = SQ_OFF + 16 * HD * 4;
+  static constexpr int SMEM_MERGE = 4 * 16 * (HD + 2) * 4;
+  static constexpr int SMEM = (SMEM_Q > SMEM_MERGE ? SMEM_Q : SMEM_MERGE) + 1024;  // + alignment slack
+};
+
+// byte offset of 16-byte chunk ch (0 .. HD/8-1) of row r in a block of XTCfg layout
+__device__ __forceinline__ uint32_t xt_off(int r, int ch) {
+  return static_cast<uint32_t>((ch >> 3) * (16 * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_constant__ CUtensorMap kvmap,
+                                                                 XattnArgs a) {
+  using C = XTCfg<HD>;
+  extern __shared__ uint8_t xraw[];
+  __shared__ uint64_t bars[4][C::STAGES];
+  __shared__ volatile int abort_flag;
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const uint32_t raw = smem_u32(xraw);
+  uint8_t* xsm = xraw + (((raw + 1023u) & ~1023u) - raw);  // 1024-aligned: the swizzle atom
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < 4; ++w)
+      for (int st = 0; st < C::STAGES; ++st) mbar_init(&bars[w][st], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  const int nh = a.nh;
+  const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
+  const int* pairs = a.plan + 4 + a.bs;
+  const uint32_t ring = smem_u32(xsm) + warp * C::RING;
+  uint8_t* ring_ptr = xsm + warp * C::RING;
+  const int64_t rows_per_kv = a.num_pages * nh * a.P;  // pool rows between a layer's keys and values
+  uint32_t jt = 0;      // blocks this warp has issued (and consumed), over all its items
+  uint32_t okm = 0;     // bit st: the block in stage st comes from a valid page
+  const uint64_t pol = l2_policy_evict_first();  // keys and values are read once
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int g = item / nh, h = item - g * nh;
+    const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
+    const int n = LDCG(a.anchor_pos + b) + 1;
+    const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
+    const int nblk = (p1 - p0 + 15) >> 4;
+    const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
+    const int nj = warp < nblk ? (nblk - warp + 3) >> 2 : 0;
+    const int32_t* r2p = a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride;
+    auto page_ids = [&](int j0) {
+      const int j = j0 + lane;
+      if (j >= nj) return -1;
+      const int pi = (p0 + ((warp + 4 * j) << 4)) / a.P;
+      return pi < a.r2p_stride ? LDCG(r2p + pi) : -1;
+    };
+    int pg = page_ids(0), pg_group = 0;
+    // the page of block j of this item (warp-uniform; -1 if invalid)
+    auto page_of = [&](int j) {
+      if ((j >> 5) != pg_group) {
+        pg_group = j >> 5;
+        pg = page_ids(j & ~31);
+      }
+      const int page = __shfl_sync(0xffffffffu, pg, j & 31);
+      return (page >= 0 && page < a.num_pages) ? page : -1;
+    };
+    auto issue = [&](int j) {
+      if (j >= nj) return;
+      const int blk = p0 + ((warp + 4 * j) << 4);
+      const int pi = blk / a.P;
+      const int page = page_of(j);
+      if (page < 0 && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
+      const uint32_t st = (jt + j) % C::STAGES;
+      okm = page < 0 ? (okm & ~(1u << st)) : (okm | (1u << st));
+      if (lane == 0) {
+        const int64_t krow = ((static_cast<int64_t>(a.layer) * 2 * a.num_pages + (page < 0 ? 0 : page)) * nh + h) * a.P +
+                             (blk - pi * a.P);
+        uint8_t* dst = ring_ptr + st * C::STAGE;
+        mbar_arrive_expect_tx(&bars[warp][st], C::STAGE);
+#pragma unroll
+        for (int bx = 0; bx < C::NB; ++bx) {
+          tma_load_2d(dst + bx * C::BOX, &kvmap, &bars[warp][st], bx * 64, static_cast<int>(krow), pol);
+          tma_load_2d(dst + C::BLK + bx * C::BOX, &kvmap, &bars[warp][st], bx * 64,
+                      static_cast<int>(krow + rows_per_kv), pol);
+        }
+      }
+    };
+#pragma unroll
+    for (int j = 0; j < C::STAGES - 1; ++j) issue(j);
+    // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
+    float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
+    load_queries<HD>(a, b, h, sq);
+    __syncthreads();
+    uint32_t qa[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = g8 + ((j & 1) << 3);
+        const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
+        qa[kk][j] = pack_bf16(sq[row * HD + col], sq[row * HD + col + 1]);
+      }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    int jdone = 0;  // blocks of this item consumed
+    for (int j = 0; j < nj; ++j) {
+      issue(j + C::STAGES - 1);
+      const uint32_t st = (jt + j) % C::STAGES, par = ((jt + j) / C::STAGES) & 1;
+      if (!mbar_wait(&bars[warp][st], par, &abort_flag)) break;
+      jdone = j + 1;
+      const int blk = p0 + ((warp + 4 * j) << 4);
+      const uint32_t kst = ring + st * C::STAGE, vst = kst + C::BLK;
+      const int valid = (okm >> st) & 1u ? min(16, p1 - blk) : 0;  // rows holding positions of the chunk
+      if (valid < 16) {  // warp-uniform: zero the value rows past them
+        uint8_t* v = ring_ptr + st * C::STAGE + C::BLK;
+        for (int i = lane; i < 16 * (HD / 8); i += 32) {
+          const int r = i / (HD / 8), ch = i - r * (HD / 8);
+          if (r >= valid) *reinterpret_cast<uint4*>(v + xt_off(r, ch)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+      }
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const int r = (lane & 7) + ((lane >> 4) << 3);
+        const int ch = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + xt_off(r, ch), b0, b1, b2, b3);
+        mma_bf16_16816(s[0], qa[kk], b0, b1);
+        mma_bf16_16816(s[1], qa[kk], b2, b3);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = nt * 8 + 2 * t4 + (e & 1);
+          s[nt][e] = r < valid ? s[nt][e] * a.scale_log2 : -INFINITY;
+        }
+      float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+      float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+      const float c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = n0 == -INFINITY ? 0.f : exp2f(s[nt][0] - n0);
+        p[nt][1] = n0 == -INFINITY ? 0.f : exp2f(s[nt][1] - n0);
+        p[nt][2] = n1 == -INFINITY ? 0.f : exp2f(s[nt][2] - n1);
+        p[nt][3] = n1 == -INFINITY ? 0.f : exp2f(s[nt][3] - n1);
+      }
+      l0 = l0 * c0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
+      l1 = l1 * c1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
+      m0 = n0;
+      m1 = n1;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        o[i][0] *= c0;
+        o[i][1] *= c0;
+        o[i][2] *= c1;
+        o[i][3] *= c1;
+      }
+      const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]), pack_bf16(p[1][0], p[1][1]),
+                              pack_bf16(p[1][2], p[1][3])};
+#pragma unroll
+      for (int dn = 0; dn < HD / 16; ++dn) {
+        const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int ch = dn * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + xt_off(r, ch), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dn], pa, b0, b1);
+        mma_bf16_16816(o[2 * dn + 1], pa, b2, b3);
+      }
+      __syncwarp();
+    }
+    if (jdone < nj) {
+      // a wait gave up: wait (bounded) for this warp's copies still in flight, so that
+      // none lands after the CTA has moved on; the CTA then stops after this item
+      const int issued = min(nj, jdone + C::STAGES - 1 + 1);
+      for (int q = jdone; q < issued; ++q) {
+        const uint32_t st = (jt + q) % C::STAGES, par = ((jt + q) / C::STAGES) & 1;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(&bars[warp][st], par) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        }
+      }
+      if (lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_TIMEOUT);
+    }
+    jt += nj;
+    // row sums over the quad
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    __syncthreads();  // every warp is done with its ring: reuse it for the merge
+    float* mm = reinterpret_cast<float*>(xsm);        // [4][16] max
+    float* ll = mm + 64;                               // [4][16] sum
+    float* oo = ll + 64;                               // [4][16][HD]
+    if (t4 == 0) {
+      mm[warp * 16 + g8] = m0;
+      mm[warp * 16 + g8 + 8] = m1;
+      ll[warp * 16 + g8] = l0;
+      ll[warp * 16 + g8 + 8] = l1;
+    }
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) {
+      float* r0 = oo + (warp * 16 + g8) * HD + i * 8 + 2 * t4;
+      float* r1 = oo + (warp * 16 + g8 + 8) * HD + i * 8 + 2 * t4;
+      r0[0] = o[i][0];
+      r0[1] = o[i][1];
+      r1[0] = o[i][2];
+      r1[1] = o[i][3];
+    }
+    __syncthreads();
+    const int64_t pidx = static_cast<int64_t>(g) * nh + h;
+    {
+      const int q = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * (HD / 8);
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 16 + q]);
+      float wgt[4], L = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = mm[w * 16 + q];
+        wgt[w] = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+        L = fmaf(wgt[w], ll[w * 16 + q], L);
+      }
+      float* po = a.part_o + pidx * 16 * HD + q * HD;
+      for (int d = d0; d < d0 + HD / 8; ++d) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc = fmaf(wgt[w], oo[(w * 16 + q) * HD + d], acc);
+        po[d] = acc;
+      }
+      if ((threadIdx.x & 7) == 0) {
+        a.part_ml[pidx * 32 + 2 * q] = M;
+        a.part_ml[pidx * 32 + 2 * q + 1] = L;
+      }
+    }
+    __syncthreads();
+    if (abort_flag) break;  // the same value in every warp after the barrier
+  }
+}
+
 // ------------------------------------------------------------------ combine
 
 // One CTA of 64 threads per (request, head, 4 query rows): the chunks' running maxima
@@ -835,12 +1106,19 @@ cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int n
                   xattn_max_chunks(L.num_sms, nh, bs), plan, L.dev_err);
 }
 
-cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args) {
+cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args, const CUtensorMap* kvmap) {
   XattnArgs a = args;
   a.dev_err = L.dev_err;
   const int grid = L.num_sms * 2;
   cudaError_t e = cudaSuccess;
-  if (dtype == FLASHMAP_BF16) {
+  // TMA-fed at small batches (fewer instructions on the latency-bound path); the
+  // cp.async kernel measured slightly faster once the pool streams at full rate
+  if (dtype == FLASHMAP_BF16 && kvmap && (a.hd == 64 || a.hd == 128) && a.bs <= kXattnTmaMaxBatch) {
+    if (a.hd == 128)
+      e = launch_k(L, xattn_items_tma_kernel<128>, dim3(grid), dim3(128), XTCfg<128>::SMEM, *kvmap, a);
+    else
+      e = launch_k(L, xattn_items_tma_kernel<64>, dim3(grid), dim3(128), XTCfg<64>::SMEM, *kvmap, a);
+  } else if (dtype == FLASHMAP_BF16) {
     FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false>, dim3(grid), dim3(128),
                                        XCfg<HD, false>::SMEM, a)));
   } else if (dtype == FLASHMAP_E4M3) {
@@ -861,6 +1139,12 @@ cudaError_t xattn_prepare() {
   FM_XATTR(128, false) FM_XATTR(64, false) FM_XATTR(32, false) FM_XATTR(128, true) FM_XATTR(64, true)
   FM_XATTR(32, true)
 #undef FM_XATTR
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(xattn_items_tma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             XTCfg<128>::SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(xattn_items_tma_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             XTCfg<64>::SMEM);
   return e;
 }
 

@@ -756,6 +756,15 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
   // 3. the DiT blocks
   const float eps_ln = m->cfg.layer_norm_eps, eps_qk = m->cfg.qk_norm_eps;
+  // the pool as rows of head_dim channels for the TMA-fed cross-attention (bf16)
+  CUtensorMap kvmap;
+  bool kvmap_ok = false;
+  {
+    const int64_t rows = 2LL * m->L * pool->num_pages * m->nh * m->P;
+    std::string err;
+    if (m->kdt == FLASHMAP_BF16 && (m->hd == 64 || m->hd == 128) && rows < (1LL << 31))
+      kvmap_ok = fm::make_tmap_bf16(&kvmap, pool->base, rows, m->hd, m->hd, 16, &err);
+  }
   fm::XattnArgs xa;
   xa.pool = pool->base;
   xa.num_pages = pool->num_pages;
@@ -788,7 +797,7 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
     xa.layer = l;
     xa.q_norm = lw.cqn;
-    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa));
+    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
     TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
     TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));

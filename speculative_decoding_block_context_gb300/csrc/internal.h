@@ -151,7 +151,9 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
 int xattn_max_chunks(int num_sms, int nh, int bs);
 size_t xattn_plan_ints(int num_sms, int nh, int bs);
 cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan);
-cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& a);
+// kvmap: the bf16 pool as rows of head_dim channels (box 64 x 16, 128B swizzle) for the
+// TMA-fed kernel, or null for the cp.async one.
+cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& a, const CUtensorMap* kvmap = nullptr);
 cudaError_t xattn_prepare();  // kernel attributes, once per device (not during capture)
 cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& a, void* out);
 
