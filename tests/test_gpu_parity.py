@@ -51,7 +51,8 @@ def test_philox_words_bit_exact():
 
 
 @pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 200, 300), (16, 4096, 4096), (37, 384, 1234),
-                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512)])
+                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512), (300, 384, 1234),
+                                      (513, 4096, 384)])
 def test_linear_bf16_tcgen05(rows, k, n):
     g = torch.Generator(device="cuda").manual_seed(rows * 7 + k)
     x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
