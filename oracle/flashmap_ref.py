@@ -667,3 +667,50 @@ def quantize_query_e4m3(q: np.ndarray) -> np.ndarray:
     scale = (np.maximum(amax, np.float32(1e-12)) / np.float32(E4M3_MAX)).astype(np.float32)
     q8 = e4m3_round((q32 / scale[None, :, None]).astype(np.float32))
     return q8 * _f64(scale)[None, :, None]
+
+
+# ---------------------------------------------------------------------------------
+# Tree drafting: the verify tree of N candidate blocks per request
+# (flashmap/sglang/tree.py, build_tree_abi)
+# ---------------------------------------------------------------------------------
+
+
+def build_tree(candidates, width: int):
+    """The verify tree of one request's candidate blocks, stated as a trie.
+
+    candidates (N, K) token ids drafted after the anchor (the tree's root). Every
+    distinct prefix c[:d+1] of a candidate is a node at depth d; its vote is how many
+    candidates share that prefix, its representative the lowest candidate index
+    having it. The width - 1 nodes ranked first by (more votes, shallower, lower
+    representative) are kept -- a node's parent always ranks before it -- and listed
+    by (depth, representative), numbered 1.. in that order (the root is 0). With fewer
+    nodes than width - 1, the list is padded with copies of the first listed node (a
+    depth-0 node, parent the root).
+
+    Returns (tokens (width-1,), ids (width-1,) = parent * width + number,
+    stats (2,) = (nodes in the trie, distinct candidates))."""
+    c = [tuple(int(t) for t in row) for row in np.asarray(candidates)]
+    n, k = len(c), len(c[0])
+    m = width - 1
+    nodes = {}  # prefix -> [votes, representative]
+    for i, row in enumerate(c):
+        for d in range(k):
+            pre = row[:d + 1]
+            if pre in nodes:
+                nodes[pre][0] += 1
+            else:
+                nodes[pre] = [1, i]
+    ranked = sorted(nodes, key=lambda p: (-nodes[p][0], len(p), nodes[p][1]))
+    kept = sorted(ranked[:m], key=lambda p: (len(p), nodes[p][1]))
+    number = {p: q + 1 for q, p in enumerate(kept)}
+    tokens, ids = [], []
+    for q, p in enumerate(kept):
+        parent = number[p[:-1]] if len(p) > 1 else 0
+        tokens.append(p[-1])
+        ids.append(parent * width + q + 1)
+    for q in range(len(kept), m):  # padding: copies of the first node under the root
+        tokens.append(kept[0][-1])
+        ids.append(0 * width + q + 1)
+    distinct = len(set(c))
+    return (np.array(tokens, dtype=np.int64), np.array(ids, dtype=np.int64),
+            np.array([len(nodes), distinct], dtype=np.int64))

@@ -442,3 +442,76 @@ def test_e4m3_constants_quantize_the_folded_head_only():
     assert Cq.head_b is C.head_b and Cq.hot is C.hot
     assert not np.array_equal(Cq.head_w, C.head_w)
     assert np.max(np.abs(Cq.head_w - C.head_w)) <= np.max(np.abs(C.head_w)) / 448 * 16
+
+
+# --------------------------------------------------------------------- verify tree
+
+
+def _read_tree_golden():
+    path = os.path.join(os.path.dirname(__file__), "golden", "tree_example.txt")
+    vals = {}
+    for ln in open(path):
+        ln = ln.strip()
+        if ln and not ln.startswith("#"):
+            key, *rest = ln.split()
+            vals[key] = [int(x) for x in rest]
+    return vals
+
+
+def test_tree_hand_worked_example():
+    g = _read_tree_golden()
+    c = np.array(g["candidates"]).reshape(g["n"][0], g["k"][0])
+    tokens, ids, stats = ref.build_tree(c, g["width"][0])
+    np.testing.assert_array_equal(tokens, g["tokens"])
+    np.testing.assert_array_equal(ids, g["ids"])
+    np.testing.assert_array_equal(stats, g["stats"])
+
+
+def _decode(tokens, ids, width):
+    """Node number -> (parent number, token, path of tokens from the root)."""
+    out = {}
+    for q, (t, i) in enumerate(zip(tokens, ids)):
+        parent, num = divmod(int(i), width)
+        assert num == q + 1
+        out[num] = (parent, int(t))
+    return out
+
+
+@pytest.mark.parametrize("seed,n,k,width,alphabet", [(0, 8, 4, 16, 3), (1, 16, 6, 40, 2), (2, 4, 3, 64, 5),
+                                                     (3, 32, 16, 64, 4), (4, 1, 5, 8, 9)])
+def test_tree_invariants_on_random_candidates(seed, n, k, width, alphabet):
+    """Every kept node's parent is kept and listed before it; each node's path from the
+    root is a prefix of some candidate with exactly as many candidates through it as
+    the trie says; no dropped prefix outranks a kept one; padding repeats the first
+    node under the root; stats count the trie's nodes and the distinct candidates."""
+    rng = np.random.default_rng(seed)
+    c = rng.integers(0, alphabet, size=(n, k))
+    tokens, ids, stats = ref.build_tree(c, width)
+    m = width - 1
+    assert tokens.shape == (m,) and ids.shape == (m,)
+    rows = [tuple(r) for r in c.tolist()]
+    prefixes = {}  # prefix -> the candidates through it, with repeats (a vote each)
+    for r in rows:
+        for d in range(k):
+            prefixes.setdefault(r[:d + 1], []).append(r)
+    assert stats[0] == len(prefixes) and stats[1] == len(set(rows))
+    nodes = _decode(tokens, ids, width)
+    kept = min(m, len(prefixes))
+    paths = {}
+    for num in range(1, kept + 1):
+        parent, t = nodes[num]
+        assert parent < num
+        paths[num] = (paths[parent] if parent else ()) + (t,)
+        assert paths[num] in prefixes
+    assert len(set(paths.values())) == kept  # distinct nodes
+    for num in range(kept + 1, m + 1):  # padding
+        assert nodes[num] == (0, nodes[1][1]) and len(paths[1]) == 1
+    # the cut: no dropped node has more votes than a kept one (ties: shallower first)
+    rank = lambda p: (-len(prefixes[p]), len(p), min(rows.index(r) for r in prefixes[p]))
+    kept_ranks = [rank(p) for p in paths.values()]
+    dropped = [rank(p) for p in prefixes if p not in set(paths.values())]
+    if dropped:
+        assert max(kept_ranks) < min(dropped)
+    # listing order: by depth, then by lowest candidate through the node
+    order = [(len(paths[q]), rank(paths[q])[2]) for q in range(1, kept + 1)]
+    assert order == sorted(order)
