@@ -285,6 +285,26 @@ flashmap_status flashmap_sample_logits_static(flashmap_model* model, int32_t bs,
                                              const uint8_t* greedy, const uint64_t* seeds, uint64_t step,
                                              int64_t* tokens_out, flashmap_stream stream);
 
+/*
+ * The verify tree of a multi-candidate draft (flashmap/sglang/tree.py, build_tree_abi;
+ * flashmap/sglang/model.py, _draft_tree). For each request, n_cand candidate blocks
+ * of block_size tokens drafted after its anchor (the tree's root) form a trie with a
+ * node per distinct prefix; a node's vote is the number of candidates through it. The
+ * width - 1 nodes with the most votes (ties: shallower, then lower candidate) are
+ * kept -- every kept node's parent is kept too -- and listed by depth, then by the
+ * lowest candidate through them, numbered 1.. (the root is 0). A trie with fewer nodes
+ * is padded with copies of the first listed node (a child of the root).
+ *   candidates  (device) int64 [bs][n_cand][block_size] token ids
+ *   tokens_out  (device) int64 [bs][width - 1] the nodes' tokens
+ *   ids_out     (device) int64 [bs][width - 1] parent * width + number
+ *   stats_out   (device) int64 [bs][2] (trie nodes before the cut, distinct candidates)
+ * Limits: 1 <= n_cand <= 64, n_cand * block_size <= 1024, 2 <= width <= 1025.
+ * Allocates nothing; enqueued on `stream`.
+ */
+flashmap_status flashmap_build_tree(const int64_t* candidates, int32_t bs, int32_t n_cand, int32_t block_size,
+                                    int32_t width, int64_t* tokens_out, int64_t* ids_out, int64_t* stats_out,
+                                    flashmap_stream stream);
+
 /* The device error word (FLASHMAP_DEVERR_* bits), then clears it. Synchronizes
  * `stream`. Returns E_DEVICE when the word was non-zero. */
 flashmap_status flashmap_get_device_error(flashmap_model* model, flashmap_stream stream,

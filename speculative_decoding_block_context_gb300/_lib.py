@@ -116,6 +116,7 @@ def lib():
         L.flashmap_debug_linear.argtypes = [_c.c_int32, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp]
         L.flashmap_debug_constants.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.flashmap_sample_logits_static.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp]
+        L.flashmap_build_tree.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp]
         L.flashmap_profile_start.argtypes = [_vp, _c.c_int32]
         L.flashmap_profile_stop.argtypes = [_vp, P(flashmap_launch_record), _c.c_int32, P(_c.c_int32)]
         for name in header_functions():
@@ -254,6 +255,13 @@ def flashmap_sample_logits_static(model: Model, bs: int, logits, anchor_pos, tem
     _check(lib().flashmap_sample_logits_static(model.handle, int(bs), _ptr(logits), _ptr(anchor_pos),
                                                _ptr(temperature), _ptr(greedy), _ptr(seeds), int(step),
                                                _ptr(tokens_out), _stream(stream)))
+
+
+def flashmap_build_tree(candidates, width: int, tokens_out, ids_out, stats_out, stream=None) -> None:
+    """candidates (bs, n_cand, block_size) int64 device -> the verify tree (in place)."""
+    bs, n, k = candidates.shape
+    _check(lib().flashmap_build_tree(_ptr(candidates), int(bs), int(n), int(k), int(width), _ptr(tokens_out),
+                                     _ptr(ids_out), _ptr(stats_out), _stream(stream)))
 
 
 def flashmap_get_device_error(model: Model, stream=None) -> int:

@@ -912,6 +912,23 @@ flashmap_status flashmap_profile_stop(flashmap_model* m, flashmap_launch_record*
   return FLASHMAP_OK;
 }
 
+flashmap_status flashmap_build_tree(const int64_t* candidates, int32_t bs, int32_t n_cand, int32_t block_size,
+                                    int32_t width, int64_t* tokens_out, int64_t* ids_out, int64_t* stats_out,
+                                    flashmap_stream stream) {
+  g_last_error.clear();
+  if (!candidates || !tokens_out || !ids_out || !stats_out || bs <= 0)
+    return fail(FLASHMAP_E_INVALID, "NULL argument or bs <= 0");
+  if (n_cand < 1 || n_cand > fm::kTreeMaxCandidates || block_size < 1 ||
+      static_cast<int64_t>(n_cand) * block_size > fm::kTreeMaxNodes || width < 2 || width > fm::kTreeMaxNodes + 1)
+    return fail(FLASHMAP_E_INVALID, "need 1 <= n_cand <= 64, n_cand * block_size <= 1024, 2 <= width <= 1025");
+  int dev = 0, sms = 0;
+  FM_CUDA(cudaGetDevice(&dev));
+  FM_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  Launch Lh{reinterpret_cast<cudaStream_t>(stream), sms, nullptr, true};
+  FM_CUDA(fm::build_tree(Lh, candidates, bs, n_cand, block_size, width, tokens_out, ids_out, stats_out));
+  return FLASHMAP_OK;
+}
+
 flashmap_status flashmap_debug_philox(const uint64_t* seeds, const uint32_t* ctr, int64_t n, uint32_t* out,
                                       float* normals, flashmap_stream stream) {
   g_last_error.clear();

@@ -167,6 +167,10 @@ cudaError_t static_sample_scratch(void** out);
 cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
                         const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters);
+// The verify tree of N candidate blocks of K tokens per request (tree.cu).
+constexpr int kTreeMaxCandidates = 64, kTreeMaxNodes = 1024;  // N, N * K
+cudaError_t build_tree(const Launch& L, const int64_t* candidates, int bs, int N, int K, int width, int64_t* tokens,
+                       int64_t* ids, int64_t* stats);
 cudaError_t full_scatter(const Launch& L, const float* logits, int rows, int Vd, const int32_t* inv, int V,
                          float* full);
 

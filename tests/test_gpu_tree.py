@@ -1,0 +1,58 @@
+"""The verify tree kernel against the oracle's trie, bit-exact, on seeded candidate
+blocks: small alphabets (many shared prefixes and repeated candidates), all-distinct
+candidates, cuts below and above the trie's size (padding), and the limits."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import flashmap_ref as ref
+from speculative_decoding_block_context_gb300 import _lib as F
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from speculative_decoding_block_context_gb300 import build
+
+    build.build()
+    F.lib()
+
+
+@pytest.mark.parametrize("bs,n,k,width,alphabet,seed", [
+    (4, 8, 16, 64, 2, 0),      # binary tokens: deep shared prefixes
+    (3, 16, 16, 32, 3, 1),
+    (2, 64, 16, 128, 4, 2),    # the most candidates, 1024 nodes
+    (5, 4, 6, 100, 5, 3),      # fewer nodes than width - 1: padding
+    (2, 1, 16, 8, 151936, 4),  # one candidate: a chain
+    (3, 32, 8, 17, 151936, 5), # all distinct at depth 0
+    (1, 64, 16, 1025, 2, 6),   # the widest tree
+])
+def test_tree_matches_oracle(bs, n, k, width, alphabet, seed):
+    g = torch.Generator().manual_seed(seed)
+    cand = torch.randint(0, alphabet, (bs, n, k), generator=g, dtype=torch.int64)
+    if n > 2:
+        cand[:, 1] = cand[:, 0]  # a repeated candidate
+    m = width - 1
+    tokens = torch.full((bs, m), -7, dtype=torch.int64, device="cuda")
+    ids = torch.full((bs, m), -7, dtype=torch.int64, device="cuda")
+    stats = torch.full((bs, 2), -7, dtype=torch.int64, device="cuda")
+    F.flashmap_build_tree(cand.cuda(), width, tokens, ids, stats)
+    torch.cuda.synchronize()
+    for b in range(bs):
+        wt, wi, ws = ref.build_tree(cand[b].numpy(), width)
+        np.testing.assert_array_equal(tokens[b].cpu().numpy(), wt)
+        np.testing.assert_array_equal(ids[b].cpu().numpy(), wi)
+        np.testing.assert_array_equal(stats[b].cpu().numpy(), ws)
+
+
+def test_tree_refuses_out_of_range_shapes():
+    cand = torch.zeros((1, 65, 2), dtype=torch.int64, device="cuda")
+    out = torch.zeros((1, 8), dtype=torch.int64, device="cuda")
+    st = torch.zeros((1, 2), dtype=torch.int64, device="cuda")
+    with pytest.raises(F.FlashmapError):
+        F.flashmap_build_tree(cand, 9, out, out, st)  # 65 candidates
+    cand = torch.zeros((1, 4, 2), dtype=torch.int64, device="cuda")
+    with pytest.raises(F.FlashmapError):
+        F.flashmap_build_tree(cand, 1, out, out, st)  # width 1
