@@ -286,6 +286,26 @@ flashmap_status flashmap_sample_logits_static(flashmap_model* model, int32_t bs,
                                              int64_t* tokens_out, flashmap_stream stream);
 
 /*
+ * flashmap_draft_block for n_cand candidate blocks per request, drafted from
+ * independent noise (tree drafting: flashmap/sglang/model.py, _draft_impl with
+ * n_cand > 1). The anchor rows are computed and written once per request; block bc =
+ * b * n_cand + c (candidate c of request b) has the request's positions and context,
+ * and its noise takes Philox counter word 3 = c, so candidate 0 is the block
+ * flashmap_draft_block drafts. The candidates of a request read the same context.
+ *   hidden_out  (device) [bs * n_cand * K][D] act_dtype, candidate-major per request
+ * Size the workspace with flashmap_workspace_size(max_bs = bs * n_cand). The blocks'
+ * tokens come from flashmap_sample_block over bs * n_cand blocks (with each request's
+ * position, seed and temperature repeated n_cand times); flashmap_build_tree merges
+ * them into the verify tree.
+ */
+flashmap_status flashmap_draft_candidates(flashmap_model* model, const flashmap_kv_pool* pool, int32_t bs,
+                                          int32_t n_cand, const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                          const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                          int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
+                                          void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                          size_t workspace_bytes, flashmap_stream stream);
+
+/*
  * The verify tree of a multi-candidate draft (flashmap/sglang/tree.py, build_tree_abi;
  * flashmap/sglang/model.py, _draft_tree). For each request, n_cand candidate blocks
  * of block_size tokens drafted after its anchor (the tree's root) form a trie with a

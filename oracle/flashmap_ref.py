@@ -36,7 +36,9 @@ Readings where the pages are silent (listed with their reasons in the design doc):
   R4 normals by Box-Muller on the word pairs (w0, w1) and (w2, w3);
   R5 Gumbel-max: token = argmax_j (l_j / T + G_j), G = -ln(-ln U); lowest index
      wins ties; T <= 0 or greedy -> argmax_j l_j;
-  R6 RoPE angle = float32(float32(p) * inv_freq), inv_freq = float32(theta^(-2i/hd)).
+  R6 RoPE angle = float32(float32(p) * inv_freq), inv_freq = float32(theta^(-2i/hd));
+  R7 candidate c of a multi-candidate (tree) draft keys its noise with counter word
+     3 = c (the single draft is candidate 0).
 
 Pinning (what fixes each function other than itself; see tests/test_oracle_pins.py):
   philox4x32_10          published known-answer vectors (tests/golden/philox_kat.txt)
@@ -182,13 +184,15 @@ def _philox_rows(seed: int, positions, ncols: int, domain: int, step: int) -> np
     return philox4x32_10(ctr.reshape(-1, 4), keys).reshape(len(pos), n4, 4)
 
 
-def draft_normals(seed: int, positions, ncols: int) -> np.ndarray:
+def draft_normals(seed: int, positions, ncols: int, candidate: int = 0) -> np.ndarray:
     """The starting noise z ~ N(0, I_H) of each slot (flashmap/vllm/model.py,
     module docstring: noise keyed by the request's seed and the slot's position;
     readings R1, R2, R4). Row i is keyed by positions[i]; returns (len, ncols):
     column j is normal j mod 4 of counter j/4, the normals of a counter being the
-    Box-Muller pairs of its words (w0, w1) and (w2, w3)."""
-    w = _philox_rows(seed, positions, ncols, domain=0, step=0)
+    Box-Muller pairs of its words (w0, w1) and (w2, w3). Candidate c of a
+    multi-candidate (tree) draft takes counter word 3 = c (reading R7), so candidate
+    0 is the single draft."""
+    w = _philox_rows(seed, positions, ncols, domain=0, step=candidate)
     n0, n1 = box_muller(w[..., 0], w[..., 1])
     n2, n3 = box_muller(w[..., 2], w[..., 3])
     out = np.stack([n0, n1, n2, n3], axis=-1).reshape(w.shape[0], -1)
@@ -443,11 +447,12 @@ def write_locations(start_pos, commit_lens, window: int, req_pool_idx, req_to_pa
 # ---------------------------------------------------------------------------------
 
 
-def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, noise_scale: float):
+def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, noise_scale: float,
+                    candidate: int = 0):
     """flashmap/sglang/model.py, _draft_impl (one jump from t = 0): the embedded
-    state u + gate * noise_norm(z L^T) with z keyed by the slot positions, then
-    x_embed. Returns (K, D)."""
-    z = noise_scale * draft_normals(seed, positions, cfg.target_hidden)
+    state u + gate * noise_norm(z L^T) with z keyed by the slot positions (and the
+    candidate), then x_embed. Returns (K, D)."""
+    z = noise_scale * draft_normals(seed, positions, cfg.target_hidden, candidate)
     y = z @ C.chol.T
     e = C.uniform + C.gate * rms_norm(y, W["noise_norm.weight"], cfg.rms_norm_eps)
     return e @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
@@ -499,18 +504,22 @@ def dit_layer(cfg: Config, W: dict, l: int, mods: np.ndarray, x: np.ndarray, pos
 
 
 def draft_requests(cfg: Config, W: dict, C: Constants, ctx_kv: list, anchor_pos: list, seeds: list,
-                   noise_scale: float = 1.0) -> np.ndarray:
+                   noise_scale: float = 1.0, candidates: list | None = None) -> np.ndarray:
     """modeling_flashmap.py, FlashMapDraftModel.draft with one step, for requests i whose
     cross-attention context (anchor included) is ctx_kv[i] = (keys, values), each
     (L, p_i + 1, heads, hd): slots at positions p_i+1 .. p_i+K; returns the final AdaLN
-    output (n_req, K, D), which the folded head maps to logits."""
+    output (n_req, K, D), which the folded head maps to logits. A tree draft's
+    candidate blocks are entries with the same context, position and seed and their
+    own candidate index (flashmap/sglang/model.py, _draft_impl with n_cand > 1: the
+    same blocks from independent noise)."""
     K = cfg.block_size
     nreq = len(anchor_pos)
+    candidates = candidates if candidates is not None else [0] * nreq
     positions = np.concatenate([p + 1 + np.arange(K) for p in anchor_pos])
     for (kc, _), p in zip(ctx_kv, anchor_pos):
         assert kc.shape[1] == p + 1, "context is positions 0..p"
-    x = np.concatenate([noise_embedding(cfg, W, C, s, p + 1 + np.arange(K), noise_scale)
-                        for s, p in zip(seeds, anchor_pos)])
+    x = np.concatenate([noise_embedding(cfg, W, C, s, p + 1 + np.arange(K), noise_scale, c)
+                        for s, p, c in zip(seeds, anchor_pos, candidates)])
     for l in range(cfg.num_layers):
         x = dit_layer(cfg, W, l, C.mods[l], x, positions, [(kc[l], vc[l]) for kc, vc in ctx_kv])
     out = layer_norm(x, cfg.layer_norm_eps) * C.final[0] + C.final[1]

@@ -117,6 +117,8 @@ def lib():
         L.flashmap_debug_constants.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.flashmap_sample_logits_static.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp]
         L.flashmap_build_tree.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp]
+        L.flashmap_draft_candidates.argtypes = [_vp, P(flashmap_kv_pool), _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp,
+                                                _c.c_int32, _vp, _c.c_float, _vp, _vp, _vp, _c.c_size_t, _vp]
         L.flashmap_profile_start.argtypes = [_vp, _c.c_int32]
         L.flashmap_profile_stop.argtypes = [_vp, P(flashmap_launch_record), _c.c_int32, P(_c.c_int32)]
         for name in header_functions():
@@ -235,6 +237,15 @@ def flashmap_draft_block(model: Model, pool: flashmap_kv_pool, bs: int, anchor_i
                          stream=None) -> None:
     _check(lib().flashmap_draft_block(
         model.handle, _c.byref(pool), int(bs), _ptr(anchor_ids), _ptr(anchor_pos), _ptr(req_pool_idx),
+        _ptr(req_to_page), int(req_to_page.stride(0)), _ptr(seeds), float(noise_scale), _ptr(hidden_out),
+        _ptr(anchor_loc_out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def flashmap_draft_candidates(model: Model, pool: flashmap_kv_pool, bs: int, n_cand: int, anchor_ids, anchor_pos,
+                              req_pool_idx, req_to_page, seeds, noise_scale: float, hidden_out, anchor_loc_out,
+                              workspace, stream=None) -> None:
+    _check(lib().flashmap_draft_candidates(
+        model.handle, _c.byref(pool), int(bs), int(n_cand), _ptr(anchor_ids), _ptr(anchor_pos), _ptr(req_pool_idx),
         _ptr(req_to_page), int(req_to_page.stride(0)), _ptr(seeds), float(noise_scale), _ptr(hidden_out),
         _ptr(anchor_loc_out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 

@@ -187,6 +187,7 @@ std::vector<float2> rope_table(int maxpos, int hd, double theta) {
 struct DraftWs {
   float *x, *acc_big, *acc_d, *acc_a, *acc_kv;
   void *act, *e_rows, *a_rows;
+  int32_t *exp_pos, *exp_rpi;  // per-block request arrays of a multi-candidate draft
   int* plan;
   float *part_o, *part_ml;
   size_t bytes;
@@ -206,6 +207,8 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   w.act = c.take<void>(R * wide * es);
   w.e_rows = c.take<void>(static_cast<size_t>(bs) * m->H * es);
   w.a_rows = c.take<void>(static_cast<size_t>(bs) * m->D * es);
+  w.exp_pos = c.take<int32_t>(static_cast<size_t>(bs) * 4);
+  w.exp_rpi = c.take<int32_t>(static_cast<size_t>(bs) * 4);
   w.plan = c.take<int>(fm::xattn_plan_ints(m->num_sms, m->nh, bs) * 4);
   const size_t chunks = fm::xattn_max_chunks(m->num_sms, m->nh, bs);
   w.part_o = c.take<float>(chunks * m->nh * 16 * m->hd * 4);
@@ -687,26 +690,31 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
   return FLASHMAP_OK;
 }
 
-flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs,
-                                     const int64_t* anchor_ids, const int32_t* anchor_pos,
-                                     const int32_t* req_pool_idx, const int32_t* req_to_page,
-                                     int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
-                                     void* hidden_out, int64_t* anchor_loc_out, void* workspace,
-                                     size_t workspace_bytes, flashmap_stream stream) {
+// The draft of n_cand candidate blocks per request (1: flashmap_draft_block): the anchor
+// rows once per request, then the noise (keyed by the candidate) and the DiT on
+// bs * n_cand blocks, block bc being candidate bc % n_cand of request bc / n_cand.
+static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs, int32_t n_cand,
+                                  const int64_t* anchor_ids, const int32_t* anchor_pos, const int32_t* req_pool_idx,
+                                  const int32_t* req_to_page, int32_t req_to_page_stride, const uint64_t* seeds,
+                                  float noise_scale, void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                  size_t workspace_bytes, flashmap_stream stream) {
   g_last_error.clear();
   if (!m || !pool || !anchor_ids || !anchor_pos || !req_pool_idx || !req_to_page || !seeds || !hidden_out || !workspace)
     return fail(FLASHMAP_E_INVALID, "NULL argument");
   if (bs <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs and the page-table stride must be positive");
+  if (n_cand < 1 || static_cast<int64_t>(bs) * n_cand * m->K > (1 << 24))
+    return fail(FLASHMAP_E_INVALID, "n_cand must be >= 1 and bs * n_cand * block_size <= 2^24");
   if (pool->dtype != m->kdt || !pool->base || pool->num_pages <= 0)
     return fail(FLASHMAP_E_INVALID, "pool dtype must equal kv_dtype, with pages");
   if (!std::isfinite(noise_scale)) return fail(FLASHMAP_E_INVALID, "noise_scale must be finite");
-  const DraftWs need = carve_draft(m, bs, nullptr);
+  const int bsc = bs * n_cand;  // blocks
+  const DraftWs need = carve_draft(m, bsc, nullptr);
   if (workspace_bytes < need.bytes)
     return fail(FLASHMAP_E_INVALID, "workspace too small: need " + std::to_string(need.bytes) + " bytes");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Launch Lh = m->launch(s);
-  const DraftWs ws = carve_draft(m, bs, workspace);
-  const int R = bs * m->K, D = m->D, H = m->H, adt = m->adt;
+  const DraftWs ws = carve_draft(m, bsc, workspace);
+  const int R = bsc * m->K, D = m->D, H = m->H, adt = m->adt;
   const size_t big = std::max({3 * static_cast<size_t>(D), static_cast<size_t>(m->F), static_cast<size_t>(H)});
   {
     fm::ZeroList z;
@@ -717,8 +725,15 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     z.add(ws.acc_kv, static_cast<int64_t>(bs) * 2 * m->L * D);
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
   }
+  // the blocks' request arrays (candidates of a request share its position and pages)
+  const int32_t *pos_x = anchor_pos, *rpi_x = req_pool_idx;
+  if (n_cand > 1) {
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::expand_requests(Lh, anchor_pos, req_pool_idx, bs, n_cand, ws.exp_pos, ws.exp_rpi));
+    pos_x = ws.exp_pos;
+    rpi_x = ws.exp_rpi;
+  }
   // split-KV plan of the cross-attention, shared by every layer
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, anchor_pos, bs, m->nh, ws.plan));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, pos_x, bsc, m->nh, ws.plan));
   // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(Lh, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
   TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
@@ -749,7 +764,7 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
   }
   // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
   TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
                        ws.act, H));
@@ -768,13 +783,13 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   fm::XattnArgs xa;
   xa.pool = pool->base;
   xa.num_pages = pool->num_pages;
-  xa.bs = bs;
+  xa.bs = bsc;
   xa.K = m->K;
   xa.nh = m->nh;
   xa.hd = m->hd;
   xa.P = m->P;
-  xa.anchor_pos = anchor_pos;
-  xa.req_pool_idx = req_pool_idx;
+  xa.anchor_pos = pos_x;
+  xa.req_pool_idx = rpi_x;
   xa.req_to_page = req_to_page;
   xa.r2p_stride = req_to_page_stride;
   xa.plan = ws.plan;
@@ -790,8 +805,8 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
     const float* md = lw.mods;
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
     TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
-    TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bs, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
-                               anchor_pos, ws.act));
+    TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
+                               pos_x, ws.act));
     TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
     TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
     TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
@@ -808,6 +823,26 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
   // 4. final AdaLN
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, m->final_mods, m->final_mods + D, eps_ln, hidden_out));
   return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs,
+                                     const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                     const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                     int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
+                                     void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                     size_t workspace_bytes, flashmap_stream stream) {
+  return draft_impl(m, pool, bs, 1, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride, seeds,
+                    noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
+}
+
+flashmap_status flashmap_draft_candidates(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs,
+                                          int32_t n_cand, const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                          const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                          int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
+                                          void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                          size_t workspace_bytes, flashmap_stream stream) {
+  return draft_impl(m, pool, bs, n_cand, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride,
+                    seeds, noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
 }
 
 flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void* hidden, const int32_t* anchor_pos,

@@ -121,7 +121,9 @@ cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* o
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out);
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
-                        int H, void* out);
+                        int H, void* out, int n_cand = 1);
+cudaError_t expand_requests(const Launch& L, const int32_t* anchor_pos, const int32_t* req_pool_idx, int bs,
+                            int n_cand, int32_t* pos_out, int32_t* rpi_out);
 cudaError_t philox_export(cudaStream_t s, const uint64_t* seeds, const uint32_t* ctr, int64_t n, uint32_t* out,
                           float* normals);
 

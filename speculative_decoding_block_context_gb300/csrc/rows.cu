@@ -276,17 +276,22 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ table, int64_t nrow
 // z[b*K + k][j] ~ N(0, 1) keyed by (seeds[b], position anchor_pos[b] + 1 + k): counter
 // (j / 4, position, 0, 0), normal j % 4 from the Box-Muller pairs (w0, w1), (w2, w3).
 template <typename T>
+// Row r is slot k = r % K of block r / K; with n_cand candidates per request, block
+// bc is candidate bc % n_cand of request bc / n_cand, keyed by counter word 3 = the
+// candidate (0 for a single draft).
 __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int32_t* __restrict__ anchor_pos,
-                                   int K, int H, int64_t total, T* __restrict__ out) {
+                                   int K, int n_cand, int H, int64_t total, T* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int n4 = (H + 3) >> 2;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int row = static_cast<int>(t / n4), j4 = static_cast<int>(t - static_cast<int64_t>(row) * n4);
-    const int b = row / K, k = row - b * K;
+    const int bc = row / K, k = row - bc * K;
+    const int b = bc / n_cand, c = bc - b * n_cand;
     const uint32_t pos = static_cast<uint32_t>(LDCG(anchor_pos + b) + 1 + k);
-    const uint4 w = philox_seeded(LDCG(seeds + b), static_cast<uint32_t>(j4), pos, kDomainDraftNoise, 0u);
+    const uint4 w = philox_seeded(LDCG(seeds + b), static_cast<uint32_t>(j4), pos, kDomainDraftNoise,
+                                  static_cast<uint32_t>(c));
     const float2 n01 = box_muller(w.x, w.y), n23 = box_muller(w.z, w.w);
     const float v[4] = {n01.x, n01.y, n23.x, n23.y};
     T* o = out + static_cast<int64_t>(row) * H + 4 * j4;
@@ -423,14 +428,34 @@ cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t n
 }
 
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
-                        int H, void* out) {
-  const int64_t total = static_cast<int64_t>(bs) * K * ((H + 3) / 4);
+                        int H, void* out, int n_cand) {
+  const int64_t total = static_cast<int64_t>(bs) * n_cand * K * ((H + 3) / 4);
   if (total <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(L.num_sms) * 16));
   cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, (e = launch_k(L, draft_noise_kernel<T>, dim3(blocks), dim3(256), 0, seeds, anchor_pos, K, H,
-                                     total, static_cast<T*>(out))));
+  FM_DISPATCH_T(dtype, (e = launch_k(L, draft_noise_kernel<T>, dim3(blocks), dim3(256), 0, seeds, anchor_pos, K,
+                                     n_cand, H, total, static_cast<T*>(out))));
   return e;
+}
+
+// Per-block copies of the request arrays for a draft of n_cand candidates per request:
+// block bc = candidate bc % n_cand of request bc / n_cand.
+__global__ void expand_kernel(const int32_t* __restrict__ anchor_pos, const int32_t* __restrict__ req_pool_idx,
+                              int bs, int n_cand, int32_t* __restrict__ pos_out, int32_t* __restrict__ rpi_out) {
+  pdl_trigger();
+  pdl_wait();
+  for (int bc = blockIdx.x * blockDim.x + threadIdx.x; bc < bs * n_cand; bc += gridDim.x * blockDim.x) {
+    const int b = bc / n_cand;
+    pos_out[bc] = LDCG(anchor_pos + b);
+    rpi_out[bc] = req_pool_idx ? LDCG(req_pool_idx + b) : b;
+  }
+}
+
+cudaError_t expand_requests(const Launch& L, const int32_t* anchor_pos, const int32_t* req_pool_idx, int bs,
+                            int n_cand, int32_t* pos_out, int32_t* rpi_out) {
+  const int n = bs * n_cand;
+  return launch_k(L, expand_kernel, dim3((n + 255) / 256), dim3(256), 0, anchor_pos, req_pool_idx, bs, n_cand, pos_out,
+                  rpi_out);
 }
 
 // ------------------------------------------------------------------ Philox export

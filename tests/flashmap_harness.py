@@ -152,6 +152,24 @@ def oracle_batch(st: ModelState, run: LibRun, subset, noise_scale: float = 1.0) 
     cfg, req = st.oracle_cfg(), run.req
     W, C = st.Wnp, st.consts
     K = cfg.block_size
+    outs, ctxs, ps, seeds = oracle_contexts(st, run, subset)
+    hidden = ref.draft_requests(cfg, W, C, ctxs, ps, seeds, noise_scale)
+    for i, b in enumerate(subset):
+        logits = ref.head_logits(C, hidden[i])
+        T = float(req["temperature"][b])
+        g = int(req["greedy"][b])
+        p = ps[i]
+        tok, _, margin = ref.sample_rows(logits, [T] * K, [g] * K, [seeds[i]] * K, p + 1 + np.arange(K),
+                                         req["step"], C.hot)
+        outs[b].update(hidden=hidden[i], logits=logits, tokens=tok, margin=margin)
+    return outs
+
+
+def oracle_contexts(st: ModelState, run: LibRun, subset):
+    """Per request of ``subset``: the oracle's written rows (dict), its cross-attention
+    context (keys, values over positions 0..p as the pool stores them), p and seed."""
+    cfg, req = st.oracle_cfg(), run.req
+    W = st.Wnp
     outs, ctxs, ps, seeds = {}, [], [], []
     for b in subset:
         ctx = req["ctx"][b]
@@ -180,16 +198,7 @@ def oracle_batch(st: ModelState, run: LibRun, subset, noise_scale: float = 1.0) 
         ps.append(p)
         seeds.append(int(req["seeds"][b]))
         outs[b] = out
-    hidden = ref.draft_requests(cfg, W, C, ctxs, ps, seeds, noise_scale)
-    for i, b in enumerate(subset):
-        logits = ref.head_logits(C, hidden[i])
-        T = float(req["temperature"][b])
-        g = int(req["greedy"][b])
-        p = ps[i]
-        tok, _, margin = ref.sample_rows(logits, [T] * K, [g] * K, [seeds[i]] * K, p + 1 + np.arange(K),
-                                         req["step"], C.hot)
-        outs[b].update(hidden=hidden[i], logits=logits, tokens=tok, margin=margin)
-    return outs
+    return outs, ctxs, ps, seeds
 
 
 def oracle_request(st: ModelState, run: LibRun, b: int, noise_scale: float = 1.0) -> dict:

@@ -56,3 +56,80 @@ def test_tree_refuses_out_of_range_shapes():
     cand = torch.zeros((1, 4, 2), dtype=torch.int64, device="cuda")
     with pytest.raises(F.FlashmapError):
         F.flashmap_build_tree(cand, 1, out, out, st)  # width 1
+
+
+# ------------------------------------------------------------------ tree drafting
+
+
+@pytest.mark.parametrize("workload,n,width,tol,margin,min_trees", [
+    ("small_bf16", 3, 12, 2e-2, 1e-2, 0),  # bf16: tokens compared where the margin is clear
+    ("tiny_fp32", 8, 16, 1e-4, 1e-4, 1),   # fp32: whole trees compared
+])
+def test_candidate_draft_and_tree_against_the_oracle(workload, n, width, tol, margin, min_trees):
+    margin_min = margin
+    """Candidate blocks per request: every block's hidden states and logits match the
+    oracle's draft with candidate-keyed noise (candidate 0 being the single draft),
+    their greedy tokens match wherever the oracle's top-2 margin is clear, and each
+    request whose candidates are all clear gets the oracle's tree, bit-exact."""
+    from oracle import flashmap_ref as ref
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    from .flashmap_harness import load_model, max_rel, oracle_contexts, run_library
+
+    st = load_model(workload)
+    run = run_library(workload, st)  # the pool now holds every written row
+    req, cfg = run.req, st.cfg
+    bs, K, D = req["bs"], cfg["block_size"], cfg["hidden"]
+    dt = syn.torch_dtype(cfg["act_dtype"])
+    pool = F.make_pool(run.pool_t, req["num_pages"], F.DTYPE_CODES[cfg["kv_dtype"]])
+    ws = torch.empty(F.flashmap_workspace_size(st.handle, bs * n, bs * (K + 1)), dtype=torch.uint8, device="cuda")
+    hidden = torch.empty((bs * n * K, D), dtype=dt, device="cuda")
+    anchor_pos = torch.tensor(req["anchor_pos"], dtype=torch.int32, device="cuda")
+    F.flashmap_draft_candidates(st.handle, pool, bs, n, req["anchor_ids"], anchor_pos, req["req_pool_idx"],
+                                req["req_to_page"], req["seeds"], 1.0, hidden, None, ws)
+    # greedy tokens of every block: the sampler over bs * n blocks
+    rep = lambda t: t.repeat_interleave(n)
+    vd = st.consts.hot.shape[0]
+    tokens = torch.empty(bs * n * K, dtype=torch.int64, device="cuda")
+    logits = torch.empty((bs * n * K, vd), dtype=torch.float32, device="cuda")
+    F.flashmap_sample_block(st.handle, bs * n, hidden, rep(anchor_pos), torch.zeros(bs * n, device="cuda"),
+                            torch.ones(bs * n, dtype=torch.uint8, device="cuda"), rep(req["seeds"]), 0, tokens,
+                            logits, None, ws)
+    t_out = torch.empty((bs, width - 1), dtype=torch.int64, device="cuda")
+    i_out = torch.empty((bs, width - 1), dtype=torch.int64, device="cuda")
+    s_out = torch.empty((bs, 2), dtype=torch.int64, device="cuda")
+    F.flashmap_build_tree(tokens.view(bs, n, K), width, t_out, i_out, s_out)
+    torch.cuda.synchronize()
+    assert F.flashmap_get_device_error(st.handle) == 0
+    # candidate 0 is the single draft (up to the GEMMs' atomic summation order)
+    h = hidden.float().view(bs, n, K, D).cpu().numpy()
+    assert max_rel(h[:, 0].reshape(bs * K, D), run.hidden.float().cpu().numpy()) < max(tol, 1e-2 if tol > 1e-3 else 1e-5)
+    _, ctxs, ps, seeds = oracle_contexts(st, run, list(range(bs)))
+    ocfg = st.oracle_cfg()
+    blocks = [(i, c) for i in range(bs) for c in range(n)]
+    want = ref.draft_requests(ocfg, st.Wnp, st.consts, [ctxs[i] for i, _ in blocks], [ps[i] for i, _ in blocks],
+                              [seeds[i] for i, _ in blocks], 1.0, [c for _, c in blocks])
+    trees_checked = 0
+    for b in range(bs):
+        otok = []
+        clear = True
+        for c in range(n):
+            assert max_rel(h[b, c], want[b * n + c]) <= tol
+            lg = ref.head_logits(st.consts, want[b * n + c])
+            got_lg = logits.view(bs, n, K, vd)[b, c].cpu().numpy()
+            assert max(max_rel(got_lg[r], lg[r]) for r in range(K)) <= tol
+            tok, _, margin = ref.sample_rows(lg, [0.0] * K, [1] * K, [seeds[b]] * K, ps[b] + 1 + np.arange(K), 0,
+                                             st.consts.hot)
+            got = tokens.view(bs, n, K)[b, c].cpu().numpy()
+            sure = margin > margin_min
+            np.testing.assert_array_equal(got[sure], tok[sure])
+            clear &= bool(sure.all())
+            otok.append(tok)
+        if clear:  # the oracle's own candidates give the same tree
+            wt, wi, wst = ref.build_tree(np.stack(otok), width)
+            np.testing.assert_array_equal(t_out[b].cpu().numpy(), wt)
+            np.testing.assert_array_equal(i_out[b].cpu().numpy(), wi)
+            np.testing.assert_array_equal(s_out[b].cpu().numpy(), wst)
+            trees_checked += 1
+    print(workload, "trees checked against the oracle:", trees_checked, "of", bs)
+    assert trees_checked >= min_trees

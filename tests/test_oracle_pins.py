@@ -515,3 +515,15 @@ def test_tree_invariants_on_random_candidates(seed, n, k, width, alphabet):
     # listing order: by depth, then by lowest candidate through the node
     order = [(len(paths[q]), rank(paths[q])[2]) for q in range(1, kept + 1)]
     assert order == sorted(order)
+
+
+def test_candidate_noise_keying():
+    """Reading R7: candidate 0's noise is the single draft's; other candidates draw
+    fresh N(0, 1) noise, uncorrelated with candidate 0's, from the same seed."""
+    pos = np.arange(100, 164)
+    z0 = ref.draft_normals(12345, pos, 256)
+    np.testing.assert_array_equal(ref.draft_normals(12345, pos, 256, candidate=0), z0)
+    z3 = ref.draft_normals(12345, pos, 256, candidate=3)
+    assert not np.allclose(z3, z0)
+    assert st.kstest(z3.reshape(-1), "norm").pvalue > 1e-3
+    assert abs(np.corrcoef(z0.reshape(-1), z3.reshape(-1))[0, 1]) < 0.02
