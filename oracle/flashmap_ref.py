@@ -38,7 +38,9 @@ Readings where the pages are silent (listed with their reasons in the design doc):
      wins ties; T <= 0 or greedy -> argmax_j l_j;
   R6 RoPE angle = float32(float32(p) * inv_freq), inv_freq = float32(theta^(-2i/hd));
   R7 candidate c of a multi-candidate (tree) draft keys its noise with counter word
-     3 = c (the single draft is candidate 0).
+     3 = c (the single draft is candidate 0);
+  R8 a several-jump draft starts from V-wide noise keyed like the one-jump noise
+     (columns 0..V-1 instead of 0..H-1).
 
 Pinning (what fixes each function other than itself; see tests/test_oracle_pins.py):
   philox4x32_10          published known-answer vectors (tests/golden/philox_kat.txt)
@@ -447,14 +449,19 @@ def write_locations(start_pos, commit_lens, window: int, req_pool_idx, req_to_pa
 # ---------------------------------------------------------------------------------
 
 
+def embed_noise(cfg: Config, W: dict, C: Constants, z: np.ndarray) -> np.ndarray:
+    """The one-jump state embedding from z ~ N(0, I_H): u + gate * noise_norm(z L^T)
+    (modeling_flashmap.py, mix_state at s = 0, the noise read as z L^T)."""
+    return C.uniform + C.gate * rms_norm(z @ C.chol.T, W["noise_norm.weight"], cfg.rms_norm_eps)
+
+
 def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, noise_scale: float,
                     candidate: int = 0):
     """flashmap/sglang/model.py, _draft_impl (one jump from t = 0): the embedded
     state u + gate * noise_norm(z L^T) with z keyed by the slot positions (and the
     candidate), then x_embed. Returns (K, D)."""
     z = noise_scale * draft_normals(seed, positions, cfg.target_hidden, candidate)
-    y = z @ C.chol.T
-    e = C.uniform + C.gate * rms_norm(y, W["noise_norm.weight"], cfg.rms_norm_eps)
+    e = embed_noise(cfg, W, C, z)
     return e @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
 
 
@@ -723,3 +730,64 @@ def build_tree(candidates, width: int):
     distinct = len(set(c))
     return (np.array(tokens, dtype=np.int64), np.array(ids, dtype=np.int64),
             np.array([len(nodes), distinct], dtype=np.int64))
+
+
+# ---------------------------------------------------------------------------------
+# Several jumps (modeling_flashmap.py, draft / embed_state / mix_state;
+# flashmap/vllm/model.py, _embed_state and the jump loop)
+# ---------------------------------------------------------------------------------
+
+
+def softmax(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(x - x.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def embed_state(cfg: Config, W: dict, C: Constants, E, state: np.ndarray, s: float, t: float) -> np.ndarray:
+    """The DiT input of a vocabulary-sized state (rows, V) jumping from s to t, before
+    x_embed: state_norm(posterior @ E) + gate * noise_norm(state @ E), the posterior
+    softmax(state * s / max(1 - s, 1e-3)^2) (uniform at s = 0, whose embedding is the
+    constant u), gate = noise_gate * (t - s) ("jump") or noise_gate ("constant")."""
+    E64 = _f64(E)
+    if s == 0:
+        post = np.broadcast_to(C.uniform, (state.shape[0], C.uniform.shape[0]))
+    else:
+        evidence = s / max(1.0 - s, 1e-3) ** 2
+        post = rms_norm(softmax(state * evidence) @ E64, W["state_norm.weight"], cfg.rms_norm_eps)
+    jump = 1.0 if cfg.noise_gate_constant else t - s
+    gate = float(np.asarray(W["noise_gate"], dtype=np.float64).reshape(-1)[0]) * jump
+    return post + gate * rms_norm(state @ E64, W["noise_norm.weight"], cfg.rms_norm_eps)
+
+
+def full_logits_of(C: Constants, W: dict, LM, hidden: np.ndarray) -> np.ndarray:
+    """The target LM head over the DiT head: LM @ (W_head h + b_head), every token --
+    what the full-vocabulary folded head computes (the fold identity)."""
+    return (hidden @ _f64(W["head.weight"]).T + _f64(W["head.bias"])) @ _f64(LM).T
+
+
+def draft_requests_multi(cfg: Config, W: dict, C: Constants, E, LM, ctx_kv: list, anchor_pos: list,
+                         seeds: list, num_steps: int, noise_scale: float = 1.0) -> np.ndarray:
+    """modeling_flashmap.py, FlashMapDraftModel.draft with num_steps jumps on the printed
+    grid (configuration_flashmap.py, DEFAULT_JUMP_GRIDS): the state starts as V-wide
+    noise keyed like the one-jump noise (reading R8); each jump s -> t embeds the state
+    (embed_state), runs the DiT with the modulations of (s, t), and, before t = 1,
+    moves the state to ((1 - t) state + (t - s) softmax(full logits)) / (1 - s).
+    Returns the last jump's final AdaLN output (n_req, K, D)."""
+    K = cfg.block_size
+    nreq = len(anchor_pos)
+    grid = DEFAULT_JUMP_GRIDS[str(num_steps)]
+    positions = np.concatenate([p + 1 + np.arange(K) for p in anchor_pos])
+    state = noise_scale * np.concatenate([draft_normals(sd, p + 1 + np.arange(K), cfg.vocab_size)
+                                          for sd, p in zip(seeds, anchor_pos)])
+    hidden = None
+    for s, t in zip(grid[:-1], grid[1:]):
+        mods, final, _ = jump_conditioning(cfg, W, s, t)
+        x = embed_state(cfg, W, C, E, state, s, t) @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
+        for l in range(cfg.num_layers):
+            x = dit_layer(cfg, W, l, mods[l], x, positions, [(kc[l], vc[l]) for kc, vc in ctx_kv])
+        hidden = layer_norm(x, cfg.layer_norm_eps) * final[0] + final[1]
+        if t < 1.0:
+            delta = softmax(full_logits_of(C, W, LM, hidden))
+            state = ((1.0 - t) * state + (t - s) * delta) / (1.0 - s)
+    return hidden.reshape(nreq, K, -1)

@@ -527,3 +527,37 @@ def test_candidate_noise_keying():
     assert not np.allclose(z3, z0)
     assert st.kstest(z3.reshape(-1), "norm").pvalue > 1e-3
     assert abs(np.corrcoef(z0.reshape(-1), z3.reshape(-1))[0, 1]) < 0.02
+
+
+# --------------------------------------------------------------------- several jumps
+
+
+def test_embed_state_at_zero_is_the_cholesky_path(tiny):
+    """At s = 0 the posterior is uniform whatever the state, and the state enters only
+    as x0 @ E: with z solving z L^T = x0 @ E, embed_state equals the one-jump
+    embedding u + gate * noise_norm(z L^T) (modeling_flashmap.py, target_constants)."""
+    cfg, W, E, LM, rank, C = tiny
+    rng = np.random.default_rng(3)
+    x0 = rng.standard_normal((6, cfg.vocab_size))
+    z = np.linalg.solve(C.chol, (x0 @ E.astype(np.float64)).T).T
+    np.testing.assert_allclose(ref.embed_state(cfg, W, C, E, x0, 0.0, 1.0), ref.embed_noise(cfg, W, C, z),
+                               rtol=1e-9, atol=1e-9)
+    # with a zero jump (gate 0) only the posterior term is left: the uniform constant
+    # at s = 0 whatever the state, a function of the state for s > 0
+    np.testing.assert_allclose(ref.embed_state(cfg, W, C, E, x0, 0.0, 0.0),
+                               np.broadcast_to(C.uniform, (6, C.uniform.shape[0])), rtol=1e-12)
+    b = ref.embed_state(cfg, W, C, E, x0, 0.5, 0.5) - ref.embed_state(cfg, W, C, E, 2 * x0, 0.5, 0.5)
+    assert not np.allclose(b, 0.0, atol=1e-6)
+
+
+def test_jump_state_update_and_grid():
+    """The state recurrence of the jump loop: with t - s the weight of the DiT's
+    distribution, a state already equal to that distribution is a fixed point, and the
+    printed grids start at 0 and end at 1 with increasing times."""
+    for n, grid in ref.DEFAULT_JUMP_GRIDS.items():
+        assert grid[0] == 0.0 and grid[-1] == 1.0 and len(grid) == int(n) + 1
+        assert all(a < b for a, b in zip(grid[:-1], grid[1:]))
+    rng = np.random.default_rng(4)
+    p = ref.softmax(rng.standard_normal((3, 50)))
+    s, t = 0.8172569274902344, 1.0
+    np.testing.assert_allclose(((1 - t) * p + (t - s) * p) / (1 - s), p, rtol=1e-12)
