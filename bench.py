@@ -115,6 +115,18 @@ def algorithmic_bytes(cfg: dict, req: dict) -> dict:
     w_head = Vd * D * wes + Vd * 4 * (wes == 1)
     kv_row = L * 2 * D * (1 if cfg.get("kv_dtype") == "e4m3" else es)
     kv_read = sum((p + 1) * kv_row for p in req["anchor_pos"])
+    n = cfg.get("num_steps", 1)
+    if n > 1:
+        # several jumps: the anchor projection and context K/V once; per jump the DiT,
+        # x_embed's projection, E^T (act dtype) and the float32 state read and written;
+        # between jumps the full-vocabulary head (act dtype); no noise factor L; every
+        # jump's cross-attention reads the context again
+        R = bs * K
+        w_draft = ((D * H + 2 * L * D * D) * wes + (D + 2 * L * D) * 4 * (wes == 1)
+                   + n * ((D * H + L * (6 * D * D + 2 * D * F)) * wes + (D + L * (6 * D + D + F)) * 4 * (wes == 1)
+                          + H * V * es + 2 * R * V * 4)
+                   + (n - 1) * V * D * es)
+        kv_read *= n
     rows_written = (sum(req["commit"]) if req["window"] else 0) + bs
     logits = bs * K * Vd * 4
     x_in = (bs * (K + 1) * Lt * H * es) if req["window"] else 0
@@ -196,8 +208,13 @@ def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: i
     # noise factor L (square H x H), which stays bf16
     H = st["cfg"]["target_hidden"]
 
+    V, D = st["cfg"]["vocab_size"], st["cfg"]["hidden"]
+    act_shapes = {(H, H)}  # the noise factor L stays in act dtype; so do E^T and the full head of several jumps
+    if st["cfg"].get("num_steps", 1) > 1:
+        act_shapes = {(H, V), (V, D)}
+
     def wbytes(n, k):
-        return n * k * es if not e4m3 or (n == H and k == H) else n * k + n * 4
+        return n * k * es if not e4m3 or (n, k) in act_shapes else n * k + n * 4
 
     byts = sum(wbytes(n, k) + rows * k * es + rows * n * 4 for _, _, rows, n, k, _ in gem) / len(gem)
     ms = sum(r[5] for r in gem) / len(gem)

@@ -71,7 +71,13 @@ typedef enum { FLASHMAP_F32 = 0, FLASHMAP_BF16 = 1, FLASHMAP_E4M3 = 2 } flashmap
  *   cond_dim, time_embed_dim, time_scale   time conditioning (FlashMapTimeEmbedding)
  *   block_size           K, draft slots per request
  *   vocab_size           V; draft_vocab_size Vd (0 or >= V: the full vocabulary)
- *   num_steps            jumps per draft; only 1 is built (else E_UNSUPPORTED)
+ *   num_steps            jumps per draft, 1..4, on the printed grids
+ *                        (flashmap/configuration_flashmap.py, DEFAULT_JUMP_GRIDS). One
+ *                        jump reads its noise as z L^T (z ~ N(0, I_H)); several jumps
+ *                        keep a vocabulary-sized float32 state per drafted row
+ *                        (flashmap/modeling_flashmap.py, draft / embed_state / mix_state):
+ *                        the load then also keeps E^T and the full-vocabulary folded
+ *                        head, and the workspace the state, its posterior and logits.
  *   noise_gate_constant  0: gate noise_gate*(t-s) ("jump"); 1: noise_gate ("constant")
  *   page_size            P, positions per pool page (a multiple of 16)
  *   max_position         positions are < max_position (sizes the RoPE table)

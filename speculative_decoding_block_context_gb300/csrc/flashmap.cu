@@ -73,6 +73,15 @@ struct flashmap_model {
   int32_t* inv_hot = nullptr;
   float2* rope = nullptr;
   const void* embedding = nullptr;
+  // several jumps (num_steps > 1): per jump (s, t) its modulations, final AdaLN and
+  // fc2 bias terms; the embedding transposed (the GEMM's weight for [posterior; state]
+  // @ E) and the full-vocabulary folded head for the state update between jumps
+  int steps = 1;
+  float grid[5] = {0.f, 1.f, 0.f, 0.f, 0.f};
+  float step_gate[4] = {1.f, 1.f, 1.f, 1.f};
+  float *step_mods = nullptr, *step_final = nullptr, *step_fc2_beta = nullptr;  // [steps][L][9][D], [steps][2][D], [steps][L][D]
+  Weight et, full_head;
+  float *full_head_b = nullptr, *state_norm_w = nullptr;
   // launch timing (flashmap_profile_start / stop)
   bool prof_on = false;
   int prof_cap = 0;
@@ -123,6 +132,14 @@ namespace {
 
 bool is_act(int d) { return d == FLASHMAP_F32 || d == FLASHMAP_BF16; }
 
+// configuration_flashmap.py, DEFAULT_JUMP_GRIDS: jump times for 1..4 steps.
+constexpr float kJumpGrids[4][5] = {
+    {0.0f, 1.0f},
+    {0.0f, 0.8172569274902344f, 1.0f},
+    {0.0f, 0.8010796308517456f, 0.8310279846191406f, 1.0f},
+    {0.0f, 0.7906050682067871f, 0.8172569274902344f, 0.8379518389701843f, 1.0f},
+};
+
 flashmap_status validate(const flashmap_config* c) {
   if (!c) return fail(FLASHMAP_E_INVALID, "config is NULL");
   const int dims[] = {c->target_hidden, c->num_target_layers, c->hidden, c->num_layers, c->num_heads, c->head_dim,
@@ -131,8 +148,8 @@ flashmap_status validate(const flashmap_config* c) {
   for (int d : dims)
     if (d <= 0) return fail(FLASHMAP_E_INVALID, "every size in the config must be positive");
   if (c->draft_vocab_size < 0) return fail(FLASHMAP_E_INVALID, "draft_vocab_size must be >= 0");
-  if (c->num_steps != 1)
-    return fail(FLASHMAP_E_UNSUPPORTED, "only one-jump drafting (num_steps = 1) is built; got " +
+  if (c->num_steps < 1 || c->num_steps > 4)
+    return fail(FLASHMAP_E_UNSUPPORTED, "num_steps must be 1..4 (the printed jump grids); got " +
                                             std::to_string(c->num_steps));
   if (c->hidden != c->num_heads * c->head_dim) return fail(FLASHMAP_E_INVALID, "hidden != num_heads * head_dim");
   if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
@@ -152,6 +169,9 @@ flashmap_status validate(const flashmap_config* c) {
     const int a[] = {c->target_hidden, c->hidden, c->intermediate};
     for (int d : a)
       if (d % 8) return fail(FLASHMAP_E_UNSUPPORTED, "target_hidden, hidden and intermediate must be multiples of 8");
+    // the state rows feed a GEMM over the vocabulary; a row spreads over at most 8 CTAs
+    if (c->num_steps > 1 && (c->vocab_size % 8 || c->vocab_size > 393216))
+      return fail(FLASHMAP_E_UNSUPPORTED, "several jumps need vocab_size a multiple of 8 and <= 393216");
     if (c->target_hidden > 16384 || c->hidden > 16384)
       return fail(FLASHMAP_E_UNSUPPORTED, "target_hidden and hidden must be <= 16384");
   }
@@ -188,6 +208,10 @@ struct DraftWs {
   float *x, *acc_big, *acc_d, *acc_a, *acc_kv;
   void *act, *e_rows, *a_rows;
   int32_t *exp_pos, *exp_rpi;  // per-block request arrays of a multi-candidate draft
+  // several jumps: the state (R x V float32), [posterior; state] in act dtype (2R x V),
+  // their embeddings (2R x H float32) and the full-vocabulary logits (R x V float32)
+  float *state = nullptr, *emb = nullptr, *logits_full = nullptr;
+  void* xbuf = nullptr;
   int* plan;
   float *part_o, *part_ml;
   size_t bytes;
@@ -209,6 +233,13 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   w.a_rows = c.take<void>(static_cast<size_t>(bs) * m->D * es);
   w.exp_pos = c.take<int32_t>(static_cast<size_t>(bs) * 4);
   w.exp_rpi = c.take<int32_t>(static_cast<size_t>(bs) * 4);
+  if (m->steps > 1) {
+    const size_t V = static_cast<size_t>(m->V);
+    w.state = c.take<float>(R * V * 4);
+    w.xbuf = c.take<void>(2 * R * V * es);
+    w.emb = c.take<float>(2 * R * m->H * 4);
+    w.logits_full = c.take<float>(R * V * 4);
+  }
   w.plan = c.take<int>(fm::xattn_plan_ints(m->num_sms, m->nh, bs) * 4);
   const size_t chunks = fm::xattn_max_chunks(m->num_sms, m->nh, bs);
   w.part_o = c.take<float>(chunks * m->nh * 16 * m->hd * 4);
@@ -347,6 +378,8 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   m->Vd = vocab_ranking ? draft_vocab(cfg) : cfg->vocab_size;  // no ranking: the full vocabulary
   m->P = cfg->page_size;
   m->maxpos = cfg->max_position;
+  m->steps = cfg->num_steps;
+  for (int i = 0; i <= m->steps; ++i) m->grid[i] = kJumpGrids[m->steps - 1][i];
   m->embedding = embedding;
   if (cudaGetDevice(&m->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
@@ -398,6 +431,15 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
     m->inv_hot = c.take<int32_t>(V * 4);
     m->rope = c.take<float2>(static_cast<size_t>(m->maxpos) * (hd / 2) * 8);
     m->dev_err = c.take<unsigned>(256);
+    if (m->steps > 1) {
+      m->et.ptr = c.take<void>(H * V * es);
+      m->full_head.ptr = c.take<void>(V * D * es);
+      m->full_head_b = c.take<float>(V * 4);
+      m->state_norm_w = c.take<float>(H * 4);
+      m->step_mods = c.take<float>(static_cast<size_t>(m->steps) * L * 9 * D * 4);
+      m->step_final = c.take<float>(static_cast<size_t>(m->steps) * 2 * D * 4);
+      m->step_fc2_beta = c.take<float>(static_cast<size_t>(m->steps) * L * D * 4);
+    }
   };
   Carver measure(nullptr);
   layout(measure);
@@ -452,6 +494,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
 
   LCHK(fm::gemm_prepare());
   LCHK(fm::xattn_prepare());
+  if (m->steps > 1) LCHK(fm::jumps_prepare(m->V));
   LCHK(cudaMemsetAsync(m->dev_err, 0, 4, s));
   auto copy = [&](void* dst, const void* src, size_t bytes) { return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s); };
   auto bytes_of = [&](int64_t rows, int64_t cols) { return static_cast<size_t>(rows) * cols * es; };
@@ -527,6 +570,26 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   }
   LCHK(fm::adaln(s, w->final_adaln_w, w->final_adaln_b, adt, cfg->cond_dim, m->D, cond, m->final_mods,
                  m->final_mods + D, nullptr));
+  // ---- several jumps: the conditioning of every jump (s, t) of the grid
+  for (int st = 0; m->steps > 1 && st < m->steps; ++st) {
+    fm::TimeCondArgs tj = ta;
+    tj.s = m->grid[st];
+    tj.t = m->grid[st + 1];
+    LCHK(fm::time_cond(s, tj, cond));
+    for (int l = 0; l < L; ++l) {
+      const flashmap_layer_weights& lw = w->layers[l];
+      float* md = m->step_mods + (static_cast<size_t>(st) * L + l) * 9 * D;
+      const void* aw[3] = {lw.self_adaln_w, lw.cross_adaln_w, lw.mlp_adaln_w};
+      const void* ab[3] = {lw.self_adaln_b, lw.cross_adaln_b, lw.mlp_adaln_b};
+      for (int j = 0; j < 3; ++j)
+        LCHK(fm::adaln(s, aw[j], ab[j], adt, cfg->cond_dim, m->D, cond, md + (3 * j) * D, md + (3 * j + 1) * D,
+                       md + (3 * j + 2) * D));
+      LCHK(fm::to_f32(s, lw.fc2_b, adt, D, tmp_d));
+      LCHK(fm::mul_vec(s, md + 8 * D, tmp_d, m->step_fc2_beta + (static_cast<size_t>(st) * L + l) * D, m->D));
+    }
+    float* fin = m->step_final + static_cast<size_t>(st) * 2 * D;
+    LCHK(fm::adaln(s, w->final_adaln_w, w->final_adaln_b, adt, cfg->cond_dim, m->D, cond, fin, fin + D, nullptr));
+  }
 
   // ---- the uniform posterior's embedding and the Cholesky factor of E^T E
   LCHK(fm::to_f32(s, w->state_norm_w, adt, H, tmp_d));
@@ -561,6 +624,16 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
     LCHK(finish(m->head, Vd, D, FLASHMAP_F32));
     LCHK(fm::simt_gemm(s, m->Vd, 1, m->H, lm_head, adt, m->hot, H, 1, w->head_b, adt, 1, 0, m->head_b,
                        FLASHMAP_F32, 1, 0));
+    if (m->steps > 1) {
+      // E^T (H x V) for [posterior; state] @ E, and the full-vocabulary folded head
+      // LM (W_head, b_head) for the state update between jumps (float32 accumulation)
+      LCHK(fm::transpose(s, adt, embedding, V, H, const_cast<void*>(m->et.ptr)));
+      LCHK(fm::simt_gemm(s, m->V, m->D, m->H, lm_head, adt, nullptr, H, 1, w->head_w, adt, D, 1,
+                         const_cast<void*>(m->full_head.ptr), adt, D, 1));
+      LCHK(fm::simt_gemm(s, m->V, 1, m->H, lm_head, adt, nullptr, H, 1, w->head_b, adt, 1, 0, m->full_head_b,
+                         FLASHMAP_F32, 1, 0));
+      LCHK(fm::to_f32(s, w->state_norm_w, adt, H, m->state_norm_w));
+    }
     // rotary table
     std::vector<float2> rt = rope_table(m->maxpos, m->hd, cfg->rope_theta);
     LCHK(cudaMemcpyAsync(m->rope, rt.data(), rt.size() * sizeof(float2), cudaMemcpyHostToDevice, s));
@@ -576,6 +649,8 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
       ng = __bfloat162float(b);
     }
     m->gate = cfg->noise_gate_constant ? ng : ng * (1.0f - 0.0f);
+    for (int st = 0; st < m->steps; ++st)  // the noise weight of jump st: noise_gate * (t - s), or noise_gate
+      m->step_gate[st] = cfg->noise_gate_constant ? ng : ng * (m->grid[st + 1] - m->grid[st]);
     LCHK(cudaStreamSynchronize(s));  // host vectors above must outlive their copies
   }
 
@@ -591,6 +666,12 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   for (Weight* x : ws)
     if (check_weight_map(*x, m->wdt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
   if (check_weight_map(m->chol, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  if (m->steps > 1) {
+    m->et.N = m->H, m->et.K = m->V;
+    m->full_head.N = m->V, m->full_head.K = m->D;
+    if (check_weight_map(m->et, adt, &err) != FLASHMAP_OK || check_weight_map(m->full_head, adt, &err) != FLASHMAP_OK)
+      return cleanup(fail(FLASHMAP_E_CUDA, err));
+  }
   for (auto& d : m->layers) {
     d.qkv.N = 3 * m->D, d.qkv.K = m->D;
     d.o.N = m->D, d.o.K = m->D;
@@ -704,6 +785,8 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   if (bs <= 0 || req_to_page_stride <= 0) return fail(FLASHMAP_E_INVALID, "bs and the page-table stride must be positive");
   if (n_cand < 1 || static_cast<int64_t>(bs) * n_cand * m->K > (1 << 24))
     return fail(FLASHMAP_E_INVALID, "n_cand must be >= 1 and bs * n_cand * block_size <= 2^24");
+  if (n_cand > 1 && m->steps > 1)  // flashmap/sglang/model.py: several candidates take one jump
+    return fail(FLASHMAP_E_UNSUPPORTED, "candidate drafts take one jump (num_steps = 1)");
   if (pool->dtype != m->kdt || !pool->base || pool->num_pages <= 0)
     return fail(FLASHMAP_E_INVALID, "pool dtype must equal kv_dtype, with pages");
   if (!std::isfinite(noise_scale)) return fail(FLASHMAP_E_INVALID, "noise_scale must be finite");
@@ -723,6 +806,10 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     z.add(ws.acc_d, static_cast<int64_t>(R) * D);
     z.add(ws.acc_a, static_cast<int64_t>(bs) * D);
     z.add(ws.acc_kv, static_cast<int64_t>(bs) * 2 * m->L * D);
+    if (m->steps > 1) {
+      z.add(ws.emb, 2LL * R * H);
+      z.add(ws.logits_full, static_cast<int64_t>(R) * m->V);
+    }
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
   }
   // the blocks' request arrays (candidates of a request share its position and pages)
@@ -763,12 +850,6 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     a.out_loc = anchor_loc_out;
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
   }
-  // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
-  TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
-                       ws.act, H));
-  TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
   // 3. the DiT blocks
   const float eps_ln = m->cfg.layer_norm_eps, eps_qk = m->cfg.qk_norm_eps;
   // the pool as rows of head_dim channels for the TMA-fed cross-attention (bf16)
@@ -800,28 +881,82 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   xa.eps = eps_qk;
   xa.rope = m->rope;
   xa.max_pos = m->maxpos;
-  for (int l = 0; l < m->L; ++l) {
-    const LayerW& lw = m->layers[l];
-    const float* md = lw.mods;
-    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
-    TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
-                               pos_x, ws.act));
-    TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
-    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
-    xa.layer = l;
-    xa.q_norm = lw.cqn;
-    TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
-    TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
-    TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
-    TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
-    TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
-    TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lh, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
-    TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, lw.fc2_beta, false));
+  // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
+  auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
+    for (int l = 0; l < m->L; ++l) {
+      const LayerW& lw = m->layers[l];
+      const float* md = mods_all ? mods_all + static_cast<size_t>(l) * 9 * D : lw.mods;
+      const float* fc2_beta = beta_all ? beta_all + static_cast<size_t>(l) * D : lw.fc2_beta;
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
+      TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
+                                 pos_x, ws.act));
+      TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
+      xa.layer = l;
+      xa.q_norm = lw.cqn;
+      TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
+      TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
+      TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lh, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
+      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, fc2_beta, false));
+    }
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, fin, fin + D, eps_ln, out));
+    return FLASHMAP_OK;
+  };
+  if (m->steps == 1) {
+    // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
+    TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
+                         ws.act, H));
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
-  // 4. final AdaLN
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, m->final_mods, m->final_mods + D, eps_ln, hidden_out));
+  // several jumps: the state starts as V-wide noise keyed like the one-jump noise
+  const int64_t V = m->V;
+  const size_t es = dt_size(adt);
+  uint8_t* xpost = static_cast<uint8_t*>(ws.xbuf);
+  uint8_t* xstate = xpost + static_cast<size_t>(R) * V * es;
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, FLASHMAP_F32, seeds, anchor_pos, bs, m->K, static_cast<int>(V),
+                                                ws.state, 1, noise_scale));
+  for (int st = 0; st < m->steps; ++st) {
+    const float s0 = m->grid[st];
+    const float ev = s0 > 0.f ? s0 / ((1.f - s0 > 1e-3f ? 1.f - s0 : 1e-3f) * (1.f - s0 > 1e-3f ? 1.f - s0 : 1e-3f))
+                              : 0.f;
+    // the previous jump's state update, then this jump's posterior and state in act dtype
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::state_prep(Lh, adt, ws.state, ws.logits_full, m->full_head_b, R,
+                                                 static_cast<int>(V), st > 0, st > 0 ? m->grid[st - 1] : 0.f, s0, ev,
+                                                 xpost, xstate, V));
+    // [posterior; state] @ E (at s = 0 only the state: the posterior is uniform)
+    if (s0 > 0.f) {
+      TIMED_GEMM(-1, m->et, 2 * R, fm::linear(Lh, m->et, xpost, 2 * R, static_cast<int>(V), ws.emb, H, nullptr,
+                                              nullptr, true));
+    } else {
+      TIMED_GEMM(-1, m->et, R, fm::linear(Lh, m->et, xstate, R, static_cast<int>(V), ws.emb + static_cast<size_t>(R) * H,
+                                          H, nullptr, nullptr, true));
+    }
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::mix_state(Lh, adt, s0 > 0.f ? ws.emb : nullptr, ws.emb + static_cast<size_t>(R) * H,
+                                                R, H, m->u, m->state_norm_w, m->noise_norm_w, m->cfg.rms_norm_eps,
+                                                m->step_gate[st], ws.act));
+    if (st > 0) {  // the residual stream restarts at x_embed of the new input
+      fm::ZeroList z;
+      z.add(ws.x, static_cast<int64_t>(R) * D);
+      TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
+    }
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    const bool last = st + 1 == m->steps;
+    const size_t L = static_cast<size_t>(m->L);
+    const flashmap_status r = dit(m->step_mods + st * L * 9 * D, m->step_fc2_beta + st * L * D,
+                                  m->step_final + static_cast<size_t>(st) * 2 * D, last ? hidden_out : ws.act);
+    if (r != FLASHMAP_OK) return r;
+    if (!last)  // the full-vocabulary logits that move the state
+      TIMED_GEMM(-1, m->full_head, R, fm::linear(Lh, m->full_head, ws.act, R, D, ws.logits_full,
+                                                 static_cast<int>(V), nullptr, nullptr, true));
+  }
   return FLASHMAP_OK;
 }
 

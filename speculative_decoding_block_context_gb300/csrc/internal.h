@@ -121,7 +121,15 @@ cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* o
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out);
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
-                        int H, void* out, int n_cand = 1);
+                        int H, void* out, int n_cand = 1, float scale = 1.f);
+// several jumps (jumps.cu); jumps_prepare sets state_prep's shared-memory limit for a
+// vocabulary of V entries (once per device, not during capture)
+cudaError_t jumps_prepare(int V);
+cudaError_t state_prep(const Launch& L, int dtype, float* state, float* logits, const float* bias, int rows,
+                       int V, bool upd, float s, float t, float ev, void* x_post, void* x_state, int64_t ld);
+cudaError_t mix_state(const Launch& L, int dtype, float* emb_post, float* emb_state, int rows, int H, const float* u,
+                      const float* state_w, const float* noise_w, float eps, float gate, void* out);
+cudaError_t transpose(cudaStream_t s, int dtype, const void* in, int64_t rows, int64_t cols, void* out);
 cudaError_t expand_requests(const Launch& L, const int32_t* anchor_pos, const int32_t* req_pool_idx, int bs,
                             int n_cand, int32_t* pos_out, int32_t* rpi_out);
 cudaError_t philox_export(cudaStream_t s, const uint64_t* seeds, const uint32_t* ctr, int64_t n, uint32_t* out,

@@ -280,7 +280,7 @@ template <typename T>
 // bc is candidate bc % n_cand of request bc / n_cand, keyed by counter word 3 = the
 // candidate (0 for a single draft).
 __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int32_t* __restrict__ anchor_pos,
-                                   int K, int n_cand, int H, int64_t total, T* __restrict__ out) {
+                                   int K, int n_cand, int H, int64_t total, float scale, T* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int n4 = (H + 3) >> 2;
@@ -293,7 +293,7 @@ __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int
     const uint4 w = philox_seeded(LDCG(seeds + b), static_cast<uint32_t>(j4), pos, kDomainDraftNoise,
                                   static_cast<uint32_t>(c));
     const float2 n01 = box_muller(w.x, w.y), n23 = box_muller(w.z, w.w);
-    const float v[4] = {n01.x, n01.y, n23.x, n23.y};
+    const float v[4] = {scale * n01.x, scale * n01.y, scale * n23.x, scale * n23.y};
     T* o = out + static_cast<int64_t>(row) * H + 4 * j4;
 #pragma unroll
     for (int e = 0; e < 4; ++e)
@@ -428,13 +428,13 @@ cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t n
 }
 
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
-                        int H, void* out, int n_cand) {
+                        int H, void* out, int n_cand, float scale) {
   const int64_t total = static_cast<int64_t>(bs) * n_cand * K * ((H + 3) / 4);
   if (total <= 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(L.num_sms) * 16));
   cudaError_t e = cudaSuccess;
   FM_DISPATCH_T(dtype, (e = launch_k(L, draft_noise_kernel<T>, dim3(blocks), dim3(256), 0, seeds, anchor_pos, K,
-                                     n_cand, H, total, static_cast<T*>(out))));
+                                     n_cand, H, total, scale, static_cast<T*>(out))));
   return e;
 }
 

@@ -74,6 +74,14 @@ WORKLOADS = {
     "qwen3_8b_fp8_bs64": dict(model="qwen3_8b", bs=64, ctx=("uniform", 1024, 16384),
                               prefill=False, window=False, temps=("greedy",),
                               full_scatter=False, seed=5, weight_dtype="e4m3"),
+    # several jumps on the printed grids (a vocabulary-sized state between jumps)
+    "tiny_fp32_2jump": dict(model="tiny", bs=1, ctx=("fixed", 64), prefill=True, window=False,
+                            temps=("greedy",), full_scatter=False, seed=20, num_steps=2),
+    "small_bf16_3jump": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
+                             window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=21,
+                             num_steps=3),
+    "qwen3_8b_bs1_2jump": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
+                               temps=("all", 1.0), full_scatter=False, seed=2, num_steps=2),
     # e4m3 draft KV pool (keys and values stored with scale 1, fp8 queries per head)
     "small_bf16_kv8": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
                            window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=12,
@@ -96,6 +104,7 @@ def model_config(workload: str) -> dict:
     if "weight_dtype" in wl:
         cfg["weight_dtype"] = wl["weight_dtype"]
     cfg["kv_dtype"] = wl.get("kv_dtype", cfg["act_dtype"])
+    cfg["num_steps"] = wl.get("num_steps", 1)
     return cfg
 
 

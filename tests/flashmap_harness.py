@@ -37,6 +37,7 @@ class ModelState:
     handle: object = None
     Wnp: dict = field(default_factory=dict)  # float32 numpy copies for the oracle
     Enp: np.ndarray = None
+    LMnp: np.ndarray = None
     consts: object = None
 
     def oracle_cfg(self):
@@ -54,8 +55,8 @@ def load_model(workload: str, device="cuda", oracle: bool = True) -> ModelState:
         st.Enp = E.float().cpu().numpy()
         if cfg["weight_dtype"] == "e4m3":  # the oracle runs on the dequantized weights
             st.Wnp = ref.e4m3_weights(st.oracle_cfg(), st.Wnp)
-        st.consts = ref.load_constants(st.oracle_cfg(), st.Wnp, st.Enp, LM.float().cpu().numpy(),
-                                       rank.cpu().numpy())
+        st.LMnp = LM.float().cpu().numpy()
+        st.consts = ref.load_constants(st.oracle_cfg(), st.Wnp, st.Enp, st.LMnp, rank.cpu().numpy())
         if cfg["weight_dtype"] == "e4m3":
             st.consts = ref.e4m3_constants(st.consts)
     return st
@@ -153,7 +154,10 @@ def oracle_batch(st: ModelState, run: LibRun, subset, noise_scale: float = 1.0) 
     W, C = st.Wnp, st.consts
     K = cfg.block_size
     outs, ctxs, ps, seeds = oracle_contexts(st, run, subset)
-    hidden = ref.draft_requests(cfg, W, C, ctxs, ps, seeds, noise_scale)
+    if cfg.num_steps > 1:
+        hidden = ref.draft_requests_multi(cfg, W, C, st.Enp, st.LMnp, ctxs, ps, seeds, cfg.num_steps, noise_scale)
+    else:
+        hidden = ref.draft_requests(cfg, W, C, ctxs, ps, seeds, noise_scale)
     for i, b in enumerate(subset):
         logits = ref.head_logits(C, hidden[i])
         T = float(req["temperature"][b])

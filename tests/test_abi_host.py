@@ -37,7 +37,9 @@ def test_validate_configs_of_every_workload(lib):
 @pytest.mark.parametrize(
     "change,status",
     [
-        (dict(num_steps=2), 2),  # more jumps: not built
+        (dict(num_steps=5), 2),  # no printed jump grid for 5 jumps
+        (dict(num_steps=2, vocab_size=1020), 2),  # the state GEMM wants V % 8 == 0
+        (dict(num_steps=2, vocab_size=400000, draft_vocab_size=512), 2),  # a state row spans <= 8 CTAs
         (dict(hidden=100), 1),  # hidden != heads * head_dim
         (dict(head_dim=48, hidden=4 * 48), 2),
         (dict(page_size=8), 2),

@@ -211,3 +211,18 @@ def test_graph_capture_replays_draft_and_sample(small):
     # equal up to the run-to-run order of float32 atomic partial-tile sums
     assert (tokens == eager.tokens).float().mean().item() > 0.95
     assert max_rel(hidden.float().cpu().numpy(), eager.hidden.float().cpu().numpy()) < 1e-2
+
+
+# ---------------------------------------------------------------------- several jumps
+
+
+@pytest.mark.parametrize("workload,tol", [("tiny_fp32_2jump", 1e-4), ("small_bf16_3jump", 2e-2)])
+def test_several_jumps_end_to_end(workload, tol):
+    """Drafting in 2 and 3 jumps: the vocabulary-sized state, its posterior and
+    linear embeddings, the per-jump modulations and the state update between jumps,
+    against the oracle's jump loop (hidden states, logits, tokens where clear)."""
+    st = load_model(workload)
+    assert st.cfg["num_steps"] > 1
+    run = run_library(workload, st)
+    assert run.dev_err == 0
+    _check_all(st, run, range(run.req["bs"]), tol)

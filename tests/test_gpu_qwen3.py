@@ -84,6 +84,22 @@ def test_qwen3_e4m3_kv_pool_bs32(qwen):
     torch.cuda.empty_cache()
 
 
+def test_qwen3_two_jumps_bs1(qwen):
+    """Drafting in two jumps (grid 0, 0.5, 1) at the full sizes: the state is 151936
+    wide per row, read through E (4096) as posterior and state, and moved by the
+    full-vocabulary head between the jumps. Same weights, loaded with num_steps 2."""
+    import dataclasses
+
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    cfg2 = syn.model_config("qwen3_8b_bs1_2jump")
+    assert cfg2["num_steps"] == 2
+    st2 = dataclasses.replace(qwen, cfg=cfg2, handle=F.flashmap_load_weights(cfg2, qwen.W, qwen.E, qwen.LM, qwen.rank))
+    run, _ = _run_and_check(st2, "qwen3_8b_bs1_2jump")
+    del run, st2
+    torch.cuda.empty_cache()
+
+
 def test_qwen3_fp8_weights_bs64_greedy(qwen):
     """Config 5: e4m3 DiT weights with per-channel scales, bf16 activations; the oracle
     runs on the dequantized weights. The bf16 model of the other tests stays loaded."""
