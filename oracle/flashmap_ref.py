@@ -744,6 +744,18 @@ def softmax(x: np.ndarray) -> np.ndarray:
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def state_posterior(state: np.ndarray, s: float) -> np.ndarray:
+    """The posterior over tokens of a state at time s (modeling_flashmap.py, embed_state):
+    softmax(state * s / max(1 - s, 1e-3)^2), rows over the vocabulary."""
+    return softmax(np.asarray(state, dtype=np.float64) * (s / max(1.0 - s, 1e-3) ** 2))
+
+
+def jump_state(state: np.ndarray, delta: np.ndarray, s: float, t: float) -> np.ndarray:
+    """The state moved from s to t toward the DiT's distribution delta
+    (modeling_flashmap.py, draft): ((1 - t) state + (t - s) delta) / (1 - s)."""
+    return ((1.0 - t) * np.asarray(state, dtype=np.float64) + (t - s) * np.asarray(delta, dtype=np.float64)) / (1.0 - s)
+
+
 def embed_state(cfg: Config, W: dict, C: Constants, E, state: np.ndarray, s: float, t: float) -> np.ndarray:
     """The DiT input of a vocabulary-sized state (rows, V) jumping from s to t, before
     x_embed: state_norm(posterior @ E) + gate * noise_norm(state @ E), the posterior
@@ -753,8 +765,7 @@ def embed_state(cfg: Config, W: dict, C: Constants, E, state: np.ndarray, s: flo
     if s == 0:
         post = np.broadcast_to(C.uniform, (state.shape[0], C.uniform.shape[0]))
     else:
-        evidence = s / max(1.0 - s, 1e-3) ** 2
-        post = rms_norm(softmax(state * evidence) @ E64, W["state_norm.weight"], cfg.rms_norm_eps)
+        post = rms_norm(state_posterior(state, s) @ E64, W["state_norm.weight"], cfg.rms_norm_eps)
     jump = 1.0 if cfg.noise_gate_constant else t - s
     gate = float(np.asarray(W["noise_gate"], dtype=np.float64).reshape(-1)[0]) * jump
     return post + gate * rms_norm(state @ E64, W["noise_norm.weight"], cfg.rms_norm_eps)
@@ -788,6 +799,5 @@ def draft_requests_multi(cfg: Config, W: dict, C: Constants, E, LM, ctx_kv: list
             x = dit_layer(cfg, W, l, mods[l], x, positions, [(kc[l], vc[l]) for kc, vc in ctx_kv])
         hidden = layer_norm(x, cfg.layer_norm_eps) * final[0] + final[1]
         if t < 1.0:
-            delta = softmax(full_logits_of(C, W, LM, hidden))
-            state = ((1.0 - t) * state + (t - s) * delta) / (1.0 - s)
+            state = jump_state(state, softmax(full_logits_of(C, W, LM, hidden)), s, t)
     return hidden.reshape(nreq, K, -1)

@@ -557,7 +557,34 @@ def test_jump_state_update_and_grid():
     for n, grid in ref.DEFAULT_JUMP_GRIDS.items():
         assert grid[0] == 0.0 and grid[-1] == 1.0 and len(grid) == int(n) + 1
         assert all(a < b for a, b in zip(grid[:-1], grid[1:]))
+    # on the interpolant x_s = (1 - s) x0 + s x1 of the flow, a jump s -> t toward
+    # x1 lands on x_t = (1 - t) x0 + t x1, over every printed grid in turn
     rng = np.random.default_rng(4)
-    p = ref.softmax(rng.standard_normal((3, 50)))
-    s, t = 0.8172569274902344, 1.0
-    np.testing.assert_allclose(((1 - t) * p + (t - s) * p) / (1 - s), p, rtol=1e-12)
+    x0 = rng.standard_normal((3, 50))
+    x1 = ref.softmax(rng.standard_normal((3, 50)))
+    for grid in ref.DEFAULT_JUMP_GRIDS.values():
+        x = x0.copy()
+        for s, t in zip(grid[:-1], grid[1:]):
+            np.testing.assert_allclose(x, (1 - s) * x0 + s * x1, rtol=1e-9, atol=1e-12)
+            x = ref.jump_state(x, x1, s, t)
+        np.testing.assert_allclose(x, x1, rtol=1e-9, atol=1e-12)
+
+
+def test_state_posterior_is_the_gaussian_bayes_posterior():
+    """At time s the state of token j is distributed N(s e_j, (1 - s)^2 I); with a
+    uniform prior, Bayes' rule over the V candidates gives the posterior the jump
+    embeds. Brute force with scipy's Gaussian log-density on a small vocabulary."""
+    from scipy.stats import multivariate_normal
+
+    rng = np.random.default_rng(5)
+    V = 7
+    for s in (0.2, 0.5, 0.8172569274902344):
+        j_true = 3
+        x = (1 - s) * rng.standard_normal(V) + s * np.eye(V)[j_true]
+        logp = np.array([multivariate_normal.logpdf(x, mean=s * np.eye(V)[j], cov=(1 - s) ** 2 * np.eye(V))
+                         for j in range(V)])
+        bayes = np.exp(logp - logp.max())
+        bayes /= bayes.sum()
+        np.testing.assert_allclose(ref.state_posterior(x[None], s)[0], bayes, rtol=1e-9)
+    # at s = 0 the posterior is uniform
+    np.testing.assert_allclose(ref.state_posterior(rng.standard_normal((2, V)), 0.0), np.full((2, V), 1 / V))
