@@ -40,7 +40,9 @@ Readings where the pages are silent (listed with their reasons in the design doc):
   R7 candidate c of a multi-candidate (tree) draft keys its noise with counter word
      3 = c (the single draft is candidate 0);
   R8 a several-jump draft starts from V-wide noise keyed like the one-jump noise
-     (columns 0..V-1 instead of 0..H-1).
+     (columns 0..V-1 instead of 0..H-1);
+  R9 the folded-noise eigenbasis lists eigenvalues ascending, and each eigenvector's
+     entry of largest magnitude (the first such) is made positive.
 
 Pinning (what fixes each function other than itself; see tests/test_oracle_pins.py):
   philox4x32_10          published known-answer vectors (tests/golden/philox_kat.txt)
@@ -54,6 +56,10 @@ Pinning (what fixes each function other than itself; see tests/test_oracle_pins.
   slots/out_loc          brute-force page walk
   sample_rows            greedy = argmax; Gumbel-max frequencies vs softmax(l/T);
                          row independence; -inf outside the draft vocabulary
+  noise_basis            closed-form 2 x 2 eigenpairs; Q diag(lam) Q^T = E^T E,
+                         Q^T Q = I; ascending; the sign rule
+  folded_noise           the fold identity against the unfolded rms_norm / x_embed;
+                         cov of z diag(sqrt lam) Q^T against E^T E
   draft_request          parity unpinned beyond the composition of the pinned
                          parts plus structural cases (zero gates, one-position
                          context, seed independence at noise_scale 0)
@@ -107,6 +113,7 @@ class Config:
     noise_gate_constant: bool = False  # False: "jump" gate, True: "constant"
     num_steps: int = 1
     kv_dtype: str = ""  # "e4m3": the draft KV pool stores e4m3 keys/values (else act dtype)
+    noise_path: int = 0  # 0: the noise read as z L^T; 1: the folded eigenbasis (one jump)
 
     @staticmethod
     def from_dict(d: dict) -> "Config":
@@ -376,8 +383,52 @@ def load_constants(cfg: Config, W: dict, E, LM, ranking, *, skip_gram: bool = Fa
     lm_hot = _f64(LM)[hot]
     head_w = lm_hot @ _f64(W["head.weight"])  # (Vd, H) @ (H, D)
     head_b = lm_hot @ _f64(W["head.bias"])
-    return Constants(mods=mods, final=final, gate=gate, uniform=uniform, gram=gram,
-                     chol=chol, hot=hot, head_w=head_w, head_b=head_b)
+    C = Constants(mods=mods, final=final, gate=gate, uniform=uniform, gram=gram,
+                  chol=chol, hot=hot, head_w=head_w, head_b=head_b)
+    if cfg.noise_path == 1:
+        C.extra["folded"] = folded_noise(cfg, W, C)
+    return C
+
+
+def noise_basis(gram: np.ndarray):
+    """flashmap/sglang/model.py, noise_basis: (lam, Q) in float64 with
+    E^T E = Q diag(lam) Q^T, lam clamped at 0. Reading R9 fixes what the pages leave to
+    the eigensolver: lam ascending, and each column of Q signed so that its entry of
+    largest magnitude (the first such) is positive."""
+    lam, Q = np.linalg.eigh(np.asarray(gram, dtype=np.float64))
+    order = np.argsort(lam, kind="stable")
+    lam, Q = lam[order], Q[:, order]
+    lead = np.argmax(np.abs(Q), axis=0)  # first index of the largest magnitude
+    sign = np.where(Q[lead, np.arange(Q.shape[1])] < 0, -1.0, 1.0)
+    return np.clip(lam, 0.0, None), Q * sign
+
+
+@dataclass
+class FoldedNoise:
+    variance: np.ndarray  # (H,) lam / H
+    proj: np.ndarray  # (H, D) M = diag(sqrt lam) Q^T diag(w) W_x^T
+    embedded_uniform: np.ndarray  # (D,) x_embed(u)
+
+
+def folded_noise(cfg: Config, W: dict, C: Constants) -> FoldedNoise:
+    """flashmap/sglang/model.py, _folded_noise: with y = (z * sqrt(lam)) @ Q^T,
+    x_embed(u + gate * noise_norm(y)) = x_embed(u) + gate * r * (z @ M),
+    r = rsqrt(sum(lam z^2) / H + eps), M = diag(sqrt(lam)) Q^T diag(w) W_x^T,
+    w the noise norm's weight."""
+    lam, Q = noise_basis(C.gram)
+    H = lam.shape[0]
+    w = _f64(W["noise_norm.weight"])
+    proj = (np.sqrt(lam)[:, None] * Q.T) * w[None, :] @ _f64(W["x_embed.weight"]).T
+    xu = C.uniform @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
+    return FoldedNoise(variance=lam / H, proj=proj, embedded_uniform=xu)
+
+
+def embed_noise_folded(cfg: Config, F: FoldedNoise, gate: float, z: np.ndarray) -> np.ndarray:
+    """The x_embed output of one jump from noise z (rows, H) by the folded path
+    (flashmap/vllm/model.py, _one_jump): x_embed(u) + gate * r * (z @ M)."""
+    z = np.asarray(z, dtype=np.float64)
+    r = 1.0 / np.sqrt((z * z) @ F.variance + cfg.rms_norm_eps)
+    return F.embedded_uniform + (gate * r)[:, None] * (z @ F.proj)
 
 
 # ---------------------------------------------------------------------------------
@@ -461,6 +512,8 @@ def noise_embedding(cfg: Config, W: dict, C: Constants, seed: int, positions, no
     state u + gate * noise_norm(z L^T) with z keyed by the slot positions (and the
     candidate), then x_embed. Returns (K, D)."""
     z = noise_scale * draft_normals(seed, positions, cfg.target_hidden, candidate)
+    if cfg.noise_path == 1:  # the folded eigenbasis (flashmap/sglang/model.py, _folded_noise)
+        return embed_noise_folded(cfg, C.extra["folded"], C.gate, z)
     e = embed_noise(cfg, W, C, z)
     return e @ _f64(W["x_embed.weight"]).T + _f64(W["x_embed.bias"])
 

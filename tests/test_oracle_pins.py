@@ -588,3 +588,70 @@ def test_state_posterior_is_the_gaussian_bayes_posterior():
         np.testing.assert_allclose(ref.state_posterior(x[None], s)[0], bayes, rtol=1e-9)
     # at s = 0 the posterior is uniform
     np.testing.assert_allclose(ref.state_posterior(rng.standard_normal((2, V)), 0.0), np.full((2, V), 1 / V))
+
+
+# --------------------------------------------------------------------- folded-noise eigenbasis
+
+
+def test_noise_basis_closed_form_2x2():
+    """A 2 x 2 gram [[a, b], [b, c]]: eigenvalues (a + c)/2 -/+ sqrt(((a - c)/2)^2 + b^2)
+    and the eigenvector of lam along (b, lam - a), signed by reading R9."""
+    for a, b, c in ((2.0, 0.7, 1.0), (1.0, -0.3, 3.0), (0.5, 0.2, 0.5)):
+        lam, Q = ref.noise_basis(np.array([[a, b], [b, c]]))
+        half, rad = (a + c) / 2, math.hypot((a - c) / 2, b)
+        np.testing.assert_allclose(lam, [half - rad, half + rad], rtol=1e-13)
+        for i, l in enumerate((half - rad, half + rad)):
+            v = np.array([b, l - a])
+            v /= np.linalg.norm(v)
+            v *= 1.0 if v[np.argmax(np.abs(v))] > 0 else -1.0
+            np.testing.assert_allclose(Q[:, i], v, rtol=1e-12, atol=1e-14)
+
+
+def test_noise_basis_reconstructs_the_gram(tiny):
+    cfg, W, E, LM, rank, C = tiny
+    lam, Q = ref.noise_basis(C.gram)
+    G = E.astype(np.float64).T @ E.astype(np.float64)
+    assert np.linalg.norm((Q * lam) @ Q.T - G) / np.linalg.norm(G) < 1e-12
+    np.testing.assert_allclose(Q.T @ Q, np.eye(G.shape[0]), atol=1e-12)
+    assert np.all(np.diff(lam) >= 0) and np.all(lam >= 0)
+    lead = Q[np.argmax(np.abs(Q), axis=0), np.arange(Q.shape[1])]
+    assert np.all(lead > 0)
+
+
+def test_folded_noise_is_the_unfolded_embedding():
+    """flashmap/sglang/model.py, _folded_noise: x_embed(u + gate * noise_norm(y)) with
+    y = (z * sqrt(lam)) @ Q^T equals x_embed(u) + gate * r * (z @ M), the unfolded side
+    written with the pinned rms_norm and a plain x_embed; a gate != 1 and a noise norm
+    weight far from 1 make a dropped factor fail."""
+    cfg, W, E, LM, rank = _tiny(noise_path=1)
+    W = dict(W)
+    rng = np.random.default_rng(8)
+    W["noise_norm.weight"] = (1.0 + 0.5 * rng.standard_normal(cfg.target_hidden)).astype(np.float32)
+    W["noise_gate"] = np.array([0.7], dtype=np.float32)
+    C = ref.load_constants(cfg, W, E, LM, rank)
+    F = C.extra["folded"]
+    lam, Q = ref.noise_basis(C.gram)
+    z = rng.standard_normal((5, cfg.target_hidden)) * 1.3
+    y = (z * np.sqrt(lam)) @ Q.T
+    e = C.uniform + C.gate * ref.rms_norm(y, W["noise_norm.weight"], cfg.rms_norm_eps)
+    unfolded = e @ W["x_embed.weight"].astype(np.float64).T + W["x_embed.bias"]
+    np.testing.assert_allclose(ref.embed_noise_folded(cfg, F, C.gate, z), unfolded, rtol=1e-10, atol=1e-12)
+    # the draft's noise embedding takes this path when noise_path = 1
+    x = ref.noise_embedding(cfg, W, C, 17, np.arange(3, 3 + cfg.block_size), 1.0)
+    z2 = ref.draft_normals(17, np.arange(3, 3 + cfg.block_size), cfg.target_hidden)
+    np.testing.assert_allclose(x, ref.embed_noise_folded(cfg, F, C.gate, z2), rtol=1e-13)
+
+
+def test_folded_noise_law_matches_embedding_covariance():
+    """(z * sqrt(lam)) @ Q^T ~ N(0, E^T E), like z L^T; a transposed basis (Q diag(lam)
+    read as rows) fails on a gram far from a multiple of the identity."""
+    rng = np.random.default_rng(9)
+    V, H, N = 512, 24, 60000
+    E = rng.standard_normal((V, H)) @ (rng.standard_normal((H, H)) + 2 * np.eye(H)) * 0.05
+    G = E.T @ E
+    lam, Q = ref.noise_basis(G)
+    z = ref.draft_normals(7, np.arange(N), H)
+    y = (z * np.sqrt(lam)) @ Q.T
+    assert np.linalg.norm(y.T @ y / N - G) / np.linalg.norm(G) < 0.05
+    wrong = (z * np.sqrt(lam)) @ Q
+    assert np.linalg.norm(wrong.T @ wrong / N - G) / np.linalg.norm(G) > 0.2
