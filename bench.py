@@ -116,6 +116,10 @@ def algorithmic_bytes(cfg: dict, req: dict) -> dict:
     kv_row = L * 2 * D * (1 if cfg.get("kv_dtype") == "e4m3" else es)
     kv_read = sum((p + 1) * kv_row for p in req["anchor_pos"])
     n = cfg.get("num_steps", 1)
+    if cfg.get("noise_path", 0) == 1:
+        # the folded eigenbasis: one act-dtype (D x H) projection instead of the noise
+        # factor L (H x H) and x_embed (D x H)
+        w_draft += D * H * es - H * H * es - D * H * wes - D * 4 * (wes == 1)
     if n > 1:
         # several jumps: the anchor projection and context K/V once; per jump the DiT,
         # x_embed's projection, E^T (act dtype) and the float32 state read and written;

@@ -102,6 +102,16 @@ typedef enum { FLASHMAP_F32 = 0, FLASHMAP_BF16 = 1, FLASHMAP_E4M3 = 2 } flashmap
  *                        max(max|q|, 1e-12) / 448 over the block's slots and channels,
  *                        descaling the scores by it (flashmap/sglang/model.py,
  *                        _paged_cross_attention_fp8). Halves the pool's bytes.
+ *   noise_path           how one jump reads its noise: 0, as z L^T then noise_norm and
+ *                        x_embed; 1, the folded eigenbasis (flashmap/sglang/model.py,
+ *                        noise_basis / _folded_noise): at load E^T E = Q diag(lam) Q^T
+ *                        (float64 one-sided Jacobi; lam ascending, each eigenvector's
+ *                        entry of largest magnitude positive), M = diag(sqrt lam) Q^T
+ *                        diag(noise_norm w) W_x^T kept in act_dtype, lam / H and
+ *                        x_embed(u); per step x = x_embed(u) + gate * r * (z @ M),
+ *                        r = rsqrt(sum(lam z^2) / H + eps): one GEMM instead of two and
+ *                        a row norm. Same z as path 0, the same law of x, other samples.
+ *                        One jump only (num_steps = 1).
  */
 typedef struct {
   int32_t target_hidden, num_target_layers, hidden, num_layers, num_heads, head_dim;
@@ -109,6 +119,7 @@ typedef struct {
   int32_t num_steps, noise_gate_constant, page_size, max_position;
   float time_scale, rope_theta, rms_norm_eps, qk_norm_eps, layer_norm_eps;
   int32_t act_dtype, weight_dtype, kv_dtype;
+  int32_t noise_path;
 } flashmap_config;
 
 /* One DiT block's raw weights (flashmap/modeling_flashmap.py, FlashMapLayer), all
@@ -392,6 +403,14 @@ flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* 
  * Any pointer may be NULL. */
 flashmap_status flashmap_debug_constants(const flashmap_model* model, float* chol, float* uniform,
                                          int64_t* hot_ids, flashmap_stream stream);
+
+/* The folded-noise constants of a model loaded with noise_path 1, copied to caller
+ * buffers (device): variance = lam / H (H) float32 in ascending order, x_embed(u) (D)
+ * float32, the projection as the GEMM holds it, M^T (D, H) in act_dtype; sweeps (host)
+ * the Jacobi sweeps the load took. Any pointer may be NULL. E_INVALID when the model
+ * was loaded with noise_path 0. */
+flashmap_status flashmap_debug_folded(const flashmap_model* model, float* variance, float* embedded_uniform,
+                                      void* proj, int32_t* sweeps, flashmap_stream stream);
 
 #ifdef __cplusplus
 }

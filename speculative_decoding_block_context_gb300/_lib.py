@@ -31,7 +31,8 @@ class flashmap_config(_c.Structure):
         "intermediate", "cond_dim", "time_embed_dim", "block_size", "vocab_size", "draft_vocab_size",
         "num_steps", "noise_gate_constant", "page_size", "max_position")] + \
         [(n, _c.c_float) for n in ("time_scale", "rope_theta", "rms_norm_eps", "qk_norm_eps", "layer_norm_eps")] + \
-        [("act_dtype", _c.c_int32), ("weight_dtype", _c.c_int32), ("kv_dtype", _c.c_int32)]
+        [("act_dtype", _c.c_int32), ("weight_dtype", _c.c_int32), ("kv_dtype", _c.c_int32),
+         ("noise_path", _c.c_int32)]
 
 
 LAYER_FIELDS = {
@@ -115,6 +116,7 @@ def lib():
         L.flashmap_debug_philox.argtypes = [_vp, _vp, _c.c_int64, _vp, _vp, _vp]
         L.flashmap_debug_linear.argtypes = [_c.c_int32, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp]
         L.flashmap_debug_constants.argtypes = [_vp, _vp, _vp, _vp, _vp]
+        L.flashmap_debug_folded.argtypes = [_vp, _vp, _vp, _vp, P(_c.c_int32), _vp]
         L.flashmap_sample_logits_static.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp]
         L.flashmap_build_tree.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp]
         L.flashmap_draft_candidates.argtypes = [_vp, P(flashmap_kv_pool), _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp,
@@ -297,6 +299,14 @@ def flashmap_debug_linear(dtype: int, x, w, out, stream=None) -> None:
 
 def flashmap_debug_constants(model: Model, chol=None, uniform=None, hot_ids=None, stream=None) -> None:
     _check(lib().flashmap_debug_constants(model.handle, _ptr(chol), _ptr(uniform), _ptr(hot_ids), _stream(stream)))
+
+
+def flashmap_debug_folded(model: Model, variance=None, embedded_uniform=None, proj=None, stream=None) -> int:
+    """Copies the folded-noise constants; returns the Jacobi sweeps the load took."""
+    sweeps = _c.c_int32(0)
+    _check(lib().flashmap_debug_folded(model.handle, _ptr(variance), _ptr(embedded_uniform), _ptr(proj),
+                                       _c.byref(sweeps), _stream(stream)))
+    return int(sweeps.value)
 
 
 def flashmap_profile_start(model: Model, capacity: int = 4096) -> None:

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libflashmap.so")
-SOURCES = ["gemm.cu", "attention.cu", "rows.cu", "sample.cu", "tree.cu", "jumps.cu", "loadtime.cu", "flashmap.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "rows.cu", "sample.cu", "tree.cu", "jumps.cu", "eigen.cu", "loadtime.cu", "flashmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE] + ARCH
 

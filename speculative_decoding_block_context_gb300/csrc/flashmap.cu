@@ -82,6 +82,11 @@ struct flashmap_model {
   float *step_mods = nullptr, *step_final = nullptr, *step_fc2_beta = nullptr;  // [steps][L][9][D], [steps][2][D], [steps][L][D]
   Weight et, full_head;
   float *full_head_b = nullptr, *state_norm_w = nullptr;
+  // folded-noise eigenbasis (noise_path 1): M = diag(sqrt lam) Q^T diag(w) W_x^T as a
+  // GEMM weight (D out, H in), lam / H, x_embed(u); the eigensolver's sweep count
+  int noise_path = 0, eig_sweeps = 0;
+  Weight fold;
+  float *fold_var = nullptr, *fold_xu = nullptr;
   // launch timing (flashmap_profile_start / stop)
   bool prof_on = false;
   int prof_cap = 0;
@@ -148,6 +153,10 @@ flashmap_status validate(const flashmap_config* c) {
   for (int d : dims)
     if (d <= 0) return fail(FLASHMAP_E_INVALID, "every size in the config must be positive");
   if (c->draft_vocab_size < 0) return fail(FLASHMAP_E_INVALID, "draft_vocab_size must be >= 0");
+  if (c->noise_path != 0 && c->noise_path != 1)
+    return fail(FLASHMAP_E_INVALID, "noise_path must be 0 (z L^T) or 1 (folded eigenbasis)");
+  if (c->noise_path == 1 && c->num_steps != 1)
+    return fail(FLASHMAP_E_UNSUPPORTED, "the folded-noise path is a one-jump path (num_steps = 1)");
   if (c->num_steps < 1 || c->num_steps > 4)
     return fail(FLASHMAP_E_UNSUPPORTED, "num_steps must be 1..4 (the printed jump grids); got " +
                                             std::to_string(c->num_steps));
@@ -379,6 +388,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   m->P = cfg->page_size;
   m->maxpos = cfg->max_position;
   m->steps = cfg->num_steps;
+  m->noise_path = cfg->noise_path;
   for (int i = 0; i <= m->steps; ++i) m->grid[i] = kJumpGrids[m->steps - 1][i];
   m->embedding = embedding;
   if (cudaGetDevice(&m->device) != cudaSuccess ||
@@ -440,6 +450,11 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
       m->step_final = c.take<float>(static_cast<size_t>(m->steps) * 2 * D * 4);
       m->step_fc2_beta = c.take<float>(static_cast<size_t>(m->steps) * L * D * 4);
     }
+    if (m->noise_path == 1) {
+      m->fold.ptr = c.take<void>(D * H * es);
+      m->fold_var = c.take<float>(H * 4);
+      m->fold_xu = c.take<float>(D * 4);
+    }
   };
   Carver measure(nullptr);
   layout(measure);
@@ -453,7 +468,9 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
 
   // Load-time scratch: gram (float64 H x H), column sums, conditioning, fc2 bias.
   void* scratch = nullptr;
-  const size_t scratch_bytes = align_up(H * H * 8) + align_up(H * 8) + align_up(C * 8) + align_up(std::max(D, H) * 4);
+  const size_t fold_bytes = m->noise_path == 1 ? align_up(fm::folded_scratch_bytes(static_cast<int>(H))) : 0;
+  const size_t scratch_bytes =
+      align_up(H * H * 8) + align_up(H * 8) + align_up(C * 8) + align_up(std::max(D, H) * 4) + fold_bytes;
   if (cudaMalloc(&scratch, scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
     return cleanup(fail(FLASHMAP_E_NOMEM, "cannot allocate load-time scratch"));
@@ -467,6 +484,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   double* colsum = sc.take<double>(H * 8);
   double* cond = sc.take<double>(C * 8);
   float* tmp_d = sc.take<float>(std::max(D, H) * 4);  // D or H floats of scratch
+  void* fold_scratch = fold_bytes ? sc.take<void>(fold_bytes) : nullptr;
   // e4m3: each weight is assembled in act_dtype (the folded head in float32) in one
   // staging buffer, then quantized into the arena; stream order serializes the reuse.
   void* stage = nullptr;
@@ -594,10 +612,24 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   // ---- the uniform posterior's embedding and the Cholesky factor of E^T E
   LCHK(fm::to_f32(s, w->state_norm_w, adt, H, tmp_d));
   LCHK(fm::uniform_constant(s, embedding, adt, V, m->H, tmp_d, cfg->rms_norm_eps, colsum, m->u));
-  LCHK(cudaMemsetAsync(gram, 0, H * H * 8, s));
-  LCHK(fm::simt_gemm(s, m->H, m->H, m->V, embedding, adt, nullptr, 1, H, embedding, adt, H, 1, gram, FLASHMAP_F32, H, 2));
+  if (m->noise_path == 1) {  // the eigenbasis is sensitive to the gram: float64 products and sums
+    LCHK(fm::gram_f64(s, embedding, adt, V, m->H, gram));
+  } else {  // float32 partial sums of 1024 products, added in float64
+    LCHK(cudaMemsetAsync(gram, 0, H * H * 8, s));
+    LCHK(fm::simt_gemm(s, m->H, m->H, m->V, embedding, adt, nullptr, 1, H, embedding, adt, H, 1, gram, FLASHMAP_F32, H, 2));
+  }
   LCHK(fm::cholesky_f64(s, gram, m->H, m->dev_err));
   LCHK(fm::chol_store(s, gram, m->H, adt, const_cast<void*>(m->chol.ptr)));
+  if (m->noise_path == 1) {
+    // the eigenbasis of E^T E from X = L^T (the factor's storage is taken over), then
+    // the folded projection, lam / H and x_embed(u)
+    std::string eerr;
+    const cudaError_t e = fm::folded_noise_constants(s, gram, m->H, fold_scratch, m->noise_norm_w, w->x_embed_w,
+                                                     w->x_embed_b, adt, m->D, m->u, const_cast<void*>(m->fold.ptr),
+                                                     m->fold_var, m->fold_xu, &m->eig_sweeps, &eerr);
+    if (e != cudaSuccess)
+      return cleanup(fail(FLASHMAP_E_CUDA, eerr.empty() ? std::string("folded noise: ") + cudaGetErrorString(e) : eerr));
+  }
 
   // ---- draft vocabulary and the folded head
   {
@@ -666,6 +698,10 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   for (Weight* x : ws)
     if (check_weight_map(*x, m->wdt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
   if (check_weight_map(m->chol, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  if (m->noise_path == 1) {
+    m->fold.N = m->D, m->fold.K = m->H;
+    if (check_weight_map(m->fold, adt, &err) != FLASHMAP_OK) return cleanup(fail(FLASHMAP_E_CUDA, err));
+  }
   if (m->steps > 1) {
     m->et.N = m->H, m->et.K = m->V;
     m->full_head.N = m->V, m->full_head.K = m->D;
@@ -907,6 +943,14 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, fin, fin + D, eps_ln, out));
     return FLASHMAP_OK;
   };
+  if (m->steps == 1 && m->noise_path == 1) {
+    // 2'. folded noise: z (Philox, as below) scaled by gate * rsqrt(sum(lam z^2) / H + eps),
+    // then one GEMM through M onto x_embed(u)
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::folded_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, n_cand, noise_scale,
+                                                   m->fold_var, m->cfg.rms_norm_eps, m->gate, ws.act));
+    TIMED_GEMM(-1, m->fold, R, fm::linear(Lh, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, false));
+    return dit(nullptr, nullptr, m->final_mods, hidden_out);
+  }
   if (m->steps == 1) {
     // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
@@ -1153,6 +1197,22 @@ flashmap_status flashmap_debug_constants(const flashmap_model* m, float* chol, f
   if (chol) FM_CUDA(fm::to_f32(s, m->chol.ptr, m->adt, static_cast<int64_t>(m->H) * m->H, chol));
   if (uniform) FM_CUDA(cudaMemcpyAsync(uniform, m->u, static_cast<size_t>(m->H) * 4, cudaMemcpyDeviceToDevice, s));
   if (hot_ids) FM_CUDA(cudaMemcpyAsync(hot_ids, m->hot, static_cast<size_t>(m->Vd) * 8, cudaMemcpyDeviceToDevice, s));
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_debug_folded(const flashmap_model* m, float* variance, float* embedded_uniform, void* proj,
+                                      int32_t* sweeps, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m) return fail(FLASHMAP_E_INVALID, "NULL model");
+  if (m->noise_path != 1) return fail(FLASHMAP_E_INVALID, "the model was loaded without the folded-noise path");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (variance) FM_CUDA(cudaMemcpyAsync(variance, m->fold_var, static_cast<size_t>(m->H) * 4, cudaMemcpyDeviceToDevice, s));
+  if (embedded_uniform)
+    FM_CUDA(cudaMemcpyAsync(embedded_uniform, m->fold_xu, static_cast<size_t>(m->D) * 4, cudaMemcpyDeviceToDevice, s));
+  if (proj)
+    FM_CUDA(cudaMemcpyAsync(proj, m->fold.ptr, static_cast<size_t>(m->D) * m->H * dt_size(m->adt),
+                            cudaMemcpyDeviceToDevice, s));
+  if (sweeps) *sweeps = m->eig_sweeps;
   return FLASHMAP_OK;
 }
 

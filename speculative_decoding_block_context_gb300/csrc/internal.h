@@ -122,6 +122,10 @@ cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t n
                         int n, void* out);
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
                         int H, void* out, int n_cand = 1, float scale = 1.f);
+// z (keyed like draft_noise) scaled per row by gate * rsqrt(sum(variance z^2) + eps): the
+// folded projection's input (rows.cu)
+cudaError_t folded_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
+                         int H, int n_cand, float scale, const float* variance, float eps, float gate, void* out);
 // several jumps (jumps.cu); jumps_prepare sets state_prep's shared-memory limit for a
 // vocabulary of V entries (once per device, not during capture)
 cudaError_t jumps_prepare(int V);
@@ -198,6 +202,15 @@ cudaError_t adaln(cudaStream_t s, const void* w, const void* b, int dtype, int C
 cudaError_t uniform_constant(cudaStream_t s, const void* E, int dtype, int64_t V, int H, const float* w, float eps,
                              double* colsum, float* u);
 cudaError_t cholesky_f64(cudaStream_t s, double* A, int n, unsigned* err);
+// folded-noise eigenbasis (eigen.cu): from the Cholesky factor's storage X (row-major
+// L, n x n float64; overwritten), the folded projection proj (D x n, dtype), lam / n
+// and x_embed(u); scratch of folded_scratch_bytes(n). Synchronizes s.
+size_t folded_scratch_bytes(int n);
+// E^T E (H x H) with float64 products and sums (eigen.cu)
+cudaError_t gram_f64(cudaStream_t s, const void* E, int dtype, int64_t V, int H, double* G);
+cudaError_t folded_noise_constants(cudaStream_t s, double* X, int n, void* scratch, const float* noise_w,
+                                   const void* xw, const void* xb, int dtype, int D, const float* u, void* proj,
+                                   float* variance, float* xu, int* sweeps_out, std::string* err);
 cudaError_t chol_store(cudaStream_t s, const double* A, int n, int dtype, void* out);
 cudaError_t quantize_e4m3(cudaStream_t s, const void* w, int dtype, int rows, int cols, void* q, float* scale);
 

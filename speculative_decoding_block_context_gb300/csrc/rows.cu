@@ -301,6 +301,65 @@ __global__ void draft_noise_kernel(const uint64_t* __restrict__ seeds, const int
   }
 }
 
+// The folded path's noise input, one CTA per drafted row: z (the draft_noise
+// normals of the row, times scale) and r = rsqrt(sum_i variance_i z_i^2 + eps), written
+// as z * gate * r (flashmap/sglang/model.py, _folded_noise; flashmap/vllm/model.py,
+// _one_jump). A thread holds up to kFoldPer groups of 4 normals between the sum and
+// the store (H <= 4 * kFoldPer * blockDim).
+constexpr int kFoldThreads = 1024, kFoldPer = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kFoldThreads) folded_noise_kernel(const uint64_t* __restrict__ seeds,
+                                                                    const int32_t* __restrict__ anchor_pos, int K,
+                                                                    int n_cand, int H, float scale,
+                                                                    const float* __restrict__ variance, float eps,
+                                                                    float gate, T* __restrict__ out) {
+  __shared__ float red[32];
+  __shared__ uint64_t s_seed;
+  __shared__ uint32_t s_pos;
+  pdl_trigger();
+  pdl_wait();
+  const int row = blockIdx.x, bc = row / K, k = row - bc * K;
+  const int b = bc / n_cand, c = bc - b * n_cand;
+  if (threadIdx.x == 0) {
+    s_seed = LDCG(seeds + b);
+    s_pos = static_cast<uint32_t>(LDCG(anchor_pos + b) + 1 + k);
+  }
+  __syncthreads();
+  const int n4 = H >> 2;
+  const float4* var4 = reinterpret_cast<const float4*>(variance);
+  float4 z[kFoldPer];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kFoldPer; ++i) {
+    const int j4 = threadIdx.x + i * blockDim.x;
+    if (j4 < n4) {
+      const uint4 w = philox_seeded(s_seed, static_cast<uint32_t>(j4), s_pos, kDomainDraftNoise,
+                                    static_cast<uint32_t>(c));
+      const float2 n01 = box_muller(w.x, w.y), n23 = box_muller(w.z, w.w);
+      z[i] = make_float4(scale * n01.x, scale * n01.y, scale * n23.x, scale * n23.y);
+      const float4 v = var4[j4];
+      ss = fmaf(v.x, z[i].x * z[i].x, ss);
+      ss = fmaf(v.y, z[i].y * z[i].y, ss);
+      ss = fmaf(v.z, z[i].z * z[i].z, ss);
+      ss = fmaf(v.w, z[i].w * z[i].w, ss);
+    }
+  }
+  ss = block_sum(ss, red);
+  const float f = gate * rsqrtf(ss + eps);
+  T* o = out + static_cast<int64_t>(row) * H;
+#pragma unroll
+  for (int i = 0; i < kFoldPer; ++i) {
+    const int j4 = threadIdx.x + i * blockDim.x;
+    if (j4 < n4) {
+      o[4 * j4 + 0] = from_f32<T>(z[i].x * f);
+      o[4 * j4 + 1] = from_f32<T>(z[i].y * f);
+      o[4 * j4 + 2] = from_f32<T>(z[i].z * f);
+      o[4 * j4 + 3] = from_f32<T>(z[i].w * f);
+    }
+  }
+}
+
 __global__ void zero_kernel(ZeroList z) {
   pdl_trigger();
   pdl_wait();
@@ -435,6 +494,18 @@ cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const
   cudaError_t e = cudaSuccess;
   FM_DISPATCH_T(dtype, (e = launch_k(L, draft_noise_kernel<T>, dim3(blocks), dim3(256), 0, seeds, anchor_pos, K,
                                      n_cand, H, total, scale, static_cast<T*>(out))));
+  return e;
+}
+
+cudaError_t folded_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
+                         int H, int n_cand, float scale, const float* variance, float eps, float gate, void* out) {
+  const int rows = bs * n_cand * K;
+  if (rows <= 0) return cudaSuccess;
+  if (H % 4 || H > 4 * kFoldPer * kFoldThreads) return cudaErrorInvalidValue;
+  const int threads = std::min(kFoldThreads, std::max(32, ((H / 4 + kFoldPer - 1) / kFoldPer + 31) / 32 * 32));
+  cudaError_t e = cudaSuccess;
+  FM_DISPATCH_T(dtype, (e = launch_k(L, folded_noise_kernel<T>, dim3(rows), dim3(threads), 0, seeds, anchor_pos, K,
+                                     n_cand, H, scale, variance, eps, gate, static_cast<T*>(out))));
   return e;
 }
 

@@ -82,6 +82,14 @@ WORKLOADS = {
                              num_steps=3),
     "qwen3_8b_bs1_2jump": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
                                temps=("all", 1.0), full_scatter=False, seed=2, num_steps=2),
+    # the folded-noise eigenbasis (noise_path 1): one GEMM through M instead of z L^T
+    "tiny_fp32_folded": dict(model="tiny", bs=1, ctx=("fixed", 64), prefill=True, window=False,
+                             temps=("greedy",), full_scatter=False, seed=30, noise_path=1),
+    "small_bf16_folded": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
+                              window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=31,
+                              noise_path=1),
+    "qwen3_8b_bs1_folded": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
+                                temps=("all", 1.0), full_scatter=False, seed=2, noise_path=1),
     # e4m3 draft KV pool (keys and values stored with scale 1, fp8 queries per head)
     "small_bf16_kv8": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
                            window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=12,
@@ -105,6 +113,7 @@ def model_config(workload: str) -> dict:
         cfg["weight_dtype"] = wl["weight_dtype"]
     cfg["kv_dtype"] = wl.get("kv_dtype", cfg["act_dtype"])
     cfg["num_steps"] = wl.get("num_steps", 1)
+    cfg["noise_path"] = wl.get("noise_path", 0)
     return cfg
 
 

@@ -38,6 +38,8 @@ def test_validate_configs_of_every_workload(lib):
     "change,status",
     [
         (dict(num_steps=5), 2),  # no printed jump grid for 5 jumps
+        (dict(noise_path=2), 1),  # 0 (z L^T) or 1 (folded eigenbasis)
+        (dict(noise_path=1, num_steps=2), 2),  # the folded path is a one-jump path
         (dict(num_steps=2, vocab_size=1020), 2),  # the state GEMM wants V % 8 == 0
         (dict(num_steps=2, vocab_size=400000, draft_vocab_size=512), 2),  # a state row spans <= 8 CTAs
         (dict(hidden=100), 1),  # hidden != heads * head_dim

@@ -226,3 +226,37 @@ def test_several_jumps_end_to_end(workload, tol):
     run = run_library(workload, st)
     assert run.dev_err == 0
     _check_all(st, run, range(run.req["bs"]), tol)
+
+
+# ---------------------------------------------------------------------- folded-noise eigenbasis
+
+
+def _check_folded_constants(st, tol):
+    """The load-time eigenbasis against the oracle's float64 eigh (reading R9: ascending,
+    each eigenvector's largest entry positive): lam / H, x_embed(u) and the projection
+    M^T as the GEMM holds it (relative to its largest entry)."""
+    H, D = st.cfg["target_hidden"], st.cfg["hidden"]
+    Fo = st.consts.extra["folded"]
+    var = torch.empty(H, dtype=torch.float32, device="cuda")
+    xu = torch.empty(D, dtype=torch.float32, device="cuda")
+    proj = torch.empty((D, H), dtype=syn.torch_dtype(st.cfg["act_dtype"]), device="cuda")
+    sweeps = F.flashmap_debug_folded(st.handle, var, xu, proj)
+    torch.cuda.synchronize()
+    assert 0 < sweeps < 60
+    np.testing.assert_allclose(var.cpu().numpy(), Fo.variance, rtol=1e-5, atol=1e-7 * Fo.variance.max())
+    assert max_rel(xu.cpu().numpy(), Fo.embedded_uniform) < 1e-5
+    assert max_rel(proj.float().cpu().numpy(), Fo.proj.T) < tol
+    return sweeps
+
+
+@pytest.mark.parametrize("workload,tol,ctol", [("tiny_fp32_folded", 1e-4, 1e-5), ("small_bf16_folded", 2e-2, 1e-2)])
+def test_folded_noise_end_to_end(workload, tol, ctol):
+    """noise_path 1: the eigenbasis found at load (float64 one-sided Jacobi) and the
+    per-step folded noise (z scaled by gate * rsqrt(sum(lam z^2) / H + eps), one GEMM
+    through M onto x_embed(u)) against the oracle's eigh and fold."""
+    st = load_model(workload)
+    _check_folded_constants(st, ctol)
+    run = run_library(workload, st)
+    assert run.dev_err == 0
+    _check_all(st, run, range(run.req["bs"]), tol)
+

@@ -100,6 +100,34 @@ def test_qwen3_two_jumps_bs1(qwen):
     torch.cuda.empty_cache()
 
 
+def test_qwen3_folded_noise_bs1(qwen):
+    """The folded-noise eigenbasis at the full sizes: the 4096 x 4096 gram's float64
+    Jacobi eigenpairs at load against the oracle's eigh (lam / H, x_embed(u), the
+    projection), then the batch-1 draft through the folded GEMM. Same weights, loaded
+    with noise_path 1; the oracle adds its fold to the constants it already has."""
+    import dataclasses
+    import time
+
+    from oracle import flashmap_ref as ref
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    from .test_gpu_parity import _check_folded_constants
+
+    cfgf = syn.model_config("qwen3_8b_bs1_folded")
+    t0 = time.perf_counter()
+    handle = F.flashmap_load_weights(cfgf, qwen.W, qwen.E, qwen.LM, qwen.rank)
+    torch.cuda.synchronize()
+    load_s = time.perf_counter() - t0
+    consts = dataclasses.replace(qwen.consts, extra=dict(qwen.consts.extra))
+    consts.extra["folded"] = ref.folded_noise(ref.Config.from_dict(cfgf), qwen.Wnp, consts)
+    stf = dataclasses.replace(qwen, cfg=cfgf, handle=handle, consts=consts)
+    sweeps = _check_folded_constants(stf, 1e-2)
+    print("folded load", round(load_s, 2), "s,", sweeps, "Jacobi sweeps")
+    run, _ = _run_and_check(stf, "qwen3_8b_bs1_folded")
+    del run, stf
+    torch.cuda.empty_cache()
+
+
 def test_qwen3_fp8_weights_bs64_greedy(qwen):
     """Config 5: e4m3 DiT weights with per-channel scales, bf16 activations; the oracle
     runs on the dequantized weights. The bf16 model of the other tests stays loaded."""

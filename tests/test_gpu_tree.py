@@ -64,6 +64,7 @@ def test_tree_refuses_out_of_range_shapes():
 @pytest.mark.parametrize("workload,n,width,tol,margin,min_trees", [
     ("small_bf16", 3, 12, 2e-2, 1e-2, 0),  # bf16: tokens compared where the margin is clear
     ("tiny_fp32", 8, 16, 1e-4, 1e-4, 1),   # fp32: whole trees compared
+    ("small_bf16_folded", 3, 12, 2e-2, 1e-2, 0),  # candidates on the folded-noise path
 ])
 def test_candidate_draft_and_tree_against_the_oracle(workload, n, width, tol, margin, min_trees):
     margin_min = margin
