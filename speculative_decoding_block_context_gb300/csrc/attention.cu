@@ -398,6 +398,32 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
+// 2^x (ex2.approx, subnormal results flushed to zero; -inf -> 0).
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Four e4m3 values (one word, lowest byte first) -> two half2 words (exact).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+// D += A B with e4m3 A (16 x 32, row) and B (32 x 8, col), float32 accumulation.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Four e4m3-representable floats -> four e4m3 bytes (exact), lowest first.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
 // bf16 operands for a bf16 pool; half for an e4m3 pool (e4m3 widens to half in one
 // conversion per pair, and the e4m3 queries and the probabilities are exact or finer
 // in half)
@@ -414,10 +440,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 }
 
 constexpr int kXStages = 3;   // bf16 pool: cp.async stages per warp
-constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage)
+constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage; 3 CTAs per SM)
 
-// Per warp: a ring of K/V blocks as they arrive and, for an e4m3 pool, one half block
-// pair (the converted current block) in the swizzled layout the ldmatrix reads use.
+// Per warp: a ring of K/V blocks as they arrive (16-byte chunks XOR-swizzled by row).
+// For an e4m3 pool the keys feed the e4m3 tensor-core product as stored; once they are
+// read, the block's values are widened to half over the same stage (the 2 x 16 x HD
+// e4m3 bytes of K and V hold exactly one 16 x HD half block) for the half product
+// with the probabilities.
 template <int HD, bool F8 = false>
 struct XCfg {
   static constexpr int ROWB = HD * 2;     // bytes of one bf16 position row
@@ -428,7 +457,10 @@ struct XCfg {
   static constexpr int CH8 = HD / 16;     // 16-byte chunks per e4m3 row
   static constexpr int STAGES = F8 ? kXStages8 : kXStages;
   static constexpr int STAGE = F8 ? 2 * BLK8 : 2 * BLK;
-  static constexpr int WORK = F8 ? 2 * BLK : 0;     // converted block pair (e4m3 only)
+  static constexpr int WORK = 0;
+  // e4m3 rows are HD bytes: chunk c of row r sits at c ^ ((r >> SW8) & (CH8 - 1)), so the
+  // 8 rows an ldmatrix reads fall on distinct banks (128-byte rows: r & 7; 64-byte: r/2 & 3)
+  static constexpr int SW8 = CH8 >= 8 ? 0 : (CH8 == 4 ? 1 : 2);
   static constexpr int RING = STAGES * STAGE + WORK;  // per warp
   static constexpr int SMEM_RING = 4 * RING;
   static constexpr int SQ_OFF = SMEM_RING;          // the item's queries, beside the rings
@@ -438,7 +470,7 @@ struct XCfg {
 };
 
 template <int HD, bool F8>
-__global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
+__global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnArgs a) {
   using C = XCfg<HD, F8>;
   extern __shared__ __align__(128) uint8_t xsm[];
   pdl_trigger();
@@ -451,8 +483,6 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
   const uint8_t* pool = static_cast<const uint8_t*>(a.pool);  // element e at byte e * (F8 ? 1 : 2)
   constexpr int ES = F8 ? 1 : 2;
   const uint32_t ring = smem_u32(xsm) + warp * C::RING;
-  const uint32_t work = ring + C::STAGES * C::STAGE;  // e4m3: the converted block pair
-  uint8_t* work_ptr = xsm + warp * C::RING + C::STAGES * C::STAGE;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     const int g = item / nh, h = item - g * nh;
     const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
@@ -473,6 +503,11 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
       return pi < a.r2p_stride ? LDCG(r2p + pi) : -1;
     };
     int pg = page_ids(0), pg_group = 0;
+    // element offsets: K of (layer, page, head, position) = head_base + page * page_stride
+    // + position * HD; V sits kv_stride further
+    const int64_t page_stride = static_cast<int64_t>(nh) * a.P * HD;
+    const int64_t head_base = (static_cast<int64_t>(a.layer) * 2 * a.num_pages * nh + h) * a.P * HD;
+    const int64_t kv_stride = static_cast<int64_t>(a.num_pages) * page_stride;
     auto issue = [&](int j) {
       if (j < nj) {
         if ((j >> 5) != pg_group) {  // warp-uniform: more than 32 blocks per warp
@@ -485,15 +520,15 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
         const bool ok = page >= 0 && page < a.num_pages;
         if (!ok && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
         const int off = blk - pi * a.P;
-        const int64_t kb = ((((static_cast<int64_t>(a.layer) * 2 + 0) * a.num_pages + (ok ? page : 0)) * nh + h) * a.P + off) * HD;
-        const int64_t vb = kb + static_cast<int64_t>(a.num_pages) * nh * a.P * HD;
+        const int64_t kb = head_base + (ok ? page : 0) * page_stride + off * HD;
+        const int64_t vb = kb + kv_stride;
         const uint32_t st = ring + (j % C::STAGES) * C::STAGE;
         if constexpr (F8) {  // rows of 16-byte chunks as stored; converted after arrival
 #pragma unroll
           for (int i = lane; i < 16 * C::CH8; i += 32) {
             const int r = i / C::CH8, ch = i - r * C::CH8;
             const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
-            const uint32_t dst = st + r * C::ROWB8 + (ch << 4);
+            const uint32_t dst = st + r * C::ROWB8 + ((ch ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4);
             cp_async16(dst, pool + (kb + r * HD) * ES + ch * 16, bytes);
             cp_async16(dst + C::BLK8, pool + (vb + r * HD) * ES + ch * 16, bytes);
           }
@@ -517,14 +552,22 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
     const float qscale = load_queries<HD, F8>(a, b, h, sq);  // 1 unless e4m3 queries
     const float s_scale = a.scale_log2 * qscale;
     __syncthreads();
-    uint32_t qa[HD / 16][4];
+    // A fragments: bf16 (m16n8k16) for a bf16 pool; e4m3 (m16n8k32: a register holds
+    // 4 channels, rows g8 / g8 + 8, channels 4 t4 + 0..3 and + 16) for an e4m3 pool
+    constexpr int KQ = F8 ? HD / 32 : HD / 16;
+    uint32_t qa[KQ][4];
 #pragma unroll
-    for (int kk = 0; kk < HD / 16; ++kk) {
+    for (int kk = 0; kk < KQ; ++kk) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int row = g8 + ((j & 1) << 3);
-        const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
-        qa[kk][j] = pack2<F8>(sq[row * HD + col], sq[row * HD + col + 1]);
+        if constexpr (F8) {
+          const float* q4 = sq + row * HD + kk * 32 + ((j >> 1) << 4) + 4 * t4;
+          qa[kk][j] = pack_e4m3x4(q4[0], q4[1], q4[2], q4[3]);
+        } else {
+          const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
+          qa[kk][j] = pack2<F8>(sq[row * HD + col], sq[row * HD + col + 1]);
+        }
       }
     }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -537,42 +580,46 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
       __syncwarp();
       const int blk = p0 + ((warp + 4 * j) << 4);
       uint32_t kst = ring + (j % C::STAGES) * C::STAGE, vst = kst + C::BLK;
-      if constexpr (F8) {
-        // e4m3 K and V rows -> half (exact) in the swizzled layout: 16-byte chunk c of
-        // a row holds channels 16c..16c+15 and becomes half chunks 2c and 2c+1
-        const uint8_t* st8 = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
-#pragma unroll
-        for (int i = lane; i < 2 * 16 * C::CH8; i += 32) {
-          const int kv = i / (16 * C::CH8), rem = i - kv * 16 * C::CH8;
-          const int r = rem / C::CH8, c = rem - r * C::CH8;
-          uint4 lo, hi;
-          e4m3x16_to_f16(*reinterpret_cast<const uint4*>(st8 + kv * C::BLK8 + r * C::ROWB8 + c * 16), lo, hi);
-          uint8_t* row = work_ptr + kv * C::BLK + r * C::ROWB;
-          *reinterpret_cast<uint4*>(row + (((2 * c) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
-        }
-        __syncwarp();
-        kst = work;
-        vst = work + C::BLK;
-      }
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if constexpr (F8) {
+        // S = Q K^T on the e4m3 keys as stored: per 32 channels one ldmatrix.x4 of the
+        // two 8-position halves x two 16-channel chunks gives both B fragments (a b16
+        // matrix row of 16 bytes = 16 e4m3 channels; a thread's word = 4 channels)
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) {
-        const int r = (lane & 7) + ((lane >> 4) << 3);
-        const int ch = kk * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-        mma16816<F8>(s[0], qa[kk], b0, b1);
-        mma16816<F8>(s[1], qa[kk], b2, b3);
-      }
-      // scale to base 2 and mask positions past the chunk
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
-          s[nt][e] = pos < p1 ? s[nt][e] * s_scale : -INFINITY;
+        for (int kk = 0; kk < HD / 32; ++kk) {
+          const int r = (lane & 7) + ((lane >> 4) << 3);
+          const int ch = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + r * C::ROWB8 + ((ch ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4), b0, b1, b2, b3);
+          mma_e4m3_16832(s[0], qa[kk], b0, b1);
+          mma_e4m3_16832(s[1], qa[kk], b2, b3);
         }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const int r = (lane & 7) + ((lane >> 4) << 3);
+          const int ch = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+          mma16816<F8>(s[0], qa[kk], b0, b1);
+          mma16816<F8>(s[1], qa[kk], b2, b3);
+        }
+      }
+      // scale to base 2 and mask positions past the chunk (the last block only)
+      if (blk + 16 <= p1) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[nt][e] *= s_scale;
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
+            s[nt][e] = pos < p1 ? s[nt][e] * s_scale : -INFINITY;
+          }
+      }
       float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
       float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -580,29 +627,62 @@ __global__ void __launch_bounds__(128, 2) xattn_items_mma_kernel(XattnArgs a) {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-      const float c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      // a finite running max only grows; c = 1 exactly while it stays
+      const float c0 = n0 == -INFINITY ? 1.f : ex2f(m0 - n0);
+      const float c1 = n1 == -INFINITY ? 1.f : ex2f(m1 - n1);
+      const float z0 = n0 == -INFINITY ? 0.f : n0, z1 = n1 == -INFINITY ? 0.f : n1;  // -inf rows: p = 0
       float p[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = n0 == -INFINITY ? 0.f : exp2f(s[nt][0] - n0);
-        p[nt][1] = n0 == -INFINITY ? 0.f : exp2f(s[nt][1] - n0);
-        p[nt][2] = n1 == -INFINITY ? 0.f : exp2f(s[nt][2] - n1);
-        p[nt][3] = n1 == -INFINITY ? 0.f : exp2f(s[nt][3] - n1);
+        p[nt][0] = ex2f(s[nt][0] - z0);
+        p[nt][1] = ex2f(s[nt][1] - z0);
+        p[nt][2] = ex2f(s[nt][2] - z1);
+        p[nt][3] = ex2f(s[nt][3] - z1);
       }
       l0 = l0 * c0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
       l1 = l1 * c1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
       m0 = n0;
       m1 = n1;
+      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
 #pragma unroll
-      for (int i = 0; i < HD / 8; ++i) {
-        o[i][0] *= c0;
-        o[i][1] *= c0;
-        o[i][2] *= c1;
-        o[i][3] *= c1;
+        for (int i = 0; i < HD / 8; ++i) {
+          o[i][0] *= c0;
+          o[i][1] *= c0;
+          o[i][2] *= c1;
+          o[i][3] *= c1;
+        }
       }
       const uint32_t pa[4] = {pack2<F8>(p[0][0], p[0][1]), pack2<F8>(p[0][2], p[0][3]), pack2<F8>(p[1][0], p[1][1]),
                               pack2<F8>(p[1][2], p[1][3])};
+      if constexpr (F8) {
+        // the keys are read: the e4m3 V rows -> half (exact) over the whole stage, in the
+        // half layout (16-byte chunk c of a row holds channels 16c..16c+15 and becomes
+        // half chunks 2c and 2c+1); every lane holds its chunks before any is written
+        const uint8_t* st8 = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
+        constexpr int NV = 16 * C::CH8 / 32;  // chunks per lane
+        uint4 raw[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          const int i = lane + 32 * u, r = i / C::CH8, c = i - r * C::CH8;
+          raw[u] = *reinterpret_cast<const uint4*>(st8 + C::BLK8 + r * C::ROWB8 +
+                                                   ((c ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
+        }
+        __syncwarp();
+        uint8_t* vh = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          const int i = lane + 32 * u, r = i / C::CH8, c = i - r * C::CH8;
+          uint4 lo, hi;
+          e4m3x4_to_f16x4(raw[u].x, lo.x, lo.y);
+          e4m3x4_to_f16x4(raw[u].y, lo.z, lo.w);
+          e4m3x4_to_f16x4(raw[u].z, hi.x, hi.y);
+          e4m3x4_to_f16x4(raw[u].w, hi.z, hi.w);
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * c) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        __syncwarp();
+        vst = kst;
+      }
 #pragma unroll
       for (int dn = 0; dn < HD / 16; ++dn) {
         const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
@@ -1122,7 +1202,8 @@ cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args, const
     FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false>, dim3(grid), dim3(128),
                                        XCfg<HD, false>::SMEM, a)));
   } else if (dtype == FLASHMAP_E4M3) {
-    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true>, dim3(grid), dim3(128),
+    // three CTAs per SM: the e4m3 kernel is latency-bound per block, not byte-bound
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true>, dim3(L.num_sms * 3), dim3(128),
                                        XCfg<HD, true>::SMEM, a)));
   } else {
     FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_simt_kernel<float, HD>, dim3(grid), dim3(128), 0, a)));
