@@ -132,7 +132,10 @@ def algorithmic_bytes(cfg: dict, req: dict) -> dict:
                    + (n - 1) * V * D * es)
         kv_read *= n
     rows_written = (sum(req["commit"]) if req["window"] else 0) + bs
-    logits = bs * K * Vd * 4
+    # a tree draft: the logits of every candidate block; the context is read once per
+    # request (the candidates share it), the algorithmic minimum
+    nc = req["tree"][0] if req.get("tree") else 1
+    logits = bs * nc * K * Vd * 4
     x_in = (bs * (K + 1) * Lt * H * es) if req["window"] else 0
     full = bs * K * V * 4 if req["full_scatter"] else 0
     total = w_write + w_draft + w_head + kv_read + rows_written * kv_row + logits + x_in + full
@@ -154,8 +157,10 @@ def setup_ours(workload: str, device: str):
     code = F.DTYPE_CODES[cfg["kv_dtype"]]
     pool_t = torch.empty(F.flashmap_pool_bytes(cfg, req["num_pages"]), dtype=torch.uint8, device=device)
     pool = F.make_pool(pool_t, req["num_pages"], code)
+    nc = req["tree"][0] if req["tree"] else 1  # drafted blocks per request
     max_rows = max(max(req["ctx"]) if req["prefill"] else 0, bs * (K + 1))
-    ws = torch.empty(F.flashmap_workspace_size(model, bs, min(max_rows, 4096)), dtype=torch.uint8, device=device)
+    ws = torch.empty(F.flashmap_workspace_size(model, bs * nc, min(max_rows, 4096)), dtype=torch.uint8,
+                     device=device)
     i32 = dict(dtype=torch.int32, device=device)
     if req["prefill"]:
         for b in range(bs):
@@ -170,14 +175,54 @@ def setup_ours(workload: str, device: str):
         F=F, cfg=cfg, model=model, E=E, req=req, pool_t=pool_t, pool=pool, ws=ws,
         start=torch.tensor(req["ctx"], **i32), commit=torch.tensor(req["commit"], **i32),
         anchor_pos=torch.tensor(req["anchor_pos"], **i32),
-        hidden=torch.empty((bs * K, cfg["hidden"]), dtype=dt, device=device),
-        tokens=torch.empty(bs * K, dtype=torch.int64, device=device),
-        logits=torch.empty((bs * K, Vd), dtype=torch.float32, device=device),
+        hidden=torch.empty((bs * nc * K, cfg["hidden"]), dtype=dt, device=device),
+        tokens=torch.empty(bs * nc * K, dtype=torch.int64, device=device),
+        logits=torch.empty((bs * nc * K, Vd), dtype=torch.float32, device=device),
         full=(torch.empty((bs * K, cfg["vocab_size"]), dtype=torch.float32, device=device)
               if req["full_scatter"] else None),
         window_loc=torch.empty(bs * (K + 1), dtype=torch.int64, device=device),
     )
+    if req["tree"]:
+        # every candidate block samples with its request's position, temperature and seed
+        n, width = req["tree"]
+        st["tree_in"] = {k: v.repeat_interleave(n) for k, v in (
+            ("anchor_pos", st["anchor_pos"]), ("temperature", req["temperature"]), ("greedy", req["greedy"]),
+            ("seeds", req["seeds"]))}
+        st["tree_out"] = [torch.empty((bs, width - 1), dtype=torch.int64, device=device) for _ in range(2)] + \
+            [torch.empty((bs, 2), dtype=torch.int64, device=device)]
     return st
+
+
+def blocks_per_step(st: dict) -> int:
+    """Drafted blocks of one step: one per request, or one per candidate of a tree draft."""
+    return st["req"]["bs"] * (st["req"]["tree"][0] if st["req"]["tree"] else 1)
+
+
+def draft_call(st: dict, stream=None) -> None:
+    F, req = st["F"], st["req"]
+    if req["tree"]:
+        F.flashmap_draft_candidates(st["model"], st["pool"], req["bs"], req["tree"][0], req["anchor_ids"],
+                                    st["anchor_pos"], req["req_pool_idx"], req["req_to_page"], req["seeds"], 1.0,
+                                    st["hidden"], None, st["ws"], stream)
+    else:
+        F.flashmap_draft_block(st["model"], st["pool"], req["bs"], req["anchor_ids"], st["anchor_pos"],
+                               req["req_pool_idx"], req["req_to_page"], req["seeds"], 1.0, st["hidden"], None,
+                               st["ws"], stream)
+
+
+def sample_call(st: dict, stream=None) -> None:
+    F, req = st["F"], st["req"]
+    if req["tree"]:
+        t = st["tree_in"]
+        F.flashmap_sample_block(st["model"], blocks_per_step(st), st["hidden"], t["anchor_pos"], t["temperature"],
+                                t["greedy"], t["seeds"], req["step"], st["tokens"], st["logits"], st["full"],
+                                st["ws"], stream)
+        n, width = req["tree"]
+        F.flashmap_build_tree(st["tokens"].view(req["bs"], n, -1), width, *st["tree_out"], stream)
+    else:
+        F.flashmap_sample_block(st["model"], req["bs"], st["hidden"], st["anchor_pos"], req["temperature"],
+                                req["greedy"], req["seeds"], req["step"], st["tokens"], st["logits"], st["full"],
+                                st["ws"], stream)
 
 
 def run_step(st: dict, stream=None) -> None:
@@ -186,10 +231,8 @@ def run_step(st: dict, stream=None) -> None:
     if req["window"]:
         F.flashmap_write_context_kv(st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"],
                                     st["start"], st["commit"], req["req_to_page"], st["window_loc"], st["ws"], stream)
-    F.flashmap_draft_block(st["model"], st["pool"], bs, req["anchor_ids"], st["anchor_pos"], req["req_pool_idx"],
-                           req["req_to_page"], req["seeds"], 1.0, st["hidden"], None, st["ws"], stream)
-    F.flashmap_sample_block(st["model"], bs, st["hidden"], st["anchor_pos"], req["temperature"], req["greedy"],
-                            req["seeds"], req["step"], st["tokens"], st["logits"], st["full"], st["ws"], stream)
+    draft_call(st, stream)
+    sample_call(st, stream)
 
 
 def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: int = 3) -> dict:
@@ -261,12 +304,8 @@ def phase_times(st: dict, stream: torch.cuda.Stream, n: int = 60) -> dict:
         calls["write"] = lambda: F.flashmap_write_context_kv(
             st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"], st["start"],
             st["commit"], req["req_to_page"], st["window_loc"], st["ws"])
-    calls["draft"] = lambda: F.flashmap_draft_block(
-        st["model"], st["pool"], bs, req["anchor_ids"], st["anchor_pos"], req["req_pool_idx"], req["req_to_page"],
-        req["seeds"], 1.0, st["hidden"], None, st["ws"])
-    calls["sample"] = lambda: F.flashmap_sample_block(
-        st["model"], bs, st["hidden"], st["anchor_pos"], req["temperature"], req["greedy"], req["seeds"],
-        req["step"], st["tokens"], st["logits"], st["full"], st["ws"])
+    calls["draft"] = lambda: draft_call(st)
+    calls["sample"] = lambda: sample_call(st)  # a tree draft's sample phase includes the tree
     out = {}
     for name, fn in calls.items():
         g = torch.cuda.CUDAGraph()
@@ -345,8 +384,8 @@ def our_arm(args, rank: int, world: int) -> dict:
         torch.distributed.barrier()
     ms = world_max(t_ev0.elapsed_time(t_ev1) / args.steps, world, device)
     clocks = sampler.stop(t0, t1)
-    tokens_per_step = bs * K * world
-    value = job_throughput(bs * K, world, ms)
+    tokens_per_step = blocks_per_step(st) * K * world
+    value = job_throughput(blocks_per_step(st) * K, world, ms)
 
     # end to end through the public API with host buffers: pinned inputs copied in,
     # the step, the sampled token ids copied out, every step
@@ -357,9 +396,15 @@ def our_arm(args, rank: int, world: int) -> dict:
     if req["window"]:
         host_in["window_hidden"] = req["window_hidden"].cpu().pin_memory()
         dev_in["window_hidden"] = req["window_hidden"]
-    tok_host = torch.empty(st["tokens"].shape, dtype=torch.int64).pin_memory()
+    result = [st["tokens"]]
+    if req["tree"]:  # candidates sample with per-block copies of the request inputs; the tree comes back
+        for k, t in st["tree_in"].items():
+            host_in["tree_" + k] = t.cpu().pin_memory()
+            dev_in["tree_" + k] = t
+        result = st["tree_out"][:2]
+    tok_host = [torch.empty(t.shape, dtype=torch.int64).pin_memory() for t in result]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = tok_host.numel() * tok_host.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in tok_host)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
@@ -367,7 +412,8 @@ def our_arm(args, rank: int, world: int) -> dict:
             for k, t in host_in.items():
                 dev_in[k].copy_(t, non_blocking=True)
             graph.replay()
-            tok_host.copy_(st["tokens"], non_blocking=True)
+            for h, t in zip(tok_host, result):
+                h.copy_(t, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = world_max(e0.elapsed_time(e1) / args.steps, world, device)
@@ -386,6 +432,7 @@ def our_arm(args, rank: int, world: int) -> dict:
                    "context": {"min": min(req["ctx"]), "max": max(req["ctx"]),
                                "mean": float(np.mean(req["ctx"]))},
                    "window_write": bool(req["window"]), "full_vocab_scatter": bool(req["full_scatter"]),
+                   "tree": ({"candidates": req["tree"][0], "width": req["tree"][1]} if req["tree"] else None),
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
                    "l2": "inputs larger than L2 (weights alone ~3 GB per step)", "cuda_graph": True},
         "e2e": {"value": round(tokens_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -428,14 +475,17 @@ def oracle_setup(workload: str, device: str, gen_model=None):
         W, E, LM, rank = gen_model
     Wnp = {k: v.double().cpu().numpy() for k, v in W.items()}
     Enp = E.float().cpu().numpy()
+    LMnp = LM.float().cpu().numpy()
     ocfg = ref.Config.from_dict(cfg)
-    C = ref.load_constants(ocfg, Wnp, Enp, LM.float().cpu().numpy(), rank.cpu().numpy(), skip_gram=True)
+    C = ref.load_constants(ocfg, Wnp, Enp, LMnp, rank.cpu().numpy(), skip_gram=True)
+    C.extra["LM"] = LMnp  # the full-vocabulary head of a several-jump draft
     return ocfg, Wnp, Enp, C
 
 
 def oracle_step(ref, ocfg, Wnp, Enp, C, req, b: int, ctx_kv, window_hidden) -> None:
-    """One request's whole step on the CPU oracle: window write, anchor row, draft,
-    folded head, sampling."""
+    """One request's whole step on the CPU oracle: window write, anchor row, draft
+    (every jump of a several-jump draft; every candidate block and the verify tree of a
+    tree draft), folded head, sampling."""
     K = ocfg.block_size
     kc, vc = ctx_kv
     if req["window"]:
@@ -446,10 +496,18 @@ def oracle_step(ref, ocfg, Wnp, Enp, C, req, b: int, ctx_kv, window_hidden) -> N
     ka, va = ref.anchor_kv(ocfg, Wnp, Enp, [int(req["anchor_ids"][b])], [p])
     kc, vc = np.concatenate([kc, ka], 1), np.concatenate([vc, va], 1)
     seed = int(req["seeds"][b])
-    hid = ref.draft_requests(ocfg, Wnp, C, [(kc, vc)], [p], [seed])[0]
-    lg = ref.head_logits(C, hid)
-    ref.sample_rows(lg, [float(req["temperature"][b])] * K, [int(req["greedy"][b])] * K, [seed] * K,
-                    p + 1 + np.arange(K), req["step"], C.hot)
+    n = req["tree"][0] if req.get("tree") else 1
+    if ocfg.num_steps > 1:
+        hids = ref.draft_requests_multi(ocfg, Wnp, C, Enp, C.extra["LM"], [(kc, vc)], [p], [seed], ocfg.num_steps)
+    else:
+        hids = ref.draft_requests(ocfg, Wnp, C, [(kc, vc)] * n, [p] * n, [seed] * n, 1.0, list(range(n)))
+    toks = []
+    for hid in hids:
+        lg = ref.head_logits(C, hid)
+        toks.append(ref.sample_rows(lg, [float(req["temperature"][b])] * K, [int(req["greedy"][b])] * K,
+                                    [seed] * K, p + 1 + np.arange(K), req["step"], C.hot)[0])
+    if req.get("tree"):
+        ref.build_tree(np.stack(toks), req["tree"][1])
 
 
 def time_oracle(workload: str, device: str, n_steps: int, budget_s: float = 90.0, warmup: int = 1,
@@ -490,8 +548,14 @@ def cores_used() -> int:
         return os.cpu_count() or 1
 
 
+def tokens_per_request(workload: str) -> int:
+    """Drafted tokens of one request-step: block_size, times the candidates of a tree draft."""
+    tree = syn.WORKLOADS[workload].get("tree")
+    return syn.model_config(workload)["block_size"] * (tree[0] if tree else 1)
+
+
 def cpu_baseline(workload: str, budget_s: float = 30.0) -> dict:
-    K = syn.model_config(workload)["block_size"]
+    K = tokens_per_request(workload)
     sec, n = time_oracle(workload, "cuda", 3, budget_s=budget_s)
     return {"value": round(K / sec, 3), "unit": UNIT, "cores": cores_used(), "kind": "oracle",
             "sample": f"{n} request-steps of {workload} (window write + anchor + draft + head + sampling of one "
@@ -500,7 +564,7 @@ def cpu_baseline(workload: str, budget_s: float = 30.0) -> dict:
 
 
 def reference_arm(args) -> dict:
-    K = syn.model_config(args.workload)["block_size"]
+    K = tokens_per_request(args.workload)
     sec, n = time_oracle(args.workload, "cuda" if torch.cuda.is_available() else "cpu", max(1, args.steps),
                          budget_s=90.0, warmup=min(args.warmup, 1))
     value = K / sec

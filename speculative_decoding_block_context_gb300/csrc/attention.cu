@@ -439,67 +439,102 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     mma_bf16_16816(d, a, b0, b1);
 }
 
-constexpr int kXStages = 3;   // bf16 pool: cp.async stages per warp
+constexpr int kXStages = 3;   // bf16 pool, one candidate: cp.async stages per warp
 constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage; 3 CTAs per SM)
 
-// Per warp: a ring of K/V blocks as they arrive (16-byte chunks XOR-swizzled by row).
-// For an e4m3 pool the keys feed the e4m3 tensor-core product as stored; once they are
-// read, the block's values are widened to half over the same stage (the 2 x 16 x HD
-// e4m3 bytes of K and V hold exactly one 16 x HD half block) for the half product
-// with the probabilities.
-template <int HD, bool F8 = false>
+__device__ __forceinline__ void bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// A CTA's 4 warps serve NC blocks that share one context: NC = 1 for a draft (one
+// block per request), 2 or 4 for the candidate blocks of a tree draft. The warps of a
+// candidate (WPC = 4 / NC of them) split the chunk's 16-position blocks by block lane
+// (warp % WPC); the NC warps of one block lane share a ring of K/V blocks, each issuing
+// part of every block's copies, so the context is read once for the NC candidates.
+// Ring layout: 16-byte chunks XOR-swizzled by row. For an e4m3 pool the keys feed the
+// e4m3 tensor-core product as stored; the values are widened to half for the half
+// product with the probabilities: over the same stage once the keys are read (NC = 1:
+// the 2 x 16 x HD e4m3 bytes of K and V hold exactly one 16 x HD half block), or into
+// a half buffer beside the ring (NC > 1, shared by the ring's warps).
+template <int HD, bool F8 = false, int NC = 1>
 struct XCfg {
+  static constexpr int WPC = 4 / NC;      // warps per candidate = rings per CTA
   static constexpr int ROWB = HD * 2;     // bytes of one bf16 position row
   static constexpr int BLK = 16 * ROWB;   // one 16-position block of K (or V), bf16
   static constexpr int CH = HD / 8;       // 16-byte chunks per bf16 row
   static constexpr int ROWB8 = HD;        // bytes of one e4m3 row
   static constexpr int BLK8 = 16 * ROWB8;
   static constexpr int CH8 = HD / 16;     // 16-byte chunks per e4m3 row
-  static constexpr int STAGES = F8 ? kXStages8 : kXStages;
+  static constexpr int STAGES = NC == 1 ? (F8 ? kXStages8 : kXStages) : NC == 4 ? 8 : (F8 ? 6 : 4);
   static constexpr int STAGE = F8 ? 2 * BLK8 : 2 * BLK;
-  static constexpr int WORK = 0;
+  static constexpr int WORK = (F8 && NC > 1) ? BLK : 0;  // the shared half V block
   // e4m3 rows are HD bytes: chunk c of row r sits at c ^ ((r >> SW8) & (CH8 - 1)), so the
   // 8 rows an ldmatrix reads fall on distinct banks (128-byte rows: r & 7; 64-byte: r/2 & 3)
   static constexpr int SW8 = CH8 >= 8 ? 0 : (CH8 == 4 ? 1 : 2);
-  static constexpr int RING = STAGES * STAGE + WORK;  // per warp
-  static constexpr int SMEM_RING = 4 * RING;
-  static constexpr int SQ_OFF = SMEM_RING;          // the item's queries, beside the rings
-  static constexpr int SMEM_Q = SQ_OFF + 16 * HD * 4;
+  static constexpr int RING = STAGES * STAGE + WORK;
+  static constexpr int SMEM_RING = WPC * RING;
+  static constexpr int SQ_OFF = SMEM_RING;          // the candidates' queries, beside the rings
+  static constexpr int SMEM_Q = SQ_OFF + NC * 16 * HD * 4;
   static constexpr int SMEM_MERGE = 4 * 16 * (HD + 2) * 4;
   static constexpr int SMEM = SMEM_Q > SMEM_MERGE ? SMEM_Q : SMEM_MERGE;
 };
 
-template <int HD, bool F8>
+template <int HD, bool F8, int NC>
 __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnArgs a) {
-  using C = XCfg<HD, F8>;
+  using C = XCfg<HD, F8, NC>;
+  constexpr int WPC = C::WPC;
   extern __shared__ __align__(128) uint8_t xsm[];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g8 = lane >> 2, t4 = lane & 3;
+  const int cw = warp / WPC, lw = warp - cw * WPC;  // this warp's candidate and block lane
   const int nh = a.nh;
-  const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
+  const int chunk_len = LDCG(a.plan + 1), chunks = LDCG(a.plan + 2);
+  const int* first = a.plan + 3;
   const int* pairs = a.plan + 4 + a.bs;
   const uint8_t* pool = static_cast<const uint8_t*>(a.pool);  // element e at byte e * (F8 ? 1 : 2)
   constexpr int ES = F8 ? 1 : 2;
-  const uint32_t ring = smem_u32(xsm) + warp * C::RING;
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
-    const int g = item / nh, h = item - g * nh;
-    const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
+  const uint32_t ring = smem_u32(xsm) + lw * C::RING;
+  // candidate groups of NC blocks of one request (NC > 1): a.n_cand blocks per request
+  const int ncand = NC > 1 ? a.n_cand : 1, groups = ncand / NC, nreq = a.bs / ncand;
+  const int total = NC > 1 ? (chunks / ncand) * nh * groups : LDCG(a.plan);
+  for (int v = blockIdx.x; v < total; v += gridDim.x) {
+    int h, b, c, gk[NC];  // head, this warp's block, chunk; every candidate's pair index
+    if constexpr (NC == 1) {
+      const int g = v / nh;
+      h = v - g * nh;
+      b = LDCG(pairs + 2 * g);
+      c = LDCG(pairs + 2 * g + 1);
+      gk[0] = g;
+    } else {
+      const int grp = v % groups, t = v / groups;
+      h = t % nh;
+      const int q = t / nh;  // the request chunk: request r's chunks are q in [F(r), F(r + 1))
+      int lo = 0, hi = nreq - 1;  // F(r) = first[r * ncand] / ncand, the largest r with F(r) <= q
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (LDCG(first + mid * ncand) / ncand <= q) lo = mid; else hi = mid - 1;
+      }
+      c = q - LDCG(first + lo * ncand) / ncand;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) gk[k] = LDCG(first + lo * ncand + grp * NC + k) + c;
+      b = lo * ncand + grp * NC + cw;
+    }
     const int n = LDCG(a.anchor_pos + b) + 1;
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
     const int nblk = (p1 - p0 + 15) >> 4;
     const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
     // The first blocks of keys and values are requested before the queries are
     // prepared (the two do not depend on each other).
-    const int nj = warp < nblk ? (nblk - warp + 3) >> 2 : 0;
-    // The page ids of this warp's blocks, 32 blocks at a time, one per lane: loaded
+    const int nj = lw < nblk ? (nblk - lw + WPC - 1) / WPC : 0;
+    // The page ids of this lane's blocks, 32 blocks at a time, one per lane: loaded
     // ahead so that no page-table load sits between a block's issue and the next.
     const int32_t* r2p = a.req_to_page + static_cast<int64_t>(rrow) * a.r2p_stride;
     auto page_ids = [&](int j0) {
       const int j = j0 + lane;
       if (j >= nj) return -1;
-      const int pi = (p0 + ((warp + 4 * j) << 4)) / a.P;
+      const int pi = (p0 + ((lw + WPC * j) << 4)) / a.P;
       return pi < a.r2p_stride ? LDCG(r2p + pi) : -1;
     };
     int pg = page_ids(0), pg_group = 0;
@@ -508,24 +543,26 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
     const int64_t page_stride = static_cast<int64_t>(nh) * a.P * HD;
     const int64_t head_base = (static_cast<int64_t>(a.layer) * 2 * a.num_pages * nh + h) * a.P * HD;
     const int64_t kv_stride = static_cast<int64_t>(a.num_pages) * page_stride;
+    // the ring's NC warps split a block's 16-byte chunks: this warp's first chunk and stride
+    const int ci0 = (NC > 1 ? cw * 32 : 0) + lane;
     auto issue = [&](int j) {
       if (j < nj) {
-        if ((j >> 5) != pg_group) {  // warp-uniform: more than 32 blocks per warp
+        if ((j >> 5) != pg_group) {  // warp-uniform: more than 32 blocks per lane
           pg_group = j >> 5;
           pg = page_ids(j & ~31);
         }
-        const int blk = p0 + ((warp + 4 * j) << 4);
+        const int blk = p0 + ((lw + WPC * j) << 4);
         const int pi = blk / a.P;
         const int page = __shfl_sync(0xffffffffu, pg, j & 31);
         const bool ok = page >= 0 && page < a.num_pages;
-        if (!ok && lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
+        if (!ok && lane == 0 && cw == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
         const int off = blk - pi * a.P;
         const int64_t kb = head_base + (ok ? page : 0) * page_stride + off * HD;
         const int64_t vb = kb + kv_stride;
         const uint32_t st = ring + (j % C::STAGES) * C::STAGE;
-        if constexpr (F8) {  // rows of 16-byte chunks as stored; converted after arrival
+        if constexpr (F8) {  // rows of 16-byte chunks, swizzled
 #pragma unroll
-          for (int i = lane; i < 16 * C::CH8; i += 32) {
+          for (int i = ci0; i < 16 * C::CH8; i += 32 * NC) {
             const int r = i / C::CH8, ch = i - r * C::CH8;
             const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
             const uint32_t dst = st + r * C::ROWB8 + ((ch ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4);
@@ -534,7 +571,7 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           }
         } else {
 #pragma unroll
-          for (int i = lane; i < 16 * C::CH; i += 32) {
+          for (int i = ci0; i < 16 * C::CH; i += 32 * NC) {
             const int r = i / C::CH, ch = i - r * C::CH;
             const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
             const uint32_t dst = st + r * C::ROWB + ((ch ^ (r & 7)) << 4);
@@ -547,11 +584,21 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
     };
 #pragma unroll
     for (int j = 0; j < C::STAGES - 1; ++j) issue(j);
-    // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
+    // every candidate's Q (normed, rotated; e4m3-rounded for an e4m3 pool), rows >= K zero
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
-    const float qscale = load_queries<HD, F8>(a, b, h, sq);  // 1 unless e4m3 queries
+    float qscale = 1.f;
+    if constexpr (NC == 1) {
+      qscale = load_queries<HD, F8>(a, b, h, sq);  // 1 unless e4m3 queries
+    } else {
+#pragma unroll 1
+      for (int k = 0; k < NC; ++k) {
+        const float s = load_queries<HD, F8>(a, b - cw + k, h, sq + k * 16 * HD);
+        if (k == cw) qscale = s;
+      }
+    }
     const float s_scale = a.scale_log2 * qscale;
     __syncthreads();
+    const float* sqw = sq + cw * 16 * HD;
     // A fragments: bf16 (m16n8k16) for a bf16 pool; e4m3 (m16n8k32: a register holds
     // 4 channels, rows g8 / g8 + 8, channels 4 t4 + 0..3 and + 16) for an e4m3 pool
     constexpr int KQ = F8 ? HD / 32 : HD / 16;
@@ -562,11 +609,11 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
       for (int j = 0; j < 4; ++j) {
         const int row = g8 + ((j & 1) << 3);
         if constexpr (F8) {
-          const float* q4 = sq + row * HD + kk * 32 + ((j >> 1) << 4) + 4 * t4;
+          const float* q4 = sqw + row * HD + kk * 32 + ((j >> 1) << 4) + 4 * t4;
           qa[kk][j] = pack_e4m3x4(q4[0], q4[1], q4[2], q4[3]);
         } else {
           const int col = kk * 16 + ((j >> 1) << 3) + 2 * t4;
-          qa[kk][j] = pack2<F8>(sq[row * HD + col], sq[row * HD + col + 1]);
+          qa[kk][j] = pack2<F8>(sqw[row * HD + col], sqw[row * HD + col + 1]);
         }
       }
     }
@@ -575,11 +622,20 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     for (int j = 0; j < nj; ++j) {
-      issue(j + C::STAGES - 1);
-      cp_async_wait<C::STAGES - 1>();
-      __syncwarp();
-      const int blk = p0 + ((warp + 4 * j) << 4);
-      uint32_t kst = ring + (j % C::STAGES) * C::STAGE, vst = kst + C::BLK;
+      if constexpr (NC == 1) {
+        issue(j + C::STAGES - 1);
+        cp_async_wait<C::STAGES - 1>();
+        __syncwarp();
+      } else {
+        // block j landed (every warp waited for its part; the barrier joins them), and
+        // every warp of the ring is done with block j - 1, whose stage is refilled next
+        cp_async_wait<C::STAGES - 2>();
+        bar_sync(1 + lw, 32 * NC);
+        issue(j + C::STAGES - 1);
+      }
+      const int blk = p0 + ((lw + WPC * j) << 4);
+      const uint32_t kst = ring + (j % C::STAGES) * C::STAGE;
+      uint32_t vst = kst + C::BLK;
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       if constexpr (F8) {
         // S = Q K^T on the e4m3 keys as stored: per 32 channels one ldmatrix.x4 of the
@@ -604,6 +660,26 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           mma16816<F8>(s[0], qa[kk], b0, b1);
           mma16816<F8>(s[1], qa[kk], b2, b3);
         }
+      }
+      if constexpr (F8 && NC > 1) {
+        // the ring's warps widen the block's e4m3 V rows into the shared half block
+        const uint8_t* v8 = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE + C::BLK8;
+        uint8_t* vh = xsm + lw * C::RING + C::STAGES * C::STAGE;
+#pragma unroll
+        for (int i = ci0; i < 16 * C::CH8; i += 32 * NC) {
+          const int r = i / C::CH8, cc = i - r * C::CH8;
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(v8 + r * C::ROWB8 + ((cc ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
+          uint4 lo, hi;
+          e4m3x4_to_f16x4(raw.x, lo.x, lo.y);
+          e4m3x4_to_f16x4(raw.y, lo.z, lo.w);
+          e4m3x4_to_f16x4(raw.z, hi.x, hi.y);
+          e4m3x4_to_f16x4(raw.w, hi.z, hi.w);
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        bar_sync(1 + lw, 32 * NC);
+        vst = ring + C::STAGES * C::STAGE;
       }
       // scale to base 2 and mask positions past the chunk (the last block only)
       if (blk + 16 <= p1) {
@@ -654,31 +730,31 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
       }
       const uint32_t pa[4] = {pack2<F8>(p[0][0], p[0][1]), pack2<F8>(p[0][2], p[0][3]), pack2<F8>(p[1][0], p[1][1]),
                               pack2<F8>(p[1][2], p[1][3])};
-      if constexpr (F8) {
+      if constexpr (F8 && NC == 1) {
         // the keys are read: the e4m3 V rows -> half (exact) over the whole stage, in the
         // half layout (16-byte chunk c of a row holds channels 16c..16c+15 and becomes
         // half chunks 2c and 2c+1); every lane holds its chunks before any is written
-        const uint8_t* st8 = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
+        const uint8_t* st8 = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE;
         constexpr int NV = 16 * C::CH8 / 32;  // chunks per lane
         uint4 raw[NV];
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
-          const int i = lane + 32 * u, r = i / C::CH8, c = i - r * C::CH8;
+          const int i = lane + 32 * u, r = i / C::CH8, cc = i - r * C::CH8;
           raw[u] = *reinterpret_cast<const uint4*>(st8 + C::BLK8 + r * C::ROWB8 +
-                                                   ((c ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
+                                                   ((cc ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
         }
         __syncwarp();
-        uint8_t* vh = xsm + warp * C::RING + (j % C::STAGES) * C::STAGE;
+        uint8_t* vh = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE;
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
-          const int i = lane + 32 * u, r = i / C::CH8, c = i - r * C::CH8;
+          const int i = lane + 32 * u, r = i / C::CH8, cc = i - r * C::CH8;
           uint4 lo, hi;
           e4m3x4_to_f16x4(raw[u].x, lo.x, lo.y);
           e4m3x4_to_f16x4(raw[u].y, lo.z, lo.w);
           e4m3x4_to_f16x4(raw[u].z, hi.x, hi.y);
           e4m3x4_to_f16x4(raw[u].w, hi.z, hi.w);
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * c) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * c + 1) ^ (r & 7)) << 4)) = hi;
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc) ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc + 1) ^ (r & 7)) << 4)) = hi;
         }
         __syncwarp();
         vst = kst;
@@ -720,24 +796,27 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
       r1[1] = o[i][3];
     }
     __syncthreads();
-    const int64_t pidx = static_cast<int64_t>(g) * nh + h;
-    {
+    // each candidate's partial: its WPC warps merged
+#pragma unroll 1
+    for (int k = 0; k < NC; ++k) {
+      const int64_t pidx = static_cast<int64_t>(gk[k]) * nh + h;
+      const int w0 = k * WPC;
       const int q = threadIdx.x >> 3, d0 = (threadIdx.x & 7) * (HD / 8);
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) M = fmaxf(M, mm[w * 16 + q]);
-      float wgt[4], L = 0.f;
+      for (int w = 0; w < WPC; ++w) M = fmaxf(M, mm[(w0 + w) * 16 + q]);
+      float wgt[WPC], L = 0.f;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = mm[w * 16 + q];
+      for (int w = 0; w < WPC; ++w) {
+        const float mw = mm[(w0 + w) * 16 + q];
         wgt[w] = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
-        L = fmaf(wgt[w], ll[w * 16 + q], L);
+        L = fmaf(wgt[w], ll[(w0 + w) * 16 + q], L);
       }
       float* po = a.part_o + pidx * 16 * HD + q * HD;
       for (int d = d0; d < d0 + HD / 8; ++d) {
         float acc = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) acc = fmaf(wgt[w], oo[(w * 16 + q) * HD + d], acc);
+        for (int w = 0; w < WPC; ++w) acc = fmaf(wgt[w], oo[((w0 + w) * 16 + q) * HD + d], acc);
         po[d] = acc;
       }
       if ((threadIdx.x & 7) == 0) {
@@ -1178,11 +1257,16 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
 }
 
 int xattn_target_items(int num_sms) { return num_sms * 8; }
-int xattn_max_chunks(int num_sms, int nh, int bs) { return xattn_target_items(num_sms) / nh + bs + 1; }
+// Room for the plan of a tree draft too, whose target is scaled by the candidates a CTA
+// serves at once (at most 4)
+int xattn_max_chunks(int num_sms, int nh, int bs) { return 4 * xattn_target_items(num_sms) / nh + bs + 1; }
+int xattn_cands_per_cta(int n_cand) { return n_cand % 4 == 0 ? 4 : n_cand % 2 == 0 ? 2 : 1; }
 size_t xattn_plan_ints(int num_sms, int nh, int bs) { return 4 + bs + 2 * static_cast<size_t>(xattn_max_chunks(num_sms, nh, bs)); }
 
-cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan) {
-  return launch_k(L, xattn_plan_kernel, dim3(1), dim3(1024), 0, anchor_pos, bs, nh, xattn_target_items(L.num_sms),
+cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan, int n_cand) {
+  // a CTA serving NC candidates runs 1/NC of the items: NC times as many keep the SMs busy
+  const int target = xattn_target_items(L.num_sms) * xattn_cands_per_cta(n_cand);
+  return launch_k(L, xattn_plan_kernel, dim3(1), dim3(1024), 0, anchor_pos, bs, nh, target,
                   xattn_max_chunks(L.num_sms, nh, bs), plan, L.dev_err);
 }
 
@@ -1193,17 +1277,36 @@ cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args, const
   cudaError_t e = cudaSuccess;
   // TMA-fed at small batches (fewer instructions on the latency-bound path); the
   // cp.async kernel measured slightly faster once the pool streams at full rate
-  if (dtype == FLASHMAP_BF16 && kvmap && (a.hd == 64 || a.hd == 128) && a.bs <= kXattnTmaMaxBatch) {
+  const int nc = xattn_cands_per_cta(a.n_cand);
+  if (nc > 1 && (dtype == FLASHMAP_BF16 || dtype == FLASHMAP_E4M3)) {
+    // candidate blocks of a tree draft: NC of them per CTA share each K/V block
+    const int g = L.num_sms * (dtype == FLASHMAP_E4M3 ? 3 : 2);
+    if (dtype == FLASHMAP_BF16) {
+      if (nc == 4)
+        FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false, 4>, dim3(g), dim3(128),
+                                           XCfg<HD, false, 4>::SMEM, a)));
+      else
+        FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false, 2>, dim3(g), dim3(128),
+                                           XCfg<HD, false, 2>::SMEM, a)));
+    } else {
+      if (nc == 4)
+        FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true, 4>, dim3(g), dim3(128),
+                                           XCfg<HD, true, 4>::SMEM, a)));
+      else
+        FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true, 2>, dim3(g), dim3(128),
+                                           XCfg<HD, true, 2>::SMEM, a)));
+    }
+  } else if (dtype == FLASHMAP_BF16 && kvmap && (a.hd == 64 || a.hd == 128) && a.bs <= kXattnTmaMaxBatch) {
     if (a.hd == 128)
       e = launch_k(L, xattn_items_tma_kernel<128>, dim3(grid), dim3(128), XTCfg<128>::SMEM, *kvmap, a);
     else
       e = launch_k(L, xattn_items_tma_kernel<64>, dim3(grid), dim3(128), XTCfg<64>::SMEM, *kvmap, a);
   } else if (dtype == FLASHMAP_BF16) {
-    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false>, dim3(grid), dim3(128),
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, false, 1>, dim3(grid), dim3(128),
                                        XCfg<HD, false>::SMEM, a)));
   } else if (dtype == FLASHMAP_E4M3) {
     // three CTAs per SM: the e4m3 kernel is latency-bound per block, not byte-bound
-    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true>, dim3(L.num_sms * 3), dim3(128),
+    FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_mma_kernel<HD, true, 1>, dim3(L.num_sms * 3), dim3(128),
                                        XCfg<HD, true>::SMEM, a)));
   } else {
     FM_DISPATCH_HD(a.hd, (e = launch_k(L, xattn_items_simt_kernel<float, HD>, dim3(grid), dim3(128), 0, a)));
@@ -1213,12 +1316,14 @@ cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& args, const
 
 cudaError_t xattn_prepare() {
   cudaError_t e = cudaSuccess;
-#define FM_XATTR(HD_, F8_)                                                                                      \
-  if (e == cudaSuccess)                                                                                         \
-    e = cudaFuncSetAttribute(xattn_items_mma_kernel<HD_, F8_>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                             XCfg<HD_, F8_>::SMEM);
-  FM_XATTR(128, false) FM_XATTR(64, false) FM_XATTR(32, false) FM_XATTR(128, true) FM_XATTR(64, true)
-  FM_XATTR(32, true)
+#define FM_XATTR(HD_, F8_, NC_)                                                                                     \
+  if (e == cudaSuccess)                                                                                             \
+    e = cudaFuncSetAttribute(xattn_items_mma_kernel<HD_, F8_, NC_>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                             XCfg<HD_, F8_, NC_>::SMEM);
+#define FM_XATTR_NC(HD_, F8_) FM_XATTR(HD_, F8_, 1) FM_XATTR(HD_, F8_, 2) FM_XATTR(HD_, F8_, 4)
+  FM_XATTR_NC(128, false) FM_XATTR_NC(64, false) FM_XATTR_NC(32, false) FM_XATTR_NC(128, true)
+  FM_XATTR_NC(64, true) FM_XATTR_NC(32, true)
+#undef FM_XATTR_NC
 #undef FM_XATTR
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(xattn_items_tma_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

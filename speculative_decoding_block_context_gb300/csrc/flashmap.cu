@@ -856,7 +856,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     rpi_x = ws.exp_rpi;
   }
   // split-KV plan of the cross-attention, shared by every layer
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, pos_x, bsc, m->nh, ws.plan));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, pos_x, bsc, m->nh, ws.plan, n_cand));
   // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(Lh, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
   TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
@@ -901,6 +901,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   xa.pool = pool->base;
   xa.num_pages = pool->num_pages;
   xa.bs = bsc;
+  xa.n_cand = n_cand;
   xa.K = m->K;
   xa.nh = m->nh;
   xa.hd = m->hd;

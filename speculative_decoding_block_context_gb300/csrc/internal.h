@@ -157,6 +157,7 @@ struct XattnArgs {
   float* part_o = nullptr;   // [chunks * nh][16][hd]
   float* part_ml = nullptr;  // [chunks * nh][16][2]
   float scale_log2 = 0.f;    // hd^-1/2 * log2(e)
+  int n_cand = 1;            // blocks per request: a tree draft's candidates share a context
   unsigned* dev_err = nullptr;
 };
 cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
@@ -164,7 +165,8 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
                            void* out);
 int xattn_max_chunks(int num_sms, int nh, int bs);
 size_t xattn_plan_ints(int num_sms, int nh, int bs);
-cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan);
+// n_cand: blocks per request (consecutive blocks of a request share its context)
+cudaError_t xattn_plan(const Launch& L, const int32_t* anchor_pos, int bs, int nh, int* plan, int n_cand = 1);
 // kvmap: the bf16 pool as rows of head_dim channels (box 64 x 16, 128B swizzle) for the
 // TMA-fed kernel, or null for the cp.async one.
 cudaError_t xattn_items(const Launch& L, int dtype, const XattnArgs& a, const CUtensorMap* kvmap = nullptr);

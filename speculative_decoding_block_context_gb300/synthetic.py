@@ -90,6 +90,11 @@ WORKLOADS = {
                               noise_path=1),
     "qwen3_8b_bs1_folded": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
                                 temps=("all", 1.0), full_scatter=False, seed=2, noise_path=1),
+    # tree drafting: 4 candidate blocks per request (greedy), the verify tree of width 16
+    "qwen3_8b_bs1_tree4": dict(model="qwen3_8b", bs=1, ctx=("fixed", 2048), prefill=True, window=True,
+                               temps=("greedy",), full_scatter=False, seed=2, tree=(4, 16)),
+    "qwen3_8b_bs32_tree4": dict(model="qwen3_8b", bs=32, ctx=("uniform", 512, 8192), prefill=False,
+                                window=False, temps=("greedy",), full_scatter=False, seed=3, tree=(4, 16)),
     # e4m3 draft KV pool (keys and values stored with scale 1, fp8 queries per head)
     "small_bf16_kv8": dict(model="small", bs=3, ctx=("list", [37, 300, 129]), prefill=True,
                            window=True, temps=("mix", 0.5, 1.2), full_scatter=False, seed=12,
@@ -250,6 +255,7 @@ def make_requests(workload: str, device, *, bs: int | None = None, seed: int | N
         temperature=temperature.to(torch.float32).to(device), greedy=greedy.to(device),
         step=int(torch.randint(0, 1000, (1,), generator=g)),
         full_scatter=wl["full_scatter"], prefill=wl["prefill"],
+        tree=wl.get("tree"),  # (candidates per request, tree width) or None
     )
     dt = torch_dtype(cfg["act_dtype"])
     gd = torch.Generator(device=device).manual_seed(seed + 1000)

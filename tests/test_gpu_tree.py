@@ -65,6 +65,13 @@ def test_tree_refuses_out_of_range_shapes():
     ("small_bf16", 3, 12, 2e-2, 1e-2, 0),  # bf16: tokens compared where the margin is clear
     ("tiny_fp32", 8, 16, 1e-4, 1e-4, 1),   # fp32: whole trees compared
     ("small_bf16_folded", 3, 12, 2e-2, 1e-2, 0),  # candidates on the folded-noise path
+    # 2, 4 and 8 candidates: a CTA's warps serve 2 or 4 candidate blocks from one read
+    # of each K/V block (8: two groups of 4)
+    ("small_bf16", 2, 8, 2e-2, 1e-2, 0),
+    ("small_bf16", 4, 16, 2e-2, 1e-2, 0),
+    ("small_bf16", 8, 24, 2e-2, 1e-2, 0),
+    ("small_bf16_kv8", 4, 16, 2e-2, 1e-2, 0),  # e4m3 pool
+    ("small_bf16_kv8", 2, 8, 2e-2, 1e-2, 0),
 ])
 def test_candidate_draft_and_tree_against_the_oracle(workload, n, width, tol, margin, min_trees):
     margin_min = margin
