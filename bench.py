@@ -588,7 +588,8 @@ def kernel_case(args) -> dict:
     from speculative_decoding_block_context_gb300 import _lib as F
 
     hbm_peak, tf_peak, src = load_peaks()
-    rows, n, k = (16, 40960, 4096) if args.kernel_case == "gemm" else (2048, 12288, 4096)
+    rows, n, k = {"gemm": (16, 40960, 4096), "gemm512": (512, 12288, 4096),
+                  "gemm2048": (2048, 12288, 4096)}[args.kernel_case]
     g = torch.Generator(device="cuda").manual_seed(0)
     x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
     w = (torch.randn((n, k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
@@ -621,7 +622,7 @@ def main() -> int:
     ap.add_argument("--workload", default="qwen3_8b_bs1", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["gemm", "gemm2048"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "gemm512", "gemm2048"], default=None,
                     help="time one kernel alone instead of the step (profiling case)")
     args = ap.parse_args()
     if args.kernel_case:

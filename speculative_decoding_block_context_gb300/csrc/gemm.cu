@@ -88,6 +88,9 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // tiles are numbered weight tile fastest (tile = r * mt + m): the CTAs running at the
+  // same time hold neighbouring ranges, so the row tiles that need one weight tile ask
+  // for it together and DRAM serves it once
   const int mt = (N + 127) >> 7, rt = (R + BN - 1) / BN, KB = (K + 63) >> 6;
   const int64_t T = static_cast<int64_t>(mt) * rt * KB;
   const int64_t it0 = T * blockIdx.x / gridDim.x, it1 = T * (blockIdx.x + 1) / gridDim.x;
@@ -127,7 +130,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
       for (int i = 0; i < pre; ++i) {
         const int64_t tile = (it0 + i) / KB;
         const int kb = static_cast<int>(it0 + i - tile * KB);
-        const int m = static_cast<int>(tile / rt);
+        const int m = static_cast<int>(tile % mt);
         mbar_arrive_expect_tx(&full_bar[i], C::TX_BYTES);
         tma_load_2d(smem + i * C::STAGE_BYTES + (F8 ? C::A_BYTES + C::B_BYTES : 0), &mapW, &full_bar[i], kb * 64,
                     m * 128, pol_w);
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
       for (int i = 0; i < pre; ++i) {
         const int64_t tile = (it0 + i) / KB;
         const int kb = static_cast<int>(it0 + i - tile * KB);
-        const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+        const int r = static_cast<int>(tile / mt), m = static_cast<int>(tile - static_cast<int64_t>(r) * mt);
         tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &mapX, &full_bar[i], kb * 64, r * BN, pol_x);
       }
       issued = pre;
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
       for (int64_t it = it0 + pre; it < it1; ++it) {
         const int64_t tile = it / KB;
         const int kb = static_cast<int>(it - tile * KB);
-        const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+        const int r = static_cast<int>(tile / mt), m = static_cast<int>(tile - static_cast<int64_t>(r) * mt);
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) break;
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
       const int64_t tile = it / KB;
       const int kb0 = static_cast<int>(it - tile * KB);
       const int64_t seg_end = min(it1, (tile + 1) * KB);
-      const int m = static_cast<int>(tile / rt), r = static_cast<int>(tile - static_cast<int64_t>(m) * rt);
+      const int r = static_cast<int>(tile / mt), m = static_cast<int>(tile - static_cast<int64_t>(r) * mt);
       const int buf = seg & 1;
       const uint32_t aph = (seg >> 1) & 1;
       if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
