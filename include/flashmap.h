@@ -308,7 +308,9 @@ flashmap_status flashmap_sample_logits_static(flashmap_model* model, int32_t bs,
  * n_cand > 1). The anchor rows are computed and written once per request; block bc =
  * b * n_cand + c (candidate c of request b) has the request's positions and context,
  * and its noise takes Philox counter word 3 = c, so candidate 0 is the block
- * flashmap_draft_block drafts. The candidates of a request read the same context.
+ * flashmap_draft_block drafts. The candidates of a request share its context: when
+ * n_cand is a multiple of 2 or 4, the cross-attention serves 2 or 4 of them from one
+ * read of each K/V block (bf16 and e4m3 pools); otherwise each reads it.
  *   hidden_out  (device) [bs * n_cand * K][D] act_dtype, candidate-major per request
  * Size the workspace with flashmap_workspace_size(max_bs = bs * n_cand). The blocks'
  * tokens come from flashmap_sample_block over bs * n_cand blocks (with each request's
