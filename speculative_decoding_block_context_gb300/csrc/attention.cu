@@ -95,30 +95,39 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
     sv[k * HD + lane * EPL + e] = v[2][e];
   }
   __syncthreads();
-  // scores of slot k against slot j = lane
+  // scores of slot k against slot j = lane (four partial sums: a short dependency chain)
   const float scale = rsqrtf(static_cast<float>(HD));
   float s = -INFINITY;
   if (lane < K) {
-    float acc = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const float4* qr = reinterpret_cast<const float4*>(sq + k * LDQ);
     const float4* kr = reinterpret_cast<const float4*>(sk + lane * LDQ);
-#pragma unroll 8
+#pragma unroll
     for (int d4 = 0; d4 < HD / 4; ++d4) {
       const float4 a4 = qr[d4], b4 = kr[d4];
-      acc = fmaf(a4.x, b4.x, acc);
-      acc = fmaf(a4.y, b4.y, acc);
-      acc = fmaf(a4.z, b4.z, acc);
-      acc = fmaf(a4.w, b4.w, acc);
+      float& c = acc[d4 & 3];
+      c = fmaf(a4.x, b4.x, c);
+      c = fmaf(a4.y, b4.y, c);
+      c = fmaf(a4.z, b4.z, c);
+      c = fmaf(a4.w, b4.w, c);
     }
-    s = acc * scale;
+    s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
   }
   const float m = warp_max(s);
   float p = lane < K ? expf(s - m) : 0.f;
   p /= warp_sum(p);
+  // the probabilities of all K (<= 16) slots in every lane, then each lane's channels
+  float pj[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pj[j] = __shfl_sync(0xffffffffu, p, j);
   T* o = out + static_cast<int64_t>(row) * D + h * HD;
-  for (int d = lane; d < HD; d += 32) {
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const int d = lane + 32 * e;
     float acc = 0.f;
-    for (int j = 0; j < K; ++j) acc = fmaf(__shfl_sync(0xffffffffu, p, j), sv[j * HD + d], acc);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < K) acc = fmaf(pj[j], sv[j * HD + d], acc);
     o[d] = from_f32<T>(acc);
   }
 }
