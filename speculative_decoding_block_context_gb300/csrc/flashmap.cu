@@ -87,6 +87,10 @@ struct flashmap_model {
   int noise_path = 0, eig_sweeps = 0;
   Weight fold;
   float *fold_var = nullptr, *fold_xu = nullptr;
+  // the anchor branch of a draft runs on this stream, forked from and joined back to
+  // the caller's stream with the two events
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // launch timing (flashmap_profile_start / stop)
   bool prof_on = false;
   int prof_cap = 0;
@@ -94,6 +98,15 @@ struct flashmap_model {
   std::vector<flashmap_launch_record> prof_recs;
   Launch launch(cudaStream_t s) const { return Launch{s, num_sms, dev_err}; }
 };
+
+// The draft's anchor branch on the side stream (1) or in line (0), and the tcgen05
+// GEMM CTAs per SM while both branches run.
+#ifndef FM_DRAFT_FORK
+#define FM_DRAFT_FORK 1
+#endif
+#ifndef FM_FORK_CTAS_PER_SM
+#define FM_FORK_CTAS_PER_SM 1
+#endif
 
 namespace {
 // Records an event pair around one launch while profiling is on.
@@ -337,6 +350,9 @@ flashmap_status flashmap_free(flashmap_model* model) {
   if (!model) return FLASHMAP_OK;
   if (model->arena) cudaFree(model->arena);
   for (cudaEvent_t e : model->prof_events) cudaEventDestroy(e);
+  if (model->ev_fork) cudaEventDestroy(model->ev_fork);
+  if (model->ev_join) cudaEventDestroy(model->ev_join);
+  if (model->side) cudaStreamDestroy(model->side);
   delete model;
   return FLASHMAP_OK;
 }
@@ -394,6 +410,10 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   if (cudaGetDevice(&m->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device) != cudaSuccess)
     return cleanup(fail(FLASHMAP_E_CUDA, "no CUDA device"));
+  if (cudaStreamCreateWithFlags(&m->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&m->ev_join, cudaEventDisableTiming) != cudaSuccess)
+    return cleanup(fail(FLASHMAP_E_CUDA, "could not create the model's side stream and events"));
   const int adt = m->adt;
   const bool e4m3 = m->wdt == FLASHMAP_E4M3;
   const size_t es = dt_size(adt);
@@ -857,11 +877,28 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   }
   // split-KV plan of the cross-attention, shared by every layer
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::xattn_plan(Lh, pos_x, bsc, m->nh, ws.plan, n_cand));
-  // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(Lh, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
-  TIMED_GEMM(-1, m->ap, bs, fm::linear(Lh, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.a_rows, D));
-  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(Lh, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, true));
+  // 1. anchor row: anchor_norm(anchor_proj(E[anchor])) -> every layer's context K/V at p.
+  // Nothing before layer 0's cross-attention reads it, so it runs on the model's side
+  // stream beside the noise embedding and layer 0's self-attention half: the two
+  // branches fill each other's gaps between weight-streaming GEMMs. Their GEMMs take one
+  // CTA per SM so that one of each branch fits on an SM at once. (Not while launches are
+  // being timed one by one.)
+  const bool fork = FM_DRAFT_FORK && !m->prof_on;
+  const Launch La = [&] {
+    Launch l = m->launch(fork ? m->side : s);
+    if (fork) l.ctas_per_sm = FM_FORK_CTAS_PER_SM;
+    return l;
+  }();
+  Launch Lm = Lh;  // the main branch until the join
+  if (fork) {
+    Lm.ctas_per_sm = FM_FORK_CTAS_PER_SM;
+    FM_CUDA(cudaEventRecord(m->ev_fork, s));
+    FM_CUDA(cudaStreamWaitEvent(m->side, m->ev_fork, 0));
+  }
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(La, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
+  TIMED_GEMM(-1, m->ap, bs, fm::linear(La, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(La, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.a_rows, D));
+  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(La, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, true));
   {
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
@@ -884,9 +921,12 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     a.max_pos = m->maxpos;
     a.pool = pool->base;
     a.out_loc = anchor_loc_out;
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(La, m->kdt, a));
   }
-  // 3. the DiT blocks
+  if (fork) FM_CUDA(cudaEventRecord(m->ev_join, m->side));
+  bool joined = !fork;
+  // 3. the DiT blocks (launches on Lc: the main branch's configuration until the join)
+  Launch Lc = Lm;
   const float eps_ln = m->cfg.layer_norm_eps, eps_qk = m->cfg.qk_norm_eps;
   // the pool as rows of head_dim channels for the TMA-fed cross-attention (bf16)
   CUtensorMap kvmap;
@@ -924,41 +964,51 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
       const LayerW& lw = m->layers[l];
       const float* md = mods_all ? mods_all + static_cast<size_t>(l) * 9 * D : lw.mods;
       const float* fc2_beta = beta_all ? beta_all + static_cast<size_t>(l) * D : lw.fc2_beta;
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.qkv, R, fm::linear(Lh, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
-      TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lh, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.qkv, R, fm::linear(Lc, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
+      TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lc, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
                                  pos_x, ws.act));
-      TIMED_GEMM(l, lw.o, R, fm::linear(Lh, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.cq, R, fm::linear(Lh, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
+      TIMED_GEMM(l, lw.o, R, fm::linear(Lc, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.cq, R, fm::linear(Lc, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
+      if (!joined) {  // the anchor rows are in the pool from here on
+        FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
+        joined = true;
+        Lc = Lh;
+      }
       xa.layer = l;
       xa.q_norm = lw.cqn;
-      TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lh, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
-      TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lh, adt, xa, ws.act));
-      TIMED_GEMM(l, lw.co, R, fm::linear(Lh, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lh, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.fc1, R, fm::linear(Lh, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lh, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
-      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lh, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, fc2_beta, false));
+      TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lc, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
+      TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lc, adt, xa, ws.act));
+      TIMED_GEMM(l, lw.co, R, fm::linear(Lc, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
+      TIMED_GEMM(l, lw.fc1, R, fm::linear(Lc, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
+      TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lc, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
+      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lc, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, fc2_beta, false));
     }
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lh, adt, ws.x, R, D, fin, fin + D, eps_ln, out));
+    if (!joined) {
+      FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
+      joined = true;
+      Lc = Lh;
+    }
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lc, adt, ws.x, R, D, fin, fin + D, eps_ln, out));
     return FLASHMAP_OK;
   };
   if (m->steps == 1 && m->noise_path == 1) {
     // 2'. folded noise: z (Philox, as below) scaled by gate * rsqrt(sum(lam z^2) / H + eps),
     // then one GEMM through M onto x_embed(u)
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::folded_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, n_cand, noise_scale,
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::folded_noise(Lc, adt, seeds, anchor_pos, bs, m->K, H, n_cand, noise_scale,
                                                    m->fold_var, m->cfg.rms_norm_eps, m->gate, ws.act));
-    TIMED_GEMM(-1, m->fold, R, fm::linear(Lh, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, false));
+    TIMED_GEMM(-1, m->fold, R, fm::linear(Lc, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, false));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   if (m->steps == 1) {
     // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
-    TIMED_GEMM(-1, m->chol, R, fm::linear(Lh, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lc, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
+    TIMED_GEMM(-1, m->chol, R, fm::linear(Lc, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lc, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
                          ws.act, H));
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   // several jumps: the state starts as V-wide noise keyed like the one-jump noise
@@ -966,40 +1016,40 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   const size_t es = dt_size(adt);
   uint8_t* xpost = static_cast<uint8_t*>(ws.xbuf);
   uint8_t* xstate = xpost + static_cast<size_t>(R) * V * es;
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lh, FLASHMAP_F32, seeds, anchor_pos, bs, m->K, static_cast<int>(V),
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lc, FLASHMAP_F32, seeds, anchor_pos, bs, m->K, static_cast<int>(V),
                                                 ws.state, 1, noise_scale));
   for (int st = 0; st < m->steps; ++st) {
     const float s0 = m->grid[st];
     const float ev = s0 > 0.f ? s0 / ((1.f - s0 > 1e-3f ? 1.f - s0 : 1e-3f) * (1.f - s0 > 1e-3f ? 1.f - s0 : 1e-3f))
                               : 0.f;
     // the previous jump's state update, then this jump's posterior and state in act dtype
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::state_prep(Lh, adt, ws.state, ws.logits_full, m->full_head_b, R,
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::state_prep(Lc, adt, ws.state, ws.logits_full, m->full_head_b, R,
                                                  static_cast<int>(V), st > 0, st > 0 ? m->grid[st - 1] : 0.f, s0, ev,
                                                  xpost, xstate, V));
     // [posterior; state] @ E (at s = 0 only the state: the posterior is uniform)
     if (s0 > 0.f) {
-      TIMED_GEMM(-1, m->et, 2 * R, fm::linear(Lh, m->et, xpost, 2 * R, static_cast<int>(V), ws.emb, H, nullptr,
+      TIMED_GEMM(-1, m->et, 2 * R, fm::linear(Lc, m->et, xpost, 2 * R, static_cast<int>(V), ws.emb, H, nullptr,
                                               nullptr, true));
     } else {
-      TIMED_GEMM(-1, m->et, R, fm::linear(Lh, m->et, xstate, R, static_cast<int>(V), ws.emb + static_cast<size_t>(R) * H,
+      TIMED_GEMM(-1, m->et, R, fm::linear(Lc, m->et, xstate, R, static_cast<int>(V), ws.emb + static_cast<size_t>(R) * H,
                                           H, nullptr, nullptr, true));
     }
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::mix_state(Lh, adt, s0 > 0.f ? ws.emb : nullptr, ws.emb + static_cast<size_t>(R) * H,
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::mix_state(Lc, adt, s0 > 0.f ? ws.emb : nullptr, ws.emb + static_cast<size_t>(R) * H,
                                                 R, H, m->u, m->state_norm_w, m->noise_norm_w, m->cfg.rms_norm_eps,
                                                 m->step_gate[st], ws.act));
     if (st > 0) {  // the residual stream restarts at x_embed of the new input
       fm::ZeroList z;
       z.add(ws.x, static_cast<int64_t>(R) * D);
-      TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
+      TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lc, z));
     }
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lh, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
     const bool last = st + 1 == m->steps;
     const size_t L = static_cast<size_t>(m->L);
     const flashmap_status r = dit(m->step_mods + st * L * 9 * D, m->step_fc2_beta + st * L * D,
                                   m->step_final + static_cast<size_t>(st) * 2 * D, last ? hidden_out : ws.act);
     if (r != FLASHMAP_OK) return r;
     if (!last)  // the full-vocabulary logits that move the state
-      TIMED_GEMM(-1, m->full_head, R, fm::linear(Lh, m->full_head, ws.act, R, D, ws.logits_full,
+      TIMED_GEMM(-1, m->full_head, R, fm::linear(Lc, m->full_head, ws.act, R, D, ws.logits_full,
                                                  static_cast<int>(V), nullptr, nullptr, true));
   }
   return FLASHMAP_OK;

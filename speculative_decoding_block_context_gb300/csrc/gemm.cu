@@ -442,7 +442,8 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   if (!make_tmap_bf16(&mapX, x, R, W.K, ldx, BN, &err)) return cudaErrorInvalidValue;
   const int64_t mt = (W.N + 127) / 128, rt = (R + BN - 1) / BN, KB = (W.K + 63) / 64;
   const int64_t T = mt * rt * KB;
-  const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * C::PER_SM));
+  const int per_sm = L.ctas_per_sm > 0 ? std::min(L.ctas_per_sm, C::PER_SM) : C::PER_SM;
+  const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * per_sm));
   return launch_k(L, tc_linear_kernel<BN, F8>, dim3(G), dim3(C::THREADS), C::SMEM, W.map, mapX, out, ldo, R, W.N,
                   W.K, alpha, beta, W.wscale, zeroed ? 1 : 0, L.dev_err);
 }

@@ -16,6 +16,7 @@ struct Launch {
   int num_sms;
   unsigned* dev_err;  // the model's device error word (may be null in debug calls)
   bool pdl = true;    // launch with programmatic stream serialization
+  int ctas_per_sm = 0;  // tcgen05 GEMM CTAs per SM (0: the kernel's own maximum)
 };
 
 // Launches `kernel` on L.stream, with programmatic stream serialization when L.pdl.
