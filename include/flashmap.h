@@ -29,6 +29,10 @@
  *     flashmap_get_device_error(). No kernel traps or spins without a time limit.
  *   - Matrices are row-major. "rows" of the draft are request-major:
  *     row b * block_size + k is slot k of request b.
+ *   - flashmap_draft_block and flashmap_draft_candidates run part of their work on a
+ *     stream the model owns, forked from `stream` by an event and joined back before
+ *     the call returns; work enqueued on `stream` after the call still sees all of it.
+ *     Drafts of one model must therefore be enqueued from one host thread at a time.
  */
 #ifndef FLASHMAP_H_
 #define FLASHMAP_H_
