@@ -62,9 +62,15 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   float* sk = sq + K * LDQ;        // [K][LDQ]
   float* sv = sk + K * LDQ;        // [K][HD]
   pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float wq[EPL], wk[EPL];  // the norm weights: constants, read before waiting
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    wq[e] = qn[lane * EPL + e];
+    wk[e] = kn[lane * EPL + e];
+  }
+  pdl_wait();
   const int D = nh * HD;
   const int k = warp;  // one warp per slot
   const int row = b * K + k;
@@ -86,8 +92,8 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
     pos = 0;
   }
   const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
-  head_norm_rope<EPL>(v[0], qn, eps, rope, lane);
-  head_norm_rope<EPL>(v[1], kn, eps, rope, lane);
+  head_norm_rope_w<EPL>(v[0], wq, eps, rope, lane);
+  head_norm_rope_w<EPL>(v[1], wk, eps, rope, lane);
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
     sq[k * LDQ + lane * EPL + e] = v[0][e];
@@ -889,7 +895,10 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();
+  // early: nothing read before the wait below (plan, page table, pool) comes from the
+  // kernel just before this one, so the first blocks are requested while it finishes
+  bool waited = a.early == 0;
+  if (waited) pdl_wait();
   const int nh = a.nh;
   const int items = LDCG(a.plan), chunk_len = LDCG(a.plan + 1);
   const int* pairs = a.plan + 4 + a.bs;
@@ -947,6 +956,10 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
     };
 #pragma unroll
     for (int j = 0; j < C::STAGES - 1; ++j) issue(j);
+    if (!waited) {  // the queries (and every buffer written below) follow the kernel before
+      pdl_wait();
+      waited = true;
+    }
     // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
     load_queries<HD>(a, b, h, sq);
@@ -1106,6 +1119,7 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
     __syncthreads();
     if (abort_flag) break;  // the same value in every warp after the barrier
   }
+  if (!waited) pdl_wait();  // no item: the grid still completes after the kernel before
 }
 
 // ------------------------------------------------------------------ combine

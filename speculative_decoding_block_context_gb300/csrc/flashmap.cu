@@ -107,6 +107,11 @@ struct flashmap_model {
 #ifndef FM_FORK_CTAS_PER_SM
 #define FM_FORK_CTAS_PER_SM 1
 #endif
+// Cross-attention at small batches: K/V requested before the dependency wait when the
+// draft is forked.
+#ifndef FM_XATTN_EARLY
+#define FM_XATTN_EARLY 1
+#endif
 
 namespace {
 // Records an event pair around one launch while profiling is on.
@@ -958,6 +963,10 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   xa.eps = eps_qk;
   xa.rope = m->rope;
   xa.max_pos = m->maxpos;
+  // Forked: the anchor rows are joined before layer 0's cross-attention and everything
+  // else its items kernels read before their dependency wait (plan, page table, pool)
+  // was complete before the fork; each later items kernel starts after layer 0's did.
+  xa.early = FM_XATTN_EARLY && fork ? 1 : 0;
   // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
   auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
     for (int l = 0; l < m->L; ++l) {

@@ -32,7 +32,7 @@ constexpr int kTcThreadsF8 = 320;
 
 // Pipeline depth of the narrow (<= 32 activation rows) GEMMs, and CTAs launched per SM.
 #ifndef FM_TC_STAGES_NARROW
-#define FM_TC_STAGES_NARROW 5
+#define FM_TC_STAGES_NARROW 4
 #endif
 #ifndef FM_TC_CTAS_PER_SM
 #define FM_TC_CTAS_PER_SM 2

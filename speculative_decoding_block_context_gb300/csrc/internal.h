@@ -159,6 +159,10 @@ struct XattnArgs {
   float* part_ml = nullptr;  // [chunks * nh][16][2]
   float scale_log2 = 0.f;    // hd^-1/2 * log2(e)
   int n_cand = 1;            // blocks per request: a tree draft's candidates share a context
+  // 1: the pool, the plan and the page table were complete before the items kernel could
+  // start (only the queries come from the kernel just before it), so its first K/V
+  // blocks are requested before it waits for that kernel
+  int early = 0;
   unsigned* dev_err = nullptr;
 };
 cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,

@@ -168,6 +168,38 @@ __device__ __forceinline__ void load_row4(const float* src, int w4, float4 (&v)[
   }
 }
 
+// Merges (count, mean, M2) statistics b into a: the combined count, mean and sum of
+// squared deviations (Chan, Golub and LeVeque's pairwise update).
+__device__ __forceinline__ void merge_mean_m2(float& n, float& mean, float& m2, float nb, float meanb, float m2b) {
+  const float nt = n + nb;
+  if (nt > 0.f) {
+    const float d = meanb - mean, f = nb / nt;
+    mean = fmaf(d, f, mean);
+    m2 = m2 + m2b + d * d * n * f;
+    n = nt;
+  }
+}
+
+// Block-wide merge of every thread's (count, mean, M2); every thread gets the same
+// result (the warps' partials are merged in warp order). red: >= 3 * warps floats.
+__device__ __forceinline__ void block_mean_m2(float& n, float& mean, float& m2, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float nb = __shfl_xor_sync(0xffffffffu, n, o), mb = __shfl_xor_sync(0xffffffffu, mean, o),
+                qb = __shfl_xor_sync(0xffffffffu, m2, o);
+    merge_mean_m2(n, mean, m2, nb, mb, qb);
+  }
+  if (lane == 0) {
+    red[3 * warp] = n;
+    red[3 * warp + 1] = mean;
+    red[3 * warp + 2] = m2;
+  }
+  __syncthreads();
+  n = 0.f, mean = 0.f, m2 = 0.f;
+  for (int w = 0; w < nw; ++w) merge_mean_m2(n, mean, m2, red[3 * w], red[3 * w + 1], red[3 * w + 2]);
+}
+
 // out = LayerNorm(x) * mscale + mshift   (no affine; biased variance)
 template <typename T, int NV>
 __global__ void __launch_bounds__(kRowThreads) ln_mod_kernel(const float* __restrict__ x, int width,
@@ -182,19 +214,26 @@ __global__ void __launch_bounds__(kRowThreads) ln_mod_kernel(const float* __rest
   load_row4<NV, false>(mh, w4, m2);
   pdl_wait();
   load_row4<NV, true>(x + static_cast<int64_t>(blockIdx.x) * width, w4, v);
-  float s = 0.f;
+  // the row's mean and squared deviations in one block reduction: each thread's own
+  // (count, mean, M2) in two passes over its registers, merged pairwise (Chan et al.)
+  float s = 0.f, cnt = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-  const float mean = block_sum(s, red) / width;
-  float s2 = 0.f;
+  for (int i = 0; i < NV; ++i) {
+    if (threadIdx.x + i * kRowThreads < w4) {
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      cnt += 4.f;
+    }
+  }
+  float mean = cnt > 0.f ? s / cnt : 0.f, dev2 = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     if (threadIdx.x + i * kRowThreads < w4) {
       const float a = v[i].x - mean, b = v[i].y - mean, c = v[i].z - mean, d = v[i].w - mean;
-      s2 += (a * a + b * b) + (c * c + d * d);
+      dev2 += (a * a + b * b) + (c * c + d * d);
     }
   }
-  const float rstd = rsqrtf(block_sum(s2, red) / width + eps);
+  block_mean_m2(cnt, mean, dev2, red);
+  const float rstd = rsqrtf(dev2 / width + eps);
   T* o = out + static_cast<int64_t>(blockIdx.x) * width;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
