@@ -584,12 +584,13 @@ def kernel_case(args) -> dict:
     """One tcgen05 GEMM timed alone over --steps launches: "gemm" is the batch-1 shape
     (16 activation rows x the all-layer context K/V weight, 40960 x 4096 bf16 = 335 MB,
     above L2; HBM-bound), "gemm2048" the batch-128 MLP shape (2048 rows x 12288 x 4096;
-    tensor-bound)."""
+    tensor-bound), "head2048" the batch-128 folded head (2048 rows x 32768 draft
+    vocabulary x 4096; tensor-bound)."""
     from speculative_decoding_block_context_gb300 import _lib as F
 
     hbm_peak, tf_peak, src = load_peaks()
     rows, n, k = {"gemm": (16, 40960, 4096), "gemm512": (512, 12288, 4096),
-                  "gemm2048": (2048, 12288, 4096)}[args.kernel_case]
+                  "gemm2048": (2048, 12288, 4096), "head2048": (2048, 32768, 4096)}[args.kernel_case]
     g = torch.Generator(device="cuda").manual_seed(0)
     x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
     w = (torch.randn((n, k), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
@@ -622,7 +623,7 @@ def main() -> int:
     ap.add_argument("--workload", default="qwen3_8b_bs1", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["gemm", "gemm512", "gemm2048"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "gemm512", "gemm2048", "head2048"], default=None,
                     help="time one kernel alone instead of the step (profiling case)")
     args = ap.parse_args()
     if args.kernel_case:

@@ -54,7 +54,7 @@ template <typename T, int EPL>
 __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const float* __restrict__ qn,
                                  const float* __restrict__ kn, float eps, const float2* __restrict__ rope_tab,
                                  int max_pos, const int32_t* __restrict__ anchor_pos, T* __restrict__ out,
-                                 unsigned* dev_err) {
+                                 int early, unsigned* dev_err) {
   constexpr int HD = EPL * 32;
   extern __shared__ float sm[];
   constexpr int LDQ = HD + 4;      // 16-byte rows, 4 banks apart: conflict-free float4 reads
@@ -70,6 +70,9 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
     wq[e] = qn[lane * EPL + e];
     wk[e] = kn[lane * EPL + e];
   }
+  __shared__ int s_anchor;
+  // early: the positions were written before the kernel just before this one started
+  if (early && threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
   pdl_wait();
   const int D = nh * HD;
   const int k = warp;  // one warp per slot
@@ -81,19 +84,28 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   float v[3][EPL];
 #pragma unroll
   for (int part = 0; part < 3; ++part) load_head_vec<EPL>(base + part * D, v[part], lane);
-  __shared__ int s_anchor;
-  if (threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
+  if (!early && threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
   __syncthreads();
-#pragma unroll
-  for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
   int pos = s_anchor + 1 + k;
   if (pos < 0 || pos >= max_pos) {
     if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
     pos = 0;
   }
   const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
-  head_norm_rope_w<EPL>(v[0], wq, eps, rope, lane);
-  head_norm_rope_w<EPL>(v[1], wk, eps, rope, lane);
+  if constexpr (EPL >= 2) {  // the slot's rotation pairs, requested before q, k and v are used
+    float2 cs[EPL / 2];
+#pragma unroll
+    for (int i = 0; i < EPL / 2; ++i) cs[i] = rope[(lane * EPL >> 1) + i];
+#pragma unroll
+    for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
+    head_norm_rot<EPL>(v[0], wq, eps, cs);
+    head_norm_rot<EPL>(v[1], wk, eps, cs);
+  } else {
+#pragma unroll
+    for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
+    head_norm_rope_w<EPL>(v[0], wq, eps, rope, lane);
+    head_norm_rope_w<EPL>(v[1], wk, eps, rope, lane);
+  }
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
     sq[k * LDQ + lane * EPL + e] = v[0][e];
@@ -210,7 +222,7 @@ __global__ void __launch_bounds__(1024) xattn_plan_kernel(const int32_t* __restr
 // p + 1 + k (flashmap/modeling_flashmap.py, FlashMapAttention.forward). Every item of a
 // (request, head) derives them from the projection accumulator; 128 threads.
 template <int HD, bool kQuant = false>
-__device__ __forceinline__ float load_queries(const XattnArgs& a, int b, int h, float* sq) {
+__device__ __forceinline__ float load_queries(const XattnArgs& a, int b, int h, float* sq, int anchor) {
   constexpr int EPL = HD / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int D = a.nh * HD;
@@ -227,7 +239,7 @@ __device__ __forceinline__ float load_queries(const XattnArgs& a, int b, int h, 
   for (int i = 0; i < 4; ++i) {
     const int q = warp + 4 * i;
     if (q < a.K) {  // warp-uniform
-      int pos = LDCG(a.anchor_pos + b) + 1 + q;
+      int pos = anchor + 1 + q;
       if (pos < 0 || pos >= a.max_pos) {
         if (lane == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_POSITION);
         pos = 0;
@@ -290,7 +302,7 @@ __global__ void __launch_bounds__(128) xattn_items_simt_kernel(XattnArgs a) {
     const int p0 = c * chunk_len, p1 = min(n, p0 + chunk_len);
     const int rrow = a.req_pool_idx ? LDCG(a.req_pool_idx + b) : b;
     __syncthreads();
-    load_queries<HD>(a, b, h, &sq[0][0]);
+    load_queries<HD>(a, b, h, &sq[0][0], LDCG(a.anchor_pos + b));
     if (tid < 16) {
       sm[tid] = -INFINITY;
       sl[tid] = 0.f;
@@ -603,11 +615,11 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
     float qscale = 1.f;
     if constexpr (NC == 1) {
-      qscale = load_queries<HD, F8>(a, b, h, sq);  // 1 unless e4m3 queries
+      qscale = load_queries<HD, F8>(a, b, h, sq, LDCG(a.anchor_pos + b));  // 1 unless e4m3 queries
     } else {
 #pragma unroll 1
       for (int k = 0; k < NC; ++k) {
-        const float s = load_queries<HD, F8>(a, b - cw + k, h, sq + k * 16 * HD);
+        const float s = load_queries<HD, F8>(a, b - cw + k, h, sq + k * 16 * HD, LDCG(a.anchor_pos + b - cw + k));
         if (k == cw) qscale = s;
       }
     }
@@ -962,7 +974,7 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
     }
     // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
-    load_queries<HD>(a, b, h, sq);
+    load_queries<HD>(a, b, h, sq, n - 1);  // n - 1: the anchor position, read above
     __syncthreads();
     uint32_t qa[HD / 16][4];
 #pragma unroll
@@ -1188,45 +1200,40 @@ __global__ void __launch_bounds__(64) xattn_combine_kernel(XattnArgs a, T* __res
 }
 
 // Small batches: one CTA of HD threads per (request, head, query row), one thread per
-// channel, for more CTAs in flight when there are few requests.
+// channel, for more CTAs in flight when there are few requests. Each thread folds the
+// chunks' partials into a running (max, sum, output) in one pass: every load is
+// independent of the others, and no block reduction is needed.
 template <typename T, int HD>
 __global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* __restrict__ out) {
-  __shared__ float sw[kMaxChunksPerRequest];
-  __shared__ float red[32];
-  __shared__ int s_g[2];
   pdl_trigger();
-  pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y, qi = blockIdx.z, d = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
-  // the request's chunk range, loaded once per CTA
-  if (d < 2) s_g[d] = LDCG(a.plan + 3 + b + d);
-  __syncthreads();
-  const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
-  float mloc = -INFINITY;
-  for (int c = d; c < nc; c += HD) {
-    const float m = LDCG(a.part_ml + ((static_cast<int64_t>(g0 + c)) * nh + h) * 32 + 2 * qi);
-    sw[c] = m;
-    mloc = fmaxf(mloc, m);
+  int g0 = 0, g1 = 0;
+  if (a.early) {  // the plan was complete before the items kernel started
+    g0 = LDCG(a.plan + 3 + b);
+    g1 = LDCG(a.plan + 4 + b);
   }
-  // block max
-  mloc = warp_max(mloc);
-  if ((d & 31) == 0) red[d >> 5] = mloc;
-  __syncthreads();
-  float M = -INFINITY;
-  for (int w = 0; w < HD / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-  float lloc = 0.f;
-  for (int c = d; c < nc; c += HD) {
-    const int64_t pidx = static_cast<int64_t>(g0 + c) * nh + h;
-    const float wgt = sw[c] == -INFINITY ? 0.f : exp2f(sw[c] - M);
-    sw[c] = wgt;
-    lloc = fmaf(wgt, LDCG(a.part_ml + pidx * 32 + 2 * qi + 1), lloc);
+  pdl_wait();
+  if (!a.early) {
+    g0 = LDCG(a.plan + 3 + b);
+    g1 = LDCG(a.plan + 4 + b);
   }
-  const float L = block_sum(lloc, red);  // synchronizes: sw complete
-  float acc = 0.f;
+  const int nc = min(g1 - g0, kMaxChunksPerRequest);
+  const float* mlp = a.part_ml + (static_cast<int64_t>(g0) * nh + h) * 32 + 2 * qi;
+  const float* po = a.part_o + (static_cast<int64_t>(g0) * nh + h) * 16 * HD + qi * HD + d;
+  const int64_t mls = static_cast<int64_t>(nh) * 32, ps = static_cast<int64_t>(nh) * 16 * HD;  // between chunks
+  float M = -INFINITY, L = 0.f, acc = 0.f;
 #pragma unroll 4
-  for (int c = 0; c < nc; ++c)
-    acc = fmaf(sw[c], LDCG(a.part_o + (static_cast<int64_t>(g0 + c) * nh + h) * 16 * HD + qi * HD + d), acc);
+  for (int c = 0; c < nc; ++c) {
+    const float2 ml = LDCG(reinterpret_cast<const float2*>(mlp + c * mls));  // (running max, sum) of chunk c
+    const float o = LDCG(po + c * ps);
+    if (ml.x == -INFINITY) continue;  // no position of the chunk: nothing to add
+    const float nM = fmaxf(M, ml.x);
+    const float s_old = exp2f(M - nM), s_new = exp2f(ml.x - nM);  // exp2(-inf) = 0
+    L = fmaf(L, s_old, ml.y * s_new);
+    acc = fmaf(acc, s_old, o * s_new);
+    M = nM;
+  }
   out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
   a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
 }
@@ -1260,7 +1267,7 @@ __global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* 
 
 cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
                            const float* kn, float eps, const float2* rope, int max_pos, const int32_t* anchor_pos,
-                           void* out) {
+                           void* out, bool early) {
   if (bs <= 0) return cudaSuccess;
   dim3 grid(bs, nh);
   const size_t smem = static_cast<size_t>(K) * ((hd + 4) * 2 + hd) * sizeof(float);
@@ -1268,13 +1275,13 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
   const dim3 block(32 * K);
   if (hd == 32) {
     FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 1>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
   } else if (hd == 64) {
     FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 2>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
   } else {
     FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 4>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), L.dev_err)));
+                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
   }
   return e;
 }

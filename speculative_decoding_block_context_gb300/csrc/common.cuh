@@ -118,6 +118,28 @@ __device__ __forceinline__ void head_norm_rope_w(float (&v)[EPL], const float (&
   }
 }
 
+// The same with the rotation's (cos, sin) pairs of this lane's channels already loaded
+// (cs[i] for the pair (lane*EPL + 2i, lane*EPL + 2i + 1)); EPL >= 2.
+template <int EPL>
+__device__ __forceinline__ void head_norm_rot(float (&v)[EPL], const float (&w)[EPL], float eps,
+                                              const float2 (&cs)[EPL / 2]) {
+  static_assert(EPL >= 2, "pairs within a lane");
+  constexpr int HD = EPL * 32;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(v[e], v[e], ss);
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss * (1.f / HD) + eps);
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) v[e] *= r * w[e];
+#pragma unroll
+  for (int e = 0; e < EPL; e += 2) {
+    const float x1 = v[e], x2 = v[e + 1];
+    v[e] = x1 * cs[e >> 1].x - x2 * cs[e >> 1].y;
+    v[e + 1] = x2 * cs[e >> 1].x + x1 * cs[e >> 1].y;
+  }
+}
+
 // The same with the norm weight read from memory (channels lane*EPL..).
 template <int EPL>
 __device__ __forceinline__ void head_norm_rope(float (&v)[EPL], const float* __restrict__ w, float eps,

@@ -966,6 +966,9 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   // Forked: the anchor rows are joined before layer 0's cross-attention and everything
   // else its items kernels read before their dependency wait (plan, page table, pool)
   // was complete before the fork; each later items kernel starts after layer 0's did.
+  // (The block self-attention reads the positions early on the same grounds: the
+  // caller's anchor positions, or a multi-candidate draft's per-block copies once the
+  // anchor branch has joined.)
   xa.early = FM_XATTN_EARLY && fork ? 1 : 0;
   // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
   auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
@@ -976,7 +979,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
       TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
       TIMED_GEMM(l, lw.qkv, R, fm::linear(Lc, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
       TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lc, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
-                                 pos_x, ws.act));
+                                 pos_x, ws.act, xa.early != 0 && (n_cand == 1 || l > 0)));
       TIMED_GEMM(l, lw.o, R, fm::linear(Lc, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
       TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
       TIMED_GEMM(l, lw.cq, R, fm::linear(Lc, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));

@@ -167,7 +167,7 @@ struct XattnArgs {
 };
 cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
                            const float* kn, float eps, const float2* rope, int max_pos, const int32_t* anchor_pos,
-                           void* out);
+                           void* out, bool early = false);
 int xattn_max_chunks(int num_sms, int nh, int bs);
 size_t xattn_plan_ints(int num_sms, int nh, int bs);
 // n_cand: blocks per request (consecutive blocks of a request share its context)

@@ -281,7 +281,20 @@ def check_request(st: ModelState, run: LibRun, b: int, o: dict, tol: float, repo
     bump("logits", e)
     assert e <= tol, f"logits max-rel {e}"
     tok = run.tokens[b * K : (b + 1) * K].cpu().numpy()
-    sure = o["margin"] > TOKEN_MARGIN
+    # A token is decided where the oracle's top-2 margin exceeds 1e-2 and also twice the
+    # row's measured logit error (divided by T on sampled rows, whose maximised quantity
+    # is l/T + G): within the logits tolerance a smaller margin may flip either way, and
+    # the GEMMs' float atomics vary the summation order, hence such near ties, run to run.
+    T, g = float(req["temperature"][b]), int(req["greedy"][b])
+    scale = 1.0 if (g or T <= 0.0) else 1.0 / T
+    err_row = np.abs(lg - o["logits"]).max(axis=1) * scale
+    report["max_token_err"] = max(report.get("max_token_err", 0.0), float(err_row.max()))
+    sure = (o["margin"] > TOKEN_MARGIN) & (o["margin"] > 2.0 * err_row)
     report["tokens_checked"] = report.get("tokens_checked", 0) + int(sure.sum())
     report["tokens_total"] = report.get("tokens_total", 0) + K
-    assert np.array_equal(tok[sure], o["tokens"][sure]), f"tokens differ: {tok} vs {o['tokens']}"
+    if not np.array_equal(tok[sure], o["tokens"][sure]):
+        bad = np.nonzero(sure & (tok != o["tokens"]))[0]
+        detail = [(int(r), float(o["margin"][r]), float(np.abs(lg[r] - o["logits"][r]).max()),
+                   float(np.abs(o["logits"][r]).max())) for r in bad]
+        raise AssertionError(f"tokens differ at (slot, oracle margin, max |logit error|, max |logit|) {detail}: "
+                             f"{tok} vs {o['tokens']}")
