@@ -50,7 +50,14 @@ __device__ __forceinline__ void clear_head_vec(float* dst, int lane) {
 
 // ------------------------------------------------------------------ block self-attention
 
-template <typename T, int EPL>
+#ifndef FM_SA_WIDE_CTAS_PER_SM
+#define FM_SA_WIDE_CTAS_PER_SM 4
+#endif
+
+// One CTA per (request, head); warp w holds slots w * SPW .. w * SPW + SPW - 1 (two
+// per warp at large batches: twice the loads in flight per thread, half the threads
+// per CTA, so more CTAs fit on an SM).
+template <typename T, int EPL, int SPW>
 __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const float* __restrict__ qn,
                                  const float* __restrict__ kn, float eps, const float2* __restrict__ rope_tab,
                                  int max_pos, const int32_t* __restrict__ anchor_pos, T* __restrict__ out,
@@ -75,78 +82,93 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   if (early && threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
   pdl_wait();
   const int D = nh * HD;
-  const int k = warp;  // one warp per slot
-  const int row = b * K + k;
-  float* base = qkv + static_cast<int64_t>(row) * 3 * D + h * HD;
-  // q, k and v of this slot and head: all loads first (one vector per lane and part),
-  // then the request's position (once per CTA), the clears and the norms, so the
+  // q, k and v of this warp's slots and head: all loads first (one vector per lane and
+  // part), then the request's position (once per CTA), the clears and the norms, so the
   // L2 round trips overlap
-  float v[3][EPL];
+  float v[SPW][3][EPL];
 #pragma unroll
-  for (int part = 0; part < 3; ++part) load_head_vec<EPL>(base + part * D, v[part], lane);
+  for (int i = 0; i < SPW; ++i) {
+    const int k = warp * SPW + i;
+    if (k < K) {  // warp-uniform
+      const float* base = qkv + static_cast<int64_t>(b * K + k) * 3 * D + h * HD;
+#pragma unroll
+      for (int part = 0; part < 3; ++part) load_head_vec<EPL>(base + part * D, v[i][part], lane);
+    }
+  }
   if (!early && threadIdx.x == 0) s_anchor = LDCG(anchor_pos + b);
   __syncthreads();
-  int pos = s_anchor + 1 + k;
-  if (pos < 0 || pos >= max_pos) {
-    if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
-    pos = 0;
-  }
-  const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
-  if constexpr (EPL >= 2) {  // the slot's rotation pairs, requested before q, k and v are used
-    float2 cs[EPL / 2];
 #pragma unroll
-    for (int i = 0; i < EPL / 2; ++i) cs[i] = rope[(lane * EPL >> 1) + i];
+  for (int i = 0; i < SPW; ++i) {
+    const int k = warp * SPW + i;
+    if (k >= K) continue;
+    float* base = qkv + static_cast<int64_t>(b * K + k) * 3 * D + h * HD;
+    int pos = s_anchor + 1 + k;
+    if (pos < 0 || pos >= max_pos) {
+      if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
+      pos = 0;
+    }
+    const float2* rope = rope_tab + static_cast<int64_t>(pos) * (HD / 2);
+    if constexpr (EPL >= 2) {  // the slot's rotation pairs, requested before q, k and v are used
+      float2 cs[EPL / 2];
 #pragma unroll
-    for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
-    head_norm_rot<EPL>(v[0], wq, eps, cs);
-    head_norm_rot<EPL>(v[1], wk, eps, cs);
-  } else {
+      for (int c = 0; c < EPL / 2; ++c) cs[c] = rope[(lane * EPL >> 1) + c];
 #pragma unroll
-    for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
-    head_norm_rope_w<EPL>(v[0], wq, eps, rope, lane);
-    head_norm_rope_w<EPL>(v[1], wk, eps, rope, lane);
-  }
+      for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
+      head_norm_rot<EPL>(v[i][0], wq, eps, cs);
+      head_norm_rot<EPL>(v[i][1], wk, eps, cs);
+    } else {
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    sq[k * LDQ + lane * EPL + e] = v[0][e];
-    sk[k * LDQ + lane * EPL + e] = v[1][e];
-    sv[k * HD + lane * EPL + e] = v[2][e];
+      for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
+      head_norm_rope_w<EPL>(v[i][0], wq, eps, rope, lane);
+      head_norm_rope_w<EPL>(v[i][1], wk, eps, rope, lane);
+    }
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      sq[k * LDQ + lane * EPL + e] = v[i][0][e];
+      sk[k * LDQ + lane * EPL + e] = v[i][1][e];
+      sv[k * HD + lane * EPL + e] = v[i][2][e];
+    }
   }
   __syncthreads();
-  // scores of slot k against slot j = lane (four partial sums: a short dependency chain)
   const float scale = rsqrtf(static_cast<float>(HD));
-  float s = -INFINITY;
-  if (lane < K) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float4* qr = reinterpret_cast<const float4*>(sq + k * LDQ);
-    const float4* kr = reinterpret_cast<const float4*>(sk + lane * LDQ);
 #pragma unroll
-    for (int d4 = 0; d4 < HD / 4; ++d4) {
-      const float4 a4 = qr[d4], b4 = kr[d4];
-      float& c = acc[d4 & 3];
-      c = fmaf(a4.x, b4.x, c);
-      c = fmaf(a4.y, b4.y, c);
-      c = fmaf(a4.z, b4.z, c);
-      c = fmaf(a4.w, b4.w, c);
+  for (int i = 0; i < SPW; ++i) {
+    const int k = warp * SPW + i;
+    if (k >= K) continue;
+    // scores of slot k against slot j = lane (four partial sums: a short dependency chain)
+    float s = -INFINITY;
+    if (lane < K) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const float4* qr = reinterpret_cast<const float4*>(sq + k * LDQ);
+      const float4* kr = reinterpret_cast<const float4*>(sk + lane * LDQ);
+#pragma unroll
+      for (int d4 = 0; d4 < HD / 4; ++d4) {
+        const float4 a4 = qr[d4], b4 = kr[d4];
+        float& c = acc[d4 & 3];
+        c = fmaf(a4.x, b4.x, c);
+        c = fmaf(a4.y, b4.y, c);
+        c = fmaf(a4.z, b4.z, c);
+        c = fmaf(a4.w, b4.w, c);
+      }
+      s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
     }
-    s = ((acc[0] + acc[1]) + (acc[2] + acc[3])) * scale;
-  }
-  const float m = warp_max(s);
-  float p = lane < K ? expf(s - m) : 0.f;
-  p /= warp_sum(p);
-  // the probabilities of all K (<= 16) slots in every lane, then each lane's channels
-  float pj[16];
+    const float m = warp_max(s);
+    float p = lane < K ? expf(s - m) : 0.f;
+    p /= warp_sum(p);
+    // the probabilities of all K (<= 16) slots in every lane, then each lane's channels
+    float pj[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) pj[j] = __shfl_sync(0xffffffffu, p, j);
-  T* o = out + static_cast<int64_t>(row) * D + h * HD;
+    for (int j = 0; j < 16; ++j) pj[j] = __shfl_sync(0xffffffffu, p, j);
+    T* o = out + static_cast<int64_t>(b * K + k) * D + h * HD;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) {
-    const int d = lane + 32 * e;
-    float acc = 0.f;
+    for (int e = 0; e < EPL; ++e) {
+      const int d = lane + 32 * e;
+      float acc = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (j < K) acc = fmaf(pj[j], sv[j * HD + d], acc);
-    o[d] = from_f32<T>(acc);
+      for (int j = 0; j < 16; ++j)
+        if (j < K) acc = fmaf(pj[j], sv[j * HD + d], acc);
+      o[d] = from_f32<T>(acc);
+    }
   }
 }
 
@@ -1272,17 +1294,24 @@ cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K
   dim3 grid(bs, nh);
   const size_t smem = static_cast<size_t>(K) * ((hd + 4) * 2 + hd) * sizeof(float);
   cudaError_t e = cudaSuccess;
-  const dim3 block(32 * K);
+  const int ea = early ? 1 : 0;
+  // two slots per warp once the grid alone holds a few CTAs per SM
+  const bool wide = static_cast<int64_t>(bs) * nh >= static_cast<int64_t>(FM_SA_WIDE_CTAS_PER_SM) * L.num_sms;
+#define FM_SA_LAUNCH(EPL_)                                                                                        \
+  FM_DISPATCH_T2(dtype, (e = wide ? launch_k(L, self_attn_kernel<T, EPL_, 2>, grid, dim3(32 * ((K + 1) / 2)),   \
+                                             smem, qkv, K, nh, qn, kn, eps, rope, max_pos, anchor_pos,          \
+                                             static_cast<T*>(out), ea, L.dev_err)                               \
+                                      : launch_k(L, self_attn_kernel<T, EPL_, 1>, grid, dim3(32 * K), smem, qkv, \
+                                                 K, nh, qn, kn, eps, rope, max_pos, anchor_pos,                 \
+                                                 static_cast<T*>(out), ea, L.dev_err)))
   if (hd == 32) {
-    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 1>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
+    FM_SA_LAUNCH(1);
   } else if (hd == 64) {
-    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 2>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
+    FM_SA_LAUNCH(2);
   } else {
-    FM_DISPATCH_T2(dtype, (e = launch_k(L, self_attn_kernel<T, 4>, grid, block, smem, qkv, K, nh, qn, kn, eps, rope,
-                                        max_pos, anchor_pos, static_cast<T*>(out), early ? 1 : 0, L.dev_err)));
+    FM_SA_LAUNCH(4);
   }
+#undef FM_SA_LAUNCH
   return e;
 }
 

@@ -181,7 +181,7 @@ cudaError_t xattn_combine(const Launch& L, int dtype, const XattnArgs& a, void* 
 // ------------------------------------------------------------------ sample.cu
 // keys: [rows] uint64 + counters [rows] uint32, zero before the first call; the
 // sampler leaves them zero again.
-int sample_splits(int Vd);
+int sample_splits(int Vd, int rows, int num_sms);
 // Sampler merge slots in a static device array (no allocation): rows <= kStaticSampleRows.
 constexpr int kStaticSampleRows = 8192;
 cudaError_t static_sample_scratch(void** out);

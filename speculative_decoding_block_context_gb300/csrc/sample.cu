@@ -202,14 +202,22 @@ cudaError_t static_sample_scratch(void** out) {
   return cudaSuccess;
 }
 
-int sample_splits(int Vd) { return std::max(1, std::min(32, (Vd + 2047) / 2048)); }
+// CTAs per row: up to one per 2048 draft-vocabulary entries, and no more than keep
+// about 16 CTAs per SM in all (a few rows are split widely; thousands of rows are not,
+// where one CTA per row already fills the GPU and the extra CTAs cost more to schedule
+// than they save).
+int sample_splits(int Vd, int rows, int num_sms) {
+  const int by_vocab = std::max(1, std::min(32, (Vd + 2047) / 2048));
+  const int by_grid = std::max(1, (16 * num_sms + rows - 1) / rows);
+  return std::min(by_vocab, by_grid);
+}
 
 cudaError_t sample_rows(const Launch& L, const float* logits, int rows, int Vd, int K, const float* temps,
                         const uint8_t* greedy, const uint64_t* seeds, const int32_t* anchor_pos, uint32_t step,
                         const int64_t* hot, int64_t* tokens, unsigned long long* keys, unsigned* counters) {
   if (rows <= 0) return cudaSuccess;
   const bool vec = Vd % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-  return launch_k(L, vec ? sample_kernel<true> : sample_kernel<false>, dim3(rows, sample_splits(Vd)), dim3(256), 0,
+  return launch_k(L, vec ? sample_kernel<true> : sample_kernel<false>, dim3(rows, sample_splits(Vd, rows, L.num_sms)), dim3(256), 0,
                   logits, Vd, K, temps, greedy, seeds, anchor_pos, step, hot, tokens, keys, counters);
 }
 
