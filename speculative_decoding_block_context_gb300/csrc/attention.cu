@@ -548,7 +548,13 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
   // candidate groups of NC blocks of one request (NC > 1): a.n_cand blocks per request
   const int ncand = NC > 1 ? a.n_cand : 1, groups = ncand / NC, nreq = a.bs / ncand;
   const int total = NC > 1 ? (chunks / ncand) * nh * groups : LDCG(a.plan);
-  for (int v = blockIdx.x; v < total; v += gridDim.x) {
+  // Items are handed out in order as CTAs free up (item lengths vary by orders of
+  // magnitude across a ragged batch): each CTA starts at its own index and claims its
+  // next one from the shared counter while it works on the current one.
+  __shared__ int s_next;
+  for (int v = blockIdx.x; v < total;) {
+    int claimed = 0;
+    if (a.next_item && threadIdx.x == 0) claimed = static_cast<int>(gridDim.x + atomicAdd(a.next_item, 1u));
     int h, b, c, gk[NC];  // head, this warp's block, chunk; every candidate's pair index
     if constexpr (NC == 1) {
       const int g = v / nh;
@@ -873,7 +879,9 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
         a.part_ml[pidx * 32 + 2 * q + 1] = L;
       }
     }
+    if (threadIdx.x == 0) s_next = a.next_item ? claimed : v + static_cast<int>(gridDim.x);
     __syncthreads();
+    v = s_next;
   }
 }
 
@@ -1172,6 +1180,7 @@ __global__ void __launch_bounds__(64) xattn_combine_kernel(XattnArgs a, T* __res
   pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
   const int nh = a.nh, D = nh * HD;
+  if (a.next_item && (b | h | blockIdx.z | t) == 0) *a.next_item = 0;  // for the next items launch
   if (t < 2) s_g[t] = LDCG(a.plan + 3 + b + t);  // the request's chunk range
   __syncthreads();
   const int g0 = s_g[0], nc = min(s_g[1] - g0, kMaxChunksPerRequest);
@@ -1236,6 +1245,7 @@ __global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* 
     g1 = LDCG(a.plan + 4 + b);
   }
   pdl_wait();
+  if (a.next_item && (b | h | qi | d) == 0) *a.next_item = 0;  // for the next items launch
   if (!a.early) {
     g0 = LDCG(a.plan + 3 + b);
     g1 = LDCG(a.plan + 4 + b);

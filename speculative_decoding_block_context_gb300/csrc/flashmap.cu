@@ -112,6 +112,10 @@ struct flashmap_model {
 #ifndef FM_XATTN_EARLY
 #define FM_XATTN_EARLY 1
 #endif
+// Cross-attention items handed out through a counter (1) or by fixed stride (0).
+#ifndef FM_XATTN_DYNAMIC
+#define FM_XATTN_DYNAMIC 1
+#endif
 
 namespace {
 // Records an event pair around one launch while profiling is on.
@@ -241,6 +245,7 @@ struct DraftWs {
   void* xbuf = nullptr;
   int* plan;
   float *part_o, *part_ml;
+  unsigned* xnext;  // the cross-attention items kernel's work counter
   size_t bytes;
 };
 
@@ -271,6 +276,7 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   const size_t chunks = fm::xattn_max_chunks(m->num_sms, m->nh, bs);
   w.part_o = c.take<float>(chunks * m->nh * 16 * m->hd * 4);
   w.part_ml = c.take<float>(chunks * m->nh * 32 * 4);
+  w.xnext = c.take<unsigned>(4);
   w.bytes = align_up(c.off);
   return w;
 }
@@ -867,6 +873,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     z.add(ws.acc_d, static_cast<int64_t>(R) * D);
     z.add(ws.acc_a, static_cast<int64_t>(bs) * D);
     z.add(ws.acc_kv, static_cast<int64_t>(bs) * 2 * m->L * D);
+    z.add(reinterpret_cast<float*>(ws.xnext), 1);  // zero bits
     if (m->steps > 1) {
       z.add(ws.emb, 2LL * R * H);
       z.add(ws.logits_full, static_cast<int64_t>(R) * m->V);
@@ -970,6 +977,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   // caller's anchor positions, or a multi-candidate draft's per-block copies once the
   // anchor branch has joined.)
   xa.early = FM_XATTN_EARLY && fork ? 1 : 0;
+  xa.next_item = FM_XATTN_DYNAMIC ? ws.xnext : nullptr;
   // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
   auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
     for (int l = 0; l < m->L; ++l) {

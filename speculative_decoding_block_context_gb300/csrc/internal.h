@@ -36,13 +36,14 @@ cudaError_t launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
-// Zeroes up to 8 float32 ranges in one launch (accumulators a call sums into).
+// Zeroes up to kZeroRanges float32 ranges in one launch (accumulators a call sums into).
 struct ZeroList {
-  float* ptr[8];
-  int64_t n[8];
+  static constexpr int kZeroRanges = 12;
+  float* ptr[kZeroRanges];
+  int64_t n[kZeroRanges];
   int count = 0;
   void add(float* p, int64_t len) {
-    if (len > 0) {
+    if (len > 0 && count < kZeroRanges) {
       ptr[count] = p;
       n[count] = len;
       ++count;
@@ -163,6 +164,9 @@ struct XattnArgs {
   // start (only the queries come from the kernel just before it), so its first K/V
   // blocks are requested before it waits for that kernel
   int early = 0;
+  // zeroed counter of the items handed out beyond each CTA's first (the cp.async items
+  // kernel); the combine that follows zeroes it again. Null: items by fixed stride.
+  unsigned* next_item = nullptr;
   unsigned* dev_err = nullptr;
 };
 cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
