@@ -950,7 +950,10 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
   uint32_t jt = 0;      // blocks this warp has issued (and consumed), over all its items
   uint32_t okm = 0;     // bit st: the block in stage st comes from a valid page
   const uint64_t pol = l2_policy_evict_first();  // keys and values are read once
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  // items from the work counter after each CTA's first, as in the cp.async kernel (the
+  // claim follows the dependency wait: the counter is zeroed by the previous combine)
+  __shared__ int s_next;
+  for (int item = blockIdx.x; item < items;) {
     const int g = item / nh, h = item - g * nh;
     const int b = LDCG(pairs + 2 * g), c = LDCG(pairs + 2 * g + 1);
     const int n = LDCG(a.anchor_pos + b) + 1;
@@ -1002,6 +1005,8 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
       pdl_wait();
       waited = true;
     }
+    int claimed = 0;
+    if (a.next_item && threadIdx.x == 0) claimed = static_cast<int>(gridDim.x + atomicAdd(a.next_item, 1u));
     // Q (normed, rotated, rounded to bf16) as A fragments; rows >= K are zero
     float* sq = reinterpret_cast<float*>(xsm + C::SQ_OFF);
     load_queries<HD>(a, b, h, sq, n - 1);  // n - 1: the anchor position, read above
@@ -1158,8 +1163,10 @@ __global__ void __launch_bounds__(128, 2) xattn_items_tma_kernel(const __grid_co
         a.part_ml[pidx * 32 + 2 * q + 1] = L;
       }
     }
+    if (threadIdx.x == 0) s_next = a.next_item ? claimed : item + static_cast<int>(gridDim.x);
     __syncthreads();
     if (abort_flag) break;  // the same value in every warp after the barrier
+    item = s_next;
   }
   if (!waited) pdl_wait();  // no item: the grid still completes after the kernel before
 }

@@ -977,7 +977,8 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   // caller's anchor positions, or a multi-candidate draft's per-block copies once the
   // anchor branch has joined.)
   xa.early = FM_XATTN_EARLY && fork ? 1 : 0;
-  xa.next_item = FM_XATTN_DYNAMIC ? ws.xnext : nullptr;
+  // (one block: every item is the same length, and a fixed stride needs no counter)
+  xa.next_item = FM_XATTN_DYNAMIC && bsc > 1 ? ws.xnext : nullptr;
   // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
   auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
     for (int l = 0; l < m->L; ++l) {

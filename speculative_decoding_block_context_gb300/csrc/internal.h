@@ -164,8 +164,8 @@ struct XattnArgs {
   // start (only the queries come from the kernel just before it), so its first K/V
   // blocks are requested before it waits for that kernel
   int early = 0;
-  // zeroed counter of the items handed out beyond each CTA's first (the cp.async items
-  // kernel); the combine that follows zeroes it again. Null: items by fixed stride.
+  // zeroed counter of the items handed out beyond each CTA's first (both items
+  // kernels); the combine that follows zeroes it again. Null: items by fixed stride.
   unsigned* next_item = nullptr;
   unsigned* dev_err = nullptr;
 };
