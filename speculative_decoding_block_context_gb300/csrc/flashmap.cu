@@ -281,13 +281,25 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   return w;
 }
 
+// A verify-window write of at least this many columns projects only the committed
+// ones (compacted on the device); smaller ones project every column and skip the
+// uncommitted ones at the scatter.
+#ifndef FM_WRITE_COMPACT_MIN_ROWS
+#define FM_WRITE_COMPACT_MIN_ROWS 48
+#endif
 struct WriteWs {
   float *acc_fc, *acc_kv;
   void* ctx;
+  void* xc = nullptr;           // the committed rows of the target hidden states
+  int32_t* row_src = nullptr;   // their window rows
+  int* rows_dev = nullptr;      // their count
 };
+// The compacted write needs the tcgen05 GEMMs (device row counts).
+bool write_can_compact(const flashmap_model* m) { return m->wdt != FLASHMAP_F32; }
 size_t write_row_bytes(const flashmap_model* m) {
+  const size_t xrow = static_cast<size_t>(m->Lt) * m->H * dt_size(m->adt);
   return static_cast<size_t>(m->D) * 4 + static_cast<size_t>(m->D) * dt_size(m->adt) +
-         static_cast<size_t>(2) * m->L * m->D * 4;
+         static_cast<size_t>(2) * m->L * m->D * 4 + (write_can_compact(m) ? xrow + 4 : 0);
 }
 WriteWs carve_write(const flashmap_model* m, int rows, void* base, size_t* bytes) {
   Carver c(base);
@@ -295,6 +307,11 @@ WriteWs carve_write(const flashmap_model* m, int rows, void* base, size_t* bytes
   w.acc_fc = c.take<float>(static_cast<size_t>(rows) * m->D * 4);
   w.ctx = c.take<void>(static_cast<size_t>(rows) * m->D * dt_size(m->adt));
   w.acc_kv = c.take<float>(static_cast<size_t>(rows) * 2 * m->L * m->D * 4);
+  if (write_can_compact(m)) {
+    w.xc = c.take<void>(static_cast<size_t>(rows) * m->Lt * m->H * dt_size(m->adt));
+    w.row_src = c.take<int32_t>(static_cast<size_t>(rows) * 4);
+    w.rows_dev = c.take<int>(4);
+  }
   *bytes = align_up(c.off);
   return w;
 }
@@ -806,11 +823,25 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     z.add(ws.acc_kv, static_cast<int64_t>(rows) * 2 * m->L * m->D);
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
     const void* x = static_cast<const uint8_t*>(target_hidden) + r0 * xrow;
+    // A large window projects only its committed columns: their rows are gathered in
+    // order and counted on the device, and every kernel below takes that count
+    // (uncommitted columns get out_loc -1 here).
+    const bool compact = commit_lens && write_can_compact(m) && rows >= FM_WRITE_COMPACT_MIN_ROWS;
+    const int* rows_dev = nullptr;
+    if (compact) {
+      TIMED(FLASHMAP_KIND_ROWS, -1, fm::window_compact(Lh, commit_lens, W, r0, rows, ws.row_src, ws.rows_dev, out_loc));
+      TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_window_rows(Lh, target_hidden, static_cast<int64_t>(xrow), ws.row_src,
+                                                           ws.rows_dev, rows, ws.xc));
+      x = ws.xc;
+      rows_dev = ws.rows_dev;
+    }
     // ctx = RMSNorm_hidden(fc(x)); kv = W_ctx ctx
-    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr, true));
+    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr, true,
+                                           rows_dev));
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, m->adt, ws.acc_fc, rows, m->D, m->hidden_norm_w, m->cfg.rms_norm_eps,
-                                               1.f, nullptr, 0.f, ws.ctx, m->D));
-    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr, nullptr, true));
+                                               1.f, nullptr, 0.f, ws.ctx, m->D, rows_dev));
+    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr,
+                                               nullptr, true, rows_dev));
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
     a.ld = 2LL * m->L * m->D;
@@ -833,6 +864,10 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     a.max_pos = m->maxpos;
     a.pool = pool->base;
     a.out_loc = out_loc;
+    if (compact) {
+      a.row_src = ws.row_src;
+      a.rows_dev = rows_dev;
+    }
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(Lh, m->kdt, a));
   }
   return FLASHMAP_OK;

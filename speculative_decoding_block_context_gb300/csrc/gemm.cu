@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                      float* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
                      const float* __restrict__ beta, const float* __restrict__ wscale, int out_zeroed,
-                     unsigned* dev_err) {
+                     const int* __restrict__ rows_dev, unsigned* dev_err) {
   using C = TcCfg<BN, F8>;
   extern __shared__ uint8_t smem_raw[];
   // full: TMA bytes landed; conv (e4m3 only): the bf16 weight tile is written;
@@ -88,12 +88,20 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
   uint8_t* smem = smem_raw + (base - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // rows_dev: the activation rows are counted on the device by the kernel before this
+  // one (at most R; the partition below follows the count, so no weight is streamed
+  // for absent rows and none is requested before the wait)
+  if (rows_dev) {
+    pdl_wait();
+    R = min(R, LDCG(rows_dev));
+  }
   // tiles are numbered weight tile fastest (tile = r * mt + m): the CTAs running at the
   // same time hold neighbouring ranges, so the row tiles that need one weight tile ask
   // for it together and DRAM serves it once
   const int mt = (N + 127) >> 7, rt = (R + BN - 1) / BN, KB = (K + 63) >> 6;
   const int64_t T = static_cast<int64_t>(mt) * rt * KB;
   const int64_t it0 = T * blockIdx.x / gridDim.x, it1 = T * (blockIdx.x + 1) / gridDim.x;
+  if (it0 == it1) return;  // fewer units than CTAs (a device row count below the launch's)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -435,7 +443,7 @@ EncodeTiledFn encode_fn() {
 
 template <int BN, bool F8>
 cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, float* out, int ldo,
-                      const float* alpha, const float* beta, bool zeroed) {
+                      const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
   using C = TcCfg<BN, F8>;
   CUtensorMap mapX;
   std::string err;
@@ -445,17 +453,17 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   const int per_sm = L.ctas_per_sm > 0 ? std::min(L.ctas_per_sm, C::PER_SM) : C::PER_SM;
   const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * per_sm));
   return launch_k(L, tc_linear_kernel<BN, F8>, dim3(G), dim3(C::THREADS), C::SMEM, W.map, mapX, out, ldo, R, W.N,
-                  W.K, alpha, beta, W.wscale, zeroed ? 1 : 0, L.dev_err);
+                  W.K, alpha, beta, W.wscale, zeroed ? 1 : 0, rows_dev, L.dev_err);
 }
 
 template <bool F8>
 cudaError_t launch_tc_rows(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                           const float* alpha, const float* beta, bool zeroed) {
-  if (rows <= 16) return launch_tc<16, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-  if (rows <= 32) return launch_tc<32, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-  if (rows <= 64) return launch_tc<64, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-  if (rows <= 128) return launch_tc<128, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
-  return launch_tc<256, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+                           const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
+  if (rows <= 16) return launch_tc<16, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+  if (rows <= 32) return launch_tc<32, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+  if (rows <= 64) return launch_tc<64, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+  if (rows <= 128) return launch_tc<128, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+  return launch_tc<256, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
 }
 
 template <int BN, bool F8>
@@ -531,16 +539,17 @@ bool make_tmap_e4m3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
 }
 
 cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta, bool zeroed) {
+                   const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
   if (rows <= 0 || W.N <= 0) return cudaSuccess;
   if (W.dtype == FLASHMAP_BF16) {
     if (!W.has_map) return cudaErrorInvalidValue;
-    return launch_tc_rows<false>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    return launch_tc_rows<false>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
   }
   if (W.dtype == FLASHMAP_E4M3) {  // e4m3 weights, bf16 activations
     if (!W.has_map || !W.wscale) return cudaErrorInvalidValue;
-    return launch_tc_rows<true>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed);
+    return launch_tc_rows<true>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
   }
+  if (rows_dev) return cudaErrorInvalidValue;  // device row counts: tcgen05 weights only
   if (W.dtype == FLASHMAP_F32) {
     const int64_t threads = static_cast<int64_t>(W.N) * 32;
     const int blocks = static_cast<int>((threads + 255) / 256);

@@ -77,8 +77,10 @@ cudaError_t gemm_prepare();
 // accumulated with float reductions (the output must hold its initial value, e.g. 0,
 // or the residual stream); zeroed = the output is known to be zero, so tiles one CTA
 // covers entirely may be stored instead. alpha / beta may be null (1 / 0). x has W.dtype.
+// rows_dev (tcgen05 weights only): the rows actually present, counted on the device,
+// at most `rows` (the launch is sized for `rows`).
 cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta, bool zeroed);
+                   const float* alpha, const float* beta, bool zeroed, const int* rows_dev = nullptr);
 
 // General strided SIMT GEMM for load-time work, float32 accumulation:
 // C(m, n) = sum_k A(m, k) B(k, n), A(m, k) = a[arow(m) * sam + k * sak] with
@@ -112,13 +114,28 @@ struct KvWriteArgs {
   int max_pos = 0;
   void* pool = nullptr;
   int64_t* out_loc = nullptr;
+  // compacted rows (window_compact): local row i is global row row_src[i], for
+  // i < *rows_dev (null: every local row, global row row0 + i)
+  const int32_t* row_src = nullptr;
+  const int* rows_dev = nullptr;
   unsigned* dev_err = nullptr;
 };
 cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a);
+// The committed columns of window rows [r0, r0 + rows) (global row g is column g % W of
+// request g / W, committed when the column is below commit_lens[g / W]), in order:
+// row_src[k] = the k-th one's global row, *rows_dev = their count; out_loc[g] = -1 for
+// the others (out_loc may be null). One CTA.
+cudaError_t window_compact(const Launch& L, const int32_t* commit_lens, int W, int64_t r0, int rows,
+                           int32_t* row_src, int* rows_dev, int64_t* out_loc);
+// xc[k] = x[row_src[k]] for k < *rows_dev; rows of row_bytes bytes (a multiple of 16,
+// 16-byte aligned). One CTA per row of the largest count.
+cudaError_t gather_window_rows(const Launch& L, const void* x, int64_t row_bytes, const int32_t* row_src,
+                               const int* rows_dev, int max_rows, void* xc);
 cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
                         const float* mh, float eps, void* out);
 cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
-                     float prescale, const float* add, float gate, void* out, int ldo);
+                     float prescale, const float* add, float gate, void* out, int ldo,
+                     const int* rows_dev = nullptr);  // rows_dev: only rows below *rows_dev
 cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* out);
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out);

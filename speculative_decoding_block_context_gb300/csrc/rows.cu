@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(1024, 2) kv_write_kernel(KvWriteArgs a) {
   pdl_trigger();
   pdl_wait();
   const int il = blockIdx.x, l = blockIdx.y;
-  const int64_t i = a.row0 + il;
+  if (a.rows_dev && il >= LDCG(a.rows_dev)) return;  // past the compacted rows (CTA-uniform)
+  const int64_t i = a.row_src ? static_cast<int64_t>(LDCG(a.row_src + il)) : a.row0 + il;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int D = a.nh * HD;
   const float* row = a.acc + static_cast<int64_t>(il) * a.ld + static_cast<int64_t>(l) * 2 * D;
@@ -252,7 +253,8 @@ template <typename T, int NV>
 __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict__ acc, int width,
                                                                const float* __restrict__ w, float eps,
                                                                float prescale, const float* __restrict__ add,
-                                                               float gate, T* __restrict__ out, int ldo) {
+                                                               float gate, T* __restrict__ out, int ldo,
+                                                               const int* __restrict__ rows_dev) {
   __shared__ float red[32];
   pdl_trigger();
   const int w4 = width >> 2;
@@ -260,6 +262,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict
   load_row4<NV, false>(w, w4, wv);
   if (add) load_row4<NV, false>(add, w4, av);
   pdl_wait();
+  if (rows_dev && static_cast<int>(blockIdx.x) >= LDCG(rows_dev)) return;  // CTA-uniform
   float* ar = acc + static_cast<int64_t>(blockIdx.x) * width;
   load_row4<NV, true>(ar, w4, v);
   float s = 0.f;
@@ -285,6 +288,57 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict
       reinterpret_cast<float4*>(ar)[f] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+}
+
+// The committed columns of a verify-window chunk, in order (sglang/model.py,
+// write_target_hidden_kv: only committed columns are written): an exclusive scan of
+// the keep flags, 1024 rows at a time.
+__global__ void __launch_bounds__(1024) window_compact_kernel(const int32_t* __restrict__ commit_lens, int W,
+                                                              int64_t r0, int rows, int32_t* __restrict__ row_src,
+                                                              int* __restrict__ rows_dev,
+                                                              int64_t* __restrict__ out_loc) {
+  __shared__ int scan[1024];
+  __shared__ int carry;
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < rows; base += 1024) {
+    const int t = base + static_cast<int>(threadIdx.x);
+    const int64_t g = r0 + t;
+    int keep = 0;
+    if (t < rows) {
+      const int64_t b = g / W;
+      keep = g - b * W < LDCG(commit_lens + b) ? 1 : 0;
+      if (!keep && out_loc) out_loc[g] = -1;
+    }
+    scan[threadIdx.x] = keep;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int x = threadIdx.x >= static_cast<unsigned>(off) ? scan[threadIdx.x - off] : 0;
+      __syncthreads();
+      scan[threadIdx.x] += x;
+      __syncthreads();
+    }
+    if (keep) row_src[carry + scan[threadIdx.x] - 1] = static_cast<int32_t>(g);
+    __syncthreads();
+    if (threadIdx.x == 1023) carry += scan[1023];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *rows_dev = carry;
+}
+
+__global__ void __launch_bounds__(256) gather_window_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
+                                                                 const int32_t* __restrict__ row_src,
+                                                                 const int* __restrict__ rows_dev,
+                                                                 uint8_t* __restrict__ xc) {
+  pdl_trigger();
+  pdl_wait();
+  const int k = blockIdx.x;
+  if (k >= LDCG(rows_dev)) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(LDCG(row_src + k)) * row_bytes);
+  uint4* dst = reinterpret_cast<uint4*>(xc + static_cast<int64_t>(k) * row_bytes);
+  for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst[i] = src[i];
 }
 
 template <typename T>
@@ -451,6 +505,22 @@ cudaError_t zero_ranges(const Launch& L, const ZeroList& z) {
     }                                             \
   } while (0)
 
+cudaError_t window_compact(const Launch& L, const int32_t* commit_lens, int W, int64_t r0, int rows,
+                           int32_t* row_src, int* rows_dev, int64_t* out_loc) {
+  if (rows <= 0 || W <= 0) return cudaSuccess;
+  return launch_k(L, window_compact_kernel, dim3(1), dim3(1024), 0, commit_lens, W, r0, rows, row_src, rows_dev,
+                  out_loc);
+}
+
+cudaError_t gather_window_rows(const Launch& L, const void* x, int64_t row_bytes, const int32_t* row_src,
+                               const int* rows_dev, int max_rows, void* xc) {
+  if (max_rows <= 0) return cudaSuccess;
+  if ((row_bytes & 15) || (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(xc) & 15))
+    return cudaErrorInvalidValue;
+  return launch_k(L, gather_window_rows_kernel, dim3(max_rows), dim3(256), 0, static_cast<const uint8_t*>(x),
+                  row_bytes, row_src, rows_dev, static_cast<uint8_t*>(xc));
+}
+
 cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a) {
   if (a.rows <= 0) return cudaSuccess;
   KvWriteArgs b = a;
@@ -499,12 +569,12 @@ cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, in
 }
 
 cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
-                     float prescale, const float* add, float gate, void* out, int ldo) {
+                     float prescale, const float* add, float gate, void* out, int ldo, const int* rows_dev) {
   if (rows <= 0) return cudaSuccess;
   cudaError_t e = cudaSuccess;
   FM_DISPATCH_T(dtype, FM_DISPATCH_NV(width, (e = launch_k(L, rms_rows_kernel<T, NV>, dim3(rows), dim3(kRowThreads),
                                                           0, acc, width, w, eps, prescale, add, gate,
-                                                          static_cast<T*>(out), ldo))));
+                                                          static_cast<T*>(out), ldo, rows_dev))));
   return e;
 }
 
