@@ -223,7 +223,9 @@ flashmap_status flashmap_workspace_size(const flashmap_model* model, int32_t max
  *   commit_lens    (device) int32 [bs] in [0, W], or NULL
  *   req_to_page    (device) int32 [rows][req_to_page_stride]
  *   out_loc        (device) int64 [bs][W]: the slot written, -1 if skipped; or NULL
- * Rows are processed in chunks of max_write_rows (flashmap_workspace_size).
+ * Rows are processed in chunks of max_write_rows (flashmap_workspace_size). A chunk of
+ * 48 or more rows with commit_lens (bf16 or e4m3 GEMM weights) projects only its
+ * committed columns, listed and counted on the device; the results are the same.
  */
 flashmap_status flashmap_write_context_kv(flashmap_model* model, const flashmap_kv_pool* pool,
                                           const void* target_hidden, int32_t bs, int32_t W,
