@@ -28,7 +28,7 @@ Sources (each function cites the page and the section it follows):
   * Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
     as 1, 2, 3" (SC'11), section 3 (the Philox round and key schedule).
 
-Readings where the pages are silent (listed with their reasons in the design doc):
+Readings where the pages are silent (each the plainest one the rest of the pages support):
   R1 the noise of slot k of request b is keyed by (seed_b, position p_b+1+k);
   R2 Philox4x32-10 with key (seed lo32, seed hi32); counter (j/4, position,
      domain, step) with domain 0 = DiT noise (step 0), 1 = Gumbel noise;
