@@ -345,8 +345,21 @@ template <typename T>
 __global__ void gelu_kernel(float* __restrict__ acc, int64_t n, T* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  // four elements per thread and step (16-byte loads and clears) over the whole groups
+  const bool aligned = !(reinterpret_cast<uintptr_t>(acc) & 15) && !(reinterpret_cast<uintptr_t>(out) & (4 * sizeof(T) - 1));
+  const int64_t n4 = aligned ? n >> 2 : 0;
+  for (int64_t i = t0; i < n4; i += stride) {
+    const float4 x = LDCG(reinterpret_cast<const float4*>(acc) + i);
+    const float g[4] = {0.5f * x.x * (1.f + erff(x.x * 0.70710678118654752f)),
+                        0.5f * x.y * (1.f + erff(x.y * 0.70710678118654752f)),
+                        0.5f * x.z * (1.f + erff(x.z * 0.70710678118654752f)),
+                        0.5f * x.w * (1.f + erff(x.w * 0.70710678118654752f))};
+    store_vec<T, 4>(out + 4 * i, g);
+    reinterpret_cast<float4*>(acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int64_t i = 4 * n4 + t0; i < n; i += stride) {
     const float x = LDCG(acc + i);
     out[i] = from_f32<T>(0.5f * x * (1.f + erff(x * 0.70710678118654752f)));
     acc[i] = 0.f;
