@@ -60,9 +60,16 @@ Pinning (what fixes each function other than itself; see tests/test_oracle_pins.
                          Q^T Q = I; ascending; the sign rule
   folded_noise           the fold identity against the unfolded rms_norm / x_embed;
                          cov of z diag(sqrt lam) Q^T against E^T E
-  draft_request          parity unpinned beyond the composition of the pinned
-                         parts plus structural cases (zero gates, one-position
-                         context, seed independence at noise_scale 0)
+  adaln / time_cond     distinct bias chunks come back as (1 + scale, shift, gate)
+                         per norm and branch; time_embed reads s, jump_embed t
+  dit_layer              each branch isolated by zero gates against scipy z-score /
+                         norm.cdf and the pinned primitives (MLP scale/shift/gate,
+                         cross-attention over one position, uniform non-causal
+                         self-attention); slot permutation equivariance
+  draft_request          slots at anchor + 1 + k (constant-query case); invariance
+                         to shifting every position at noise_scale 0; zero gates
+                         give the plain LayerNorm of the embedding
+  quantize_query_e4m3    a hand-worked per-head case (ties, the 1e-12 floor)
 """
 
 from __future__ import annotations

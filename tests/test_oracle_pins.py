@@ -655,3 +655,258 @@ def test_folded_noise_law_matches_embedding_covariance():
     assert np.linalg.norm(y.T @ y / N - G) / np.linalg.norm(G) < 0.05
     wrong = (z * np.sqrt(lam)) @ Q
     assert np.linalg.norm(wrong.T @ wrong / N - G) / np.linalg.norm(G) > 0.2
+
+
+# --------------------------------------------------------------------- DiT wiring
+#
+# modeling_flashmap.py, FlashMapAdaLayerNorm.modulation / forward, FlashMapLayer.forward,
+# FlashMapDraftModel.time_conditioning and draft fix which modulation chunk is the scale,
+# the shift and the gate, which branch each AdaLN feeds, that time_embed reads the jump's
+# start s and jump_embed its end t, and where the block's slots sit (anchor + 1 + k).
+# Every expected value below is built from scipy routines or from the pinned primitives
+# (rms_norm, apply_rope, attention, time_embedding); a swapped chunk, branch, time or
+# position fails one of them.
+
+
+def _zero_adaln(W, cfg, biases):
+    """Zero every AdaLN weight and set its bias: biases[name] = (scale, shift, gate)
+    vectors (missing names: all zero). Returns the modified copy of W."""
+    W = dict(W)
+    D = cfg.hidden
+    names = [f"layers.{l}.{n}" for l in range(cfg.num_layers)
+             for n in ("self_attn_adaln", "cross_attn_adaln", "mlp_adaln")] + ["final_adaln"]
+    for n in names:
+        W[f"{n}.linear.weight"] = np.zeros((3 * D, cfg.cond_dim))
+        sc, sh, g = biases.get(n, (np.zeros(D), np.zeros(D), np.zeros(D)))
+        W[f"{n}.linear.bias"] = np.concatenate([sc, sh, g])
+    return W
+
+
+def test_adaln_chunks_are_scale_shift_gate():
+    """FlashMapAdaLayerNorm.modulation returns (scale, shift, gate), used as
+    norm(x) * (1 + scale) + shift with gate on the residual: zero weights and distinct
+    bias chunks must come back as (1 + b_scale, b_shift, b_gate) per norm, in the
+    order (self-attention, cross-attention, MLP), and (1 + b_scale, b_shift) for the
+    final norm."""
+    cfg, W, E, LM, rank = _tiny()
+    rng = np.random.default_rng(40)
+    D = cfg.hidden
+    biases = {}
+    for l in range(cfg.num_layers):
+        for j, n in enumerate(("self_attn_adaln", "cross_attn_adaln", "mlp_adaln")):
+            biases[f"layers.{l}.{n}"] = tuple(rng.standard_normal(D) + 10 * (9 * l + 3 * j + c) for c in range(3))
+    biases["final_adaln"] = tuple(rng.standard_normal(D) - 10 * (c + 1) for c in range(3))
+    W = _zero_adaln(W, cfg, biases)
+    mods, final, _ = ref.jump_conditioning(cfg, W, 0.0, 1.0)
+    for l in range(cfg.num_layers):
+        for j, n in enumerate(("self_attn_adaln", "cross_attn_adaln", "mlp_adaln")):
+            sc, sh, g = biases[f"layers.{l}.{n}"]
+            np.testing.assert_array_equal(mods[l, 3 * j + 0], 1.0 + sc)
+            np.testing.assert_array_equal(mods[l, 3 * j + 1], sh)
+            np.testing.assert_array_equal(mods[l, 3 * j + 2], g)
+    sc, sh, _ = biases["final_adaln"]
+    np.testing.assert_array_equal(final[0], 1.0 + sc)
+    np.testing.assert_array_equal(final[1], sh)
+
+
+def _te(W, name, t, cfg):
+    return ref.time_embedding(t, W[f"{name}.linear_1.weight"], W[f"{name}.linear_1.bias"],
+                              W[f"{name}.linear_2.weight"], W[f"{name}.linear_2.bias"],
+                              cfg.time_embed_dim, cfg.time_scale)
+
+
+@pytest.mark.parametrize("s,t", [(0.0, 1.0), (0.8172569274902344, 1.0), (0.7906050682067871, 0.8172569274902344)])
+def test_time_conditioning_reads_s_in_time_embed_and_t_in_jump_embed(s, t):
+    """time_conditioning: cond = time_embed(s) + jump_embed(t). With time_embed's
+    output layer zeroed, cond is jump_embed at t (not at s); with jump_embed's zeroed,
+    time_embed at s (not at t)."""
+    cfg, W, E, LM, rank = _tiny()
+    H1 = cfg.cond_dim
+    zero_te = dict(W, **{"time_embed.linear_2.weight": np.zeros((H1, H1)), "time_embed.linear_2.bias": np.zeros(H1)})
+    _, _, cond = ref.jump_conditioning(cfg, zero_te, s, t)
+    np.testing.assert_allclose(cond, _te(W, "jump_embed", t, cfg), rtol=1e-13, atol=1e-15)
+    assert np.max(np.abs(cond - _te(W, "jump_embed", s, cfg))) > 1e-3  # the test can tell s from t
+    zero_je = dict(W, **{"jump_embed.linear_2.weight": np.zeros((H1, H1)), "jump_embed.linear_2.bias": np.zeros(H1)})
+    _, _, cond = ref.jump_conditioning(cfg, zero_je, s, t)
+    np.testing.assert_allclose(cond, _te(W, "time_embed", s, cfg), rtol=1e-13, atol=1e-15)
+    assert np.max(np.abs(cond - _te(W, "time_embed", t, cfg))) > 1e-3
+
+
+def _layer_case(seed, **over):
+    """The tiny model with one DiT layer and layer_norm_eps 0 (so that LayerNorm is
+    scipy's z-score), a block x of K slots and a random rotated context."""
+    cfg, W, E, LM, rank = _tiny(num_layers=1, layer_norm_eps=0.0, **over)
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((cfg.block_size, cfg.hidden)) * 2 + 0.5
+    return cfg, W, rng, x
+
+
+def _mods_from(W, cfg):
+    return ref.jump_conditioning(cfg, W, 0.0, 1.0)[0][0]
+
+
+def test_mlp_branch_wiring():
+    """FlashMapLayer.forward's last branch with the two attention gates zero:
+    x + gate * fc2(gelu(fc1(z(x) * (1 + scale) + shift))). fc1 = [I; 0] and
+    fc2 = [I, 0] with zero biases make the MLP gelu(h) = h * Phi(h) (scipy), so a
+    swapped scale/shift, a missing (1 + .) or a gate on the wrong chunk fails."""
+    cfg, W, rng, x = _layer_case(41)
+    D, F = cfg.hidden, cfg.intermediate
+    sc, sh, g = rng.standard_normal(D) * 0.5, rng.standard_normal(D), rng.standard_normal(D)
+    W = _zero_adaln(W, cfg, {"layers.0.mlp_adaln": (sc, sh, g)})  # attention gates 0
+    W["layers.0.mlp.fc1.weight"] = np.eye(F, D)
+    W["layers.0.mlp.fc1.bias"] = np.zeros(F)
+    W["layers.0.mlp.fc2.weight"] = np.eye(D, F)
+    W["layers.0.mlp.fc2.bias"] = np.zeros(D)
+    p = 6
+    ctx = [(rng.standard_normal((p + 1, cfg.num_heads, cfg.head_dim)),) * 2]
+    out = ref.dit_layer(cfg, W, 0, _mods_from(W, cfg), x, p + 1 + np.arange(cfg.block_size), ctx)
+    h = st.zscore(x, axis=-1) * (1.0 + sc) + sh
+    np.testing.assert_allclose(out, x + g * (h * st.norm.cdf(h)), rtol=1e-11, atol=1e-12)
+
+
+def test_cross_attention_wiring_one_position_context():
+    """With every gate but the cross-attention's zero and a context of one position,
+    the layer adds gate * (v W_o^T) to every slot whatever its query: the softmax over
+    one key is 1 (FlashMapLayer.forward, FlashMapAttention.forward)."""
+    cfg, W, rng, x = _layer_case(42)
+    D = cfg.hidden
+    g = rng.standard_normal(D)
+    W = _zero_adaln(W, cfg, {"layers.0.cross_attn_adaln": (rng.standard_normal(D), rng.standard_normal(D), g)})
+    k1 = rng.standard_normal((1, cfg.num_heads, cfg.head_dim))
+    v1 = rng.standard_normal((1, cfg.num_heads, cfg.head_dim))
+    out = ref.dit_layer(cfg, W, 0, _mods_from(W, cfg), x, 1 + np.arange(cfg.block_size), [(k1, v1)])
+    want = x + g * (v1.reshape(1, D) @ np.asarray(W["layers.0.cross_attn.o_proj.weight"], np.float64).T)
+    np.testing.assert_allclose(out, want, rtol=1e-12, atol=1e-12)
+
+
+def test_self_attention_wiring_uniform_scores_average_the_whole_block():
+    """With q_proj = 0 the normed queries are 0, every score is 0 and the attention
+    averages the values of all K slots of the block, the later ones included (the
+    block attends non-causally). Only the self-attention gate is nonzero: the layer
+    adds gate * mean_k(v_k) W_o^T, v = W_v (z(x) * (1 + scale) + shift); a causal mask
+    (prefix means) or the shift/scale swapped fails."""
+    cfg, W, rng, x = _layer_case(43)
+    D = cfg.hidden
+    sc, sh, g = rng.standard_normal(D) * 0.5, rng.standard_normal(D), rng.standard_normal(D)
+    W = _zero_adaln(W, cfg, {"layers.0.self_attn_adaln": (sc, sh, g)})
+    W["layers.0.self_attn.q_proj.weight"] = np.zeros((D, D))
+    p = 3
+    ctx = [(rng.standard_normal((p + 1, cfg.num_heads, cfg.head_dim)),) * 2]
+    out = ref.dit_layer(cfg, W, 0, _mods_from(W, cfg), x, p + 1 + np.arange(cfg.block_size), ctx)
+    h = st.zscore(x, axis=-1) * (1.0 + sc) + sh
+    v = h @ np.asarray(W["layers.0.self_attn.v_proj.weight"], np.float64).T
+    o = np.asarray(W["layers.0.self_attn.o_proj.weight"], np.float64)
+    want = x + g * (v.mean(axis=0, keepdims=True) @ o.T)
+    np.testing.assert_allclose(out, want, rtol=1e-11, atol=1e-12)
+
+
+def test_layer_is_equivariant_to_permuting_slots_with_their_positions():
+    """Non-causal self-attention and row-wise everything else: permuting a request's
+    slots together with their positions permutes the layer's output rows (all weights
+    random, every gate nonzero). A causal mask or a position taken from the row index
+    instead of the given position fails."""
+    cfg, W, rng, x = _layer_case(44)
+    p = 9
+    pos = p + 1 + np.arange(cfg.block_size)
+    kc = rng.standard_normal((p + 1, cfg.num_heads, cfg.head_dim))
+    vc = rng.standard_normal((p + 1, cfg.num_heads, cfg.head_dim))
+    mods = _mods_from(W, cfg)
+    out = ref.dit_layer(cfg, W, 0, mods, x, pos, [(kc, vc)])
+    perm = np.array([2, 0, 3, 1])
+    out_p = ref.dit_layer(cfg, W, 0, mods, x[perm], pos[perm], [(kc, vc)])
+    np.testing.assert_allclose(out_p, out[perm], rtol=1e-12, atol=1e-12)
+    # a permutation of the rows that keeps the positions in place changes the result
+    out_q = ref.dit_layer(cfg, W, 0, mods, x[perm], pos, [(kc, vc)])
+    assert np.max(np.abs(out_q - out[perm])) > 1e-4
+
+
+def _context_at(cfg, W, E, hid, anchor, start):
+    """Every layer's rotated context for target hidden states at positions start ..
+    start+p-1 and the anchor at start+p (write_rows_kv, anchor_kv)."""
+    p = hid.shape[0]
+    kw, vw = ref.write_rows_kv(cfg, W, hid, start + np.arange(p))
+    ka, va = ref.anchor_kv(cfg, W, E, anchor, [start + p])
+    return np.concatenate([kw, ka], axis=1), np.concatenate([vw, va], axis=1)
+
+
+def test_draft_is_invariant_to_shifting_every_position():
+    """RoPE makes every attention score a function of position differences, so at
+    noise_scale 0 (no position-keyed noise) moving a whole request by delta -- context
+    at delta..delta+p-1, anchor at delta+p, slots from delta+p+1 -- leaves every
+    layer's output unchanged up to the float32 angles. Queries rotated at other
+    positions than the keys (here: left unshifted) fail."""
+    cfg, W, E, LM, rank = _tiny(num_layers=2)
+    C = ref.load_constants(cfg, W, E, LM, rank)
+    rng = np.random.default_rng(45)
+    p, K = 12, cfg.block_size
+    hid = rng.standard_normal((p, cfg.num_target_layers * cfg.target_hidden))
+    anchor = [int(rng.integers(cfg.vocab_size))]
+
+    def layers(start, slot_start):
+        kc, vc = _context_at(cfg, W, E, hid, anchor, start)
+        pos = slot_start + np.arange(K)
+        x = ref.noise_embedding(cfg, W, C, 5, pos, 0.0)
+        for l in range(cfg.num_layers):
+            x = ref.dit_layer(cfg, W, l, C.mods[l], x, pos, [(kc[l], vc[l])])
+        return x
+
+    base = layers(0, p + 1)
+    np.testing.assert_allclose(layers(7, p + 8), base, rtol=0, atol=2e-5 * np.max(np.abs(base)))
+    np.testing.assert_allclose(layers(300, p + 301), base, rtol=0, atol=2e-4 * np.max(np.abs(base)))
+    assert np.max(np.abs(layers(7, p + 1) - base)) > 1e-2 * np.max(np.abs(base))  # the test can tell
+
+
+def test_slots_sit_after_the_anchor():
+    """modeling_flashmap.py, draft: the block's slots are at anchor + 1 + k and attend
+    to the context 0..anchor. One layer whose only nonzero gate is the cross-attention's
+    and whose cross modulation has scale -1 (so 1 + scale = 0) gives every slot the same
+    pre-rotation query q = q_norm(W_q shift); the slots then differ only by the
+    rotation of q at their positions. At noise_scale 0 and with a final AdaLN of scale 0
+    and shift 0, the draft is z(x0 + gate * attention(R_pos q, K, V) W_o^T), built here
+    from the pinned rms_norm, apply_rope and attention. Slots at anchor + k fail."""
+    cfg, W, E, LM, rank = _tiny(num_layers=1, layer_norm_eps=0.0)
+    rng = np.random.default_rng(46)
+    D, nh, hd, K = cfg.hidden, cfg.num_heads, cfg.head_dim, cfg.block_size
+    shift, g = rng.standard_normal(D), rng.standard_normal(D)
+    W = _zero_adaln(W, cfg, {"layers.0.cross_attn_adaln": (-np.ones(D), shift, g)})
+    C = ref.load_constants(cfg, W, E, LM, rank)
+    p = 5
+    kc = rng.standard_normal((1, p + 1, nh, hd)) * 3
+    vc = rng.standard_normal((1, p + 1, nh, hd))
+    out = ref.draft_requests(cfg, W, C, [(kc, vc)], [p], [9], noise_scale=0.0)[0]
+
+    x0 = ref.noise_embedding(cfg, W, C, 9, p + 1 + np.arange(K), 0.0)
+    wq = np.asarray(W["layers.0.cross_attn.q_proj.weight"], np.float64)
+    q = ref.rms_norm((shift @ wq.T).reshape(1, nh, hd), W["layers.0.cross_attn.q_norm.weight"], cfg.qk_norm_eps)
+    wo = np.asarray(W["layers.0.cross_attn.o_proj.weight"], np.float64)
+
+    def expected(first_slot):
+        pos = first_slot + np.arange(K)
+        qr = ref.apply_rope(np.repeat(q, K, axis=0), pos, cfg.rope_theta)
+        att = ref.attention(qr, kc[0], vc[0]).reshape(K, D)
+        return st.zscore(x0 + g * (att @ wo.T), axis=-1)
+
+    np.testing.assert_allclose(out, expected(p + 1), rtol=1e-10, atol=1e-10)
+    assert np.max(np.abs(out - expected(p))) > 1e-3  # the test can tell
+
+
+def test_e4m3_query_quantization_hand_worked():
+    """flashmap/sglang/model.py, _paged_cross_attention_fp8: per (request, head) the
+    query scale is max(max|q|, 1e-12) / 448 and q8 = e4m3(q / scale). Worked by hand:
+    head 0 has max|q| = 448, so its scale is 1 and q8 is q rounded to e4m3 -- 1.0625
+    lies halfway between 1 and 1.125 (step 1/8 in [1, 2)) and goes to the even 1.0;
+    -3.3 lies in [2, 4) (step 1/4) nearest -3.25; 300 lies in [256, 512) (step 32)
+    nearest 288. Head 1's largest magnitude 1e-13 is below the 1e-12 floor: its scale
+    is 1e-12 / 448 and 1e-13 / scale = 44.8 lies in [32, 64) (step 4), nearest 44.
+    The two slots share one scale per head."""
+    q = np.zeros((2, 2, 4))
+    q[0, 0] = [448.0, 1.0625, -3.3, 0.0]
+    q[1, 0] = [300.0, 0.0, 0.0, 0.0]
+    q[0, 1] = [1e-13, -0.5e-13, 0.0, 0.0]
+    got = ref.quantize_query_e4m3(q)
+    np.testing.assert_array_equal(got[0, 0], [448.0, 1.0, -3.25, 0.0])
+    np.testing.assert_array_equal(got[1, 0], [288.0, 0.0, 0.0, 0.0])
+    s1 = float(np.float32(np.float32(1e-12) / np.float32(448.0)))
+    # -0.5e-13 / s1 = -22.4: [16, 32) has step 2, nearest -22
+    np.testing.assert_allclose(got[0, 1], [44.0 * s1, -22.0 * s1, 0.0, 0.0], rtol=1e-6)
