@@ -99,17 +99,20 @@ class ClockSampler:
 # --------------------------------------------------------------------------- our arm
 
 
-def algorithmic_bytes(cfg: dict, req: dict) -> dict:
+def algorithmic_bytes(cfg: dict, req: dict, deferred_write: bool = False) -> dict:
     """Bytes the step must move: every weight once (bf16, or e4m3 plus one float32
     scale per output channel), the context K/V of positions 0..p of every request, the
-    window and anchor rows written, the logits."""
+    window and anchor rows written, the logits. With the window write deferred into the
+    draft the all-layer context K/V weight is read once for both (the separate write
+    call reads it again)."""
     H, Lt, D, L, F, Vd, V, K = (cfg[k] for k in ("target_hidden", "num_target_layers", "hidden", "num_layers",
                                                  "intermediate", "draft_vocab_size", "vocab_size", "block_size"))
     es = 4 if cfg["act_dtype"] == "f32" else 2
     wes = 1 if cfg.get("weight_dtype") == "e4m3" else es  # e4m3 weights: one byte (+ a scale per row)
     Vd = Vd if 0 < Vd < V else V
     bs = req["bs"]
-    w_write = ((D * Lt * H + 2 * L * D * D) * wes + (D + 2 * L * D) * 4 * (wes == 1)) if req["window"] else 0
+    w_write = ((D * Lt * H + (0 if deferred_write else 2 * L * D * D)) * wes
+               + (D + (0 if deferred_write else 2 * L * D)) * 4 * (wes == 1)) if req["window"] else 0
     w_draft = ((D * H + 2 * L * D * D + D * H + L * (6 * D * D + 2 * D * F)) * wes + H * H * es
                + (D + 2 * L * D + D + L * (6 * D + D + F)) * 4 * (wes == 1))
     w_head = Vd * D * wes + Vd * 4 * (wes == 1)
@@ -225,14 +228,61 @@ def sample_call(st: dict, stream=None) -> None:
                                 st["ws"], stream)
 
 
-def run_step(st: dict, stream=None) -> None:
+def deferred(st: dict) -> bool:
+    """The verify-window write goes into the draft call (one context K/V GEMM for the
+    window rows and the anchors) unless --separate-write asks for three calls; tree
+    drafts keep the separate write."""
+    return bool(st["req"]["window"]) and not st["req"]["tree"] and not st.get("separate_write")
+
+
+def write_call(st: dict, stream=None) -> None:
     F, req, cfg = st["F"], st["req"], st["cfg"]
-    bs, K = req["bs"], cfg["block_size"]
-    if req["window"]:
-        F.flashmap_write_context_kv(st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"],
-                                    st["start"], st["commit"], req["req_to_page"], st["window_loc"], st["ws"], stream)
-    draft_call(st, stream)
+    F.flashmap_write_context_kv(st["model"], st["pool"], req["window_hidden"], req["bs"], cfg["block_size"] + 1,
+                                req["req_pool_idx"], st["start"], st["commit"], req["req_to_page"], st["window_loc"],
+                                st["ws"], stream)
+
+
+def draft_with_write_call(st: dict, stream=None) -> None:
+    F, req, cfg = st["F"], st["req"], st["cfg"]
+    F.flashmap_draft_block_with_write(st["model"], st["pool"], req["window_hidden"], cfg["block_size"] + 1,
+                                      st["start"], st["commit"], st["window_loc"], req["bs"], req["anchor_ids"],
+                                      st["anchor_pos"], req["req_pool_idx"], req["req_to_page"], req["seeds"], 1.0,
+                                      st["hidden"], None, st["ws"], stream)
+
+
+def run_step(st: dict, stream=None) -> None:
+    if deferred(st):
+        draft_with_write_call(st, stream)
+    else:
+        if st["req"]["window"]:
+            write_call(st, stream)
+        draft_call(st, stream)
     sample_call(st, stream)
+
+
+def roofline_entry(roof: dict, chain, hbm_peak: float, peak_src: str, ms_step: float, workload: str) -> dict:
+    """The roofline object of the dominant kernel (the tcgen05 GEMM): from the GEMM
+    chain timed as one graph where it applies, else from the eager per-launch events."""
+    traffic = profiled_traffic(workload)
+    out = {"bound": "hbm", "peak": hbm_peak, "unit": "GB/s", "peak_source": f"{peak_src} hbm_gbs",
+           "kernel": "tc_linear_kernel (tcgen05 GEMM, every launch of a step)", "traffic": traffic,
+           "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum per GEMM launch, from "
+                              f"profiles/tc_linear_step_{workload}.md, whose kernel source hash matches csrc/gemm.cu"
+                              if traffic is not None else "no ncu summary for the current csrc/gemm.cu")}
+    if chain is not None:
+        out.update(achieved=round(chain["achieved_gbs"], 1), frac=round(chain["achieved_gbs"] / hbm_peak, 4),
+                   bytes_per_launch=round(chain["bytes_per_launch"]), us_per_launch=round(chain["us_per_launch"], 2),
+                   launches_per_step=chain["launches"],
+                   gemm_ms_per_step=round(chain["ms_chain"], 4),
+                   gemm_time_within_step=bool(chain["ms_chain"] <= ms_step),
+                   timing=("the step's GEMM launches alone (flashmap_profile_gemm_chain), one CUDA graph replayed "
+                           "between one event pair; achieved = algorithmic bytes / graph time"))
+    else:
+        out.update(achieved=round(roof["achieved_gbs"], 1), frac=round(roof["achieved_gbs"] / hbm_peak, 4),
+                   bytes_per_launch=round(roof["bytes_per_launch"]), us_per_launch=round(roof["ms_per_launch"] * 1e3, 2),
+                   launches_per_step=roof["launches_per_step"],
+                   timing="eager step with an event pair around every launch (several-jump drafts)")
+    return out
 
 
 def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: int = 3) -> dict:
@@ -272,6 +322,36 @@ def gemm_roofline(st: dict, stream: torch.cuda.Stream, hbm_peak: float, steps: i
             "launches_per_step_total": len(recs) // steps}
 
 
+def gemm_chain_roofline(st: dict, stream: torch.cuda.Stream, n: int = 30):
+    """The step's tcgen05 GEMM launches alone (flashmap_profile_gemm_chain: the same
+    shapes, weights and launch configuration, back to back with programmatic
+    dependent launch), captured in one CUDA graph and replayed n times between one
+    pair of events on the launch stream: algorithmic bytes per launch over the mean
+    launch duration. None where the chain does not apply (several jumps)."""
+    F, req, cfg = st["F"], st["req"], st["cfg"]
+    if cfg.get("num_steps", 1) > 1:
+        return None
+    bs = blocks_per_step(st)
+    window = cfg["block_size"] + 1 if req["window"] else 0
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        byts, launches = F.flashmap_profile_gemm_chain(st["model"], bs, window, st["hidden"], st["ws"])
+        with torch.cuda.graph(g, stream=stream):
+            F.flashmap_profile_gemm_chain(st["model"], bs, window, st["hidden"], st["ws"])
+        for _ in range(3):
+            g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"bytes_per_chain": byts, "launches": launches, "ms_chain": ms, "bytes_per_launch": byts / launches,
+            "us_per_launch": ms * 1e3 / launches, "achieved_gbs": byts / (ms * 1e-3) / 1e9}
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per GEMM launch from the committed ncu summary of this workload, or
     None when there is none or csrc/gemm.cu changed since the counters were taken."""
@@ -301,10 +381,10 @@ def phase_times(st: dict, stream: torch.cuda.Stream, n: int = 60) -> dict:
     bs, K = req["bs"], cfg["block_size"]
     calls = {}
     if req["window"]:
-        calls["write"] = lambda: F.flashmap_write_context_kv(
-            st["model"], st["pool"], req["window_hidden"], bs, K + 1, req["req_pool_idx"], st["start"],
-            st["commit"], req["req_to_page"], st["window_loc"], st["ws"])
+        calls["write"] = lambda: write_call(st)  # the separate write call, for reference
     calls["draft"] = lambda: draft_call(st)
+    if deferred(st):
+        calls["draft_with_write"] = lambda: draft_with_write_call(st)
     calls["sample"] = lambda: sample_call(st)  # a tree draft's sample phase includes the tree
     out = {}
     for name, fn in calls.items():
@@ -324,6 +404,55 @@ def phase_times(st: dict, stream: torch.cuda.Stream, n: int = 60) -> dict:
         torch.cuda.synchronize()
         us = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
         out[name] = {"median_us": round(float(np.median(us)), 1), "p90_us": round(float(np.percentile(us, 90)), 1)}
+    return out
+
+
+# Configurations the default (batch-1) run also times, each on its own model and pool
+# after the batch-1 line is measured: batch 32 (ragged contexts), batch 128 (window
+# write and full-vocabulary scatter), e4m3 weights at batch 64.
+EXTRA_WORKLOADS = ("qwen3_8b_bs32", "qwen3_8b_bs128", "qwen3_8b_fp8_bs64")
+
+
+def time_workload(workload: str, device: str, stream: torch.cuda.Stream, hbm_peak: float, steps: int = 20,
+                  warmup: int = 3) -> dict:
+    """One workload's step as a replayed CUDA graph (events around `steps` replays on
+    the launch stream, after `warmup` replays), its per-call phases and its step
+    roofline; the model and pool are released afterwards."""
+    st = setup_ours(workload, device)
+    F, cfg, req = st["F"], st["cfg"], st["req"]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            run_step(st)
+    torch.cuda.synchronize()
+    err = F.flashmap_get_device_error(st["model"])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            run_step(st)
+        for _ in range(warmup):
+            graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    phases = phase_times(st, stream, n=20)
+    ab = algorithmic_bytes(cfg, req, deferred(st))
+    tokens = blocks_per_step(st) * cfg["block_size"]
+    out = {"ms_per_step": round(ms, 4), "value": round(tokens / (ms * 1e-3), 1), "unit": UNIT, "steps": steps,
+           "batch": req["bs"], "dtype": cfg["act_dtype"], "weight_dtype": cfg["weight_dtype"],
+           "context": {"min": min(req["ctx"]), "max": max(req["ctx"]), "mean": float(np.mean(req["ctx"]))},
+           "phases": phases, "device_error": err,
+           "step_roofline": {"algorithmic_bytes": ab["total"],
+                             "achieved_gbs": round(ab["total"] / (ms * 1e-3) / 1e9, 1),
+                             "frac_of_measured_hbm": round(ab["total"] / (ms * 1e-3) / 1e9 / hbm_peak, 4),
+                             "frac_of_8tbs": round(ab["total"] / (ms * 1e-3) / 1e9 / 8000.0, 4)}}
+    del graph, st
+    torch.cuda.empty_cache()
     return out
 
 
@@ -347,6 +476,7 @@ def our_arm(args, rank: int, world: int) -> dict:
     torch.cuda.set_device(device)
     hbm_peak, tf_peak, peak_src = load_peaks()
     st = setup_ours(args.workload, device)
+    st["separate_write"] = args.separate_write
     F, cfg, req = st["F"], st["cfg"], st["req"]
     bs, K = req["bs"], cfg["block_size"]
     stream = torch.cuda.Stream(device=device)
@@ -405,22 +535,33 @@ def our_arm(args, rank: int, world: int) -> dict:
     tok_host = [torch.empty(t.shape, dtype=torch.int64).pin_memory() for t in result]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in tok_host)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_loop(step_fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                for k, t in host_in.items():
+                    dev_in[k].copy_(t, non_blocking=True)
+                step_fn()
+                for h, t in zip(tok_host, result):
+                    h.copy_(t, non_blocking=True)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return world_max(e0.elapsed_time(e1) / n, world, device)
+
+    # the three C-ABI calls (write, draft, sample) issued every step, no graph
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            for k, t in host_in.items():
-                dev_in[k].copy_(t, non_blocking=True)
-            graph.replay()
-            for h, t in zip(tok_host, result):
-                h.copy_(t, non_blocking=True)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = world_max(e0.elapsed_time(e1) / args.steps, world, device)
+        for _ in range(3):
+            run_step(st)
+    e2e_ms = e2e_loop(lambda: run_step(st), args.steps)
+    # the same step replayed from the captured graph
+    e2e_graph_ms = e2e_loop(graph.replay, args.steps)
 
     roof = gemm_roofline(st, stream, hbm_peak)
+    chain = gemm_chain_roofline(st, stream)
     phases = phase_times(st, stream)
-    ab = algorithmic_bytes(cfg, req)
+    ab = algorithmic_bytes(cfg, req, deferred(st))
     t_ds = (phases["draft"]["median_us"] + phases["sample"]["median_us"]) * 1e-6
     launches = roof["launches_per_step_total"]
     line = {
@@ -431,17 +572,24 @@ def our_arm(args, rank: int, world: int) -> dict:
         "config": {"workload": args.workload, "batch": bs, "block_size": K,
                    "context": {"min": min(req["ctx"]), "max": max(req["ctx"]),
                                "mean": float(np.mean(req["ctx"]))},
-                   "window_write": bool(req["window"]), "full_vocab_scatter": bool(req["full_scatter"]),
+                   "window_write": ("deferred into the draft call" if deferred(st) else
+                                    "its own call" if req["window"] else None),
+                   "full_vocab_scatter": bool(req["full_scatter"]),
                    "tree": ({"candidates": req["tree"][0], "width": req["tree"][1]} if req["tree"] else None),
                    "parallelism": f"replicas x{world} (requests sharded, no collective)",
                    "l2": "inputs larger than L2 (weights alone ~3 GB per step)", "cuda_graph": True},
         "e2e": {"value": round(tokens_per_step / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "how": "every step: pinned host inputs copied in, the step's C-ABI calls ("
+                       + ("flashmap_draft_block_with_write, flashmap_sample_block" if deferred(st) else
+                          "flashmap_write_context_kv, flashmap_draft_block, flashmap_sample_block" if req["window"] else
+                          "flashmap_draft_block, flashmap_sample_block")
+                       + ") made through the Python binding (no graph), token ids copied out"},
+        "e2e_graph": {"value": round(tokens_per_step / (e2e_graph_ms * 1e-3), 1), "unit": UNIT,
+                      "ms_per_step": round(e2e_graph_ms, 4),
+                      "how": "the same copies around a replay of the step's captured CUDA graph"},
         "gpu_launches": launches * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1), "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(roof["achieved_gbs"] / hbm_peak, 4), "traffic": profiled_traffic(args.workload),
-                     "peak_source": f"{peak_src} hbm_gbs", "kernel": roof["kernel"],
-                     "bytes_per_launch": round(roof["bytes_per_launch"]), "us_per_launch": round(roof["ms_per_launch"] * 1e3, 2)},
+        "roofline": roofline_entry(roof, chain, hbm_peak, peak_src, ms, args.workload),
         "step_roofline": {"algorithmic_bytes": ab["total"], "achieved_gbs": round(ab["total"] / (ms * 1e-3) / 1e9, 1),
                           "frac_of_measured_hbm": round(ab["total"] / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                           "frac_of_8tbs": round(ab["total"] / (ms * 1e-3) / 1e9 / 8000.0, 4)},
@@ -457,6 +605,11 @@ def our_arm(args, rank: int, world: int) -> dict:
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+    if world == 1 and args.workload == "qwen3_8b_bs1" and not args.no_extra_configs:
+        # the other configurations, timed after the batch-1 line (not part of its value)
+        del graph, st
+        torch.cuda.empty_cache()
+        line["other_configs"] = {w: time_workload(w, device, stream, hbm_peak) for w in EXTRA_WORKLOADS}
     return line
 
 
@@ -622,6 +775,10 @@ def main() -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen3_8b_bs1", choices=sorted(syn.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-write", action="store_true",
+                    help="run the verify-window write as its own call instead of deferring it into the draft")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="skip the batch-32, batch-128 and e4m3 batch-64 steps the default run also times")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--kernel-case", choices=["gemm", "gemm512", "gemm2048", "head2048"], default=None,
                     help="time one kernel alone instead of the step (profiling case)")

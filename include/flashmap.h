@@ -204,7 +204,9 @@ flashmap_status flashmap_free(flashmap_model* model);
 flashmap_status flashmap_get_config(const flashmap_model* model, flashmap_config* cfg);
 
 /* Workspace bytes needed by write/draft/sample for batches of up to max_bs requests
- * and writes of up to max_write_rows (bs * window) rows at once. */
+ * and writes of up to max_write_rows (bs * window) rows at once, including a draft
+ * with a deferred write of up to max_write_rows rows (flashmap_draft_block_with_write,
+ * which does not split its write into chunks). */
 flashmap_status flashmap_workspace_size(const flashmap_model* model, int32_t max_bs,
                                         int32_t max_write_rows, size_t* bytes);
 
@@ -262,6 +264,37 @@ flashmap_status flashmap_draft_block(flashmap_model* model, const flashmap_kv_po
                                      float noise_scale, void* hidden_out, int64_t* anchor_loc_out,
                                      void* workspace, size_t workspace_bytes, flashmap_stream stream);
 
+/* A verify-window context-KV write handed to the next draft instead of run on its
+ * own (flashmap/vllm/model.py, defer_context_kv): the fields of
+ * flashmap_write_context_kv for bs requests (the draft's bs, req_pool_idx and page
+ * table). */
+typedef struct {
+  const void* target_hidden;   /* (device) [bs][W][Lt*H] act_dtype, 16-byte aligned */
+  int32_t W;                   /* window columns per request */
+  const int32_t* start_pos;    /* (device) int32 [bs], position of window column 0 */
+  const int32_t* commit_lens;  /* (device) int32 [bs] in [0, W], or NULL (every column) */
+  int64_t* out_loc;            /* (device) int64 [bs][W]: the slot written, -1 if skipped; or NULL */
+} flashmap_pending_write;
+
+/*
+ * flashmap_draft_block with a pending verify-window write done in the same call
+ * (flashmap/vllm/model.py, defer_context_kv and _prologue: the pending context rows
+ * and the anchors go through one GEMM over the all-layer context K/V weight). The
+ * window's committed columns are written exactly as flashmap_write_context_kv writes
+ * them (same slots, keys and values, out_loc) and the anchors as flashmap_draft_block
+ * writes them; the all-layer context K/V weight is read once for both instead of once
+ * per call. The write completes before any cross-attention reads the pool. The
+ * workspace must hold the draft and the bs * W write rows at once
+ * (flashmap_workspace_size with max_write_rows >= bs * W); the write is not chunked.
+ */
+flashmap_status flashmap_draft_block_with_write(flashmap_model* model, const flashmap_kv_pool* pool,
+                                                const flashmap_pending_write* pending, int32_t bs,
+                                                const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                                const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                                int32_t req_to_page_stride, const uint64_t* seeds,
+                                                float noise_scale, void* hidden_out, int64_t* anchor_loc_out,
+                                                void* workspace, size_t workspace_bytes, flashmap_stream stream);
+
 /*
  * Whole-block sampling (flashmap/sglang/sampler.py, FlashMapDraftSampler, fused
  * variant; flashmap/sglang/model.py, head_logits): logits l = W_f hidden + b_f over
@@ -298,7 +331,9 @@ flashmap_status flashmap_sample_block(flashmap_model* model, int32_t bs, const v
  * receives the same token ids flashmap_sample_block draws from those logits. The
  * per-row merge slots live in a fixed array inside the library (96 KB on every GPU
  * that loads it, kept until the process exits), so bs * block_size may not exceed
- * 8192 rows (E_INVALID otherwise). The first call on a device looks up that array's
+ * 8192 rows (E_INVALID otherwise). The model's device must be the current device
+ * (E_INVALID otherwise: the array's address is per device). The first call on a
+ * device looks up that array's
  * device address; make it before any stream capture on that device. The array is
  * shared by every call and keeps the last call's contents (the call clears what it
  * uses): calls that overlap on the GPU, on any stream, race and give wrong tokens.
@@ -385,9 +420,33 @@ flashmap_status flashmap_profile_start(flashmap_model* model, int32_t capacity);
 flashmap_status flashmap_profile_stop(flashmap_model* model, flashmap_launch_record* out, int32_t capacity,
                                       int32_t* count);
 
+/* The tcgen05 GEMM launches of one one-jump step of `bs` requests, with the shapes,
+ * weights and launch configuration the calls use, back to back on `stream` and with
+ * nothing else between them: the verify-window write's two linears over bs * window
+ * columns (none when window = 0), the draft's anchor, noise and DiT linears and the
+ * sampler's folded head (reading `hidden`, device [bs * K][D] act dtype). They read
+ * and write the workspace (sized for bs requests and bs * window write rows); what
+ * they leave there is not a result, and the chain clears only the GEMMs' own
+ * counters (three small memsets). A measurement hook: captured in a CUDA graph and
+ * replayed, it times the GEMM kernel the way a step runs it, without the time of
+ * the kernels between the GEMMs. *bytes_out receives the chain's algorithmic bytes
+ * (each weight once, e4m3 weights one byte and a float32 scale per output channel;
+ * activations read; outputs written), *launches_out the number of GEMM launches.
+ * E_UNSUPPORTED for several-jump drafts and float32 weights. */
+flashmap_status flashmap_profile_gemm_chain(flashmap_model* model, int32_t bs, int32_t window, const void* hidden,
+                                           void* workspace, size_t workspace_bytes, int64_t* bytes_out,
+                                           int32_t* launches_out, flashmap_stream stream);
+
 /* ----------------------------------------------------------------------------------
  * Test and inspection exports. They run the library's own kernels on small inputs.
  * ---------------------------------------------------------------------------------- */
+
+/* The timeout path of the kernels' pipeline waits, exercised without any fault: one
+ * warp on `stream` waits limit_ns (at most 100 ms, else E_INVALID) on an mbarrier
+ * that nothing arrives on, through the same bounded wait every pipeline uses, gives
+ * up, sets FLASHMAP_DEVERR_TIMEOUT in the model's device error word and returns (read
+ * it with flashmap_get_device_error). No copy or MMA is issued. Test-only. */
+flashmap_status flashmap_debug_wait_timeout(flashmap_model* model, uint64_t limit_ns, flashmap_stream stream);
 
 /* Raw Philox4x32-10 words (Salmon et al., SC'11, section 3) for n (key, counter)
  * pairs: seeds (device) uint64 [n] (key = lo32, hi32), ctr (device) uint32 [n][4];

@@ -73,6 +73,11 @@ class flashmap_kv_pool(_c.Structure):
     _fields_ = [("base", _vp), ("num_pages", _c.c_int64), ("dtype", _c.c_int32)]
 
 
+class flashmap_pending_write(_c.Structure):
+    _fields_ = [("target_hidden", _vp), ("W", _c.c_int32), ("start_pos", _vp), ("commit_lens", _vp),
+                ("out_loc", _vp)]
+
+
 class flashmap_launch_record(_c.Structure):
     _fields_ = [("kind", _c.c_int32), ("layer", _c.c_int32), ("rows", _c.c_int32), ("n", _c.c_int32),
                 ("k", _c.c_int32), ("ms", _c.c_float)]
@@ -110,6 +115,9 @@ def lib():
                                                 _vp, _vp, _c.c_int32, _vp, _vp, _c.c_size_t, _vp]
         L.flashmap_draft_block.argtypes = [_vp, P(flashmap_kv_pool), _c.c_int32, _vp, _vp, _vp, _vp, _c.c_int32,
                                            _vp, _c.c_float, _vp, _vp, _vp, _c.c_size_t, _vp]
+        L.flashmap_draft_block_with_write.argtypes = [_vp, P(flashmap_kv_pool), P(flashmap_pending_write), _c.c_int32,
+                                                      _vp, _vp, _vp, _vp, _c.c_int32, _vp, _c.c_float, _vp, _vp, _vp,
+                                                      _c.c_size_t, _vp]
         L.flashmap_sample_block.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp, _vp,
                                             _vp, _c.c_size_t, _vp]
         L.flashmap_get_device_error.argtypes = [_vp, _vp, P(_c.c_uint32)]
@@ -118,6 +126,9 @@ def lib():
         L.flashmap_debug_constants.argtypes = [_vp, _vp, _vp, _vp, _vp]
         L.flashmap_debug_folded.argtypes = [_vp, _vp, _vp, _vp, P(_c.c_int32), _vp]
         L.flashmap_sample_logits_static.argtypes = [_vp, _c.c_int32, _vp, _vp, _vp, _vp, _vp, _c.c_uint64, _vp, _vp]
+        L.flashmap_debug_wait_timeout.argtypes = [_vp, _c.c_uint64, _vp]
+        L.flashmap_profile_gemm_chain.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp, _vp, _c.c_size_t,
+                                                  P(_c.c_int64), P(_c.c_int32), _vp]
         L.flashmap_build_tree.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp]
         L.flashmap_draft_candidates.argtypes = [_vp, P(flashmap_kv_pool), _c.c_int32, _c.c_int32, _vp, _vp, _vp, _vp,
                                                 _c.c_int32, _vp, _c.c_float, _vp, _vp, _vp, _c.c_size_t, _vp]
@@ -243,6 +254,17 @@ def flashmap_draft_block(model: Model, pool: flashmap_kv_pool, bs: int, anchor_i
         _ptr(anchor_loc_out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def flashmap_draft_block_with_write(model: Model, pool: flashmap_kv_pool, target_hidden, W: int, start_pos, commit_lens,
+                                    out_loc, bs: int, anchor_ids, anchor_pos, req_pool_idx, req_to_page, seeds,
+                                    noise_scale: float, hidden_out, anchor_loc_out, workspace, stream=None) -> None:
+    pending = flashmap_pending_write(_ptr(target_hidden), int(W), _ptr(start_pos), _ptr(commit_lens), _ptr(out_loc))
+    _check(lib().flashmap_draft_block_with_write(
+        model.handle, _c.byref(pool), _c.byref(pending), int(bs), _ptr(anchor_ids), _ptr(anchor_pos),
+        _ptr(req_pool_idx), _ptr(req_to_page), int(req_to_page.stride(0)), _ptr(seeds), float(noise_scale),
+        _ptr(hidden_out), _ptr(anchor_loc_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
 def flashmap_draft_candidates(model: Model, pool: flashmap_kv_pool, bs: int, n_cand: int, anchor_ids, anchor_pos,
                               req_pool_idx, req_to_page, seeds, noise_scale: float, hidden_out, anchor_loc_out,
                               workspace, stream=None) -> None:
@@ -319,3 +341,19 @@ def flashmap_profile_stop(model: Model, capacity: int = 4096) -> list:
     n = _c.c_int32()
     _check(lib().flashmap_profile_stop(model.handle, recs, int(capacity), _c.byref(n)))
     return [(KINDS.get(r.kind, str(r.kind)), r.layer, r.rows, r.n, r.k, r.ms) for r in recs[: min(n.value, capacity)]]
+
+
+def flashmap_profile_gemm_chain(model: Model, bs: int, window: int, hidden, workspace, stream=None) -> tuple:
+    """Launches the GEMMs of one step back to back (see the header); returns
+    (algorithmic bytes, launches)."""
+    b = _c.c_int64()
+    n = _c.c_int32()
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib().flashmap_profile_gemm_chain(model.handle, int(bs), int(window), _ptr(hidden), _ptr(workspace),
+                                             ws_bytes, _c.byref(b), _c.byref(n), _stream(stream)))
+    return b.value, n.value
+
+
+def flashmap_debug_wait_timeout(model: Model, limit_ns: int, stream=None) -> None:
+    """One warp waits limit_ns on an mbarrier nothing arrives on and reports the timeout."""
+    _check(lib().flashmap_debug_wait_timeout(model.handle, int(limit_ns), _stream(stream)))

@@ -36,17 +36,6 @@ __device__ __forceinline__ void load_head_vec(const float* src, float (&v)[EPL],
     v[0] = LDCG(p);
   }
 }
-template <int EPL>
-__device__ __forceinline__ void clear_head_vec(float* dst, int lane) {
-  float* p = dst + lane * EPL;
-  if constexpr (EPL == 4) {
-    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else if constexpr (EPL == 2) {
-    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
-  } else {
-    p[0] = 0.f;
-  }
-}
 
 // ------------------------------------------------------------------ block self-attention
 
@@ -58,7 +47,7 @@ __device__ __forceinline__ void clear_head_vec(float* dst, int lane) {
 // per warp at large batches: twice the loads in flight per thread, half the threads
 // per CTA, so more CTAs fit on an SM).
 template <typename T, int EPL, int SPW>
-__global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const float* __restrict__ qn,
+__global__ void self_attn_kernel(const float* __restrict__ qkv, int K, int nh, const float* __restrict__ qn,
                                  const float* __restrict__ kn, float eps, const float2* __restrict__ rope_tab,
                                  int max_pos, const int32_t* __restrict__ anchor_pos, T* __restrict__ out,
                                  int early, unsigned* dev_err) {
@@ -83,8 +72,8 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   pdl_wait();
   const int D = nh * HD;
   // q, k and v of this warp's slots and head: all loads first (one vector per lane and
-  // part), then the request's position (once per CTA), the clears and the norms, so the
-  // L2 round trips overlap
+  // part), then the request's position (once per CTA) and the norms, so the L2 round
+  // trips overlap
   float v[SPW][3][EPL];
 #pragma unroll
   for (int i = 0; i < SPW; ++i) {
@@ -101,7 +90,6 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
   for (int i = 0; i < SPW; ++i) {
     const int k = warp * SPW + i;
     if (k >= K) continue;
-    float* base = qkv + static_cast<int64_t>(b * K + k) * 3 * D + h * HD;
     int pos = s_anchor + 1 + k;
     if (pos < 0 || pos >= max_pos) {
       if (lane == 0) set_dev_error(dev_err, FLASHMAP_DEVERR_POSITION);
@@ -112,13 +100,9 @@ __global__ void self_attn_kernel(float* __restrict__ qkv, int K, int nh, const f
       float2 cs[EPL / 2];
 #pragma unroll
       for (int c = 0; c < EPL / 2; ++c) cs[c] = rope[(lane * EPL >> 1) + c];
-#pragma unroll
-      for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
       head_norm_rot<EPL>(v[i][0], wq, eps, cs);
       head_norm_rot<EPL>(v[i][1], wk, eps, cs);
     } else {
-#pragma unroll
-      for (int part = 0; part < 3; ++part) clear_head_vec<EPL>(base + part * D, lane);
       head_norm_rope_w<EPL>(v[i][0], wq, eps, rope, lane);
       head_norm_rope_w<EPL>(v[i][1], wk, eps, rope, lane);
     }
@@ -1232,7 +1216,6 @@ __global__ void __launch_bounds__(64) xattn_combine_kernel(XattnArgs a, T* __res
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
       out[r + 16 * v] = from_f32<T>(L > 0.f ? acc[v] * inv : 0.f);
-      a.qacc[r + 16 * v] = 0.f;  // every item has read it
     }
   }
 }
@@ -1274,7 +1257,6 @@ __global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* 
     M = nM;
   }
   out[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = from_f32<T>(L > 0.f ? acc / L : 0.f);
-  a.qacc[(static_cast<int64_t>(b) * a.K + qi) * D + h * HD + d] = 0.f;  // every item has read it
 }
 
 }  // namespace
@@ -1304,7 +1286,7 @@ __global__ void __launch_bounds__(HD) xattn_combine_rows_kernel(XattnArgs a, T* 
     }                               \
   } while (0)
 
-cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
+cudaError_t self_attention(const Launch& L, int dtype, const float* qkv, int bs, int K, int nh, int hd, const float* qn,
                            const float* kn, float eps, const float2* rope, int max_pos, const int32_t* anchor_pos,
                            void* out, bool early) {
   if (bs <= 0) return cudaSuccess;

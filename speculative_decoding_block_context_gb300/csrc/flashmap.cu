@@ -237,8 +237,18 @@ std::vector<float2> rope_table(int maxpos, int hd, double theta) {
 
 struct DraftWs {
   float *x, *acc_big, *acc_d, *acc_a, *acc_kv;
-  void *act, *e_rows, *a_rows;
+  void *act, *e_rows;
+  void* kv_in;  // rows the all-layer context K/V GEMM projects: the anchors, then a deferred write's
+  // a deferred verify-window write (draft with write): its fc accumulator, the committed
+  // rows gathered, their window rows, their count and anchors + count
+  float* acc_fc = nullptr;
+  void* xc = nullptr;
+  int32_t* row_src = nullptr;
+  int *wcnt = nullptr, *wtotal = nullptr;
+  void* act_f;  // the MLP's hidden activations GELU(fc1), [R][F] act dtype
   int32_t *exp_pos, *exp_rpi;  // per-block request arrays of a multi-candidate draft
+  // GEMM split-tile scratch of the main stream and of the anchor branch
+  fm::GemmScratch red_main, red_side;
   // several jumps: the state (R x V float32), [posterior; state] in act dtype (2R x V),
   // their embeddings (2R x H float32) and the full-vocabulary logits (R x V float32)
   float *state = nullptr, *emb = nullptr, *logits_full = nullptr;
@@ -249,20 +259,33 @@ struct DraftWs {
   size_t bytes;
 };
 
-DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
+bool write_can_compact(const flashmap_model* m);
+
+// bs: the blocks drafted; wrows: the rows of a deferred verify-window write (0: none).
+DraftWs carve_draft(const flashmap_model* m, int bs, void* base, int wrows = 0) {
   Carver c(base);
   const size_t R = static_cast<size_t>(bs) * m->K, es = dt_size(m->adt);
-  const size_t big = std::max({3 * static_cast<size_t>(m->D), static_cast<size_t>(m->F), static_cast<size_t>(m->H)});
-  const size_t wide = std::max({static_cast<size_t>(m->D), static_cast<size_t>(m->F), static_cast<size_t>(m->H)});
+  const size_t big = std::max(3 * static_cast<size_t>(m->D), static_cast<size_t>(m->H));  // qkv, or the noise z L^T
+  const size_t wide = std::max(static_cast<size_t>(m->D), static_cast<size_t>(m->H));  // the MLP's F: act_f
   DraftWs w;
   w.x = c.take<float>(R * m->D * 4);
   w.acc_big = c.take<float>(R * big * 4);
   w.acc_d = c.take<float>(R * m->D * 4);
   w.acc_a = c.take<float>(static_cast<size_t>(bs) * m->D * 4);
-  w.acc_kv = c.take<float>(static_cast<size_t>(bs) * 2 * m->L * m->D * 4);
+  w.acc_kv = c.take<float>(static_cast<size_t>(bs + wrows) * 2 * m->L * m->D * 4);
   w.act = c.take<void>(R * wide * es);
+  w.act_f = c.take<void>(R * static_cast<size_t>(m->F) * es);
   w.e_rows = c.take<void>(static_cast<size_t>(bs) * m->H * es);
-  w.a_rows = c.take<void>(static_cast<size_t>(bs) * m->D * es);
+  w.kv_in = c.take<void>(static_cast<size_t>(bs + wrows) * m->D * es);
+  if (wrows > 0) {
+    w.acc_fc = c.take<float>(static_cast<size_t>(wrows) * m->D * 4);
+    if (write_can_compact(m)) {
+      w.xc = c.take<void>(static_cast<size_t>(wrows) * m->Lt * m->H * es);
+      w.row_src = c.take<int32_t>(static_cast<size_t>(wrows) * 4);
+      w.wcnt = c.take<int>(4);
+      w.wtotal = c.take<int>(4);
+    }
+  }
   w.exp_pos = c.take<int32_t>(static_cast<size_t>(bs) * 4);
   w.exp_rpi = c.take<int32_t>(static_cast<size_t>(bs) * 4);
   if (m->steps > 1) {
@@ -277,6 +300,13 @@ DraftWs carve_draft(const flashmap_model* m, int bs, void* base) {
   w.part_o = c.take<float>(chunks * m->nh * 16 * m->hd * 4);
   w.part_ml = c.take<float>(chunks * m->nh * 32 * 4);
   w.xnext = c.take<unsigned>(4);
+  {
+    const int main_rows = static_cast<int>(m->steps > 1 ? 2 * R : R);
+    w.red_main = fm::gemm_scratch_carve(c.take<uint8_t>(fm::gemm_scratch_bytes(main_rows, m->num_sms)), main_rows,
+                                        m->num_sms);
+    w.red_side = fm::gemm_scratch_carve(c.take<uint8_t>(fm::gemm_scratch_bytes(bs + wrows, m->num_sms)), bs + wrows,
+                                        m->num_sms);
+  }
   w.bytes = align_up(c.off);
   return w;
 }
@@ -293,6 +323,7 @@ struct WriteWs {
   void* xc = nullptr;           // the committed rows of the target hidden states
   int32_t* row_src = nullptr;   // their window rows
   int* rows_dev = nullptr;      // their count
+  fm::GemmScratch red;          // GEMM split-tile scratch
 };
 // The compacted write needs the tcgen05 GEMMs (device row counts).
 bool write_can_compact(const flashmap_model* m) { return m->wdt != FLASHMAP_F32; }
@@ -312,6 +343,7 @@ WriteWs carve_write(const flashmap_model* m, int rows, void* base, size_t* bytes
     w.row_src = c.take<int32_t>(static_cast<size_t>(rows) * 4);
     w.rows_dev = c.take<int>(4);
   }
+  w.red = fm::gemm_scratch_carve(c.take<uint8_t>(fm::gemm_scratch_bytes(rows, m->num_sms)), rows, m->num_sms);
   *bytes = align_up(c.off);
   return w;
 }
@@ -322,6 +354,7 @@ struct SampleWs {
   unsigned long long* keys;
   unsigned* counters;
   float* logits;
+  fm::GemmScratch red;  // GEMM split-tile scratch
   size_t bytes;
 };
 SampleWs carve_sample(const flashmap_model* m, int bs, bool own_logits, void* base) {
@@ -331,6 +364,8 @@ SampleWs carve_sample(const flashmap_model* m, int bs, bool own_logits, void* ba
   w.keys = c.take<unsigned long long>(R * 8);
   w.counters = c.take<unsigned>(R * 4);
   w.logits = own_logits ? c.take<float>(R * m->Vd * 4) : nullptr;
+  w.red = fm::gemm_scratch_carve(c.take<uint8_t>(fm::gemm_scratch_bytes(static_cast<int>(R), m->num_sms)),
+                                 static_cast<int>(R), m->num_sms);
   w.bytes = align_up(c.off);
   return w;
 }
@@ -783,7 +818,8 @@ flashmap_status flashmap_workspace_size(const flashmap_model* m, int32_t max_bs,
   if (!m || !bytes || max_bs <= 0 || max_write_rows < 0) return fail(FLASHMAP_E_INVALID, "bad workspace query");
   size_t wb = 0;
   carve_write(m, std::max(max_write_rows, 1), nullptr, &wb);
-  *bytes = std::max({carve_draft(m, max_bs, nullptr).bytes, carve_sample(m, max_bs, true, nullptr).bytes, wb});
+  *bytes = std::max({carve_draft(m, max_bs, nullptr, max_write_rows).bytes, carve_sample(m, max_bs, true, nullptr).bytes,
+                     wb});
   return FLASHMAP_OK;
 }
 
@@ -818,10 +854,11 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
     const int rows = static_cast<int>(std::min<int64_t>(chunk, total - r0));
     size_t b = 0;
     WriteWs ws = carve_write(m, rows, workspace, &b);
-    fm::ZeroList z;
-    z.add(ws.acc_fc, static_cast<int64_t>(rows) * m->D);
-    z.add(ws.acc_kv, static_cast<int64_t>(rows) * 2 * m->L * m->D);
-    TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
+    Launch Lw = Lh;
+    Lw.red = ws.red;
+    fm::ZeroList z;  // the GEMMs' split-tile counters (their outputs are written whole)
+    z.add(reinterpret_cast<float*>(ws.red.cnt), ws.red.cnt_cap);  // zero bits
+    TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lw, z));
     const void* x = static_cast<const uint8_t*>(target_hidden) + r0 * xrow;
     // A large window projects only its committed columns: their rows are gathered in
     // order and counted on the device, and every kernel below takes that count
@@ -836,12 +873,12 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
       rows_dev = ws.rows_dev;
     }
     // ctx = RMSNorm_hidden(fc(x)); kv = W_ctx ctx
-    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lh, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr, true,
+    TIMED_GEMM(-1, m->fc, rows, fm::linear(Lw, m->fc, x, rows, m->Lt * m->H, ws.acc_fc, m->D, nullptr, nullptr, fm::Out::Store,
                                            rows_dev));
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lh, m->adt, ws.acc_fc, rows, m->D, m->hidden_norm_w, m->cfg.rms_norm_eps,
                                                1.f, nullptr, 0.f, ws.ctx, m->D, rows_dev));
-    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lh, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr,
-                                               nullptr, true, rows_dev));
+    TIMED_GEMM(-1, m->ctx_kv, rows, fm::linear(Lw, m->ctx_kv, ws.ctx, rows, m->D, ws.acc_kv, 2 * m->L * m->D, nullptr,
+                                               nullptr, fm::Out::Store, rows_dev));
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
     a.ld = 2LL * m->L * m->D;
@@ -876,7 +913,8 @@ flashmap_status flashmap_write_context_kv(flashmap_model* m, const flashmap_kv_p
 // The draft of n_cand candidate blocks per request (1: flashmap_draft_block): the anchor
 // rows once per request, then the noise (keyed by the candidate) and the DiT on
 // bs * n_cand blocks, block bc being candidate bc % n_cand of request bc / n_cand.
-static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs, int32_t n_cand,
+static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* pool, const flashmap_pending_write* pw,
+                                  int32_t bs, int32_t n_cand,
                                   const int64_t* anchor_ids, const int32_t* anchor_pos, const int32_t* req_pool_idx,
                                   const int32_t* req_to_page, int32_t req_to_page_stride, const uint64_t* seeds,
                                   float noise_scale, void* hidden_out, int64_t* anchor_loc_out, void* workspace,
@@ -892,27 +930,34 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   if (pool->dtype != m->kdt || !pool->base || pool->num_pages <= 0)
     return fail(FLASHMAP_E_INVALID, "pool dtype must equal kv_dtype, with pages");
   if (!std::isfinite(noise_scale)) return fail(FLASHMAP_E_INVALID, "noise_scale must be finite");
+  int wrows = 0;  // rows of a deferred verify-window write
+  if (pw) {
+    if (!pw->target_hidden || !pw->start_pos || pw->W <= 0)
+      return fail(FLASHMAP_E_INVALID, "the pending write needs target_hidden, start_pos and W > 0");
+    if (m->adt == FLASHMAP_BF16 && (reinterpret_cast<uintptr_t>(pw->target_hidden) & 15))
+      return fail(FLASHMAP_E_INVALID, "target_hidden must be 16-byte aligned");
+    if (static_cast<int64_t>(bs) * pw->W > (1 << 24)) return fail(FLASHMAP_E_INVALID, "bs * W must be <= 2^24");
+    wrows = bs * pw->W;
+  }
   const int bsc = bs * n_cand;  // blocks
-  const DraftWs need = carve_draft(m, bsc, nullptr);
+  const DraftWs need = carve_draft(m, bsc, nullptr, wrows);
   if (workspace_bytes < need.bytes)
     return fail(FLASHMAP_E_INVALID, "workspace too small: need " + std::to_string(need.bytes) + " bytes");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const Launch Lh = m->launch(s);
-  const DraftWs ws = carve_draft(m, bsc, workspace);
+  const DraftWs ws = carve_draft(m, bsc, workspace, wrows);
+  const Launch Lh = [&] {
+    Launch l = m->launch(s);
+    l.red = ws.red_main;
+    return l;
+  }();
   const int R = bsc * m->K, D = m->D, H = m->H, adt = m->adt;
-  const size_t big = std::max({3 * static_cast<size_t>(D), static_cast<size_t>(m->F), static_cast<size_t>(H)});
   {
+    // counters only: every GEMM output is written whole (the residual stream starts as
+    // x_embed's output, stored)
     fm::ZeroList z;
-    z.add(ws.x, static_cast<int64_t>(R) * D);
-    z.add(ws.acc_big, static_cast<int64_t>(R) * static_cast<int64_t>(big));
-    z.add(ws.acc_d, static_cast<int64_t>(R) * D);
-    z.add(ws.acc_a, static_cast<int64_t>(bs) * D);
-    z.add(ws.acc_kv, static_cast<int64_t>(bs) * 2 * m->L * D);
     z.add(reinterpret_cast<float*>(ws.xnext), 1);  // zero bits
-    if (m->steps > 1) {
-      z.add(ws.emb, 2LL * R * H);
-      z.add(ws.logits_full, static_cast<int64_t>(R) * m->V);
-    }
+    z.add(reinterpret_cast<float*>(ws.red_main.cnt), ws.red_main.cnt_cap);
+    z.add(reinterpret_cast<float*>(ws.red_side.cnt), ws.red_side.cnt_cap);
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
   }
   // the blocks' request arrays (candidates of a request share its position and pages)
@@ -934,6 +979,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   const Launch La = [&] {
     Launch l = m->launch(fork ? m->side : s);
     if (fork) l.ctas_per_sm = FM_FORK_CTAS_PER_SM;
+    l.red = ws.red_side;
     return l;
   }();
   Launch Lm = Lh;  // the main branch until the join
@@ -943,9 +989,69 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     FM_CUDA(cudaStreamWaitEvent(m->side, m->ev_fork, 0));
   }
   TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_rows(La, adt, m->embedding, m->V, H, anchor_ids, bs, ws.e_rows));
-  TIMED_GEMM(-1, m->ap, bs, fm::linear(La, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, true));
-  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(La, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.a_rows, D));
-  TIMED_GEMM(-1, m->ctx_kv, bs, fm::linear(La, m->ctx_kv, ws.a_rows, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, true));
+  TIMED_GEMM(-1, m->ap, bs, fm::linear(La, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, fm::Out::Store));
+  TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(La, adt, ws.acc_a, bs, D, m->anchor_norm_w, m->cfg.rms_norm_eps, 1.f, nullptr, 0.f, ws.kv_in, D));
+  // A deferred verify-window write (flashmap/vllm/model.py, defer_context_kv /
+  // _prologue): its rows hidden_norm(fc(target hidden)) follow the anchor rows, and one
+  // all-layer context K/V GEMM projects both. A large window lists its committed
+  // columns first (as flashmap_write_context_kv does); the GEMM then takes the anchors
+  // plus their count from the device.
+  int kv_rows = bs;
+  const int* kv_rows_dev = nullptr;
+  bool wcompact = false;
+  if (wrows > 0) {
+    const void* xw = pw->target_hidden;
+    const int* wdev = nullptr;
+    wcompact = pw->commit_lens && write_can_compact(m) && wrows >= FM_WRITE_COMPACT_MIN_ROWS;
+    if (wcompact) {
+      const size_t xrow = static_cast<size_t>(m->Lt) * H * dt_size(adt);
+      TIMED(FLASHMAP_KIND_ROWS, -1, fm::window_compact(La, pw->commit_lens, pw->W, 0, wrows, ws.row_src, ws.wcnt,
+                                                       pw->out_loc, ws.wtotal, bs));
+      TIMED(FLASHMAP_KIND_ROWS, -1, fm::gather_window_rows(La, pw->target_hidden, static_cast<int64_t>(xrow),
+                                                           ws.row_src, ws.wcnt, wrows, ws.xc));
+      xw = ws.xc;
+      wdev = ws.wcnt;
+      kv_rows_dev = ws.wtotal;
+    }
+    TIMED_GEMM(-1, m->fc, wrows, fm::linear(La, m->fc, xw, wrows, m->Lt * H, ws.acc_fc, D, nullptr, nullptr,
+                                             fm::Out::Store, wdev));
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(La, adt, ws.acc_fc, wrows, D, m->hidden_norm_w, m->cfg.rms_norm_eps,
+                                               1.f, nullptr, 0.f,
+                                               static_cast<uint8_t*>(ws.kv_in) + static_cast<size_t>(bs) * D * dt_size(adt),
+                                               D, wdev));
+    kv_rows = bs + wrows;
+  }
+  TIMED_GEMM(-1, m->ctx_kv, kv_rows, fm::linear(La, m->ctx_kv, ws.kv_in, kv_rows, D, ws.acc_kv, 2 * m->L * D, nullptr,
+                                                nullptr, fm::Out::Store, kv_rows_dev));
+  if (wrows > 0) {
+    fm::KvWriteArgs a;
+    a.acc = ws.acc_kv + static_cast<size_t>(bs) * 2 * m->L * D;
+    a.ld = 2LL * m->L * D;
+    a.rows = wrows;
+    a.W = pw->W;
+    a.row0 = 0;
+    a.start_pos = pw->start_pos;
+    a.commit_lens = pw->commit_lens;
+    a.req_pool_idx = req_pool_idx;
+    a.req_to_page = req_to_page;
+    a.r2p_stride = req_to_page_stride;
+    a.L = m->L;
+    a.nh = m->nh;
+    a.hd = m->hd;
+    a.P = m->P;
+    a.num_pages = pool->num_pages;
+    a.k_norm = m->ctx_knorm;
+    a.eps = m->cfg.qk_norm_eps;
+    a.rope = m->rope;
+    a.max_pos = m->maxpos;
+    a.pool = pool->base;
+    a.out_loc = pw->out_loc;
+    if (wcompact) {
+      a.row_src = ws.row_src;
+      a.rows_dev = ws.wcnt;
+    }
+    TIMED(FLASHMAP_KIND_ROWS, -1, fm::kv_write(La, m->kdt, a));
+  }
   {
     fm::KvWriteArgs a;
     a.acc = ws.acc_kv;
@@ -1021,12 +1127,12 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
       const float* md = mods_all ? mods_all + static_cast<size_t>(l) * 9 * D : lw.mods;
       const float* fc2_beta = beta_all ? beta_all + static_cast<size_t>(l) * D : lw.fc2_beta;
       TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.qkv, R, fm::linear(Lc, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, true));
+      TIMED_GEMM(l, lw.qkv, R, fm::linear(Lc, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, fm::Out::Store));
       TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lc, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
                                  pos_x, ws.act, xa.early != 0 && (n_cand == 1 || l > 0)));
-      TIMED_GEMM(l, lw.o, R, fm::linear(Lc, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, false));
+      TIMED_GEMM(l, lw.o, R, fm::linear(Lc, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, fm::Out::Add));
       TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.cq, R, fm::linear(Lc, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, true));
+      TIMED_GEMM(l, lw.cq, R, fm::linear(Lc, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, fm::Out::Store));
       if (!joined) {  // the anchor rows are in the pool from here on
         FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
         joined = true;
@@ -1036,11 +1142,11 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
       xa.q_norm = lw.cqn;
       TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lc, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
       TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lc, adt, xa, ws.act));
-      TIMED_GEMM(l, lw.co, R, fm::linear(Lc, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, false));
+      TIMED_GEMM(l, lw.co, R, fm::linear(Lc, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, fm::Out::Add));
       TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
-      TIMED_GEMM(l, lw.fc1, R, fm::linear(Lc, lw.fc1, ws.act, R, D, ws.acc_big, m->F, nullptr, lw.fc1_b, true));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::gelu_rows(Lc, adt, ws.acc_big, static_cast<int64_t>(R) * m->F, ws.act));
-      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lc, lw.fc2, ws.act, R, m->F, ws.x, D, md + 8 * D, fc2_beta, false));
+      // fc1 + bias + GELU in the GEMM's epilogue, written in the activation dtype
+      TIMED_GEMM(l, lw.fc1, R, fm::linear(Lc, lw.fc1, ws.act, R, D, ws.act_f, m->F, nullptr, lw.fc1_b, fm::Out::GeluAct));
+      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lc, lw.fc2, ws.act_f, R, m->F, ws.x, D, md + 8 * D, fc2_beta, fm::Out::Add));
     }
     if (!joined) {
       FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
@@ -1055,16 +1161,16 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     // then one GEMM through M onto x_embed(u)
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::folded_noise(Lc, adt, seeds, anchor_pos, bs, m->K, H, n_cand, noise_scale,
                                                    m->fold_var, m->cfg.rms_norm_eps, m->gate, ws.act));
-    TIMED_GEMM(-1, m->fold, R, fm::linear(Lc, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, false));
+    TIMED_GEMM(-1, m->fold, R, fm::linear(Lc, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, fm::Out::Store));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   if (m->steps == 1) {
     // 2. noise: z (Philox, keyed by seed and slot position) -> z L^T -> u + gate * noise_norm -> x_embed
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::draft_noise(Lc, adt, seeds, anchor_pos, bs, m->K, H, ws.act, n_cand));
-    TIMED_GEMM(-1, m->chol, R, fm::linear(Lc, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, true));
+    TIMED_GEMM(-1, m->chol, R, fm::linear(Lc, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, fm::Out::Store));
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lc, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
                          ws.act, H));
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   // several jumps: the state starts as V-wide noise keyed like the one-jump noise
@@ -1085,20 +1191,16 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     // [posterior; state] @ E (at s = 0 only the state: the posterior is uniform)
     if (s0 > 0.f) {
       TIMED_GEMM(-1, m->et, 2 * R, fm::linear(Lc, m->et, xpost, 2 * R, static_cast<int>(V), ws.emb, H, nullptr,
-                                              nullptr, true));
+                                              nullptr, fm::Out::Store));
     } else {
       TIMED_GEMM(-1, m->et, R, fm::linear(Lc, m->et, xstate, R, static_cast<int>(V), ws.emb + static_cast<size_t>(R) * H,
-                                          H, nullptr, nullptr, true));
+                                          H, nullptr, nullptr, fm::Out::Store));
     }
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::mix_state(Lc, adt, s0 > 0.f ? ws.emb : nullptr, ws.emb + static_cast<size_t>(R) * H,
                                                 R, H, m->u, m->state_norm_w, m->noise_norm_w, m->cfg.rms_norm_eps,
                                                 m->step_gate[st], ws.act));
-    if (st > 0) {  // the residual stream restarts at x_embed of the new input
-      fm::ZeroList z;
-      z.add(ws.x, static_cast<int64_t>(R) * D);
-      TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lc, z));
-    }
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, false));
+    // the residual stream (re)starts at x_embed of this jump's input
+    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
     const bool last = st + 1 == m->steps;
     const size_t L = static_cast<size_t>(m->L);
     const flashmap_status r = dit(m->step_mods + st * L * 9 * D, m->step_fc2_beta + st * L * D,
@@ -1106,7 +1208,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     if (r != FLASHMAP_OK) return r;
     if (!last)  // the full-vocabulary logits that move the state
       TIMED_GEMM(-1, m->full_head, R, fm::linear(Lc, m->full_head, ws.act, R, D, ws.logits_full,
-                                                 static_cast<int>(V), nullptr, nullptr, true));
+                                                 static_cast<int>(V), nullptr, nullptr, fm::Out::Store));
   }
   return FLASHMAP_OK;
 }
@@ -1117,8 +1219,23 @@ flashmap_status flashmap_draft_block(flashmap_model* m, const flashmap_kv_pool* 
                                      int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
                                      void* hidden_out, int64_t* anchor_loc_out, void* workspace,
                                      size_t workspace_bytes, flashmap_stream stream) {
-  return draft_impl(m, pool, bs, 1, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride, seeds,
-                    noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
+  return draft_impl(m, pool, nullptr, bs, 1, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride,
+                    seeds, noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
+}
+
+flashmap_status flashmap_draft_block_with_write(flashmap_model* m, const flashmap_kv_pool* pool,
+                                                const flashmap_pending_write* pending, int32_t bs,
+                                                const int64_t* anchor_ids, const int32_t* anchor_pos,
+                                                const int32_t* req_pool_idx, const int32_t* req_to_page,
+                                                int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
+                                                void* hidden_out, int64_t* anchor_loc_out, void* workspace,
+                                                size_t workspace_bytes, flashmap_stream stream) {
+  if (!pending) {
+    g_last_error.clear();
+    return fail(FLASHMAP_E_INVALID, "NULL pending write");
+  }
+  return draft_impl(m, pool, pending, bs, 1, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride,
+                    seeds, noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
 }
 
 flashmap_status flashmap_draft_candidates(flashmap_model* m, const flashmap_kv_pool* pool, int32_t bs,
@@ -1127,8 +1244,9 @@ flashmap_status flashmap_draft_candidates(flashmap_model* m, const flashmap_kv_p
                                           int32_t req_to_page_stride, const uint64_t* seeds, float noise_scale,
                                           void* hidden_out, int64_t* anchor_loc_out, void* workspace,
                                           size_t workspace_bytes, flashmap_stream stream) {
-  return draft_impl(m, pool, bs, n_cand, anchor_ids, anchor_pos, req_pool_idx, req_to_page, req_to_page_stride,
-                    seeds, noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes, stream);
+  return draft_impl(m, pool, nullptr, bs, n_cand, anchor_ids, anchor_pos, req_pool_idx, req_to_page,
+                    req_to_page_stride, seeds, noise_scale, hidden_out, anchor_loc_out, workspace, workspace_bytes,
+                    stream);
 }
 
 flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void* hidden, const int32_t* anchor_pos,
@@ -1148,16 +1266,17 @@ flashmap_status flashmap_sample_block(flashmap_model* m, int32_t bs, const void*
   const SampleWs ws = carve_sample(m, bs, draft_logits_out == nullptr, workspace);
   float* logits = draft_logits_out ? draft_logits_out : ws.logits;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const Launch Lh = m->launch(s);
+  Launch Lh = m->launch(s);
+  Lh.red = ws.red;
   const int R = bs * m->K;
   {
     fm::ZeroList z;
-    z.add(logits, static_cast<int64_t>(R) * m->Vd);
     z.add(reinterpret_cast<float*>(ws.keys), 2LL * R);
     z.add(reinterpret_cast<float*>(ws.counters), R);
+    z.add(reinterpret_cast<float*>(ws.red.cnt), ws.red.cnt_cap);
     TIMED(FLASHMAP_KIND_MEMSET, -1, fm::zero_ranges(Lh, z));
   }
-  TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b, true));
+  TIMED_GEMM(-1, m->head, R, fm::linear(Lh, m->head, hidden, R, m->D, logits, m->Vd, nullptr, m->head_b, fm::Out::Store));
   TIMED(FLASHMAP_KIND_SAMPLE, -1, fm::sample_rows(Lh, logits, R, m->Vd, m->K, temperature, greedy, seeds, anchor_pos,
                                                    static_cast<uint32_t>(step), m->hot, tokens_out, ws.keys,
                                                    ws.counters));
@@ -1178,6 +1297,12 @@ flashmap_status flashmap_sample_logits_static(flashmap_model* m, int32_t bs, con
   if (rows > fm::kStaticSampleRows)
     return fail(FLASHMAP_E_INVALID, "bs * block_size = " + std::to_string(rows) + " rows exceeds the " +
                                         std::to_string(fm::kStaticSampleRows) + " rows of the static sampler scratch");
+  // The array's address is looked up for the current device: it must be the model's.
+  int dev = -1;
+  FM_CUDA(cudaGetDevice(&dev));
+  if (dev != m->device)
+    return fail(FLASHMAP_E_INVALID, "the current device (" + std::to_string(dev) + ") is not the model's device (" +
+                                        std::to_string(m->device) + ")");
   void* scratch = nullptr;
   FM_CUDA(fm::static_sample_scratch(&scratch));
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1230,6 +1355,95 @@ flashmap_status flashmap_profile_stop(flashmap_model* m, flashmap_launch_record*
   if (out)
     for (int i = 0; i < std::min(n, static_cast<int>(capacity)); ++i) out[i] = m->prof_recs[i];
   *count = n;
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32_t window, const void* hidden,
+                                           void* workspace, size_t workspace_bytes, int64_t* bytes_out,
+                                           int32_t* launches_out, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m || !hidden || !workspace || !bytes_out || !launches_out || bs <= 0 || window < 0)
+    return fail(FLASHMAP_E_INVALID, "bad argument");
+  if (reinterpret_cast<uintptr_t>(hidden) & 15) return fail(FLASHMAP_E_INVALID, "hidden must be 16-byte aligned");
+  if (m->steps != 1 || m->wdt == FLASHMAP_F32)
+    return fail(FLASHMAP_E_UNSUPPORTED, "the GEMM chain covers one-jump drafts with tcgen05 weights");
+  const int64_t wrows = static_cast<int64_t>(bs) * window;
+  const DraftWs need = carve_draft(m, bs, nullptr);
+  size_t wneed = 0;
+  if (wrows > 0) carve_write(m, static_cast<int>(wrows), nullptr, &wneed);
+  const SampleWs sneed = carve_sample(m, bs, true, nullptr);
+  if (workspace_bytes < std::max({need.bytes, wneed, sneed.bytes}))
+    return fail(FLASHMAP_E_INVALID, "workspace too small for the chain");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int R = bs * m->K, D = m->D, H = m->H;
+  const size_t es = dt_size(m->adt);
+  int64_t bytes = 0;
+  int32_t n = 0;
+  // algorithmic bytes of one launch: weights once (e4m3: one byte and a float32 scale
+  // per output channel), activations read, outputs written (float32, or act dtype)
+  auto count = [&](const Weight& W, int rows, size_t out_es) {
+    const size_t wb = W.dtype == FLASHMAP_E4M3 ? static_cast<size_t>(W.N) * W.K + static_cast<size_t>(W.N) * 4
+                                                : static_cast<size_t>(W.N) * W.K * es;
+    bytes += static_cast<int64_t>(wb + static_cast<size_t>(rows) * W.K * es + static_cast<size_t>(rows) * W.N * out_es);
+    ++n;
+  };
+  if (wrows > 0) {
+    size_t b = 0;
+    const WriteWs ws = carve_write(m, static_cast<int>(wrows), workspace, &b);
+    Launch L = m->launch(s);
+    L.red = ws.red;
+    FM_CUDA(cudaMemsetAsync(ws.red.cnt, 0, static_cast<size_t>(ws.red.cnt_cap) * 4, s));
+    FM_CUDA(fm::linear(L, m->fc, ws.xc, static_cast<int>(wrows), m->Lt * H, ws.acc_fc, D, nullptr, nullptr,
+                       fm::Out::Store));
+    count(m->fc, static_cast<int>(wrows), 4);
+    FM_CUDA(fm::linear(L, m->ctx_kv, ws.ctx, static_cast<int>(wrows), D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr,
+                       fm::Out::Store));
+    count(m->ctx_kv, static_cast<int>(wrows), 4);
+  }
+  {
+    const DraftWs ws = carve_draft(m, bs, workspace);
+    Launch L = m->launch(s);
+    L.red = ws.red_main;
+    FM_CUDA(cudaMemsetAsync(ws.red_main.cnt, 0, static_cast<size_t>(ws.red_main.cnt_cap) * 4, s));
+    FM_CUDA(fm::linear(L, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, fm::Out::Store));
+    count(m->ap, bs, 4);
+    FM_CUDA(fm::linear(L, m->ctx_kv, ws.kv_in, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, fm::Out::Store));
+    count(m->ctx_kv, bs, 4);
+    if (m->noise_path == 1) {
+      FM_CUDA(fm::linear(L, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, fm::Out::Store));
+      count(m->fold, R, 4);
+    } else {
+      FM_CUDA(fm::linear(L, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, fm::Out::Store));
+      count(m->chol, R, 4);
+      FM_CUDA(fm::linear(L, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
+      count(m->xe, R, 4);
+    }
+    for (int l = 0; l < m->L; ++l) {
+      const LayerW& lw = m->layers[l];
+      FM_CUDA(fm::linear(L, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, fm::Out::Store));
+      count(lw.qkv, R, 4);
+      FM_CUDA(fm::linear(L, lw.o, ws.act, R, D, ws.x, D, lw.mods + 2 * D, nullptr, fm::Out::Add));
+      count(lw.o, R, 4);
+      FM_CUDA(fm::linear(L, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, fm::Out::Store));
+      count(lw.cq, R, 4);
+      FM_CUDA(fm::linear(L, lw.co, ws.act, R, D, ws.x, D, lw.mods + 5 * D, nullptr, fm::Out::Add));
+      count(lw.co, R, 4);
+      FM_CUDA(fm::linear(L, lw.fc1, ws.act, R, D, ws.act_f, m->F, nullptr, lw.fc1_b, fm::Out::GeluAct));
+      count(lw.fc1, R, es);
+      FM_CUDA(fm::linear(L, lw.fc2, ws.act_f, R, m->F, ws.x, D, lw.mods + 8 * D, lw.fc2_beta, fm::Out::Add));
+      count(lw.fc2, R, 4);
+    }
+  }
+  {
+    const SampleWs ws = carve_sample(m, bs, true, workspace);
+    Launch L = m->launch(s);
+    L.red = ws.red;
+    FM_CUDA(cudaMemsetAsync(ws.red.cnt, 0, static_cast<size_t>(ws.red.cnt_cap) * 4, s));
+    FM_CUDA(fm::linear(L, m->head, hidden, R, D, ws.logits, m->Vd, nullptr, m->head_b, fm::Out::Store));
+    count(m->head, R, 4);
+  }
+  *bytes_out = bytes;
+  *launches_out = n;
   return FLASHMAP_OK;
 }
 
@@ -1290,9 +1504,27 @@ flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* 
     return fail(FLASHMAP_E_CUDA, err);
   }
   Launch Lh{s, sms, nullptr, true};
-  const cudaError_t e = fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, false);
+  // the GEMM's split-tile scratch for this one launch (a test hook: it may allocate)
+  void* red = nullptr;
+  const size_t red_bytes = fm::gemm_scratch_bytes(rows, sms);
+  cudaError_t e = cudaMallocAsync(&red, red_bytes, s);
+  if (e == cudaSuccess) {
+    Lh.red = fm::gemm_scratch_carve(red, rows, sms);
+    e = cudaMemsetAsync(Lh.red.cnt, 0, static_cast<size_t>(Lh.red.cnt_cap) * 4, s);
+  }
+  if (e == cudaSuccess)
+    e = fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, fm::Out::Add);
+  if (red) cudaFreeAsync(red, s);
   if (q) cudaFreeAsync(q, s);
   FM_CUDA(e);
+  return FLASHMAP_OK;
+}
+
+flashmap_status flashmap_debug_wait_timeout(flashmap_model* m, uint64_t limit_ns, flashmap_stream stream) {
+  g_last_error.clear();
+  if (!m) return fail(FLASHMAP_E_INVALID, "NULL model");
+  if (limit_ns == 0 || limit_ns > 100000000ull) return fail(FLASHMAP_E_INVALID, "limit_ns must be in (0, 100 ms]");
+  FM_CUDA(fm::wait_timeout_probe(m->launch(reinterpret_cast<cudaStream_t>(stream)), limit_ns));
   return FLASHMAP_OK;
 }
 

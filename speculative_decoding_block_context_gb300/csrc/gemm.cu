@@ -7,10 +7,17 @@
 // dimension is spent on the weights and no row padding to 128 is needed. The
 // iteration space (output tile, 64-wide k block) is cut into equal contiguous ranges,
 // one per CTA (stream-K), so every SM streams the same number of weight bytes whatever
-// the shape; partial tiles are summed with float atomics into the caller's output.
+// the shape. A tile split over several CTAs is summed in a fixed order, so results
+// repeat bit for bit: every CTA but one leaves its partial tile in a scratch slot and
+// counts it; the CTA holding the tile's first k blocks (it reaches them last, at the
+// end of its range) finds the others counted, adds their partials in CTA order while
+// its own MMAs finish, then adds its own and writes the tile. If it arrives before
+// all the others it leaves its partial too, and whichever arrives last sums the slots
+// in the same order. No CTA waits for another.
 // Roles: warp 0 issues TMA loads (128B-swizzled, weights with an evict-first L2
 // policy), warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 drain the double-
-// buffered TMEM accumulator (tcgen05.ld) into global memory.
+// buffered TMEM accumulator (tcgen05.ld) into global memory, each warp its own 32
+// output channels of a tile (split-tile counting is per warp as well).
 //
 // float32: SIMT kernels (the float32 path must match a float64 reference to 1e-4,
 // which TF32 tensor cores cannot), and a general strided SIMT GEMM for load-time work.
@@ -36,6 +43,11 @@ constexpr int kTcThreadsF8 = 320;
 #endif
 #ifndef FM_TC_CTAS_PER_SM
 #define FM_TC_CTAS_PER_SM 2
+#endif
+// Largest thread-block cluster of the cluster split-K mode (0: stream-K only; above 8
+// needs the non-portable cluster sizes, at most 16).
+#ifndef FM_GEMM_CLUSTER_MAX
+#define FM_GEMM_CLUSTER_MAX 8
 #endif
 
 // One pipeline stage: the bf16 weight tile (A, 128 x 64, 128B-swizzled), the
@@ -67,12 +79,87 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
+// The CTA whose stream-K range [T c / G, T (c + 1) / G) holds unit u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t T, int G) {
+  int c = static_cast<int>(u * G / T);
+  while (c + 1 < G && T * (c + 1) / G <= u) ++c;
+  while (c > 0 && T * c / G > u) --c;
+  return c;
+}
+// The scratch slot of CTA c's partial of tile `tile`: 2c for the first tile of its
+// range, 2c + 1 for its last (only the first and the last tile of a range can be split).
+__device__ __forceinline__ int64_t split_slot(int c, int64_t tile, int64_t T, int G, int KB) {
+  return 2LL * c + ((T * c / G) / KB == tile ? 0 : 1);
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+__device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
+
+// A tile's final value y of (row, n), written as `mode` (an Out) says.
+__device__ __forceinline__ void emit_out(int mode, void* out, int ldo, int row, int n, float y) {
+  const int64_t o = static_cast<int64_t>(row) * ldo + n;
+  if (mode == static_cast<int>(Out::Add))
+    atomicAdd(static_cast<float*>(out) + o, y);  // the one addition this element gets
+  else if (mode == static_cast<int>(Out::Store))
+    static_cast<float*>(out)[o] = y;
+  else
+    static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(gelu_erf(y));
+}
+
+// Thread-block clusters: every thread of every CTA of the cluster arrives, then waits
+// (release / acquire: shared-memory writes before it are visible to the cluster after).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// s[0..15] = sum over the CTAs c_lo + 1 .. c_hi, in that order, of their partials of
+// `tile` (rows c0 .. c0 + 15 of this thread's channel). Stream-K ranges of at least a
+// tile's k blocks give a split tile two parts, so this is one partial's loads.
+template <int BN>
+__device__ __forceinline__ void sum_partials(const float* __restrict__ slots, int c_lo, int c_hi, int64_t tile,
+                                             int64_t T, int G, int KB, int chan, int c0, float (&s)[16]) {
+  float4 acc[4];
+  for (int c = c_lo + 1; c <= c_hi; ++c) {
+    const float4* p = reinterpret_cast<const float4*>(slots + split_slot(c, tile, T, G, KB) * (BN * 128) +
+                                                      static_cast<int64_t>(chan) * BN + c0);
+    float4 t[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = __ldcg(p + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = c == c_lo + 1 ? t[i] : add4(acc[i], t[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    s[4 * i] = acc[i].x, s[4 * i + 1] = acc[i].y, s[4 * i + 2] = acc[i].z, s[4 * i + 3] = acc[i].w;
+  }
+}
+
 template <int BN, bool F8>
-__global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
+__global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
     tc_linear_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
-                     float* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
-                     const float* __restrict__ beta, const float* __restrict__ wscale, int out_zeroed,
-                     const int* __restrict__ rows_dev, unsigned* dev_err) {
+                     void* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
+                     const float* __restrict__ beta, const float* __restrict__ wscale, int mode,
+                     const int* __restrict__ rows_dev, unsigned* red_cnt, float* red_slots, int cs,
+                     unsigned* dev_err) {
   using C = TcCfg<BN, F8>;
   extern __shared__ uint8_t smem_raw[];
   // full: TMA bytes landed; conv (e4m3 only): the bf16 weight tile is written;
@@ -100,8 +187,20 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
   // for it together and DRAM serves it once
   const int mt = (N + 127) >> 7, rt = (R + BN - 1) / BN, KB = (K + 63) >> 6;
   const int64_t T = static_cast<int64_t>(mt) * rt * KB;
-  const int64_t it0 = T * blockIdx.x / gridDim.x, it1 = T * (blockIdx.x + 1) / gridDim.x;
-  if (it0 == it1) return;  // fewer units than CTAs (a device row count below the launch's)
+  int64_t it0, it1;
+  if (cs) {
+    // cluster split-K (fewer tiles than CTAs): cluster c takes tile c, its cs CTAs one
+    // share of the k blocks each, in rank order; the tile is summed through the
+    // cluster's shared memory below. A cluster past the tiles present leaves whole.
+    const int c = blockIdx.x / cs, rk = blockIdx.x - c * cs;
+    if (c >= mt * rt) return;
+    it0 = static_cast<int64_t>(c) * KB + KB * rk / cs;
+    it1 = static_cast<int64_t>(c) * KB + KB * (rk + 1) / cs;
+  } else {
+    it0 = T * blockIdx.x / gridDim.x;
+    it1 = T * (blockIdx.x + 1) / gridDim.x;
+    if (it0 == it1) return;  // fewer units than CTAs (a device row count below the launch's)
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -238,58 +337,204 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
         phase ^= 1u;
       }
     }
-  } else {  // epilogue: warps 2..5, TMEM lane quadrant warp % 4
+  } else {  // epilogue: warps 2..5, TMEM lane quadrant warp % 4, output channels q*32..q*32+31
     pdl_wait();
-    const int q = warp & 3;
+    const int q = warp & 3, chan = q * 32 + lane, G = gridDim.x, bid = blockIdx.x;
+    auto emit = [&](int row, int n, float y) { emit_out(mode, out, ldo, row, n, y); };
+    if (cs) {  // one segment: the raw partial goes to this CTA's shared memory (stage area,
+               // free once the MMAs completed), channel-major with rows padded by 4
+      if (mbar_wait(&acc_full[0], 0, &abort_flag)) {
+        tc_fence_after();
+        float* part = reinterpret_cast<float*>(smem) + chan * (BN + 4);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c0), v);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            reinterpret_cast<float4*>(part + c0)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+    }
     int seg = 0;
-    int64_t it = it0;
+    int64_t it = cs ? it1 : it0;
     while (it < it1) {
       const int64_t tile = it / KB;
       const int kb0 = static_cast<int>(it - tile * KB);
-      const int64_t seg_end = min(it1, (tile + 1) * KB);
+      const int64_t tile_end = (tile + 1) * KB;
+      const int64_t seg_end = min(it1, tile_end);
       const int r = static_cast<int>(tile / mt), m = static_cast<int>(tile - static_cast<int64_t>(r) * mt);
       const int buf = seg & 1;
       const uint32_t aph = (seg >> 1) & 1;
-      if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
-      tc_fence_after();
-      const int n = m * 128 + q * 32 + lane;
-      // No loads here (a load per chunk would stall the drain behind the next tile's
-      // MMAs): a tile whose whole k range is in this segment and whose output starts at
-      // zero is stored; everything else is added with fire-and-forget reductions.
-      const bool store = out_zeroed && kb0 == 0 && seg_end == (tile + 1) * KB;
+      const int n = m * 128 + chan;
       float a = 1.f, b = 0.f;
       if (n < N) {
         if (alpha) a = alpha[n];
         if (F8) a *= wscale[n];  // the weight's per-output-channel scale
-        if (beta && kb0 == 0) b = beta[n];
+        if (beta) b = beta[n];
       }
+      const bool head = kb0 == 0, tail = seg_end == tile_end;
+      const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      if (head && tail) {  // the whole k range is here
+        if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
+        tc_fence_after();
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * BN + c0), v);
-        const int row0 = r * BN + c0;
-        if (n < N) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+          const int row0 = r * BN + c0;
+          if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (row0 + j < R) {
-              float* o = out + static_cast<int64_t>(row0 + j) * ldo + n;
-              if (store)
-                *o = fmaf(a, v[j], b);
-              else
-                atomicAdd(o, fmaf(a, v[j], b));
+            for (int j = 0; j < 16; ++j)
+              if (row0 + j < R) emit(row0 + j, n, fmaf(a, v[j], b));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      } else {  // a split tile: CTAs c_lo .. c_hi hold its k range in order
+        const int c_lo = head ? bid : unit_owner(tile * KB, T, G);
+        const int c_hi = tail ? bid : unit_owner(tile_end - 1, T, G);
+        unsigned* cnt = red_cnt + 4 * c_lo + q;
+        float* mine = red_slots + split_slot(bid, tile, T, G, KB) * (BN * 128) + static_cast<int64_t>(chan) * BN;
+        // The first k blocks' CTA (head) comes here at the end of its range, after the
+        // others; once it sees all of them counted it is the one that sums, and it
+        // loads their partials while its own MMAs finish (narrow tiles: in registers).
+        bool reduce_here = false;
+        constexpr int PRE = 16;
+        float pre[PRE];
+        if (head) {
+          // every lane reads the count with acquire order; all must see it complete
+          reduce_here = __all_sync(0xffffffffu, ld_acquire_u32(cnt) == static_cast<unsigned>(c_hi - c_lo));
+          if (reduce_here && BN == 16) {
+#pragma unroll
+            for (int c0 = 0; c0 < PRE; c0 += 16) {
+              float s16[16];
+              sum_partials<BN>(red_slots, c_lo, c_hi, tile, T, G, KB, chan, c0, s16);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) pre[c0 + j] = s16[j];
             }
           }
         }
+        if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
+        tc_fence_after();
+        if (reduce_here) {  // (others, in CTA order) + own, written out
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16], s16[16];
+            tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+            if constexpr (BN == 16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) s16[j] = pre[c0 + j];
+            } else {
+              sum_partials<BN>(red_slots, c_lo, c_hi, tile, T, G, KB, chan, c0, s16);
+            }
+            const int row0 = r * BN + c0;
+            if (n < N) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (row0 + j < R) emit(row0 + j, n, fmaf(a, s16[j] + v[j], b));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&acc_empty[buf]);
+            *cnt = 0;  // every other CTA of the tile has counted: ready for the next launch
+          }
+        } else {  // leave the partial and count it; the last to count sums
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float v[16];
+            tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+            float4* p = reinterpret_cast<float4*>(mine + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          __threadfence();  // this lane's partial is visible before the count
+          __syncwarp();
+          unsigned ticket = 0;
+          if (lane == 0) {
+            ticket = atomicAdd(cnt, 1u);
+            __threadfence();
+          }
+          ticket = __shfl_sync(0xffffffffu, ticket, 0);
+          if (ticket == static_cast<unsigned>(c_hi - c_lo)) {  // last of all c_hi - c_lo + 1 CTAs
+            __threadfence();
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              float s16[16];
+              sum_partials<BN>(red_slots, c_lo, c_hi, tile, T, G, KB, chan, c0, s16);
+              const float4* p0 = reinterpret_cast<const float4*>(
+                  red_slots + split_slot(c_lo, tile, T, G, KB) * (BN * 128) + static_cast<int64_t>(chan) * BN + c0);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 t = __ldcg(p0 + i);
+                v[4 * i] = t.x, v[4 * i + 1] = t.y, v[4 * i + 2] = t.z, v[4 * i + 3] = t.w;
+              }
+              const int row0 = r * BN + c0;
+              if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row0 + j < R) emit(row0 + j, n, fmaf(a, s16[j] + v[j], b));
+              }
+            }
+            __syncwarp();
+            if (lane == 0) *cnt = 0;
+          }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
       it = seg_end;
       ++seg;
     }
   }
 
   __syncthreads();
+  if (cs) {
+    // Every rank's partial is in its shared memory after the first cluster barrier;
+    // rank rk sums channels [128 rk / cs, 128 (rk + 1) / cs) of the tile over ranks
+    // 0..cs-1 in order and writes them; the second barrier keeps each CTA's shared
+    // memory alive until its peers have read it.
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp >= 2 && warp < 6) {
+      const int c = blockIdx.x / cs, rk = blockIdx.x - c * cs;
+      const int rtile = c / mt, m = c - rtile * mt;
+      const int ch0 = 128 * rk / cs, nch = 128 * (rk + 1) / cs - ch0, groups = BN / 4;
+      const uint32_t pbase = smem_u32(smem);
+      for (int i = threadIdx.x - 64; i < nch * groups; i += 128) {
+        const int g = i / nch, ch = ch0 + (i - g * nch);  // neighbouring threads: neighbouring channels
+        const uint32_t off = pbase + static_cast<uint32_t>((ch * (BN + 4) + 4 * g) * 4);
+        // every rank's value requested before the in-order sum (one round trip, not cs)
+        constexpr int kMaxCs = FM_GEMM_CLUSTER_MAX > 8 ? 16 : 8;
+        float4 t[kMaxCs];
+#pragma unroll
+        for (int k = 0; k < kMaxCs; ++k)
+          if (k < cs) t[k] = ld_dsmem4(cluster_map(off, static_cast<uint32_t>(k)));
+        float4 acc = t[0];
+#pragma unroll
+        for (int k = 1; k < kMaxCs; ++k)
+          if (k < cs) acc = add4(acc, t[k]);
+        const int n = m * 128 + ch;
+        if (n < N) {
+          float a = alpha ? alpha[n] : 1.f;
+          if (F8) a *= wscale[n];
+          const float b = beta ? beta[n] : 0.f;
+          const int row0 = rtile * BN + 4 * g;
+          const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (row0 + e < R) emit_out(mode, out, ldo, row0 + e, n, fmaf(a, v4[e], b));
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();
+  }
   if (threadIdx.x == 0 && abort_flag) {
     // Wait (bounded) for the TMA loads still in flight before the CTA exits.
     for (int64_t i = consumed; i < issued; ++i) {
@@ -310,9 +555,9 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, 1)
 template <typename T>
 __global__ void __launch_bounds__(256) linear_warp_kernel(const T* __restrict__ x, int R, int ldx,
                                                           const T* __restrict__ w, int N, int K,
-                                                          float* __restrict__ out, int ldo,
+                                                          void* __restrict__ out, int ldo,
                                                           const float* __restrict__ alpha,
-                                                          const float* __restrict__ beta) {
+                                                          const float* __restrict__ beta, int mode) {
   constexpr int RB = 4;
   pdl_trigger();
   pdl_wait();
@@ -332,7 +577,16 @@ __global__ void __launch_bounds__(256) linear_warp_kernel(const T* __restrict__ 
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       const float s = warp_sum(acc[j]);
-      if (lane == 0 && r0 + j < R) atomicAdd(out + static_cast<int64_t>(r0 + j) * ldo + n, fmaf(a, s, b));
+      if (lane == 0 && r0 + j < R) {  // one writer per element
+        const int64_t o = static_cast<int64_t>(r0 + j) * ldo + n;
+        const float y = fmaf(a, s, b);
+        if (mode == static_cast<int>(Out::Add))
+          static_cast<float*>(out)[o] = LDCG(static_cast<const float*>(out) + o) + y;
+        else if (mode == static_cast<int>(Out::Store))
+          static_cast<float*>(out)[o] = y;
+        else
+          static_cast<T*>(out)[o] = from_f32<T>(gelu_erf(y));
+      }
     }
   }
 }
@@ -442,8 +696,8 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int BN, bool F8>
-cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, float* out, int ldo,
-                      const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
+cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, int ldx, void* out, int ldo,
+                      const float* alpha, const float* beta, Out mode, const int* rows_dev) {
   using C = TcCfg<BN, F8>;
   CUtensorMap mapX;
   std::string err;
@@ -451,25 +705,59 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   const int64_t mt = (W.N + 127) / 128, rt = (R + BN - 1) / BN, KB = (W.K + 63) / 64;
   const int64_t T = mt * rt * KB;
   const int per_sm = L.ctas_per_sm > 0 ? std::min(L.ctas_per_sm, C::PER_SM) : C::PER_SM;
-  const int G = static_cast<int>(std::min<int64_t>(T, static_cast<int64_t>(L.num_sms) * per_sm));
-  return launch_k(L, tc_linear_kernel<BN, F8>, dim3(G), dim3(C::THREADS), C::SMEM, W.map, mapX, out, ldo, R, W.N,
-                  W.K, alpha, beta, W.wscale, zeroed ? 1 : 0, rows_dev, L.dev_err);
+  const int64_t Gmax = static_cast<int64_t>(L.num_sms) * per_sm, tiles = mt * rt;
+  // At most half as many tiles as CTAs: cluster split-K, cs CTAs per tile (cs <= 8, a
+  // portable cluster), summed in the cluster's shared memory. Otherwise stream-K over
+  // every CTA, whose ranges then cover at least half a tile's k blocks each.
+  const int cs = FM_GEMM_CLUSTER_MAX >= 2 && 2 * tiles <= Gmax && KB >= 2
+                     ? static_cast<int>(std::min<int64_t>({FM_GEMM_CLUSTER_MAX, Gmax / tiles, KB}))
+                     : 0;
+  const int G = cs ? static_cast<int>(tiles * cs) : static_cast<int>(std::min<int64_t>(T, Gmax));
+  // the stream-K split-tile scratch: four counters and two BN x 128 slots per CTA
+  if (!cs && (!L.red.cnt || !L.red.slots || 4LL * G > L.red.cnt_cap || 2LL * G * BN * 128 > L.red.slot_cap))
+    return cudaErrorInvalidValue;
+  return launch_kc(L, tc_linear_kernel<BN, F8>, dim3(G), dim3(C::THREADS), C::SMEM, cs, W.map, mapX, out, ldo, R,
+                  W.N, W.K, alpha, beta, W.wscale, static_cast<int>(mode), rows_dev, L.red.cnt, L.red.slots, cs,
+                  L.dev_err);
 }
 
+int tc_bn(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : rows <= 128 ? 128 : 256; }
+
 template <bool F8>
-cudaError_t launch_tc_rows(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                           const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
-  if (rows <= 16) return launch_tc<16, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
-  if (rows <= 32) return launch_tc<32, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
-  if (rows <= 64) return launch_tc<64, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
-  if (rows <= 128) return launch_tc<128, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
-  return launch_tc<256, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+cudaError_t launch_tc_rows(const Launch& L, const Weight& W, const void* x, int rows, int ldx, void* out, int ldo,
+                           const float* alpha, const float* beta, Out mode, const int* rows_dev) {
+  switch (tc_bn(rows)) {
+    case 16: return launch_tc<16, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
+    case 32: return launch_tc<32, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
+    case 64: return launch_tc<64, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
+    case 128: return launch_tc<128, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
+    default: return launch_tc<256, F8>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
+  }
 }
+
+// The most CTAs a launch of BN-row tiles can have (either weight type).
+template <int BN>
+int64_t tc_max_ctas(int num_sms) {
+  return static_cast<int64_t>(num_sms) * std::max(TcCfg<BN, false>::PER_SM, TcCfg<BN, true>::PER_SM);
+}
+int64_t tc_slot_floats(int bn, int num_sms) {
+  switch (bn) {
+    case 16: return 2 * tc_max_ctas<16>(num_sms) * 16 * 128;
+    case 32: return 2 * tc_max_ctas<32>(num_sms) * 32 * 128;
+    case 64: return 2 * tc_max_ctas<64>(num_sms) * 64 * 128;
+    case 128: return 2 * tc_max_ctas<128>(num_sms) * 128 * 128;
+    default: return 2 * tc_max_ctas<256>(num_sms) * 256 * 128;
+  }
+}
+int64_t tc_cnt_entries(int num_sms) { return 4LL * num_sms * FM_TC_CTAS_PER_SM; }
 
 template <int BN, bool F8>
 cudaError_t set_tc_attr() {
-  return cudaFuncSetAttribute(tc_linear_kernel<BN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              TcCfg<BN, F8>::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(tc_linear_kernel<BN, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcCfg<BN, F8>::SMEM);
+  if (e == cudaSuccess && FM_GEMM_CLUSTER_MAX > 8)
+    e = cudaFuncSetAttribute(tc_linear_kernel<BN, F8>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 template <bool F8>
@@ -538,23 +826,40 @@ bool make_tmap_e4m3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
   return true;
 }
 
-cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta, bool zeroed, const int* rows_dev) {
+size_t gemm_scratch_bytes(int max_rows, int num_sms) {
+  int64_t slots = 0;
+  for (int bn = 16; bn <= tc_bn(std::max(max_rows, 1)); bn *= 2) slots = std::max(slots, tc_slot_floats(bn, num_sms));
+  const size_t cnt = (static_cast<size_t>(tc_cnt_entries(num_sms)) * 4 + 255) / 256 * 256;
+  return cnt + static_cast<size_t>(slots) * 4;
+}
+
+GemmScratch gemm_scratch_carve(void* base, int max_rows, int num_sms) {
+  GemmScratch g;
+  const size_t cnt = (static_cast<size_t>(tc_cnt_entries(num_sms)) * 4 + 255) / 256 * 256;
+  g.cnt = static_cast<unsigned*>(base);
+  g.cnt_cap = tc_cnt_entries(num_sms);
+  g.slots = reinterpret_cast<float*>(static_cast<uint8_t*>(base) + cnt);
+  g.slot_cap = static_cast<int64_t>((gemm_scratch_bytes(max_rows, num_sms) - cnt) / 4);
+  return g;
+}
+
+cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, void* out, int ldo,
+                   const float* alpha, const float* beta, Out mode, const int* rows_dev) {
   if (rows <= 0 || W.N <= 0) return cudaSuccess;
   if (W.dtype == FLASHMAP_BF16) {
     if (!W.has_map) return cudaErrorInvalidValue;
-    return launch_tc_rows<false>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+    return launch_tc_rows<false>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
   }
   if (W.dtype == FLASHMAP_E4M3) {  // e4m3 weights, bf16 activations
     if (!W.has_map || !W.wscale) return cudaErrorInvalidValue;
-    return launch_tc_rows<true>(L, W, x, rows, ldx, out, ldo, alpha, beta, zeroed, rows_dev);
+    return launch_tc_rows<true>(L, W, x, rows, ldx, out, ldo, alpha, beta, mode, rows_dev);
   }
   if (rows_dev) return cudaErrorInvalidValue;  // device row counts: tcgen05 weights only
   if (W.dtype == FLASHMAP_F32) {
     const int64_t threads = static_cast<int64_t>(W.N) * 32;
     const int blocks = static_cast<int>((threads + 255) / 256);
     return launch_k(L, linear_warp_kernel<float>, dim3(blocks), dim3(256), 0, static_cast<const float*>(x), rows,
-                    ldx, static_cast<const float*>(W.ptr), W.N, W.K, out, ldo, alpha, beta);
+                    ldx, static_cast<const float*>(W.ptr), W.N, W.K, out, ldo, alpha, beta, static_cast<int>(mode));
   }
   return cudaErrorInvalidValue;
 }

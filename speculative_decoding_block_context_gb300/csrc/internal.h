@@ -11,29 +11,54 @@
 
 namespace fm {
 
+// Scratch of the tcgen05 GEMM's fixed-order split-tile sums: four counters per CTA of
+// a launch (one per epilogue warp, i.e. per 32 output channels of a tile) and two
+// partial-tile slots per CTA (BN x 128 float32 each). The counters must be zero when a
+// launch starts; every launch that completes leaves them zero. One scratch serves one
+// stream: launches that may overlap on the GPU need their own.
+struct GemmScratch {
+  unsigned* cnt = nullptr;
+  float* slots = nullptr;
+  int64_t cnt_cap = 0, slot_cap = 0;  // capacities in counters and in floats
+};
+
 struct Launch {
   cudaStream_t stream;
   int num_sms;
   unsigned* dev_err;  // the model's device error word (may be null in debug calls)
   bool pdl = true;    // launch with programmatic stream serialization
   int ctas_per_sm = 0;  // tcgen05 GEMM CTAs per SM (0: the kernel's own maximum)
+  GemmScratch red;      // the tcgen05 GEMM's split-tile scratch on this stream
 };
 
-// Launches `kernel` on L.stream, with programmatic stream serialization when L.pdl.
+// Launches `kernel` on L.stream, with programmatic stream serialization when L.pdl,
+// in thread-block clusters of `cluster` CTAs along x when cluster > 1.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                     Args&&... args) {
+cudaError_t launch_kc(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, int cluster,
+                      Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = L.stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = L.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const Launch& L, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     Args&&... args) {
+  return launch_kc(L, kernel, grid, block, smem, 1, static_cast<Args&&>(args)...);
 }
 
 // Zeroes up to kZeroRanges float32 ranges in one launch (accumulators a call sums into).
@@ -51,6 +76,8 @@ struct ZeroList {
   }
 };
 cudaError_t zero_ranges(const Launch& L, const ZeroList& z);
+// One warp waiting limit_ns on an mbarrier nothing arrives on (sets the TIMEOUT bit).
+cudaError_t wait_timeout_probe(const Launch& L, uint64_t limit_ns);
 
 // A GEMM weight W (N out, K in), row-major in device memory.
 struct Weight {
@@ -73,14 +100,26 @@ bool make_tmap_e4m3(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
 // per device before launching; not during stream capture).
 cudaError_t gemm_prepare();
 
-// out[r * ldo + n] += alpha[n] * sum_k x[r * ldx + k] * W[n][k] + beta[n]   (r < rows, n < N)
-// accumulated with float reductions (the output must hold its initial value, e.g. 0,
-// or the residual stream); zeroed = the output is known to be zero, so tiles one CTA
-// covers entirely may be stored instead. alpha / beta may be null (1 / 0). x has W.dtype.
-// rows_dev (tcgen05 weights only): the rows actually present, counted on the device,
-// at most `rows` (the launch is sized for `rows`).
-cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, float* out, int ldo,
-                   const float* alpha, const float* beta, bool zeroed, const int* rows_dev = nullptr);
+// What a linear does with y[r][n] = alpha[n] * sum_k x[r * ldx + k] * W[n][k] + beta[n]:
+//   Add:      float32 out[r * ldo + n] += y  (one addition per element: the residual stream)
+//   Store:    float32 out[r * ldo + n]  = y
+//   GeluAct:  out[r * ldo + n] = GELU_erf(y) in the activation dtype (bf16 for tcgen05
+//             weights, float32 for float32 weights)
+// Every element is finished by one thread with a fixed summation order, so results do
+// not change from run to run.
+enum class Out { Add = 0, Store = 1, GeluAct = 2 };
+
+// Sizes (bytes) of the GEMM scratch for launches of at most max_rows activation rows,
+// and its carving out of `base` (256-byte aligned; counters first).
+size_t gemm_scratch_bytes(int max_rows, int num_sms);
+GemmScratch gemm_scratch_carve(void* base, int max_rows, int num_sms);
+
+// y = x W^T (+ alpha, beta) for r < rows, n < N, written as `mode` says. alpha / beta may
+// be null (1 / 0). x has W.dtype (bf16 for E4M3 weights). rows_dev (tcgen05 weights
+// only): the rows actually present, counted on the device, at most `rows` (the launch
+// is sized for `rows`). tcgen05 launches need L.red large enough for `rows`.
+cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, int ldx, void* out, int ldo,
+                   const float* alpha, const float* beta, Out mode, const int* rows_dev = nullptr);
 
 // General strided SIMT GEMM for load-time work, float32 accumulation:
 // C(m, n) = sum_k A(m, k) B(k, n), A(m, k) = a[arow(m) * sam + k * sak] with
@@ -97,7 +136,7 @@ namespace fm {
 
 // ------------------------------------------------------------------ rows.cu
 struct KvWriteArgs {
-  float* acc = nullptr;  // [rows][ld] float32 projections: per layer [k (D) | v (D)]
+  const float* acc = nullptr;  // [rows][ld] float32 projections: per layer [k (D) | v (D)]
   int64_t ld = 0;
   int rows = 0, W = 1;   // local row i is global row row0 + i = column % W of request / W
   int64_t row0 = 0;
@@ -124,19 +163,20 @@ cudaError_t kv_write(const Launch& L, int dtype, const KvWriteArgs& a);
 // The committed columns of window rows [r0, r0 + rows) (global row g is column g % W of
 // request g / W, committed when the column is below commit_lens[g / W]), in order:
 // row_src[k] = the k-th one's global row, *rows_dev = their count; out_loc[g] = -1 for
-// the others (out_loc may be null). One CTA.
+// the others (out_loc may be null); *total_dev = total_base + the count when total_dev
+// is given. One CTA.
 cudaError_t window_compact(const Launch& L, const int32_t* commit_lens, int W, int64_t r0, int rows,
-                           int32_t* row_src, int* rows_dev, int64_t* out_loc);
+                           int32_t* row_src, int* rows_dev, int64_t* out_loc, int* total_dev = nullptr,
+                           int total_base = 0);
 // xc[k] = x[row_src[k]] for k < *rows_dev; rows of row_bytes bytes (a multiple of 16,
 // 16-byte aligned). One CTA per row of the largest count.
 cudaError_t gather_window_rows(const Launch& L, const void* x, int64_t row_bytes, const int32_t* row_src,
                                const int* rows_dev, int max_rows, void* xc);
 cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, int width, const float* ms,
                         const float* mh, float eps, void* out);
-cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
+cudaError_t rms_rows(const Launch& L, int dtype, const float* acc, int rows, int width, const float* w, float eps,
                      float prescale, const float* add, float gate, void* out, int ldo,
                      const int* rows_dev = nullptr);  // rows_dev: only rows below *rows_dev
-cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* out);
 cudaError_t gather_rows(const Launch& L, int dtype, const void* table, int64_t nrows, int width, const int64_t* ids,
                         int n, void* out);
 cudaError_t draft_noise(const Launch& L, int dtype, const uint64_t* seeds, const int32_t* anchor_pos, int bs, int K,
@@ -160,7 +200,7 @@ cudaError_t philox_export(cudaStream_t s, const uint64_t* seeds, const uint32_t*
 
 // ------------------------------------------------------------------ attention.cu
 struct XattnArgs {
-  float* qacc = nullptr;        // [bs * K][D] float32 query projections (cleared by the combine)
+  const float* qacc = nullptr;  // [bs * K][D] float32 query projections
   const float* q_norm = nullptr;  // [hd] the layer's cross-attention q_norm weight
   float eps = 0.f;
   const float2* rope = nullptr;   // [max_pos][hd / 2]
@@ -186,7 +226,7 @@ struct XattnArgs {
   unsigned* next_item = nullptr;
   unsigned* dev_err = nullptr;
 };
-cudaError_t self_attention(const Launch& L, int dtype, float* qkv, int bs, int K, int nh, int hd, const float* qn,
+cudaError_t self_attention(const Launch& L, int dtype, const float* qkv, int bs, int K, int nh, int hd, const float* qn,
                            const float* kn, float eps, const float2* rope, int max_pos, const int32_t* anchor_pos,
                            void* out, bool early = false);
 int xattn_max_chunks(int num_sms, int nh, int bs);

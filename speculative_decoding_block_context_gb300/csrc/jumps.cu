@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kPrepThreads) state_prep_kernel(float* __restr
   const int n4 = max(0, min(chunk, V - v0)) >> 2;
   float4* st4 = reinterpret_cast<float4*>(state + row * V + v0);
   if (upd) {
-    float4* lg4 = reinterpret_cast<float4*>(logits + row * V + v0);  // a GEMM accumulator: cleared here
+    const float4* lg4 = reinterpret_cast<const float4*>(logits + row * V + v0);  // the GEMM's output
     const float4* b4 = reinterpret_cast<const float4*>(bias + v0);
     float m = -INFINITY, l = 0.f;
     for (int i = threadIdx.x; i < n4; i += blockDim.x) {
@@ -139,7 +139,6 @@ __global__ void __launch_bounds__(kPrepThreads) state_prep_kernel(float* __restr
                                    (keep * o.w + move * expf(x.w - tot.x)) * inv_1s);
       st4[i] = y;
       buf[i] = y;
-      lg4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   } else {
     for (int i = threadIdx.x; i < n4; i += blockDim.x) buf[i] = __ldcg(st4 + i);
@@ -171,8 +170,8 @@ __global__ void __launch_bounds__(kPrepThreads) state_prep_kernel(float* __restr
 }
 
 // The DiT input of a jump, per row (one CTA): state_norm(emb_post) (or the uniform
-// constant u when the posterior is uniform) + gate * noise_norm(emb_state). The
-// embeddings are float32 GEMM accumulators, cleared here.
+// constant u when the posterior is uniform) + gate * noise_norm(emb_state), from the
+// float32 embeddings the GEMM through E^T wrote.
 template <typename T>
 __global__ void __launch_bounds__(256) mix_state_kernel(float* __restrict__ emb_post, float* __restrict__ emb_state,
                                                         int H, const float* __restrict__ u,
@@ -183,8 +182,8 @@ __global__ void __launch_bounds__(256) mix_state_kernel(float* __restrict__ emb_
   pdl_trigger();
   pdl_wait();
   const int64_t row = blockIdx.x;
-  float* ep = emb_post ? emb_post + row * H : nullptr;
-  float* es = emb_state + row * H;
+  const float* ep = emb_post ? emb_post + row * H : nullptr;
+  const float* es = emb_state + row * H;
   float ss_p = 0.f, ss_s = 0.f;
   for (int h = threadIdx.x; h < H; h += blockDim.x) {
     const float a = LDCG(es + h);
@@ -202,8 +201,6 @@ __global__ void __launch_bounds__(256) mix_state_kernel(float* __restrict__ emb_
     const float post = ep ? LDCG(ep + h) * rp * state_w[h] : u[h];
     const float noise = LDCG(es + h) * rs * noise_w[h];
     o[h] = from_f32<T>(post + gate * noise);
-    es[h] = 0.f;
-    if (ep) ep[h] = 0.f;
   }
 }
 

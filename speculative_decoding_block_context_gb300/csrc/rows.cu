@@ -1,9 +1,7 @@
 // Row-wise kernels of the FlashMap step: modulated LayerNorm, RMSNorm variants
-// (context, anchor, noise embedding), GELU, the seeded draft noise, per-head q/k
-// RMSNorm + interleaved RoPE, and the paged context-KV write. Every kernel that
-// reads a GEMM's float32 accumulator also clears it, so the next GEMM into the same
-// buffer starts from zero; the KV write is the exception (its accumulator is zeroed
-// by the caller before each all-layer KV GEMM).
+// (context, anchor, noise embedding), the seeded draft noise, per-head q/k RMSNorm +
+// interleaved RoPE, and the paged context-KV write. The float32 GEMM outputs they read
+// are written whole by their GEMM (every element once), so nothing here clears them.
 
 #include <algorithm>
 #include <climits>
@@ -15,25 +13,7 @@
 namespace fm {
 namespace {
 
-// Loads (and clears) the EPL channels lane*EPL.. of one head vector in one go.
-template <int EPL>
-__device__ __forceinline__ void load_clear_head(float* src, float (&v)[EPL], int lane) {
-  float* p = src + lane * EPL;
-  if constexpr (EPL == 4) {
-    const float4 t = LDCG(reinterpret_cast<const float4*>(p));
-    v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
-    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
-  } else if constexpr (EPL == 2) {
-    const float2 t = LDCG(reinterpret_cast<const float2*>(p));
-    v[0] = t.x, v[1] = t.y;
-    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
-  } else {
-    v[0] = LDCG(p);
-    p[0] = 0.f;
-  }
-}
-
-// Loads the EPL channels lane*EPL.. of one head vector (L2, no clearing).
+// Loads the EPL channels lane*EPL.. of one head vector (L2).
 template <int EPL>
 __device__ __forceinline__ void load_head(const float* src, float (&v)[EPL], int lane) {
   const float* p = src + lane * EPL;
@@ -82,8 +62,7 @@ __device__ __forceinline__ void store_vec(T* dst, const float* v) {
 // loads of per-request scalars) and hands it to the CTA through shared memory, while
 // every warp already streams its head's key and value from the accumulator. Loading
 // the scalars once per CTA instead of once per warp keeps thousands of CTAs from
-// queueing on the same few L2 sectors. The accumulator is left as it is: the caller
-// zeroes it before the GEMM that fills it.
+// queueing on the same few L2 sectors.
 template <typename T, int EPL>
 __global__ void __launch_bounds__(1024, 2) kv_write_kernel(KvWriteArgs a) {
   constexpr int HD = EPL * 32;
@@ -247,10 +226,9 @@ __global__ void __launch_bounds__(kRowThreads) ln_mod_kernel(const float* __rest
   }
 }
 
-// y = prescale * acc; v = y * w * rsqrt(mean(y^2) + eps); out = add ? add + gate * v : v;
-// the accumulator row is cleared.
+// y = prescale * acc; v = y * w * rsqrt(mean(y^2) + eps); out = add ? add + gate * v : v.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict__ acc, int width,
+__global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(const float* __restrict__ acc, int width,
                                                                const float* __restrict__ w, float eps,
                                                                float prescale, const float* __restrict__ add,
                                                                float gate, T* __restrict__ out, int ldo,
@@ -263,7 +241,7 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict
   if (add) load_row4<NV, false>(add, w4, av);
   pdl_wait();
   if (rows_dev && static_cast<int>(blockIdx.x) >= LDCG(rows_dev)) return;  // CTA-uniform
-  float* ar = acc + static_cast<int64_t>(blockIdx.x) * width;
+  const float* ar = acc + static_cast<int64_t>(blockIdx.x) * width;
   load_row4<NV, true>(ar, w4, v);
   float s = 0.f;
 #pragma unroll
@@ -285,7 +263,6 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict
         q[3] = fmaf(gate, q[3], av[i].w);
       }
       store_vec<T, 4>(o + 4 * f, q);
-      reinterpret_cast<float4*>(ar)[f] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 }
@@ -296,7 +273,8 @@ __global__ void __launch_bounds__(kRowThreads) rms_rows_kernel(float* __restrict
 __global__ void __launch_bounds__(1024) window_compact_kernel(const int32_t* __restrict__ commit_lens, int W,
                                                               int64_t r0, int rows, int32_t* __restrict__ row_src,
                                                               int* __restrict__ rows_dev,
-                                                              int64_t* __restrict__ out_loc) {
+                                                              int64_t* __restrict__ out_loc, int* __restrict__ total_dev,
+                                                              int total_base) {
   __shared__ int scan[1024];
   __shared__ int carry;
   pdl_trigger();
@@ -325,7 +303,10 @@ __global__ void __launch_bounds__(1024) window_compact_kernel(const int32_t* __r
     if (threadIdx.x == 1023) carry += scan[1023];
     __syncthreads();
   }
-  if (threadIdx.x == 0) *rows_dev = carry;
+  if (threadIdx.x == 0) {
+    *rows_dev = carry;
+    if (total_dev) *total_dev = total_base + carry;
+  }
 }
 
 __global__ void __launch_bounds__(256) gather_window_rows_kernel(const uint8_t* __restrict__ x, int64_t row_bytes,
@@ -339,31 +320,6 @@ __global__ void __launch_bounds__(256) gather_window_rows_kernel(const uint8_t* 
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(LDCG(row_src + k)) * row_bytes);
   uint4* dst = reinterpret_cast<uint4*>(xc + static_cast<int64_t>(k) * row_bytes);
   for (int64_t i = threadIdx.x; i < row_bytes / 16; i += blockDim.x) dst[i] = src[i];
-}
-
-template <typename T>
-__global__ void gelu_kernel(float* __restrict__ acc, int64_t n, T* __restrict__ out) {
-  pdl_trigger();
-  pdl_wait();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  // four elements per thread and step (16-byte loads and clears) over the whole groups
-  const bool aligned = !(reinterpret_cast<uintptr_t>(acc) & 15) && !(reinterpret_cast<uintptr_t>(out) & (4 * sizeof(T) - 1));
-  const int64_t n4 = aligned ? n >> 2 : 0;
-  for (int64_t i = t0; i < n4; i += stride) {
-    const float4 x = LDCG(reinterpret_cast<const float4*>(acc) + i);
-    const float g[4] = {0.5f * x.x * (1.f + erff(x.x * 0.70710678118654752f)),
-                        0.5f * x.y * (1.f + erff(x.y * 0.70710678118654752f)),
-                        0.5f * x.z * (1.f + erff(x.z * 0.70710678118654752f)),
-                        0.5f * x.w * (1.f + erff(x.w * 0.70710678118654752f))};
-    store_vec<T, 4>(out + 4 * i, g);
-    reinterpret_cast<float4*>(acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int64_t i = 4 * n4 + t0; i < n; i += stride) {
-    const float x = LDCG(acc + i);
-    out[i] = from_f32<T>(0.5f * x * (1.f + erff(x * 0.70710678118654752f)));
-    acc[i] = 0.f;
-  }
 }
 
 // Row copies in 16-byte chunks: grid (rows, chunk blocks).
@@ -466,6 +422,23 @@ __global__ void __launch_bounds__(kFoldThreads) folded_noise_kernel(const uint64
   }
 }
 
+// The timeout path of a pipeline wait, exercised on purpose: one warp waits on an
+// mbarrier that nothing arrives on, with the given limit, through the same bounded
+// wait the pipelines use; the wait gives up and the kernel reports
+// FLASHMAP_DEVERR_TIMEOUT in the error word and returns. No copy or MMA is issued.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns, unsigned* dev_err) {
+  __shared__ uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = mbar_wait_for(&bar, 0, &abort_flag, limit_ns);
+  if (threadIdx.x == 0 && !ok) set_dev_error(dev_err, FLASHMAP_DEVERR_TIMEOUT);
+}
+
 __global__ void zero_kernel(ZeroList z) {
   pdl_trigger();
   pdl_wait();
@@ -484,6 +457,10 @@ __global__ void zero_kernel(ZeroList z) {
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+
+cudaError_t wait_timeout_probe(const Launch& L, uint64_t limit_ns) {
+  return launch_k(L, wait_timeout_probe_kernel, dim3(1), dim3(32), 0, limit_ns, L.dev_err);
+}
 
 cudaError_t zero_ranges(const Launch& L, const ZeroList& z) {
   int64_t total = 0;
@@ -519,10 +496,10 @@ cudaError_t zero_ranges(const Launch& L, const ZeroList& z) {
   } while (0)
 
 cudaError_t window_compact(const Launch& L, const int32_t* commit_lens, int W, int64_t r0, int rows,
-                           int32_t* row_src, int* rows_dev, int64_t* out_loc) {
+                           int32_t* row_src, int* rows_dev, int64_t* out_loc, int* total_dev, int total_base) {
   if (rows <= 0 || W <= 0) return cudaSuccess;
   return launch_k(L, window_compact_kernel, dim3(1), dim3(1024), 0, commit_lens, W, r0, rows, row_src, rows_dev,
-                  out_loc);
+                  out_loc, total_dev, total_base);
 }
 
 cudaError_t gather_window_rows(const Launch& L, const void* x, int64_t row_bytes, const int32_t* row_src,
@@ -581,21 +558,13 @@ cudaError_t ln_mod_rows(const Launch& L, int dtype, const float* x, int rows, in
   return e;
 }
 
-cudaError_t rms_rows(const Launch& L, int dtype, float* acc, int rows, int width, const float* w, float eps,
+cudaError_t rms_rows(const Launch& L, int dtype, const float* acc, int rows, int width, const float* w, float eps,
                      float prescale, const float* add, float gate, void* out, int ldo, const int* rows_dev) {
   if (rows <= 0) return cudaSuccess;
   cudaError_t e = cudaSuccess;
   FM_DISPATCH_T(dtype, FM_DISPATCH_NV(width, (e = launch_k(L, rms_rows_kernel<T, NV>, dim3(rows), dim3(kRowThreads),
                                                           0, acc, width, w, eps, prescale, add, gate,
                                                           static_cast<T*>(out), ldo, rows_dev))));
-  return e;
-}
-
-cudaError_t gelu_rows(const Launch& L, int dtype, float* acc, int64_t n, void* out) {
-  if (n <= 0) return cudaSuccess;
-  const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(L.num_sms) * 16));
-  cudaError_t e = cudaSuccess;
-  FM_DISPATCH_T(dtype, (e = launch_k(L, gelu_kernel<T>, dim3(blocks), dim3(256), 0, acc, n, static_cast<T*>(out))));
   return e;
 }
 

@@ -4,9 +4,11 @@ Some callers cannot allocate device memory (a host runtime that owns all device
 memory and hands a plugin only its input and output buffers, for instance). For them
 the library keeps the sampler's per-row merge slots in a fixed array of its own. This
 checks, through the C ABI, that the entry point draws exactly the tokens that
-flashmap_sample_block draws from the same logits, on two calls in a row (the array
-keeps the previous call's contents, which each call must clear), and that batches
-beyond the array's 8192 rows are refused before anything runs.
+flashmap_sample_block draws from the same logits, on two calls in a row with
+different batch sizes (the array keeps the previous call's contents, which each call
+must clear), with rows sampled by one CTA and by several CTAs that merge through the
+array, and that batches beyond the array's 8192 rows are refused before anything
+runs.
 """
 
 import pytest
@@ -18,16 +20,24 @@ from speculative_decoding_block_context_gb300 import synthetic as syn
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def model():
+def _load(draft_vocab):
     from speculative_decoding_block_context_gb300 import build
 
     build.build()
     cfg = syn.model_config("small_bf16")
+    cfg["draft_vocab_size"] = draft_vocab
     W, E, LM, rank = syn.make_model(cfg, "cuda")
     handle = F.flashmap_load_weights(cfg, W, E, LM, rank)
     torch.cuda.synchronize()
     return cfg, handle, E
+
+
+# Two draft vocabularies: 1234 entries (one CTA per row, scalar loads: 1234 is not a
+# multiple of 4) and 4996 (a multiple of 4 above 4096: three CTAs per row on the
+# vectorised path, merging through the array's per-row keys and counters).
+@pytest.fixture(scope="module", params=[1234, 4996], ids=["vd1234_one_cta_per_row", "vd4996_split_rows"])
+def model(request):
+    return _load(request.param)
 
 
 def _inputs(cfg, bs, seed):
@@ -42,11 +52,14 @@ def _inputs(cfg, bs, seed):
 
 
 def test_static_sampler_matches_sample_block_on_two_calls(model):
+    """Two calls in a row, the larger batch first: the second call's counters start at
+    a lower offset of the array (they follow its bs * K keys), over bytes the first
+    call used as keys."""
     cfg, handle, _ = model
-    bs, K = 5, cfg["block_size"]
+    K = cfg["block_size"]
     vd = cfg["draft_vocab_size"]
-    ws = torch.empty(F.flashmap_workspace_size(handle, bs, 1), dtype=torch.uint8, device="cuda")
-    for call, step in enumerate((7, 8)):
+    ws = torch.empty(F.flashmap_workspace_size(handle, 7, 1), dtype=torch.uint8, device="cuda")
+    for call, (bs, step) in enumerate(((7, 7), (3, 8))):
         hidden, anchor_pos, temperature, greedy, seeds = _inputs(cfg, bs, 100 + call)
         want = torch.empty(bs * K, dtype=torch.int64, device="cuda")
         logits = torch.empty((bs * K, vd), dtype=torch.float32, device="cuda")
@@ -60,8 +73,8 @@ def test_static_sampler_matches_sample_block_on_two_calls(model):
     assert F.flashmap_get_device_error(handle) == 0
 
 
-def test_static_sampler_refuses_batches_beyond_its_array(model):
-    cfg, handle, _ = model
+def test_static_sampler_refuses_batches_beyond_its_array():
+    cfg, handle, _ = _load(1234)
     K = cfg["block_size"]
     bs = 8192 // K + 1
     t = torch.zeros(1, device="cuda")
