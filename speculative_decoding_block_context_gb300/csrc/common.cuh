@@ -62,6 +62,26 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ------------------------------------------------------------------ stream-K partition
+// (the tcgen05 GEMM's units (tile, 64-wide k block) cut into G contiguous ranges
+// [T c / G, T (c + 1) / G); a reader of its split outputs repeats the same arithmetic)
+
+// The CTA whose range holds unit u.
+__host__ __device__ __forceinline__ int unit_owner(int64_t u, int64_t T, int G) {
+  int c = static_cast<int>(u * G / T);
+  while (c + 1 < G && T * (c + 1) / G <= u) ++c;
+  while (c > 0 && T * c / G > u) --c;
+  return c;
+}
+// The scratch slot of CTA c's part of tile `tile`: 2c for the first tile of its range,
+// 2c + 1 for its last (ranges of at most a tile's k blocks touch two tiles).
+__host__ __device__ __forceinline__ int64_t split_slot(int c, int64_t tile, int64_t T, int G, int KB) {
+  return 2LL * c + ((T * c / G) / KB == tile ? 0 : 1);
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

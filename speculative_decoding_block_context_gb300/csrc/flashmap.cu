@@ -553,7 +553,8 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   void* scratch = nullptr;
   const size_t fold_bytes = m->noise_path == 1 ? align_up(fm::folded_scratch_bytes(static_cast<int>(H))) : 0;
   const size_t scratch_bytes =
-      align_up(H * H * 8) + align_up(H * 8) + align_up(C * 8) + align_up(std::max(D, H) * 4) + fold_bytes;
+      align_up(H * H * 8) + align_up(static_cast<size_t>(fm::colsum_doubles(m->V, m->H)) * 8) + align_up(C * 8) +
+      align_up(std::max(D, H) * 4) + fold_bytes;
   if (cudaMalloc(&scratch, scratch_bytes) != cudaSuccess) {
     cudaGetLastError();
     return cleanup(fail(FLASHMAP_E_NOMEM, "cannot allocate load-time scratch"));
@@ -564,7 +565,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   } guard{scratch};
   Carver sc(scratch);
   double* gram = sc.take<double>(H * H * 8);
-  double* colsum = sc.take<double>(H * 8);
+  double* colsum = sc.take<double>(static_cast<size_t>(fm::colsum_doubles(m->V, m->H)) * 8);
   double* cond = sc.take<double>(C * 8);
   float* tmp_d = sc.take<float>(std::max(D, H) * 4);  // D or H floats of scratch
   void* fold_scratch = fold_bytes ? sc.take<void>(fold_bytes) : nullptr;
@@ -697,8 +698,7 @@ flashmap_status flashmap_load_weights(const flashmap_config* cfg, const flashmap
   LCHK(fm::uniform_constant(s, embedding, adt, V, m->H, tmp_d, cfg->rms_norm_eps, colsum, m->u));
   if (m->noise_path == 1) {  // the eigenbasis is sensitive to the gram: float64 products and sums
     LCHK(fm::gram_f64(s, embedding, adt, V, m->H, gram));
-  } else {  // float32 partial sums of 1024 products, added in float64
-    LCHK(cudaMemsetAsync(gram, 0, H * H * 8, s));
+  } else {  // float32 partial sums of 1024 products, added in float64 in order
     LCHK(fm::simt_gemm(s, m->H, m->H, m->V, embedding, adt, nullptr, 1, H, embedding, adt, H, 1, gram, FLASHMAP_F32, H, 2));
   }
   LCHK(fm::cholesky_f64(s, gram, m->H, m->dev_err));
@@ -1120,18 +1120,34 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
   xa.early = FM_XATTN_EARLY && fork ? 1 : 0;
   // (one block: every item is the same length, and a fixed stride needs no counter)
   xa.next_item = FM_XATTN_DYNAMIC && bsc > 1 ? ws.xnext : nullptr;
+  // The residual stream x: x_embed (or the folded noise) stores its start, the gated o,
+  // cross-o and fc2 outputs are added to it once per element.
+  auto resid_linear = [&](const Launch& Lx, int layer, const Weight& W, const void* in, int ldx, const float* alpha,
+                          const float* beta, bool add) -> flashmap_status {
+    TIMED_GEMM(layer, W, R, fm::linear(Lx, W, in, R, ldx, ws.x, D, alpha, beta, add ? fm::Out::Add : fm::Out::Store));
+    return FLASHMAP_OK;
+  };
+  auto ln_mod = [&](const Launch& Lx, int layer, const float* scale, const float* shift, void* out) -> flashmap_status {
+    TIMED(FLASHMAP_KIND_ROWS, layer, fm::ln_mod_rows(Lx, adt, ws.x, R, D, scale, shift, eps_ln, out));
+    return FLASHMAP_OK;
+  };
+#define FM_TRY(call)                             \
+  do {                                           \
+    const flashmap_status st_ = (call);          \
+    if (st_ != FLASHMAP_OK) return st_;          \
+  } while (0)
   // the DiT blocks and the final AdaLN with one jump's modulations (null: the one jump's)
   auto dit = [&](const float* mods_all, const float* beta_all, const float* fin, void* out) -> flashmap_status {
     for (int l = 0; l < m->L; ++l) {
       const LayerW& lw = m->layers[l];
       const float* md = mods_all ? mods_all + static_cast<size_t>(l) * 9 * D : lw.mods;
       const float* fc2_beta = beta_all ? beta_all + static_cast<size_t>(l) * D : lw.fc2_beta;
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 0 * D, md + 1 * D, eps_ln, ws.act));
+      FM_TRY(ln_mod(Lc, l, md + 0 * D, md + 1 * D, ws.act));
       TIMED_GEMM(l, lw.qkv, R, fm::linear(Lc, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, fm::Out::Store));
       TIMED(FLASHMAP_KIND_SELF_ATTN, l, fm::self_attention(Lc, adt, ws.acc_big, bsc, m->K, m->nh, m->hd, lw.qn, lw.kn, eps_qk, m->rope, m->maxpos,
                                  pos_x, ws.act, xa.early != 0 && (n_cand == 1 || l > 0)));
-      TIMED_GEMM(l, lw.o, R, fm::linear(Lc, lw.o, ws.act, R, D, ws.x, D, md + 2 * D, nullptr, fm::Out::Add));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 3 * D, md + 4 * D, eps_ln, ws.act));
+      FM_TRY(resid_linear(Lc, l, lw.o, ws.act, D, md + 2 * D, nullptr, true));
+      FM_TRY(ln_mod(Lc, l, md + 3 * D, md + 4 * D, ws.act));
       TIMED_GEMM(l, lw.cq, R, fm::linear(Lc, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, fm::Out::Store));
       if (!joined) {  // the anchor rows are in the pool from here on
         FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
@@ -1142,18 +1158,18 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
       xa.q_norm = lw.cqn;
       TIMED(FLASHMAP_KIND_XATTN, l, fm::xattn_items(Lc, m->kdt, xa, kvmap_ok ? &kvmap : nullptr));
       TIMED(FLASHMAP_KIND_XCOMBINE, l, fm::xattn_combine(Lc, adt, xa, ws.act));
-      TIMED_GEMM(l, lw.co, R, fm::linear(Lc, lw.co, ws.act, R, D, ws.x, D, md + 5 * D, nullptr, fm::Out::Add));
-      TIMED(FLASHMAP_KIND_ROWS, l, fm::ln_mod_rows(Lc, adt, ws.x, R, D, md + 6 * D, md + 7 * D, eps_ln, ws.act));
+      FM_TRY(resid_linear(Lc, l, lw.co, ws.act, D, md + 5 * D, nullptr, true));
+      FM_TRY(ln_mod(Lc, l, md + 6 * D, md + 7 * D, ws.act));
       // fc1 + bias + GELU in the GEMM's epilogue, written in the activation dtype
       TIMED_GEMM(l, lw.fc1, R, fm::linear(Lc, lw.fc1, ws.act, R, D, ws.act_f, m->F, nullptr, lw.fc1_b, fm::Out::GeluAct));
-      TIMED_GEMM(l, lw.fc2, R, fm::linear(Lc, lw.fc2, ws.act_f, R, m->F, ws.x, D, md + 8 * D, fc2_beta, fm::Out::Add));
+      FM_TRY(resid_linear(Lc, l, lw.fc2, ws.act_f, m->F, md + 8 * D, fc2_beta, true));
     }
     if (!joined) {
       FM_CUDA(cudaStreamWaitEvent(s, m->ev_join, 0));
       joined = true;
       Lc = Lh;
     }
-    TIMED(FLASHMAP_KIND_ROWS, -1, fm::ln_mod_rows(Lc, adt, ws.x, R, D, fin, fin + D, eps_ln, out));
+    FM_TRY(ln_mod(Lc, -1, fin, fin + D, out));
     return FLASHMAP_OK;
   };
   if (m->steps == 1 && m->noise_path == 1) {
@@ -1161,7 +1177,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     // then one GEMM through M onto x_embed(u)
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::folded_noise(Lc, adt, seeds, anchor_pos, bs, m->K, H, n_cand, noise_scale,
                                                    m->fold_var, m->cfg.rms_norm_eps, m->gate, ws.act));
-    TIMED_GEMM(-1, m->fold, R, fm::linear(Lc, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, fm::Out::Store));
+    FM_TRY(resid_linear(Lc, -1, m->fold, ws.act, H, nullptr, m->fold_xu, false));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   if (m->steps == 1) {
@@ -1170,7 +1186,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
     TIMED_GEMM(-1, m->chol, R, fm::linear(Lc, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, fm::Out::Store));
     TIMED(FLASHMAP_KIND_ROWS, -1, fm::rms_rows(Lc, adt, ws.acc_big, R, H, m->noise_norm_w, m->cfg.rms_norm_eps, noise_scale, m->u, m->gate,
                          ws.act, H));
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
+    FM_TRY(resid_linear(Lc, -1, m->xe, ws.act, H, nullptr, m->xe_b, false));
     return dit(nullptr, nullptr, m->final_mods, hidden_out);
   }
   // several jumps: the state starts as V-wide noise keyed like the one-jump noise
@@ -1200,7 +1216,7 @@ static flashmap_status draft_impl(flashmap_model* m, const flashmap_kv_pool* poo
                                                 R, H, m->u, m->state_norm_w, m->noise_norm_w, m->cfg.rms_norm_eps,
                                                 m->step_gate[st], ws.act));
     // the residual stream (re)starts at x_embed of this jump's input
-    TIMED_GEMM(-1, m->xe, R, fm::linear(Lc, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
+    FM_TRY(resid_linear(Lc, -1, m->xe, ws.act, H, nullptr, m->xe_b, false));
     const bool last = st + 1 == m->steps;
     const size_t L = static_cast<size_t>(m->L);
     const flashmap_status r = dit(m->step_mods + st * L * 9 * D, m->step_fc2_beta + st * L * D,
@@ -1381,6 +1397,11 @@ flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32
   int32_t n = 0;
   // algorithmic bytes of one launch: weights once (e4m3: one byte and a float32 scale
   // per output channel), activations read, outputs written (float32, or act dtype)
+  // the residual-stream linears: x_embed stores, the gated outputs add
+  auto resid = [&](const Launch& L, const Weight& W, const void* in, int rows, int ldx, float* x, const float* alpha,
+                   const float* beta, bool add) -> cudaError_t {
+    return fm::linear(L, W, in, rows, ldx, x, D, alpha, beta, add ? fm::Out::Add : fm::Out::Store);
+  };
   auto count = [&](const Weight& W, int rows, size_t out_es) {
     const size_t wb = W.dtype == FLASHMAP_E4M3 ? static_cast<size_t>(W.N) * W.K + static_cast<size_t>(W.N) * 4
                                                 : static_cast<size_t>(W.N) * W.K * es;
@@ -1410,27 +1431,27 @@ flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32
     FM_CUDA(fm::linear(L, m->ctx_kv, ws.kv_in, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, fm::Out::Store));
     count(m->ctx_kv, bs, 4);
     if (m->noise_path == 1) {
-      FM_CUDA(fm::linear(L, m->fold, ws.act, R, H, ws.x, D, nullptr, m->fold_xu, fm::Out::Store));
+      FM_CUDA(resid(L, m->fold, ws.act, R, H, ws.x, nullptr, m->fold_xu, false));
       count(m->fold, R, 4);
     } else {
       FM_CUDA(fm::linear(L, m->chol, ws.act, R, H, ws.acc_big, H, nullptr, nullptr, fm::Out::Store));
       count(m->chol, R, 4);
-      FM_CUDA(fm::linear(L, m->xe, ws.act, R, H, ws.x, D, nullptr, m->xe_b, fm::Out::Store));
+      FM_CUDA(resid(L, m->xe, ws.act, R, H, ws.x, nullptr, m->xe_b, false));
       count(m->xe, R, 4);
     }
     for (int l = 0; l < m->L; ++l) {
       const LayerW& lw = m->layers[l];
       FM_CUDA(fm::linear(L, lw.qkv, ws.act, R, D, ws.acc_big, 3 * D, nullptr, nullptr, fm::Out::Store));
       count(lw.qkv, R, 4);
-      FM_CUDA(fm::linear(L, lw.o, ws.act, R, D, ws.x, D, lw.mods + 2 * D, nullptr, fm::Out::Add));
+      FM_CUDA(resid(L, lw.o, ws.act, R, D, ws.x, lw.mods + 2 * D, nullptr, true));
       count(lw.o, R, 4);
       FM_CUDA(fm::linear(L, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, fm::Out::Store));
       count(lw.cq, R, 4);
-      FM_CUDA(fm::linear(L, lw.co, ws.act, R, D, ws.x, D, lw.mods + 5 * D, nullptr, fm::Out::Add));
+      FM_CUDA(resid(L, lw.co, ws.act, R, D, ws.x, lw.mods + 5 * D, nullptr, true));
       count(lw.co, R, 4);
       FM_CUDA(fm::linear(L, lw.fc1, ws.act, R, D, ws.act_f, m->F, nullptr, lw.fc1_b, fm::Out::GeluAct));
       count(lw.fc1, R, es);
-      FM_CUDA(fm::linear(L, lw.fc2, ws.act_f, R, m->F, ws.x, D, lw.mods + 8 * D, lw.fc2_beta, fm::Out::Add));
+      FM_CUDA(resid(L, lw.fc2, ws.act_f, R, m->F, ws.x, lw.mods + 8 * D, lw.fc2_beta, true));
       count(lw.fc2, R, 4);
     }
   }
@@ -1504,17 +1525,25 @@ flashmap_status flashmap_debug_linear(int32_t dtype, const void* x, const void* 
     return fail(FLASHMAP_E_CUDA, err);
   }
   Launch Lh{s, sms, nullptr, true};
-  // the GEMM's split-tile scratch for this one launch (a test hook: it may allocate)
-  void* red = nullptr;
+  // the GEMM's split-tile scratch (a test hook: it keeps one buffer per device, grown
+  // when a call needs more, so that timing it measures the kernel, not allocation)
+  static std::vector<std::pair<void*, size_t>> scratch(64, {nullptr, 0});
   const size_t red_bytes = fm::gemm_scratch_bytes(rows, sms);
-  cudaError_t e = cudaMallocAsync(&red, red_bytes, s);
-  if (e == cudaSuccess) {
-    Lh.red = fm::gemm_scratch_carve(red, rows, sms);
-    e = cudaMemsetAsync(Lh.red.cnt, 0, static_cast<size_t>(Lh.red.cnt_cap) * 4, s);
+  cudaError_t e = cudaSuccess;
+  if (dev < 0 || dev >= 64) e = cudaErrorInvalidDevice;
+  if (e == cudaSuccess && scratch[dev].second < red_bytes) {
+    if (scratch[dev].first) cudaFree(scratch[dev].first);  // synchronizes: a test hook
+    scratch[dev] = {nullptr, 0};
+    e = cudaMalloc(&scratch[dev].first, red_bytes);
+    if (e == cudaSuccess) {
+      scratch[dev].second = red_bytes;
+      e = cudaMemset(scratch[dev].first, 0, red_bytes);  // counters start at zero; launches leave them so
+    }
   }
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    Lh.red = fm::gemm_scratch_carve(scratch[dev].first, rows, sms);
     e = fm::linear(Lh, W, x, rows, in_features, out, out_features, nullptr, nullptr, fm::Out::Add);
-  if (red) cudaFreeAsync(red, s);
+  }
   if (q) cudaFreeAsync(q, s);
   FM_CUDA(e);
   return FLASHMAP_OK;

@@ -44,6 +44,11 @@ constexpr int kTcThreadsF8 = 320;
 #ifndef FM_TC_CTAS_PER_SM
 #define FM_TC_CTAS_PER_SM 2
 #endif
+// Whole tiles of 64 rows or more added onto the output by read-add-write (1) or by L2
+// reductions (0).
+#ifndef FM_GEMM_ADD_RMW
+#define FM_GEMM_ADD_RMW 1
+#endif
 // Largest thread-block cluster of the cluster split-K mode (0: stream-K only; above 8
 // needs the non-portable cluster sizes, at most 16).
 #ifndef FM_GEMM_CLUSTER_MAX
@@ -79,33 +84,18 @@ __device__ __forceinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
-// The CTA whose stream-K range [T c / G, T (c + 1) / G) holds unit u.
-__device__ __forceinline__ int unit_owner(int64_t u, int64_t T, int G) {
-  int c = static_cast<int>(u * G / T);
-  while (c + 1 < G && T * (c + 1) / G <= u) ++c;
-  while (c > 0 && T * c / G > u) --c;
-  return c;
-}
-// The scratch slot of CTA c's partial of tile `tile`: 2c for the first tile of its
-// range, 2c + 1 for its last (only the first and the last tile of a range can be split).
-__device__ __forceinline__ int64_t split_slot(int c, int64_t tile, int64_t T, int G, int KB) {
-  return 2LL * c + ((T * c / G) / KB == tile ? 0 : 1);
-}
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-__device__ __forceinline__ float4 add4(float4 a, float4 b) {
-  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 __device__ __forceinline__ float gelu_erf(float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); }
 
 // A tile's final value y of (row, n), written as `mode` (an Out) says.
 __device__ __forceinline__ void emit_out(int mode, void* out, int ldo, int row, int n, float y) {
   const int64_t o = static_cast<int64_t>(row) * ldo + n;
-  if (mode == static_cast<int>(Out::Add))
-    atomicAdd(static_cast<float*>(out) + o, y);  // the one addition this element gets
+  if (mode == static_cast<int>(Out::Add))  // the one addition this element gets: a reduction, no return value
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(static_cast<float*>(out) + o), "f"(y) : "memory");
   else if (mode == static_cast<int>(Out::Store))
     static_cast<float*>(out)[o] = y;
   else
@@ -380,9 +370,25 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 16) {
+          const int row0 = r * BN + c0;
+          if (FM_GEMM_ADD_RMW && BN >= 64 && mode == static_cast<int>(Out::Add)) {
+            // one writer per element: read, add and write back (the 16 rows' loads
+            // issued together, before the accumulator read) instead of L2 reductions
+            float o16[16];
+            float* op = static_cast<float*>(out) + static_cast<int64_t>(row0) * ldo + n;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o16[j] = (n < N && row0 + j < R) ? __ldcg(op + static_cast<int64_t>(j) * ldo) : 0.f;
+            float v[16];
+            tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+            if (n < N) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (row0 + j < R) op[static_cast<int64_t>(j) * ldo] = o16[j] + fmaf(a, v[j], b);
+            }
+            continue;
+          }
           float v[16];
           tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
-          const int row0 = r * BN + c0;
           if (n < N) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -419,21 +425,54 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
         if (!mbar_wait(&acc_full[buf], aph, &abort_flag)) break;
         tc_fence_after();
         if (reduce_here) {  // (others, in CTA order) + own, written out
-#pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 16) {
-            float v[16], s16[16];
-            tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
-            if constexpr (BN == 16) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) s16[j] = pre[c0 + j];
-            } else {
-              sum_partials<BN>(red_slots, c_lo, c_hi, tile, T, G, KB, chan, c0, s16);
-            }
-            const int row0 = r * BN + c0;
+          if constexpr (BN == 16) {
+            float v[16];
+            tmem_ld16(tacc, v);
+            const int row0 = r * BN;
             if (n < N) {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (row0 + j < R) emit(row0 + j, n, fmaf(a, s16[j] + v[j], b));
+                if (row0 + j < R) emit(row0 + j, n, fmaf(a, pre[j] + v[j], b));
+            }
+          } else if (c_hi == c_lo + 1) {
+            // the usual case (tiles at least as many as CTAs: two parts): the other
+            // part's next 16 rows are requested while this chunk is summed
+            const float4* op = reinterpret_cast<const float4*>(
+                red_slots + split_slot(c_hi, tile, T, G, KB) * (BN * 128) + static_cast<int64_t>(chan) * BN);
+            float4 cur[4], nxt[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) cur[i] = __ldcg(op + i);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              if (c0 + 16 < BN) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) nxt[i] = __ldcg(op + (c0 + 16) / 4 + i);
+              }
+              float v[16];
+              tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+              const float o16[16] = {cur[0].x, cur[0].y, cur[0].z, cur[0].w, cur[1].x, cur[1].y, cur[1].z, cur[1].w,
+                                     cur[2].x, cur[2].y, cur[2].z, cur[2].w, cur[3].x, cur[3].y, cur[3].z, cur[3].w};
+              const int row0 = r * BN + c0;
+              if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row0 + j < R) emit(row0 + j, n, fmaf(a, o16[j] + v[j], b));
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+            }
+          } else {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+              float v[16], s16[16];
+              tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+              sum_partials<BN>(red_slots, c_lo, c_hi, tile, T, G, KB, chan, c0, s16);
+              const int row0 = r * BN + c0;
+              if (n < N) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (row0 + j < R) emit(row0 + j, n, fmaf(a, s16[j] + v[j], b));
+              }
             }
           }
           tc_fence_before();
@@ -605,8 +644,17 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(int M, int N, int K, int
   __shared__ float As[16][65], Bs[16][65];
   const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  const int kbeg = blockIdx.z * kchunk, kend = min(K, kbeg + kchunk);
-  float acc[4][4] = {};
+  // mode 2: the k range in chunks of kchunk, each summed in float32 and added into
+  // float64 in chunk order (one block owns its tile: no atomics, a fixed order)
+  const int nchunks = mode == 2 ? (K + kchunk - 1) / kchunk : 1;
+  double acc64[4][4] = {};
+  float acc[4][4];
+  for (int chunk = 0; chunk < nchunks; ++chunk) {
+  const int kbeg = mode == 2 ? chunk * kchunk : blockIdx.z * kchunk, kend = min(K, kbeg + kchunk);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   for (int k0 = kbeg; k0 < kend; k0 += 16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -654,6 +702,13 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(int M, int N, int K, int
     }
     __syncthreads();
   }
+  if (mode == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc64[i][j] += static_cast<double>(acc[i][j]);
+  }
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int gm = m0 + tm * 4 + i;
@@ -671,7 +726,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(int M, int N, int K, int
         else
           static_cast<__nv_bfloat16*>(c)[idx] = __float2bfloat16_rn(acc[i][j]);
       } else {
-        atomicAdd(static_cast<double*>(c) + idx, static_cast<double>(acc[i][j]));
+        static_cast<double*>(c)[idx] = acc64[i][j];
       }
     }
   }
@@ -712,7 +767,11 @@ cudaError_t launch_tc(const Launch& L, const Weight& W, const void* x, int R, in
   const int cs = FM_GEMM_CLUSTER_MAX >= 2 && 2 * tiles <= Gmax && KB >= 2
                      ? static_cast<int>(std::min<int64_t>({FM_GEMM_CLUSTER_MAX, Gmax / tiles, KB}))
                      : 0;
-  const int G = cs ? static_cast<int>(tiles * cs) : static_cast<int>(std::min<int64_t>(T, Gmax));
+  // Between half as many tiles as CTAs and as many: one whole tile per CTA (stream-K
+  // over all the CTAs would give a tile up to three parts, summed at the end of the
+  // kernel by its last CTA). From as many tiles as CTAs up: stream-K, two parts at most.
+  const int G = cs ? static_cast<int>(tiles * cs)
+                   : static_cast<int>(tiles < Gmax ? std::min<int64_t>(tiles, T) : std::min<int64_t>(T, Gmax));
   // the stream-K split-tile scratch: four counters and two BN x 128 slots per CTA
   if (!cs && (!L.red.cnt || !L.red.slots || 4LL * G > L.red.cnt_cap || 2LL * G * BN * 128 > L.red.slot_cap))
     return cudaErrorInvalidValue;
@@ -868,12 +927,9 @@ cudaError_t simt_gemm(cudaStream_t s, int M, int N, int K, const void* a, int a_
                       int64_t sam, int64_t sak, const void* b, int b_dtype, int64_t sbk, int64_t sbn, void* c,
                       int c_dtype, int64_t ldc, int mode) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
-  int kchunk = K, kz = 1;
-  if (mode == 2) {  // float32 partial sums over 1024-long k ranges, added in float64
-    kchunk = 1024;
-    kz = (K + kchunk - 1) / kchunk;
-  }
-  dim3 grid((N + 63) / 64, (M + 63) / 64, kz);
+  // mode 2: float32 partial sums over 1024-long k ranges, added in float64 in order
+  const int kchunk = mode == 2 ? 1024 : K;
+  dim3 grid((N + 63) / 64, (M + 63) / 64, 1);
   simt_gemm_kernel<<<grid, 256, 0, s>>>(M, N, K, kchunk, a, a_dtype, a_rows, sam, sak, b, b_dtype, sbk, sbn, c,
                                         c_dtype, ldc, mode);
   return cudaGetLastError();

@@ -124,8 +124,9 @@ cudaError_t linear(const Launch& L, const Weight& W, const void* x, int rows, in
 // General strided SIMT GEMM for load-time work, float32 accumulation:
 // C(m, n) = sum_k A(m, k) B(k, n), A(m, k) = a[arow(m) * sam + k * sak] with
 // arow(m) = a_rows ? a_rows[m] : m, B(k, n) = b[k * sbk + n * sbn]; types by dtype codes.
-// mode 0: c_f32[m * ldc + n] = acc;  mode 1: c (dtype c_dtype) = acc;  mode 2: atomic
-// double add into c_f64[m * ldc + n].
+// mode 0: c_f32[m * ldc + n] = acc;  mode 1: c (dtype c_dtype) = acc;  mode 2:
+// c_f64[m * ldc + n] = the float64 sum, in k order, of float32 sums over 1024-long k
+// chunks (deterministic).
 cudaError_t simt_gemm(cudaStream_t s, int M, int N, int K, const void* a, int a_dtype, const int64_t* a_rows,
                       int64_t sam, int64_t sak, const void* b, int b_dtype, int64_t sbk, int64_t sbn, void* c,
                       int c_dtype, int64_t ldc, int mode);
@@ -269,6 +270,8 @@ cudaError_t adaln(cudaStream_t s, const void* w, const void* b, int dtype, int C
                   float* s1, float* sh, float* gate);
 cudaError_t uniform_constant(cudaStream_t s, const void* E, int dtype, int64_t V, int H, const float* w, float eps,
                              double* colsum, float* u);
+// The doubles uniform_constant's colsum scratch holds (per-row-block column sums).
+int64_t colsum_doubles(int64_t V, int H);
 cudaError_t cholesky_f64(cudaStream_t s, double* A, int n, unsigned* err);
 // folded-noise eigenbasis (eigen.cu): from the Cholesky factor's storage X (row-major
 // L, n x n float64; overwritten), the folded projection proj (D x n, dtype), lam / n

@@ -82,7 +82,10 @@ __global__ void adaln_kernel(const void* w, const void* b, int dtype, int C, int
     gate[j - 2 * D] = static_cast<float>(acc);
 }
 
-// Column sums of E in float64.
+constexpr int kColsumRows = 2048;
+
+// Column sums of E in float64 over blocks of rows: out[block][col] (summed in block
+// order by uniform_kernel, so the result does not depend on scheduling).
 __global__ void colsum_kernel(const void* E, int dtype, int64_t V, int H, int rows_per_block, double* out) {
   const int col = blockIdx.x * blockDim.x + threadIdx.x;
   if (col >= H) return;
@@ -90,12 +93,18 @@ __global__ void colsum_kernel(const void* E, int dtype, int64_t V, int H, int ro
   const int64_t r1 = r0 + rows_per_block < V ? r0 + rows_per_block : V;
   double acc = 0.0;
   for (int64_t r = r0; r < r1; ++r) acc += load_as_f32(E, dtype, r * H + col);
-  atomicAdd(out + col, acc);
+  out[static_cast<int64_t>(blockIdx.y) * H + col] = acc;
 }
 
-// u = state_norm(colsum / V): RMSNorm with weight w (float32 out). One block.
-__global__ void uniform_kernel(const double* colsum, int64_t V, int H, const float* w, float eps, float* u) {
+// u = state_norm(colsum / V): RMSNorm with weight w (float32 out), colsum the column
+// sums of `blocks` row blocks, added in block order first. One block.
+__global__ void uniform_kernel(double* colsum, int blocks, int64_t V, int H, const float* w, float eps, float* u) {
   __shared__ double red[32];
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    double c = colsum[i];
+    for (int b = 1; b < blocks; ++b) c += colsum[static_cast<int64_t>(b) * H + i];
+    colsum[i] = c;
+  }
   double s = 0.0;
   for (int i = threadIdx.x; i < H; i += blockDim.x) {
     const double m = colsum[i] / static_cast<double>(V);
@@ -261,14 +270,14 @@ cudaError_t adaln(cudaStream_t s, const void* w, const void* b, int dtype, int C
   return cudaGetLastError();
 }
 
+int64_t colsum_doubles(int64_t V, int H) { return (V + kColsumRows - 1) / kColsumRows * H; }
+
 cudaError_t uniform_constant(cudaStream_t s, const void* E, int dtype, int64_t V, int H, const float* w, float eps,
                              double* colsum, float* u) {
-  cudaError_t e = cudaMemsetAsync(colsum, 0, sizeof(double) * H, s);
-  if (e != cudaSuccess) return e;
-  const int rpb = 2048;
-  dim3 grid((H + 255) / 256, static_cast<unsigned>((V + rpb - 1) / rpb));
-  colsum_kernel<<<grid, 256, 0, s>>>(E, dtype, V, H, rpb, colsum);
-  uniform_kernel<<<1, 1024, 0, s>>>(colsum, V, H, w, eps, u);
+  const int blocks = static_cast<int>((V + kColsumRows - 1) / kColsumRows);
+  dim3 grid((H + 255) / 256, static_cast<unsigned>(blocks));
+  colsum_kernel<<<grid, 256, 0, s>>>(E, dtype, V, H, kColsumRows, colsum);
+  uniform_kernel<<<1, 1024, 0, s>>>(colsum, blocks, V, H, w, eps, u);
   return cudaGetLastError();
 }
 

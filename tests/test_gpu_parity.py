@@ -279,6 +279,25 @@ def _assert_same_bits(a, b, cfg):
     assert torch.equal(a.tokens, b.tokens)
 
 
+def test_load_is_repeatable():
+    """Two loads of the same weights derive the same constants bit for bit (the gram
+    and the column sums of E are summed in a fixed order) and so draft the same blocks."""
+    a = load_model("small_bf16", oracle=False)
+    b = load_model("small_bf16", oracle=False)
+    H = a.cfg["target_hidden"]
+    got = []
+    for st in (a, b):
+        chol = torch.empty((H, H), dtype=torch.float32, device="cuda")
+        u = torch.empty(H, dtype=torch.float32, device="cuda")
+        F.flashmap_debug_constants(st.handle, chol, u, None)
+        got.append((chol, u))
+    torch.cuda.synchronize()
+    assert torch.equal(got[0][0].view(torch.int32), got[1][0].view(torch.int32))
+    assert torch.equal(got[0][1].view(torch.int32), got[1][1].view(torch.int32))
+    req = syn.make_requests("small_bf16", "cuda")
+    _assert_same_bits(run_library("small_bf16", a, req=req), run_library("small_bf16", b, req=req), a.cfg)
+
+
 @pytest.mark.parametrize("workload", ["small_bf16", "tiny_fp32", "small_bf16_3jump", "small_bf16_folded"])
 def test_draft_repeats_bit_for_bit(workload):
     """flashmap/vllm/model.py, module docstring: a seeded request drafts the same

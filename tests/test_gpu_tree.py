@@ -75,17 +75,19 @@ def test_tree_refuses_out_of_range_shapes():
 ])
 def test_candidate_draft_and_tree_against_the_oracle(workload, n, width, tol, margin):
     """Candidate blocks per request: every block's hidden states and logits match the
-    oracle's draft with candidate-keyed noise (candidate 0 being the single draft, bit
-    for bit), greedy tokens match wherever the oracle's top-2 margin is clear, and every
+    oracle's draft with candidate-keyed noise (candidate 0 being the single draft),
+    greedy tokens match wherever the oracle's top-2 margin is clear, and every
     request's tree is the oracle's trie over those tokens (see check_candidates)."""
-    from .flashmap_harness import check_candidates, load_model, run_candidates, run_library
+    from .flashmap_harness import check_candidates, load_model, max_rel, run_candidates, run_library
 
     st = load_model(workload)
     run = run_library(workload, st)  # the pool now holds every written row
     out = run_candidates(st, run, n, width)
     bs, K = run.req["bs"], st.cfg["block_size"]
-    h0 = out[0].view(bs, n, K, -1)[:, 0].reshape(bs * K, -1)
-    assert torch.equal(h0, run.hidden), "candidate 0 differs from the single draft"
+    # candidate 0 is the single draft (up to rounding: the candidate draft's GEMMs run on
+    # n times the rows, so their tiles are split differently)
+    h0 = out[0].view(bs, n, K, -1)[:, 0].reshape(bs * K, -1).float().cpu().numpy()
+    assert max_rel(h0, run.hidden.float().cpu().numpy()) < (1e-2 if tol > 1e-3 else 1e-5)
     counts = check_candidates(st, run, n, width, tol, margin, range(bs), out)
     print(workload, n, counts)
     assert counts["trees"] == bs
