@@ -158,8 +158,10 @@ typedef struct {
  * keys and values; tokenspeed dflash.py: req_to_page / page_size addressing).
  * Layout (device, kv_dtype): [num_layers][2 (key, value)][num_pages][num_heads]
  * [page_size][head_dim]; the slot of position pos of the request in page-table row
- * r is req_to_page[r][pos / P] * P + pos % P. Caller-owned; size it with
- * flashmap_pool_bytes.
+ * r is req_to_page[r][pos / P] * P + pos % P. An E4M3 pool stores each (page, head)
+ * block of VALUES channel-major instead, [head_dim][page_size] (keys as above), so
+ * that the cross-attention's value product reads it without a transpose. The size is
+ * the same either way. Caller-owned; size it with flashmap_pool_bytes.
  */
 typedef struct {
   void* base;
@@ -422,12 +424,14 @@ flashmap_status flashmap_profile_stop(flashmap_model* model, flashmap_launch_rec
 
 /* The tcgen05 GEMM launches of one one-jump step of `bs` requests, with the shapes,
  * weights and launch configuration the calls use, back to back on `stream` and with
- * nothing else between them: the verify-window write's two linears over bs * window
- * columns (none when window = 0), the draft's anchor, noise and DiT linears and the
- * sampler's folded head (reading `hidden`, device [bs * K][D] act dtype). They read
- * and write the workspace (sized for bs requests and bs * window write rows); what
- * they leave there is not a result, and the chain clears only the GEMMs' own
- * counters (three small memsets). A measurement hook: captured in a CUDA graph and
+ * nothing else between them: flashmap_draft_block_with_write's linears (fc over the
+ * bs * window verify-window rows, none when window = 0; the anchor projection; one
+ * all-layer context K/V GEMM over the anchors and the window rows; the noise and DiT
+ * linears) and the sampler's folded head (reading `hidden`, device [bs * K][D] act
+ * dtype). The linears a draft runs on its two branches side by side take one CTA per
+ * SM here too. They read and write the workspace (sized for bs requests and bs *
+ * window write rows); what they leave there is not a result, and the chain clears
+ * only the GEMMs' own counters (three small memsets). A measurement hook: captured in a CUDA graph and
  * replayed, it times the GEMM kernel the way a step runs it, without the time of
  * the kernels between the GEMMs. *bytes_out receives the chain's algorithmic bytes
  * (each weight once, e4m3 weights one byte and a float32 scale per output channel;

@@ -472,6 +472,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     mma_bf16_16816(d, a, b0, b1);
 }
 
+// Score column n of a 16-position block of an e4m3 pool is position kPerm(n): columns
+// 2t, 2t+1 hold positions 4t, 4t+1 and columns 8+2t, 9+2t positions 4t+2, 4t+3 (the
+// order in which an ldmatrix of the channel-major values delivers them); kPermInv is
+// the ring row of position p.
+__device__ __forceinline__ int kPerm(int n) { return 4 * ((n & 7) >> 1) + 2 * (n >> 3) + (n & 1); }
+__device__ __forceinline__ int kPermInv(int p) { return 8 * ((p >> 1) & 1) + 2 * (p >> 2) + (p & 1); }
+
 constexpr int kXStages = 3;   // bf16 pool, one candidate: cp.async stages per warp
 constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage; 3 CTAs per SM)
 
@@ -485,10 +492,13 @@ __device__ __forceinline__ void bar_sync(int id, int threads) {
 // (warp % WPC); the NC warps of one block lane share a ring of K/V blocks, each issuing
 // part of every block's copies, so the context is read once for the NC candidates.
 // Ring layout: 16-byte chunks XOR-swizzled by row. For an e4m3 pool the keys feed the
-// e4m3 tensor-core product as stored; the values are widened to half for the half
-// product with the probabilities: over the same stage once the keys are read (NC = 1:
-// the 2 x 16 x HD e4m3 bytes of K and V hold exactly one 16 x HD half block), or into
-// a half buffer beside the ring (NC > 1, shared by the ring's warps).
+// e4m3 tensor-core product as stored, and the values arrive channel-major (the pool
+// keeps each (page, head) block of values that way): one 16-byte row per channel holds
+// the block's 16 positions, so a plain ldmatrix hands each thread four consecutive
+// positions of one channel, widened to half in registers for the half product with the
+// probabilities. The four are positions 4t..4t+3 where the product's fragment wants
+// k = 2t, 2t+1, 2t+8, 2t+9: the keys are placed in the ring in the matching order
+// (score column n is position kPerm(n)), so the product over k is unchanged.
 template <int HD, bool F8 = false, int NC = 1>
 struct XCfg {
   static constexpr int WPC = 4 / NC;      // warps per candidate = rings per CTA
@@ -500,7 +510,7 @@ struct XCfg {
   static constexpr int CH8 = HD / 16;     // 16-byte chunks per e4m3 row
   static constexpr int STAGES = NC == 1 ? (F8 ? kXStages8 : kXStages) : NC == 4 ? 8 : (F8 ? 6 : 4);
   static constexpr int STAGE = F8 ? 2 * BLK8 : 2 * BLK;
-  static constexpr int WORK = (F8 && NC > 1) ? BLK : 0;  // the shared half V block
+  static constexpr int WORK = 0;
   // e4m3 rows are HD bytes: chunk c of row r sits at c ^ ((r >> SW8) & (CH8 - 1)), so the
   // 8 rows an ldmatrix reads fall on distinct banks (128-byte rows: r & 7; 64-byte: r/2 & 3)
   static constexpr int SW8 = CH8 >= 8 ? 0 : (CH8 == 4 ? 1 : 2);
@@ -599,15 +609,22 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
         const int64_t kb = head_base + (ok ? page : 0) * page_stride + off * HD;
         const int64_t vb = kb + kv_stride;
         const uint32_t st = ring + (j % C::STAGES) * C::STAGE;
-        if constexpr (F8) {  // rows of 16-byte chunks, swizzled
+        if constexpr (F8) {
+          // keys: rows of 16-byte chunks, swizzled, position r at ring row kPermInv(r)
 #pragma unroll
           for (int i = ci0; i < 16 * C::CH8; i += 32 * NC) {
-            const int r = i / C::CH8, ch = i - r * C::CH8;
+            const int r = i / C::CH8, ch = i - r * C::CH8, rr = kPermInv(r);
             const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
-            const uint32_t dst = st + r * C::ROWB8 + ((ch ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4);
+            const uint32_t dst = st + rr * C::ROWB8 + ((ch ^ ((rr >> C::SW8) & (C::CH8 - 1))) << 4);
             cp_async16(dst, pool + (kb + r * HD) * ES + ch * 16, bytes);
-            cp_async16(dst + C::BLK8, pool + (vb + r * HD) * ES + ch * 16, bytes);
           }
+          // values: channel c of the block is 16 bytes at c * P + off in the (page, head)
+          // block, positions past the chunk zero-filled
+          const int64_t vblk = kb - off * HD + kv_stride;
+          const uint32_t vbytes = ok ? static_cast<uint32_t>(max(0, min(16, p1 - blk))) : 0u;
+#pragma unroll
+          for (int i = ci0; i < HD; i += 32 * NC)
+            cp_async16(st + C::BLK8 + i * 16, pool + vblk + static_cast<int64_t>(i) * a.P + off, vbytes);
         } else {
 #pragma unroll
           for (int i = ci0; i < 16 * C::CH; i += 32 * NC) {
@@ -700,26 +717,7 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           mma16816<F8>(s[1], qa[kk], b2, b3);
         }
       }
-      if constexpr (F8 && NC > 1) {
-        // the ring's warps widen the block's e4m3 V rows into the shared half block
-        const uint8_t* v8 = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE + C::BLK8;
-        uint8_t* vh = xsm + lw * C::RING + C::STAGES * C::STAGE;
-#pragma unroll
-        for (int i = ci0; i < 16 * C::CH8; i += 32 * NC) {
-          const int r = i / C::CH8, cc = i - r * C::CH8;
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(v8 + r * C::ROWB8 + ((cc ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
-          uint4 lo, hi;
-          e4m3x4_to_f16x4(raw.x, lo.x, lo.y);
-          e4m3x4_to_f16x4(raw.y, lo.z, lo.w);
-          e4m3x4_to_f16x4(raw.z, hi.x, hi.y);
-          e4m3x4_to_f16x4(raw.w, hi.z, hi.w);
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc + 1) ^ (r & 7)) << 4)) = hi;
-        }
-        bar_sync(1 + lw, 32 * NC);
-        vst = ring + C::STAGES * C::STAGE;
-      }
+      if constexpr (F8) vst = kst + C::BLK8;  // the channel-major e4m3 values
       // scale to base 2 and mask positions past the chunk (the last block only)
       if (blk + 16 <= p1) {
 #pragma unroll
@@ -731,7 +729,8 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
+            const int n = nt * 8 + 2 * t4 + (e & 1);
+            const int pos = blk + (F8 ? kPerm(n) : n);
             s[nt][e] = pos < p1 ? s[nt][e] * s_scale : -INFINITY;
           }
       }
@@ -769,43 +768,31 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
       }
       const uint32_t pa[4] = {pack2<F8>(p[0][0], p[0][1]), pack2<F8>(p[0][2], p[0][3]), pack2<F8>(p[1][0], p[1][1]),
                               pack2<F8>(p[1][2], p[1][3])};
-      if constexpr (F8 && NC == 1) {
-        // the keys are read: the e4m3 V rows -> half (exact) over the whole stage, in the
-        // half layout (16-byte chunk c of a row holds channels 16c..16c+15 and becomes
-        // half chunks 2c and 2c+1); every lane holds its chunks before any is written
-        const uint8_t* st8 = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE;
-        constexpr int NV = 16 * C::CH8 / 32;  // chunks per lane
-        uint4 raw[NV];
+      if constexpr (F8) {
+        // P V with the channel-major e4m3 values: per 32 channels one ldmatrix.x4 (lane L
+        // addresses channel row 32 g + L) gives each thread 4 positions of 4 channels;
+        // each word widens (exactly) to the two half pairs of one B fragment
 #pragma unroll
-        for (int u = 0; u < NV; ++u) {
-          const int i = lane + 32 * u, r = i / C::CH8, cc = i - r * C::CH8;
-          raw[u] = *reinterpret_cast<const uint4*>(st8 + C::BLK8 + r * C::ROWB8 +
-                                                   ((cc ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4));
+        for (int g = 0; g < HD / 32; ++g) {
+          uint32_t w[4];
+          ldsm_x4(vst + (g * 32 + lane) * 16, w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x4(w[i], b0, b1);
+            mma16816<F8>(o[4 * g + i], pa, b0, b1);
+          }
         }
-        __syncwarp();
-        uint8_t* vh = xsm + lw * C::RING + (j % C::STAGES) * C::STAGE;
+      } else {
 #pragma unroll
-        for (int u = 0; u < NV; ++u) {
-          const int i = lane + 32 * u, r = i / C::CH8, cc = i - r * C::CH8;
-          uint4 lo, hi;
-          e4m3x4_to_f16x4(raw[u].x, lo.x, lo.y);
-          e4m3x4_to_f16x4(raw[u].y, lo.z, lo.w);
-          e4m3x4_to_f16x4(raw[u].z, hi.x, hi.y);
-          e4m3x4_to_f16x4(raw[u].w, hi.z, hi.w);
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc) ^ (r & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(vh + r * C::ROWB + (((2 * cc + 1) ^ (r & 7)) << 4)) = hi;
+        for (int dn = 0; dn < HD / 16; ++dn) {
+          const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int ch = dn * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
+          mma16816<F8>(o[2 * dn], pa, b0, b1);
+          mma16816<F8>(o[2 * dn + 1], pa, b2, b3);
         }
-        __syncwarp();
-        vst = kst;
-      }
-#pragma unroll
-      for (int dn = 0; dn < HD / 16; ++dn) {
-        const int r = (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int ch = dn * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vst + r * C::ROWB + ((ch ^ (r & 7)) << 4), b0, b1, b2, b3);
-        mma16816<F8>(o[2 * dn], pa, b0, b1);
-        mma16816<F8>(o[2 * dn + 1], pa, b2, b3);
       }
       __syncwarp();
     }

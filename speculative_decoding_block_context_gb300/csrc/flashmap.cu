@@ -1384,11 +1384,10 @@ flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32
   if (m->steps != 1 || m->wdt == FLASHMAP_F32)
     return fail(FLASHMAP_E_UNSUPPORTED, "the GEMM chain covers one-jump drafts with tcgen05 weights");
   const int64_t wrows = static_cast<int64_t>(bs) * window;
-  const DraftWs need = carve_draft(m, bs, nullptr);
-  size_t wneed = 0;
-  if (wrows > 0) carve_write(m, static_cast<int>(wrows), nullptr, &wneed);
+  if (wrows > (1 << 24)) return fail(FLASHMAP_E_INVALID, "bs * window must be <= 2^24");
+  const DraftWs need = carve_draft(m, bs, nullptr, static_cast<int>(wrows));
   const SampleWs sneed = carve_sample(m, bs, true, nullptr);
-  if (workspace_bytes < std::max({need.bytes, wneed, sneed.bytes}))
+  if (workspace_bytes < std::max(need.bytes, sneed.bytes))
     return fail(FLASHMAP_E_INVALID, "workspace too small for the chain");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int R = bs * m->K, D = m->D, H = m->H;
@@ -1408,28 +1407,30 @@ flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32
     bytes += static_cast<int64_t>(wb + static_cast<size_t>(rows) * W.K * es + static_cast<size_t>(rows) * W.N * out_es);
     ++n;
   };
-  if (wrows > 0) {
-    size_t b = 0;
-    const WriteWs ws = carve_write(m, static_cast<int>(wrows), workspace, &b);
-    Launch L = m->launch(s);
-    L.red = ws.red;
-    FM_CUDA(cudaMemsetAsync(ws.red.cnt, 0, static_cast<size_t>(ws.red.cnt_cap) * 4, s));
-    FM_CUDA(fm::linear(L, m->fc, ws.xc, static_cast<int>(wrows), m->Lt * H, ws.acc_fc, D, nullptr, nullptr,
-                       fm::Out::Store));
-    count(m->fc, static_cast<int>(wrows), 4);
-    FM_CUDA(fm::linear(L, m->ctx_kv, ws.ctx, static_cast<int>(wrows), D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr,
-                       fm::Out::Store));
-    count(m->ctx_kv, static_cast<int>(wrows), 4);
-  }
   {
-    const DraftWs ws = carve_draft(m, bs, workspace);
+    // the draft with the verify-window write deferred into it (as the step runs it): fc
+    // over the window rows, the anchor projection, then one all-layer context K/V GEMM
+    // over the anchors and the window rows
+    const DraftWs ws = carve_draft(m, bs, workspace, static_cast<int>(wrows));
+    // the anchor branch and the main branch up to layer 0's cross-attention run side by
+    // side in a draft, one GEMM CTA per SM each; the rest with the kernel's own maximum
     Launch L = m->launch(s);
     L.red = ws.red_main;
+    L.ctas_per_sm = FM_DRAFT_FORK ? FM_FORK_CTAS_PER_SM : 0;
+    Launch La = L;
+    La.red = ws.red_side;
     FM_CUDA(cudaMemsetAsync(ws.red_main.cnt, 0, static_cast<size_t>(ws.red_main.cnt_cap) * 4, s));
-    FM_CUDA(fm::linear(L, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, fm::Out::Store));
+    FM_CUDA(cudaMemsetAsync(ws.red_side.cnt, 0, static_cast<size_t>(ws.red_side.cnt_cap) * 4, s));
+    if (wrows > 0) {
+      FM_CUDA(fm::linear(La, m->fc, ws.xc, static_cast<int>(wrows), m->Lt * H, ws.acc_fc, D, nullptr, nullptr,
+                         fm::Out::Store));
+      count(m->fc, static_cast<int>(wrows), 4);
+    }
+    FM_CUDA(fm::linear(La, m->ap, ws.e_rows, bs, H, ws.acc_a, D, nullptr, m->ap_b, fm::Out::Store));
     count(m->ap, bs, 4);
-    FM_CUDA(fm::linear(L, m->ctx_kv, ws.kv_in, bs, D, ws.acc_kv, 2 * m->L * D, nullptr, nullptr, fm::Out::Store));
-    count(m->ctx_kv, bs, 4);
+    FM_CUDA(fm::linear(La, m->ctx_kv, ws.kv_in, bs + static_cast<int>(wrows), D, ws.acc_kv, 2 * m->L * D, nullptr,
+                       nullptr, fm::Out::Store));
+    count(m->ctx_kv, bs + static_cast<int>(wrows), 4);
     if (m->noise_path == 1) {
       FM_CUDA(resid(L, m->fold, ws.act, R, H, ws.x, nullptr, m->fold_xu, false));
       count(m->fold, R, 4);
@@ -1447,6 +1448,7 @@ flashmap_status flashmap_profile_gemm_chain(flashmap_model* m, int32_t bs, int32
       count(lw.o, R, 4);
       FM_CUDA(fm::linear(L, lw.cq, ws.act, R, D, ws.acc_d, D, nullptr, nullptr, fm::Out::Store));
       count(lw.cq, R, 4);
+      L.ctas_per_sm = 0;  // the branches have joined
       FM_CUDA(resid(L, lw.co, ws.act, R, D, ws.x, lw.mods + 5 * D, nullptr, true));
       count(lw.co, R, 4);
       FM_CUDA(fm::linear(L, lw.fc1, ws.act, R, D, ws.act_f, m->F, nullptr, lw.fc1_b, fm::Out::GeluAct));

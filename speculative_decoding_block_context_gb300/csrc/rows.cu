@@ -125,7 +125,18 @@ __global__ void __launch_bounds__(1024, 2) kv_write_kernel(KvWriteArgs a) {
     head_norm_rope_w<EPL>(k, kw, a.eps, rope, lane);
     const int64_t r = kbase + static_cast<int64_t>(h) * a.P;
     store_vec<T, EPL>(pool + r * HD + lane * EPL, k);
-    store_vec<T, EPL>(pool + (r + kv_stride) * HD + lane * EPL, v);
+    if constexpr (sizeof(T) == 1) {
+      // an e4m3 pool keeps each (page, head) block of values channel-major: channel c of
+      // the block's positions is a row of P bytes (the cross-attention reads it as the
+      // B operand of its P V product without a transpose)
+      T* vb = pool + (r - off + kv_stride) * HD + off;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        vb[static_cast<int64_t>(lane * EPL + e) * a.P] =
+            static_cast<T>(__nv_cvt_float_to_fp8(v[e], __NV_SATFINITE, __NV_E4M3));
+    } else {
+      store_vec<T, EPL>(pool + (r + kv_stride) * HD + lane * EPL, v);
+    }
   }
 }
 

@@ -62,28 +62,44 @@ def load_model(workload: str, device="cuda", oracle: bool = True) -> ModelState:
     return st
 
 
-def pool_view(cfg: dict, pool_t: torch.Tensor, num_pages: int) -> torch.Tensor:
+def pool_view(cfg: dict, pool_t: torch.Tensor, num_pages: int) -> tuple:
+    """Views of the pool's keys and values, each (L, pages, heads, P, hd) position-major.
+    An e4m3 pool keeps each (page, head) block of values channel-major (hd, P): that view
+    is a transposed one. No copy."""
     dt = syn.torch_dtype(cfg["kv_dtype"])
-    return pool_t.view(dt).view(cfg["num_layers"], 2, num_pages, cfg["num_heads"], cfg["page_size"], cfg["head_dim"])
+    L, nh, P, hd = cfg["num_layers"], cfg["num_heads"], cfg["page_size"], cfg["head_dim"]
+    kv = pool_t.view(dt).view(L, 2, num_pages * nh * P * hd)
+    k = kv[:, 0].view(L, num_pages, nh, P, hd)
+    if cfg["kv_dtype"] == "e4m3":
+        v = kv[:, 1].view(L, num_pages, nh, hd, P).transpose(-1, -2)
+    else:
+        v = kv[:, 1].view(L, num_pages, nh, P, hd)
+    return k, v
 
 
-def gather_context(cfg: dict, pool6: torch.Tensor, req_to_page_row: torch.Tensor, n: int):
+def slot_rows(cfg: dict, kv: tuple, s: torch.Tensor) -> tuple:
+    """The (L, n, heads, hd) keys and values at pool slots s (a device int64 tensor)."""
+    P = cfg["page_size"]
+    return tuple(t.permute(1, 3, 0, 2, 4)[s // P, s % P].permute(1, 0, 2, 3) for t in kv)
+
+
+def gather_context(cfg: dict, kv: tuple, req_to_page_row: torch.Tensor, n: int):
     """Keys and values of positions 0..n-1 of one request, read through its page-table
     row: numpy (L, n, heads, hd) x 2."""
     P = cfg["page_size"]
     npages = (n + P - 1) // P
     pages = req_to_page_row[:npages].long()
-    g = pool6[:, :, pages]  # (L, 2, np, nh, P, hd)
-    g = g.permute(0, 1, 2, 4, 3, 5).reshape(cfg["num_layers"], 2, npages * P, cfg["num_heads"], cfg["head_dim"])
-    g = g[:, :, :n].float().cpu().numpy()
-    return g[:, 0], g[:, 1]
+    out = []
+    for t in kv:
+        g = t[:, pages].permute(0, 1, 3, 2, 4).reshape(cfg["num_layers"], npages * P, cfg["num_heads"], cfg["head_dim"])
+        out.append(g[:, :n].float().cpu().numpy())
+    return out[0], out[1]
 
 
 @dataclass
 class LibRun:
     req: dict
     pool_t: torch.Tensor
-    pool6: torch.Tensor
     prefill_loc: list
     window_loc: torch.Tensor
     anchor_loc: torch.Tensor
@@ -93,6 +109,12 @@ class LibRun:
     full: torch.Tensor
     prefilled_ctx: dict  # b -> (K, V) numpy of the drawn context (prefilled workloads)
     dev_err: int
+    cfg: dict
+
+    @property
+    def kv(self) -> tuple:
+        """Views of the pool's keys and values (see pool_view)."""
+        return pool_view(self.cfg, self.pool_t, self.req["num_pages"])
 
 
 def run_library(workload: str, st: ModelState, *, noise_scale: float = 1.0, check_subset=None,
@@ -105,13 +127,13 @@ def run_library(workload: str, st: ModelState, *, noise_scale: float = 1.0, chec
     dt = syn.torch_dtype(cfg["act_dtype"])
     code = F.DTYPE_CODES[cfg["kv_dtype"]]
     pool_t = torch.empty(F.flashmap_pool_bytes(cfg, req["num_pages"]), dtype=torch.uint8, device=dev)
-    pool6 = pool_view(cfg, pool_t, req["num_pages"])
     prefilled = {}
     if not req["prefill"]:
         syn.fill_pool_random(pool_t.view(syn.torch_dtype(cfg["kv_dtype"])), req["kv_generator_seed"])
+        kv = pool_view(cfg, pool_t, req["num_pages"])
         for b in (check_subset or []):
             row = req["req_to_page"][int(req["req_pool_idx"][b])]
-            prefilled[b] = gather_context(cfg, pool6, row, req["ctx"][b])
+            prefilled[b] = gather_context(cfg, kv, row, req["ctx"][b])
     pool = F.make_pool(pool_t, req["num_pages"], code)
     max_rows = max(max(req["ctx"]) if req["prefill"] else 0, bs * (K + 1))
     ws = torch.empty(F.flashmap_workspace_size(st.handle, bs, min(max_rows, 4096)), dtype=torch.uint8, device=dev)
@@ -152,8 +174,8 @@ def run_library(workload: str, st: ModelState, *, noise_scale: float = 1.0, chec
                             req["step"], tokens, logits, full, ws)
     torch.cuda.synchronize()
     err = F.flashmap_get_device_error(st.handle)
-    return LibRun(req, pool_t, pool6, prefill_loc, window_loc, anchor_loc, hidden, tokens, logits, full,
-                  prefilled, err)
+    return LibRun(req, pool_t, prefill_loc, window_loc, anchor_loc, hidden, tokens, logits, full,
+                  prefilled, err, cfg)
 
 
 def oracle_batch(st: ModelState, run: LibRun, subset, noise_scale: float = 1.0) -> dict:
@@ -223,13 +245,11 @@ def slot_ids(req: dict, b: int, positions, P: int) -> np.ndarray:
     return np.array([ref.slot_of(r2p, row, int(q), P) for q in positions], dtype=np.int64)
 
 
-def pool_rows(cfg: dict, pool6: torch.Tensor, slots) -> tuple:
-    """(L, n, heads, hd) keys and values stored at the given slots."""
-    P = cfg["page_size"]
-    s = torch.as_tensor(np.asarray(slots), device=pool6.device)
-    g = pool6.permute(2, 4, 0, 1, 3, 5)[s // P, s % P]  # (n, L, 2, nh, hd)
-    g = g.permute(1, 2, 0, 3, 4).float().cpu().numpy()
-    return g[:, 0], g[:, 1]
+def pool_rows(cfg: dict, kv: tuple, slots) -> tuple:
+    """(L, n, heads, hd) keys and values stored at the given slots, numpy."""
+    s = torch.as_tensor(np.asarray(slots), device=kv[0].device)
+    k, v = slot_rows(cfg, kv, s)
+    return k.float().cpu().numpy(), v.float().cpu().numpy()
 
 
 def kv_err(cfg: dict, got, want, tol: float) -> float:
@@ -259,7 +279,7 @@ def check_request(st: ModelState, run: LibRun, b: int, o: dict, tol: float, repo
         got = run.prefill_loc[b].cpu().numpy()
         assert np.array_equal(got, want), "prefill out_loc differs"
         pick = np.unique(np.linspace(0, ctx - 1, min(ctx, 64)).astype(int))
-        k, v = pool_rows(cfg, run.pool6, want[pick])
+        k, v = pool_rows(cfg, run.kv, want[pick])
         e = max(kv_err(cfg, k, o["prefill_kv"][0][:, pick], tol), kv_err(cfg, v, o["prefill_kv"][1][:, pick], tol))
         bump("write_kv", e)
         assert e <= tol, f"prefill K/V max-rel {e}"
@@ -270,13 +290,13 @@ def check_request(st: ModelState, run: LibRun, b: int, o: dict, tol: float, repo
         want = np.full(W, -1, dtype=np.int64)
         want[:m] = slot_ids(req, b, ctx + np.arange(m), P)
         assert np.array_equal(got, want), "window out_loc differs"
-        k, v = pool_rows(cfg, run.pool6, want[:m])
+        k, v = pool_rows(cfg, run.kv, want[:m])
         e = max(kv_err(cfg, k, o["window_kv"][0], tol), kv_err(cfg, v, o["window_kv"][1], tol))
         bump("write_kv", e)
         assert e <= tol, f"window K/V max-rel {e}"
     aslot = slot_ids(req, b, [p], P)
     assert int(run.anchor_loc[b]) == int(aslot[0]), "anchor slot differs"
-    k, v = pool_rows(cfg, run.pool6, aslot)
+    k, v = pool_rows(cfg, run.kv, aslot)
     e = max(kv_err(cfg, k, o["anchor_kv"][0], tol), kv_err(cfg, v, o["anchor_kv"][1], tol))
     bump("anchor_kv", e)
     assert e <= tol, f"anchor K/V max-rel {e}"

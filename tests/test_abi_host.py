@@ -93,6 +93,21 @@ def test_null_model_calls_fail_cleanly(lib):
                                     None) == 1
 
 
+def test_new_entry_points_reject_null_arguments_before_any_device_work(lib):
+    """The draft with a deferred write, the GEMM chain hook, the wait-timeout probe and
+    the static sampler refuse NULL arguments with E_INVALID and a message (no model, no
+    device needed)."""
+    import ctypes
+
+    b, n = ctypes.c_int64(), ctypes.c_int32()
+    assert lib.flashmap_draft_block_with_write(None, None, None, 1, None, None, None, None, 1, None, 1.0, None,
+                                               None, None, 0, None) == 1
+    assert F.flashmap_last_error()
+    assert lib.flashmap_profile_gemm_chain(None, 1, 17, None, None, 0, ctypes.byref(b), ctypes.byref(n), None) == 1
+    assert lib.flashmap_debug_wait_timeout(None, 1000000, None) == 1
+    assert lib.flashmap_sample_logits_static(None, 1, None, None, None, None, None, 0, None, None) == 1
+
+
 def test_e4m3_pool_is_half_the_bf16_pool(lib):
     cfg = syn.model_config("qwen3_8b_bs32_kv8")
     assert cfg["kv_dtype"] == "e4m3"

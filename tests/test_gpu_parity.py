@@ -14,7 +14,7 @@ from oracle import flashmap_ref as ref
 from speculative_decoding_block_context_gb300 import _lib as F
 from speculative_decoding_block_context_gb300 import synthetic as syn
 
-from .flashmap_harness import TOL, check_request, load_model, max_rel, oracle_batch, oracle_request, run_library
+from .flashmap_harness import TOL, check_request, load_model, max_rel, oracle_batch, oracle_request, run_library, slot_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -262,15 +262,13 @@ def test_graph_capture_replays_draft_and_sample(small):
 def _assert_same_bits(a, b, cfg):
     """Two library runs of the same inputs: written pool rows, hidden states, logits,
     the full-vocabulary scatter and tokens bitwise equal."""
-    P = cfg["page_size"]
     slots = [loc for loc in a.prefill_loc] + [a.anchor_loc]
     if a.window_loc is not None:
         slots.append(a.window_loc[a.window_loc >= 0])
     for i, loc in enumerate(slots):
         s = loc.long()
-        ga = a.pool6.permute(2, 4, 0, 1, 3, 5)[s // P, s % P]
-        gb = b.pool6.permute(2, 4, 0, 1, 3, 5)[s // P, s % P]
-        assert torch.equal(ga.view(torch.uint8), gb.view(torch.uint8)), f"written rows {i} differ"
+        for ga, gb in zip(slot_rows(cfg, a.kv, s), slot_rows(cfg, b.kv, s)):
+            assert torch.equal(ga.contiguous().view(torch.uint8), gb.contiguous().view(torch.uint8)), f"written rows {i} differ"
     assert torch.equal(a.hidden.view(torch.int16) if a.hidden.dtype == torch.bfloat16 else a.hidden.view(torch.int32),
                        b.hidden.view(torch.int16) if b.hidden.dtype == torch.bfloat16 else b.hidden.view(torch.int32))
     assert torch.equal(a.logits.view(torch.int32), b.logits.view(torch.int32))

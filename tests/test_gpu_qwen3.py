@@ -108,6 +108,22 @@ def test_qwen3_e4m3_kv_pool_bs32(qwen):
     torch.cuda.empty_cache()
 
 
+def test_qwen3_e4m3_kv_pool_bs128(qwen):
+    """The batch-128 workload (log-uniform contexts 16..32768, verify-window write,
+    full-vocabulary scatter) over an e4m3 pool: the window rows are written through the
+    e4m3 store (values channel-major per (page, head) block), then read back by the
+    oracle and by the e4m3 cross-attention."""
+    import dataclasses
+
+    from speculative_decoding_block_context_gb300 import synthetic as syn
+
+    cfg8 = syn.model_config("qwen3_8b_bs128_kv8")
+    st8 = dataclasses.replace(qwen, cfg=cfg8, handle=F.flashmap_load_weights(cfg8, qwen.W, qwen.E, qwen.LM, qwen.rank))
+    run, _ = _run_and_check(st8, "qwen3_8b_bs128_kv8")
+    del run, st8
+    torch.cuda.empty_cache()
+
+
 def test_qwen3_two_jumps_bs1(qwen):
     """Drafting in two jumps on the printed grid (0, 0.8172569274902344, 1) at the full
     sizes: the state is 151936
