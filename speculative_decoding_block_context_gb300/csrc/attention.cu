@@ -479,6 +479,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ int kPerm(int n) { return 4 * ((n & 7) >> 1) + 2 * (n >> 3) + (n & 1); }
 __device__ __forceinline__ int kPermInv(int p) { return 8 * ((p >> 1) & 1) + 2 * (p >> 2) + (p & 1); }
 
+constexpr float kLazyLog2 = 8.f;  // the running max's slack: p <= 2^8
 constexpr int kXStages = 3;   // bf16 pool, one candidate: cp.async stages per warp
 constexpr int kXStages8 = 4;  // e4m3 pool (half the bytes per stage; 3 CTAs per SM)
 
@@ -594,6 +595,7 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
     const int64_t kv_stride = static_cast<int64_t>(a.num_pages) * page_stride;
     // the ring's NC warps split a block's 16-byte chunks: this warp's first chunk and stride
     const int ci0 = (NC > 1 ? cw * 32 : 0) + lane;
+    const int p_shift = (a.P & (a.P - 1)) == 0 ? __ffs(a.P) - 1 : -1;  // a power-of-two page size
     auto issue = [&](int j) {
       if (j < nj) {
         if ((j >> 5) != pg_group) {  // warp-uniform: more than 32 blocks per lane
@@ -601,7 +603,7 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           pg = page_ids(j & ~31);
         }
         const int blk = p0 + ((lw + WPC * j) << 4);
-        const int pi = blk / a.P;
+        const int pi = p_shift >= 0 ? blk >> p_shift : blk / a.P;
         const int page = __shfl_sync(0xffffffffu, pg, j & 31);
         const bool ok = page >= 0 && page < a.num_pages;
         if (!ok && lane == 0 && cw == 0) set_dev_error(a.dev_err, FLASHMAP_DEVERR_PAGE);
@@ -740,24 +742,18 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      // a finite running max only grows; c = 1 exactly while it stays
-      const float c0 = n0 == -INFINITY ? 1.f : ex2f(m0 - n0);
-      const float c1 = n1 == -INFINITY ? 1.f : ex2f(m1 - n1);
-      const float z0 = n0 == -INFINITY ? 0.f : n0, z1 = n1 == -INFINITY ? 0.f : n1;  // -inf rows: p = 0
-      float p[2][4];
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        p[nt][0] = ex2f(s[nt][0] - z0);
-        p[nt][1] = ex2f(s[nt][1] - z0);
-        p[nt][2] = ex2f(s[nt][2] - z1);
-        p[nt][3] = ex2f(s[nt][3] - z1);
-      }
-      l0 = l0 * c0 + p[0][0] + p[0][1] + p[1][0] + p[1][1];
-      l1 = l1 * c1 + p[0][2] + p[0][3] + p[1][2] + p[1][3];
-      m0 = n0;
-      m1 = n1;
-      if (__any_sync(0xffffffffu, c0 != 1.f || c1 != 1.f)) {
+      // The reference max of a row moves only when a score passes it by more than
+      // kLazyLog2 (base 2): then every row of the warp takes its running max and o, l
+      // are rescaled; otherwise p <= 2^kLazyLog2 (well inside the half / bf16 range) and the
+      // rescale is skipped. The sum is the same softmax; only its reference differs.
+      if (__any_sync(0xffffffffu, mx0 > m0 + kLazyLog2 || mx1 > m1 + kLazyLog2)) {
+        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+        const float c0 = n0 == -INFINITY ? 1.f : ex2f(m0 - n0);
+        const float c1 = n1 == -INFINITY ? 1.f : ex2f(m1 - n1);
+        l0 *= c0;
+        l1 *= c1;
+        m0 = n0;
+        m1 = n1;
 #pragma unroll
         for (int i = 0; i < HD / 8; ++i) {
           o[i][0] *= c0;
@@ -766,6 +762,17 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           o[i][3] *= c1;
         }
       }
+      const float z0 = m0 == -INFINITY ? 0.f : m0, z1 = m1 == -INFINITY ? 0.f : m1;  // -inf rows: p = 0
+      float p[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        p[nt][0] = ex2f(s[nt][0] - z0);
+        p[nt][1] = ex2f(s[nt][1] - z0);
+        p[nt][2] = ex2f(s[nt][2] - z1);
+        p[nt][3] = ex2f(s[nt][3] - z1);
+      }
+      l0 += p[0][0] + p[0][1] + p[1][0] + p[1][1];
+      l1 += p[0][2] + p[0][3] + p[1][2] + p[1][3];
       const uint32_t pa[4] = {pack2<F8>(p[0][0], p[0][1]), pack2<F8>(p[0][2], p[0][3]), pack2<F8>(p[1][0], p[1][1]),
                               pack2<F8>(p[1][2], p[1][3])};
       if constexpr (F8) {
@@ -1301,7 +1308,7 @@ cudaError_t self_attention(const Launch& L, int dtype, const float* qkv, int bs,
   return e;
 }
 
-int xattn_target_items(int num_sms) { return num_sms * 8; }
+int xattn_target_items(int num_sms) { return num_sms * 16; }
 // Room for the plan of a tree draft too, whose target is scaled by the candidates a CTA
 // serves at once (at most 4)
 int xattn_max_chunks(int num_sms, int nh, int bs) { return 4 * xattn_target_items(num_sms) / nh + bs + 1; }

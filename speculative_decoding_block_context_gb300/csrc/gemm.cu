@@ -68,7 +68,12 @@ struct TcCfg {
   static constexpr int A8_BYTES = F8 ? 128 * 64 : 0;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + A8_BYTES;
   static constexpr uint32_t TX_BYTES = (F8 ? A8_BYTES : A_BYTES) + B_BYTES;  // bytes TMA writes per stage
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
+  // Narrow bf16 tiles sum a cluster split-K tile by pushing: each rank stores its
+  // partial of rank o's channels into o's receive area (one slot per sending rank,
+  // channel-major, rows padded by 4), beside the ring.
+  static constexpr bool PUSH = !F8 && BN <= 32 && FM_GEMM_CLUSTER_MAX >= 2;
+  static constexpr int RECV_BYTES = PUSH ? (128 + FM_GEMM_CLUSTER_MAX) * (BN + 4) * 4 : 0;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + RECV_BYTES + 1024;
   static constexpr uint32_t TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int THREADS = F8 ? kTcThreadsF8 : kTcThreads;
   static constexpr int FIT = (228 * 1024) / (SMEM + 1024);
@@ -106,6 +111,34 @@ __device__ __forceinline__ void emit_out(int mode, void* out, int ldo, int row, 
 // (release / acquire: shared-memory writes before it are visible to the cluster after).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// A 16-byte store into a peer CTA's shared memory that counts its bytes on the peer's
+// mbarrier (both addresses shared::cluster).
+__device__ __forceinline__ void st_async4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+               : "memory");
+}
+// Waits (at most kWaitLimitNs) for a phase completed by other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_wait_cluster_timed(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   uint32_t r;
@@ -155,7 +188,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
   // full: TMA bytes landed; conv (e4m3 only): the bf16 weight tile is written;
   // empty: the MMAs reading the stage completed
   __shared__ uint64_t full_bar[C::STAGES], conv_bar[C::STAGES], empty_bar[C::STAGES], acc_full[2], acc_empty[2],
-      drain_bar;
+      drain_bar, recv_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
   __shared__ int64_t issued, consumed;
@@ -206,6 +239,12 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
     abort_flag = 0;
     issued = 0;
     consumed = 0;
+    if (C::PUSH && cs) {
+      // every rank's share of this rank's channels: cs x nch x BN floats
+      const int rk = blockIdx.x % cs, nch = 128 * (rk + 1) / cs - 128 * rk / cs;
+      mbar_init(&recv_bar, 1);
+      mbar_arrive_expect_tx(&recv_bar, static_cast<uint32_t>(cs * nch * BN * 4));
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -216,6 +255,9 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // push mode: the peers push only after this barrier phase, once every receive
+  // barrier of the cluster is initialised
+  if (C::PUSH && cs) cluster_arrive_relaxed();
 
   pdl_trigger();
   if (warp == 0) {
@@ -236,7 +278,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
       for (int i = 0; i < pre; ++i) {
         const int64_t tile = (it0 + i) / KB;
         const int kb = static_cast<int>(it0 + i - tile * KB);
-        const int r = static_cast<int>(tile / mt), m = static_cast<int>(tile - static_cast<int64_t>(r) * mt);
+        const int r = static_cast<int>(tile / mt);
         tma_load_2d(smem + i * C::STAGE_BYTES + C::A_BYTES, &mapX, &full_bar[i], kb * 64, r * BN, pol_x);
       }
       issued = pre;
@@ -331,8 +373,28 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
     pdl_wait();
     const int q = warp & 3, chan = q * 32 + lane, G = gridDim.x, bid = blockIdx.x;
     auto emit = [&](int row, int n, float y) { emit_out(mode, out, ldo, row, n, y); };
-    if (cs) {  // one segment: the raw partial goes to this CTA's shared memory (stage area,
-               // free once the MMAs completed), channel-major with rows padded by 4
+    if (C::PUSH && cs) {  // one segment: each channel's partial goes to the rank that sums it
+      cluster_wait();
+      if (mbar_wait(&acc_full[0], 0, &abort_flag)) {
+        tc_fence_after();
+        const int rk = bid % cs, nmax = (128 + cs - 1) / cs;
+        const int o = ((chan + 1) * cs - 1) >> 7;  // the largest o with 128 o / cs <= chan
+        const uint32_t slot = smem_u32(smem + C::STAGES * C::STAGE_BYTES) +
+                              static_cast<uint32_t>(((rk * nmax + chan - 128 * o / cs) * (BN + 4)) * 4);
+        const uint32_t dst = cluster_map(slot, static_cast<uint32_t>(o));
+        const uint32_t bar = cluster_map(smem_u32(&recv_bar), static_cast<uint32_t>(o));
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c0), v);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_async4(dst + static_cast<uint32_t>((c0 + 4 * i) * 4), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3],
+                      bar);
+        }
+      }
+    } else if (cs) {  // one segment: the raw partial goes to this CTA's shared memory (stage
+                      // area, free once the MMAs completed), channel-major, rows padded by 4
       if (mbar_wait(&acc_full[0], 0, &abort_flag)) {
         tc_fence_after();
         float* part = reinterpret_cast<float*>(smem) + chan * (BN + 4);
@@ -533,7 +595,43 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
   }
 
   __syncthreads();
-  if (cs) {
+  if (C::PUSH && cs) {
+    // Rank rk sums channels [128 rk / cs, 128 (rk + 1) / cs) over the ranks' slots in
+    // rank order once its receive barrier has counted every byte. The barrier phase
+    // after it keeps every CTA resident until all pushes have landed.
+    if (warp >= 2 && warp < 6) {
+      const bool got = mbar_wait_cluster_timed(&recv_bar, 0);
+      cluster_arrive();
+      if (got) {
+        const int c = blockIdx.x / cs, rk = blockIdx.x - c * cs, nmax = (128 + cs - 1) / cs;
+        const int rtile = c / mt, m = c - rtile * mt;
+        const int ch0 = 128 * rk / cs, nch = 128 * (rk + 1) / cs - ch0, groups = BN / 4;
+        const float* recv = reinterpret_cast<const float*>(smem + C::STAGES * C::STAGE_BYTES);
+        for (int i = threadIdx.x - 64; i < nch * groups; i += 128) {
+          const int g = i / nch, ch = i - g * nch;  // neighbouring threads: neighbouring channels
+          const float* src = recv + ch * (BN + 4) + 4 * g;
+          float4 acc = *reinterpret_cast<const float4*>(src);
+          for (int k = 1; k < cs; ++k)
+            acc = add4(acc, *reinterpret_cast<const float4*>(src + k * nmax * (BN + 4)));
+          const int n = m * 128 + ch0 + ch;
+          if (n < N) {
+            const float a = alpha ? alpha[n] : 1.f, b = beta ? beta[n] : 0.f;
+            const int row0 = rtile * BN + 4 * g;
+            const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (row0 + e < R) emit_out(mode, out, ldo, row0 + e, n, fmaf(a, v4[e], b));
+          }
+        }
+      } else if (threadIdx.x == 64) {
+        abort_flag = 1;
+      }
+    } else {
+      cluster_wait();  // the first phase (the epilogue warps waited before pushing)
+      cluster_arrive();
+    }
+    cluster_wait();
+  } else if (cs) {
     // Every rank's partial is in its shared memory after the first cluster barrier;
     // rank rk sums channels [128 rk / cs, 128 (rk + 1) / cs) of the tile over ranks
     // 0..cs-1 in order and writes them; the second barrier keeps each CTA's shared
