@@ -56,11 +56,14 @@ def test_philox_words_bit_exact():
 # 16 x 4096 -> 4096 in clusters of 8, 16 x 4096 -> 12288 in clusters of 3) and
 # stream-K over every CTA with two or three parts per tile summed through the scratch
 # (16 x 4096 -> 40960: 320 tiles; 200 x 4096 -> 12288: 96 tiles of 256 rows on one CTA
-# per SM, about 40 of a tile's 64 k blocks per CTA).
+# per SM, about 40 of a tile's 64 k blocks per CTA). The last four run on SM pairs
+# (tcgen05 cta_group::2, 256 x 256 tiles, stream-K over 76 pairs: 5.05, 8.3, 1.26 and
+# 4.1 tiles per pair, so most pairs hold a split tile; ragged rows, and last tiles whose
+# second half lies past N).
 @pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 200, 300), (16, 4096, 4096), (37, 384, 1234),
                                       (100, 256, 384), (300, 512, 256), (2048, 1024, 512), (300, 384, 1234),
                                       (513, 4096, 384), (16, 4096, 12288), (16, 12288, 4096), (16, 4096, 40960),
-                                      (200, 4096, 12288), (64, 4096, 12288)])
+                                      (200, 4096, 12288), (64, 4096, 12288), (2048, 512, 12288), (1000, 256, 40000), (512, 1024, 12288), (300, 384, 40000)])
 def test_linear_bf16_tcgen05(rows, k, n):
     """y = x W^T added onto a nonzero output (the residual stream's mode), against
     float64; a second call on the same inputs gives the same bits (every split tile is
