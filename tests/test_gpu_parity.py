@@ -83,9 +83,11 @@ def test_linear_bf16_tcgen05(rows, k, n):
 
 
 @pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 208, 300), (16, 4096, 4096), (37, 384, 1234),
-                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512)])
+                                      (100, 256, 384), (300, 512, 256), (2048, 1024, 512), (1024, 512, 12288),
+                                      (300, 256, 40000)])
 def test_linear_e4m3_tcgen05(rows, k, n):
-    """W8A16: w quantized per output channel at call time, expanded to bf16 on chip."""
+    """W8A16: w quantized per output channel at call time, expanded to bf16 on chip (the
+    last two with 256-row tiles, split over the SMs by stream-K)."""
     g = torch.Generator(device="cuda").manual_seed(rows * 11 + k)
     x = torch.randn((rows, k), generator=g, device="cuda").to(torch.bfloat16)
     w = (torch.randn((n, k), generator=g, device="cuda") / k**0.5).to(torch.bfloat16)
