@@ -59,12 +59,7 @@ constexpr int kTcThreadsF8 = 320;
 #ifndef FM_GEMM_PAIR_MIN_TILES
 #define FM_GEMM_PAIR_MIN_TILES 1
 #endif
-// The pair kernel's partition: whole tiles (0), or stream-K over the pairs (1; slower
-// on every measured shape: 170 vs 152 us on 2048 x 12288 x 4096, 392 vs 348 us on the
-// 2048-row folded head, 72 vs 60 us at 512 rows).
-#ifndef FM_PAIR_STREAMK
-#define FM_PAIR_STREAMK 0
-#endif
+
 
 // One pipeline stage: the bf16 weight tile (A, 128 x 64, 128B-swizzled), the
 // activation tile (B, BN x 64, 128B-swizzled) and, for e4m3 weights, the raw e4m3
@@ -710,9 +705,7 @@ __global__ void __launch_bounds__(TcCfg<BN, F8>::THREADS, TcCfg<BN, F8>::PER_SM)
 // their bytes on rank 0's mbarrier (the pair form of the TMA copy), and rank 0's MMA
 // commits free the stage and hand over the accumulator on both ranks (multicast
 // commits). Whole tiles: pair p takes tiles p, p + P, ..., numbered activation tile
-// fastest (or, with FM_PAIR_STREAMK, stream-K over the pairs with split tiles summed per
-// rank in pair order through the scratch, as in the one-SM kernel). Every tcgen05
-// instruction of the kernel is of the pair form.
+// fastest. Every tcgen05 instruction of the kernel is of the pair form.
 
 // Pair pipeline depth (6 x 32 KB) and threads: warp 0 TMA, warp 1 MMA (rank 0),
 // warps 2-5 epilogue.
@@ -723,9 +716,10 @@ struct PairCfg {
   static constexpr int B_BYTES = 128 * 64 * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TX_BYTES = 2 * STAGE_BYTES;  // both ranks' bytes of a stage, counted at rank 0
-  // 16 KB past the ring: a 256-row read of the last stage's B operand would still stay
-  // inside this CTA's shared memory (each rank's MMA operand halves are 128 rows)
-  static constexpr int SMEM = kPairStages * STAGE_BYTES + 16384 + 1024;
+  // The whole of the SM's shared memory (227 KB less the static part): no CTA of
+  // another kernel shares an SM with a pair CTA. (It also leaves 16 KB and more past the
+  // ring, so a 256-row read of the last stage's B operand would stay inside it.)
+  static constexpr int SMEM = 227 * 1024 - 1024;
   static constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
 };
 
@@ -810,8 +804,7 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, vol
 __global__ void __launch_bounds__(kPairThreads, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX,
                    void* __restrict__ out, int ldo, int R, int N, int K, const float* __restrict__ alpha,
-                   const float* __restrict__ beta, int mode, unsigned* red_cnt, float* red_slots,
-                   unsigned* dev_err) {
+                   const float* __restrict__ beta, int mode, unsigned* dev_err) {
   using C = PairCfg;
   constexpr int S = kPairStages;
   extern __shared__ uint8_t smem_raw[];
@@ -820,7 +813,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __shared__ uint64_t full_bar[S], empty_bar[S], acc_full[2], acc_empty[2], drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ int64_t issued, consumed;
+  __shared__ int issued, consumed;
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // the same offset in both ranks
@@ -829,33 +822,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   const uint32_t rank = cluster_rank();
   const int pair = blockIdx.x >> 1, P = gridDim.x >> 1;
   const int mt2 = (N + 255) >> 8, rt = (R + 255) >> 8, KB = (K + 63) >> 6;
-  // Units (tile, 64-wide k block). Stream-K (FM_PAIR_STREAMK): pair p takes the
-  // contiguous range [T p / P, T (p + 1) / P), tiles numbered weight tile fastest, so
-  // the pairs that need one weight tile reach it at about the same step. Whole tiles:
-  // pair p takes tiles p, p + P, ..., numbered activation tile fastest, so the pairs
-  // running together share a few weight tiles; its units are numbered locally.
-  const int64_t T2 = static_cast<int64_t>(mt2) * rt, T = T2 * KB;
-  int64_t it0, it1;
-  if (FM_PAIR_STREAMK) {
-    it0 = T * pair / P;
-    it1 = T * (pair + 1) / P;
-  } else {
-    it0 = 0;
-    it1 = pair < T2 ? ((T2 - 1 - pair) / P + 1) * KB : 0;
-  }
-  if (it0 == it1) return;  // both ranks of the pair
-  // (weight tile m2, activation tile r) of unit it's tile
-  auto tile_mr = [&](int64_t it, int& m2, int& r) {
-    if (FM_PAIR_STREAMK) {
-      const int64_t t = it / KB;
-      r = static_cast<int>(t / mt2);
-      m2 = static_cast<int>(t - static_cast<int64_t>(r) * mt2);
-    } else {
-      const int64_t t = pair + (it / KB) * P;
-      m2 = static_cast<int>(t / rt);
-      r = static_cast<int>(t - static_cast<int64_t>(m2) * rt);
-    }
-  };
+  // Whole tiles, numbered activation tile fastest (t = m2 * rt + r) so that the pairs
+  // running together share a few weight tiles: pair p takes tiles p, p + P, ...
+  const int T2 = mt2 * rt;
+  const int ntile = pair < T2 ? (T2 - 1 - pair) / P + 1 : 0;
+  const int total = ntile * KB;  // this pair's units (64-wide k blocks)
+  if (total == 0) return;        // both ranks of the pair
+  auto seg_tile = [&](int g) { return pair + g * P; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -888,41 +861,40 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       const uint64_t pol_w = l2_policy_evict_first(), pol_x = l2_policy_evict_last();
       const uint32_t full0 = cluster_map(smem_u32(&full_bar[0]), 0u);  // rank 0's barriers
       const int row_off = static_cast<int>(rank) * 128;
-      // the position (k block, tile) advances by one unit per stage; the tile's (m2, r)
-      // is recomputed once per tile (no division per stage on this single thread)
+      // the position advances by one unit per stage; the tile's (m2, r) is recomputed
+      // once per segment (no division per stage on this single thread)
       struct Cur {
-        int64_t it;
-        int kb, m2, r;
+        int u, g, kb, m2, r;
       };
-      auto start = [&](int64_t it) {
-        Cur c;
-        c.it = it;
-        c.kb = static_cast<int>(it % KB);
-        tile_mr(it, c.m2, c.r);
-        return c;
+      auto enter = [&](Cur& c, int g) {
+        c.g = g;
+        const int t = seg_tile(g);
+        c.m2 = t / rt;
+        c.r = t - c.m2 * rt;
+        c.kb = 0;
       };
       auto next = [&](Cur& c) {
-        ++c.it;
-        if (++c.kb == KB) {
-          c.kb = 0;
-          if (c.it < it1) tile_mr(c.it, c.m2, c.r);
-        }
+        ++c.u;
+        if (++c.kb == KB && c.u < total) enter(c, c.g + 1);
       };
-      const int pre = static_cast<int>(min(static_cast<int64_t>(S), it1 - it0));
-      Cur c = start(it0);
+      const int pre = min(S, total);
+      Cur c;
+      c.u = 0;
+      enter(c, 0);
       for (int i = 0; i < pre; ++i, next(c)) {  // weights first: they depend on no earlier kernel
         if (rank == 0) mbar_arrive_expect_tx(&full_bar[i], C::TX_BYTES);
         tma_load_2d_pair(smem + i * C::STAGE_BYTES, &mapW, full0 + i * 8, c.kb * 64, c.m2 * 256 + row_off, pol_w);
       }
       pdl_wait();
-      c = start(it0);
+      c.u = 0;
+      enter(c, 0);
       for (int i = 0; i < pre; ++i, next(c))
         tma_load_2d_pair(smem + i * C::STAGE_BYTES + C::A_BYTES, &mapX, full0 + i * 8, c.kb * 64, c.r * 256 + row_off,
                          pol_x);
       issued = pre;
       int stage = pre % S;
       uint32_t phase = pre == S ? 1u : 0u;
-      for (; c.it < it1; next(c)) {
+      for (; c.u < total; next(c)) {
         if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) break;
         uint8_t* sa = smem + stage * C::STAGE_BYTES;
         if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
@@ -936,22 +908,18 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {  // the MMA issuer for the pair: one segment per tile piece
+    if (lane == 0 && rank == 0) {  // the MMA issuer for the pair: one accumulator per tile
       constexpr uint32_t idesc = idesc_bf16_f32(256, 256);
       int stage = 0;
       uint32_t phase = 0;
-      int seg = 0;
-      int64_t it = it0;
       bool ok = true;
-      while (ok && it < it1) {
-        const int64_t seg_end = min(it1, (it / KB + 1) * KB);
-        const int buf = seg & 1;
-        const uint32_t aph = (seg >> 1) & 1;
+      for (int g = 0; ok && g < ntile; ++g) {
+        const int buf = g & 1;
+        const uint32_t aph = (g >> 1) & 1;
         if (!mbar_wait_cl(&acc_empty[buf], aph ^ 1u, &abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(buf * 256);
-        bool first = true;
-        for (; it < seg_end; ++it) {
+        for (int k64 = 0; k64 < KB; ++k64) {
           if (!mbar_wait_cl(&full_bar[stage], phase, &abort_flag)) {
             ok = false;
             break;
@@ -961,8 +929,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const uint32_t sa = base + stage * C::STAGE_BYTES;
           const uint64_t ad = sdesc_sw128(sa), bd = sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) umma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-          first = false;
+          for (int k = 0; k < 4; ++k) umma_bf16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (k64 == 0 && k == 0) ? 0u : 1u);
           umma_commit_pair_both(&empty_bar[stage]);
           if (++stage == S) {
             stage = 0;
@@ -971,7 +938,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         }
         if (!ok) break;
         umma_commit_pair_both(&acc_full[buf]);
-        ++seg;
       }
       umma_commit_pair_self(&drain_bar);  // every MMA issued above has completed past this wait
       if (!mbar_wait_timed(&drain_bar, 0)) abort_flag = 1;
@@ -980,28 +946,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     pdl_wait();
     const int q = warp & 3, chan = q * 32 + lane;
     const uint32_t empty0 = cluster_map(smem_u32(&acc_empty[0]), 0u);
-    // this rank's scratch slot of pair c's part of `tile` (two per pair and rank)
-    auto slot_of = [&](int c, int64_t tile) {
-      return red_slots + (split_slot(c, tile, T, P, KB) * 2 + rank) * (256 * 128) + static_cast<int64_t>(chan) * 256;
-    };
-    int seg = 0;
-    int64_t it = it0;
-    while (it < it1) {
-      const int64_t tile = it / KB;
-      const int64_t tile_end = (tile + 1) * KB;
-      const int64_t seg_end = min(it1, tile_end);
-      int m2, r;
-      tile_mr(it, m2, r);
+    const bool add = mode == static_cast<int>(Out::Add);
+    for (int g = 0; g < ntile; ++g) {
+      const int t = seg_tile(g), m2 = t / rt, r = t - m2 * rt;
       const int n = m2 * 256 + static_cast<int>(rank) * 128 + chan;
       float a = 1.f, b = 0.f;
       if (n < N) {
         if (alpha) a = alpha[n];
         if (beta) b = beta[n];
       }
-      const int buf = seg & 1;
-      const bool head = it == tile * KB, tail = seg_end == tile_end;
+      const int buf = g & 1;
       const uint32_t tacc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * 256);
-      const bool add = mode == static_cast<int>(Out::Add);
       float* op = static_cast<float*>(out) + static_cast<int64_t>(r) * 256 * ldo + n;  // (row r * 256, n)
       // the 16 output values of rows c0 .. c0 + 15 that an addition reads (issued a
       // chunk ahead)
@@ -1010,114 +965,33 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         for (int j = 0; j < 16; ++j)
           o16[j] = (n < N && r * 256 + c0 + j < R) ? __ldcg(op + static_cast<int64_t>(c0 + j) * ldo) : 0.f;
       };
-      // rows c0 .. c0 + 15 of this channel: y = a * v + b, added onto o16 or written
-      auto write16 = [&](int c0, const float (&v)[16], const float (&o16)[16]) {
-        if (n >= N) return;
-        const int row0 = r * 256 + c0;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          if (row0 + j >= R) break;
-          if (add)
-            op[static_cast<int64_t>(c0 + j) * ldo] = o16[j] + fmaf(a, v[j], b);
-          else
-            emit_out(mode, out, ldo, row0 + j, n, fmaf(a, v[j], b));
-        }
-      };
-      // the sum of pairs c_lo + 1 .. c_hi's parts of rows c0 .. c0 + 15, in pair order
-      auto others16 = [&](int c_lo, int c_hi, int c0, float (&s16)[16]) {
-        for (int c = c_lo + 1; c <= c_hi; ++c) {
-          const float4* p4 = reinterpret_cast<const float4*>(slot_of(c, tile) + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 t4 = __ldcg(p4 + i);
-            const float t[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s16[4 * i + e] = c == c_lo + 1 ? t[e] : s16[4 * i + e] + t[e];
-          }
-        }
-      };
       const int nrows = min(256, R - r * 256);  // rows of this tile present (> 0)
-      bool counted = true;  // the split-tile counter is complete (or not needed)
-      int c_lo = pair, c_hi = pair;
-      unsigned* cnt = nullptr;
-      if (!(head && tail)) {
-        c_lo = head ? pair : unit_owner(tile * KB, T, P);
-        c_hi = tail ? pair : unit_owner(tile_end - 1, T, P);
-        cnt = red_cnt + 8 * c_lo + 4 * static_cast<int>(rank) + q;
-        // the first k blocks' pair (head) usually arrives last: then it sums
-        counted = head && __all_sync(0xffffffffu, ld_acquire_u32(cnt) == static_cast<unsigned>(c_hi - c_lo));
-      }
       float on[16];
-      if (counted && add) load_out(0, on);  // the first chunk's output, before the accumulator wait
-      if (!mbar_wait(&acc_full[buf], (seg >> 1) & 1, &abort_flag)) break;
+      if (add) load_out(0, on);  // the first chunk's output, before the accumulator wait
+      if (!mbar_wait(&acc_full[buf], (g >> 1) & 1, &abort_flag)) break;
       tc_fence_after();
-      if (counted) {  // whole tile, or the head with every other part counted: sum, in pair order
 #pragma unroll 1
-        for (int c0 = 0; c0 < nrows; c0 += 16) {
-          float o16[16], v[16], s16[16];
+      for (int c0 = 0; c0 < nrows; c0 += 16) {
+        float o16[16], v[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o16[j] = on[j];
-          if (add && c0 + 16 < nrows) load_out(c0 + 16, on);
-          if (!(head && tail)) others16(c_lo, c_hi, c0, s16);
-          tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
-          if (!(head && tail)) {
+        for (int j = 0; j < 16; ++j) o16[j] = on[j];
+        if (add && c0 + 16 < nrows) load_out(c0 + 16, on);
+        tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
+        if (n < N) {  // rows c0 .. c0 + 15 of this channel: y = a v + b, added onto o16 or written
+          const int row0 = r * 256 + c0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = s16[j] + v[j];
+          for (int j = 0; j < 16; ++j) {
+            if (row0 + j >= R) break;
+            if (add)
+              op[static_cast<int64_t>(c0 + j) * ldo] = o16[j] + fmaf(a, v[j], b);
+            else
+              emit_out(mode, out, ldo, row0 + j, n, fmaf(a, v[j], b));
           }
-          write16(c0, v, o16);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_cluster(empty0 + static_cast<uint32_t>(buf * 8));
-          if (!(head && tail)) *cnt = 0;  // every other part has counted: ready for the next launch
-        }
-      } else {  // leave this part and count it; the last to count sums
-        float* mine = slot_of(pair, tile);
-#pragma unroll 1
-        for (int c0 = 0; c0 < 256; c0 += 16) {
-          float v[16];
-          tmem_ld16(tacc + static_cast<uint32_t>(c0), v);
-          float4* p4 = reinterpret_cast<float4*>(mine + c0);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) p4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(empty0 + static_cast<uint32_t>(buf * 8));
-        __threadfence();  // this lane's part is visible before the count
-        __syncwarp();
-        unsigned ticket = 0;
-        if (lane == 0) {
-          ticket = atomicAdd(cnt, 1u);
-          __threadfence();
-        }
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        if (ticket == static_cast<unsigned>(c_hi - c_lo)) {  // last of all c_hi - c_lo + 1 parts
-          __threadfence();
-          if (add) load_out(0, on);
-#pragma unroll 1
-          for (int c0 = 0; c0 < nrows; c0 += 16) {
-            float o16[16], v[16], s16[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) o16[j] = on[j];
-            if (add && c0 + 16 < nrows) load_out(c0 + 16, on);
-            others16(c_lo, c_hi, c0, s16);
-            const float4* p0 = reinterpret_cast<const float4*>(slot_of(c_lo, tile) + c0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 t4 = __ldcg(p0 + i);
-              v[4 * i] = s16[4 * i] + t4.x, v[4 * i + 1] = s16[4 * i + 1] + t4.y;
-              v[4 * i + 2] = s16[4 * i + 2] + t4.z, v[4 * i + 3] = s16[4 * i + 3] + t4.w;
-            }
-            write16(c0, v, o16);
-          }
-          __syncwarp();
-          if (lane == 0) *cnt = 0;
         }
       }
-      it = seg_end;
-      ++seg;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(empty0 + static_cast<uint32_t>(buf * 8));
     }
   }
 
@@ -1125,8 +999,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (threadIdx.x == 0 && rank == 0 && abort_flag) {
     // Wait (bounded) for the loads still in flight: rank 0's stage barriers count both
     // ranks' bytes of every stage it armed.
-    for (int64_t i = consumed; i < issued; ++i)
-      mbar_wait_timed(&full_bar[i % S], static_cast<uint32_t>((i / S) & 1));
+    for (int i = consumed; i < issued; ++i) mbar_wait_timed(&full_bar[i % S], static_cast<uint32_t>((i / S) & 1));
   }
   tc_fence_before();
   __syncthreads();
@@ -1371,13 +1244,9 @@ cudaError_t launch_pair(const Launch& L, const Weight& W, const void* x, int R, 
   std::string err;
   if (!make_tmap_bf16(&mapX, x, R, W.K, ldx, 128, &err)) return cudaErrorInvalidValue;
   const int P = static_cast<int>(std::min<int64_t>(T2, pairs));
-  // the split-tile scratch: four counters per pair and rank, two 128 x 256 slots per
-  // pair and rank
-  if (!L.red.cnt || !L.red.slots || 8LL * P > L.red.cnt_cap || 4LL * P * 256 * 128 > L.red.slot_cap)
-    return cudaErrorInvalidValue;
   *used = true;
   return launch_kc(L, tc_pair_kernel, dim3(2 * P), dim3(kPairThreads), PairCfg::SMEM, 2, W.map, mapX, out, ldo, R,
-                   W.N, W.K, alpha, beta, static_cast<int>(mode), L.red.cnt, L.red.slots, L.dev_err);
+                   W.N, W.K, alpha, beta, static_cast<int>(mode), L.dev_err);
 }
 
 template <bool F8>
