@@ -159,9 +159,12 @@ typedef struct {
  * Layout (device, kv_dtype): [num_layers][2 (key, value)][num_pages][num_heads]
  * [page_size][head_dim]; the slot of position pos of the request in page-table row
  * r is req_to_page[r][pos / P] * P + pos % P. An E4M3 pool stores each (page, head)
- * block of VALUES channel-major instead, [head_dim][page_size] (keys as above), so
- * that the cross-attention's value product reads it without a transpose. The size is
- * the same either way. Caller-owned; size it with flashmap_pool_bytes.
+ * block of VALUES channel-major instead, [head_dim][page_size] (keys as above), and
+ * within every 16 positions of a channel row position 2t + e at byte 4t + e and
+ * position 8 + 2t + e at byte 4t + 2 + e (t < 4, e < 2): the order in which the
+ * cross-attention's value product takes them, so that it reads the block without a
+ * transpose. The size is the same either way. Caller-owned; size it with
+ * flashmap_pool_bytes.
  */
 typedef struct {
   void* base;

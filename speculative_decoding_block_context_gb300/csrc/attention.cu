@@ -472,12 +472,8 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
     mma_bf16_16816(d, a, b0, b1);
 }
 
-// Score column n of a 16-position block of an e4m3 pool is position kPerm(n): columns
-// 2t, 2t+1 hold positions 4t, 4t+1 and columns 8+2t, 9+2t positions 4t+2, 4t+3 (the
-// order in which an ldmatrix of the channel-major values delivers them); kPermInv is
-// the ring row of position p.
-__device__ __forceinline__ int kPerm(int n) { return 4 * ((n & 7) >> 1) + 2 * (n >> 3) + (n & 1); }
-__device__ __forceinline__ int kPermInv(int p) { return 8 * ((p >> 1) & 1) + 2 * (p >> 2) + (p & 1); }
+// The byte of position p (< 16) in a 16-byte row of an e4m3 pool's channel-major values.
+__device__ __forceinline__ int vbyte_of(int p) { return 4 * ((p & 7) >> 1) + 2 * (p >> 3) + (p & 1); }
 
 constexpr float kLazyLog2 = 8.f;  // the running max's slack: p <= 2^8
 constexpr int kXStages = 3;   // bf16 pool, one candidate: cp.async stages per warp
@@ -496,10 +492,9 @@ __device__ __forceinline__ void bar_sync(int id, int threads) {
 // e4m3 tensor-core product as stored, and the values arrive channel-major (the pool
 // keeps each (page, head) block of values that way): one 16-byte row per channel holds
 // the block's 16 positions, so a plain ldmatrix hands each thread four consecutive
-// positions of one channel, widened to half in registers for the half product with the
-// probabilities. The four are positions 4t..4t+3 where the product's fragment wants
-// k = 2t, 2t+1, 2t+8, 2t+9: the keys are placed in the ring in the matching order
-// (score column n is position kPerm(n)), so the product over k is unchanged.
+// bytes of one channel, widened to half in registers for the half product with the
+// probabilities. The pool orders each 16 positions so that bytes 4t..4t+3 are positions
+// 2t, 2t+1, 2t+8, 2t+9, the k rows the product's fragment wants from thread t.
 template <int HD, bool F8 = false, int NC = 1>
 struct XCfg {
   static constexpr int WPC = 4 / NC;      // warps per candidate = rings per CTA
@@ -612,18 +607,19 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
         const int64_t vb = kb + kv_stride;
         const uint32_t st = ring + (j % C::STAGES) * C::STAGE;
         if constexpr (F8) {
-          // keys: rows of 16-byte chunks, swizzled, position r at ring row kPermInv(r)
+          // keys: rows of 16-byte chunks, swizzled
 #pragma unroll
           for (int i = ci0; i < 16 * C::CH8; i += 32 * NC) {
-            const int r = i / C::CH8, ch = i - r * C::CH8, rr = kPermInv(r);
+            const int r = i / C::CH8, ch = i - r * C::CH8;
             const uint32_t bytes = (ok && blk + r < p1) ? 16u : 0u;
-            const uint32_t dst = st + rr * C::ROWB8 + ((ch ^ ((rr >> C::SW8) & (C::CH8 - 1))) << 4);
+            const uint32_t dst = st + r * C::ROWB8 + ((ch ^ ((r >> C::SW8) & (C::CH8 - 1))) << 4);
             cp_async16(dst, pool + (kb + r * HD) * ES + ch * 16, bytes);
           }
           // values: channel c of the block is 16 bytes at c * P + off in the (page, head)
-          // block, positions past the chunk zero-filled
+          // block (an invalid page's zero-filled; positions past the chunk are zeroed
+          // once they have landed)
           const int64_t vblk = kb - off * HD + kv_stride;
-          const uint32_t vbytes = ok ? static_cast<uint32_t>(max(0, min(16, p1 - blk))) : 0u;
+          const uint32_t vbytes = ok ? 16u : 0u;
 #pragma unroll
           for (int i = ci0; i < HD; i += 32 * NC)
             cp_async16(st + C::BLK8 + i * 16, pool + vblk + static_cast<int64_t>(i) * a.P + off, vbytes);
@@ -719,7 +715,16 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
           mma16816<F8>(s[1], qa[kk], b2, b3);
         }
       }
-      if constexpr (F8) vst = kst + C::BLK8;  // the channel-major e4m3 values
+      if constexpr (F8) {
+        vst = kst + C::BLK8;  // the channel-major e4m3 values
+        if (blk + 16 > p1) {  // the chunk's last block: zero the values of positions past it
+          const int valid = max(0, p1 - blk);
+          uint8_t* vrow = xsm + (vst - smem_u32(xsm));
+          for (int ch = lane; ch < HD; ch += 32)
+            for (int p = valid; p < 16; ++p) vrow[ch * 16 + vbyte_of(p)] = 0;
+          __syncwarp();
+        }
+      }
       // scale to base 2 and mask positions past the chunk (the last block only)
       if (blk + 16 <= p1) {
 #pragma unroll
@@ -731,8 +736,7 @@ __global__ void __launch_bounds__(128, F8 ? 3 : 2) xattn_items_mma_kernel(XattnA
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int n = nt * 8 + 2 * t4 + (e & 1);
-            const int pos = blk + (F8 ? kPerm(n) : n);
+            const int pos = blk + nt * 8 + 2 * t4 + (e & 1);
             s[nt][e] = pos < p1 ? s[nt][e] * s_scale : -INFINITY;
           }
       }

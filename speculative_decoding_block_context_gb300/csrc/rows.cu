@@ -127,9 +127,12 @@ __global__ void __launch_bounds__(1024, 2) kv_write_kernel(KvWriteArgs a) {
     store_vec<T, EPL>(pool + r * HD + lane * EPL, k);
     if constexpr (sizeof(T) == 1) {
       // an e4m3 pool keeps each (page, head) block of values channel-major: channel c of
-      // the block's positions is a row of P bytes (the cross-attention reads it as the
-      // B operand of its P V product without a transpose)
-      T* vb = pool + (r - off + kv_stride) * HD + off;
+      // the block's positions is a row of P bytes, and within each 16 positions position
+      // 2t + e sits at byte 4t + e and position 8 + 2t + e at 4t + 2 + e (t < 4, e < 2),
+      // the order in which the cross-attention's P V product takes them (a plain
+      // ldmatrix gives each thread 4 consecutive bytes)
+      const int o16 = static_cast<int>(off & 15);
+      T* vb = pool + (r - off + kv_stride) * HD + (off & ~15LL) + (4 * ((o16 & 7) >> 1) + 2 * (o16 >> 3) + (o16 & 1));
 #pragma unroll
       for (int e = 0; e < EPL; ++e)
         vb[static_cast<int64_t>(lane * EPL + e) * a.P] =

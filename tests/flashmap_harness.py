@@ -62,10 +62,22 @@ def load_model(workload: str, device="cuda", oracle: bool = True) -> ModelState:
     return st
 
 
+def value_byte(cfg: dict) -> torch.Tensor:
+    """Where each position of a page sits in an e4m3 pool's channel-major value rows:
+    within every 16 positions, position 2t + e at byte 4t + e and position 8 + 2t + e at
+    byte 4t + 2 + e (t < 4, e < 2); the identity for other pools."""
+    p = torch.arange(cfg["page_size"])
+    if cfg["kv_dtype"] != "e4m3":
+        return p
+    o = p % 16
+    return p - o + 4 * ((o % 8) // 2) + 2 * (o // 8) + o % 2
+
+
 def pool_view(cfg: dict, pool_t: torch.Tensor, num_pages: int) -> tuple:
-    """Views of the pool's keys and values, each (L, pages, heads, P, hd) position-major.
-    An e4m3 pool keeps each (page, head) block of values channel-major (hd, P): that view
-    is a transposed one. No copy."""
+    """Views of the pool's keys and values as stored: keys (L, pages, heads, P, hd); values
+    the same for a bf16 or f32 pool, and for an e4m3 pool, which keeps each (page, head)
+    block of values channel-major (hd, P) with the positions in value_byte order, a
+    transposed view (L, pages, heads, P, hd) indexed by byte. No copy."""
     dt = syn.torch_dtype(cfg["kv_dtype"])
     L, nh, P, hd = cfg["num_layers"], cfg["num_heads"], cfg["page_size"], cfg["head_dim"]
     kv = pool_t.view(dt).view(L, 2, num_pages * nh * P * hd)
@@ -80,7 +92,10 @@ def pool_view(cfg: dict, pool_t: torch.Tensor, num_pages: int) -> tuple:
 def slot_rows(cfg: dict, kv: tuple, s: torch.Tensor) -> tuple:
     """The (L, n, heads, hd) keys and values at pool slots s (a device int64 tensor)."""
     P = cfg["page_size"]
-    return tuple(t.permute(1, 3, 0, 2, 4)[s // P, s % P].permute(1, 0, 2, 3) for t in kv)
+    vb = value_byte(cfg).to(s.device)
+    k, v = kv
+    return (k.permute(1, 3, 0, 2, 4)[s // P, s % P].permute(1, 0, 2, 3),
+            v.permute(1, 3, 0, 2, 4)[s // P, vb[s % P]].permute(1, 0, 2, 3))
 
 
 def gather_context(cfg: dict, kv: tuple, req_to_page_row: torch.Tensor, n: int):
@@ -89,9 +104,13 @@ def gather_context(cfg: dict, kv: tuple, req_to_page_row: torch.Tensor, n: int):
     P = cfg["page_size"]
     npages = (n + P - 1) // P
     pages = req_to_page_row[:npages].long()
+    vb = value_byte(cfg).to(pages.device)
     out = []
-    for t in kv:
-        g = t[:, pages].permute(0, 1, 3, 2, 4).reshape(cfg["num_layers"], npages * P, cfg["num_heads"], cfg["head_dim"])
+    for i, t in enumerate(kv):
+        g = t[:, pages]
+        if i == 1:
+            g = g[:, :, :, vb]  # positions in order
+        g = g.permute(0, 1, 3, 2, 4).reshape(cfg["num_layers"], npages * P, cfg["num_heads"], cfg["head_dim"])
         out.append(g[:, :n].float().cpu().numpy())
     return out[0], out[1]
 
