@@ -1,19 +1,23 @@
 // Dense contractions of the FlashMap step.
 //
-// bf16: a persistent, warp-specialized tcgen05 kernel. Every linear of the step is
-// "weights x activations" with few activation rows (16 at batch 1), so the weight
-// matrix W (N x K) is the MMA's A operand (M = 128 output channels per tile) and the
-// activation rows are the B operand (N = 16..256 rows): the tensor core's large M
-// dimension is spent on the weights and no row padding to 128 is needed. The
-// iteration space (output tile, 64-wide k block) is cut into equal contiguous ranges,
-// one per CTA (stream-K), so every SM streams the same number of weight bytes whatever
-// the shape. A tile split over several CTAs is summed in a fixed order, so results
-// repeat bit for bit: every CTA but one leaves its partial tile in a scratch slot and
-// counts it; the CTA holding the tile's first k blocks (it reaches them last, at the
-// end of its range) finds the others counted, adds their partials in CTA order while
-// its own MMAs finish, then adds its own and writes the tile. If it arrives before
-// all the others it leaves its partial too, and whichever arrives last sums the slots
-// in the same order. No CTA waits for another.
+// bf16 and e4m3 weights: a persistent, warp-specialized tcgen05 kernel. Every linear of
+// the step is "weights x activations" with few activation rows (16 at batch 1), so the
+// weight matrix W (N x K) is the MMA's A operand (M = 128 output channels per tile) and
+// the activation rows are the B operand (N = 16..256 rows): the tensor core's large M
+// dimension is spent on the weights and no row padding to 128 is needed. With at most
+// half as many tiles as CTAs, a thread-block cluster splits each tile's k range and
+// sums it through shared memory in rank order. Otherwise the iteration space (output
+// tile, 64-wide k block) is cut into equal contiguous ranges, one per CTA (stream-K),
+// so every SM streams the same number of weight bytes whatever the shape. A tile split
+// over several CTAs is summed in a fixed order, so results repeat bit for bit: every
+// CTA but one leaves its partial tile in a scratch slot and counts it; the CTA holding
+// the tile's first k blocks (it reaches them last, at the end of its range) finds the
+// others counted, adds their partials in CTA order while its own MMAs finish, then adds
+// its own and writes the tile. If it arrives before all the others it leaves its
+// partial too, and whichever arrives last sums the slots in the same order. No CTA
+// waits for another's counter.
+// Above 128 rows, bf16 GEMMs with a 256 x 256 tile for every SM pair run on SM pairs
+// instead (tc_pair_kernel, tcgen05 cta_group::2: half of both operands per SM).
 // Roles: warp 0 issues TMA loads (128B-swizzled, weights with an evict-first L2
 // policy), warp 1 owns TMEM and issues tcgen05.mma, warps 2-5 drain the double-
 // buffered TMEM accumulator (tcgen05.ld) into global memory, each warp its own 32
