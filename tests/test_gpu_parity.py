@@ -51,14 +51,13 @@ def test_philox_words_bit_exact():
     np.testing.assert_allclose(normals[:4096].cpu().numpy(), np.stack([n0, n1, n2, n3], 1), rtol=2e-5, atol=2e-5)
 
 
-# Shapes span both ways a tile's k range is split: thread-block clusters of up to 8
-# CTAs summing through shared memory (at most half as many weight tiles as CTAs, e.g.
-# 16 x 4096 -> 4096 in clusters of 8, 16 x 4096 -> 12288 in clusters of 3) and
+# Shapes span both ways a tile's k range is split on one SM: thread-block clusters of up
+# to 8 CTAs summing through shared memory (at most half as many weight tiles as CTAs,
+# e.g. 16 x 4096 -> 4096 in clusters of 8, 16 x 4096 -> 12288 in clusters of 3) and
 # stream-K over every CTA with two or three parts per tile summed through the scratch
-# (16 x 4096 -> 40960: 320 tiles; 200 x 4096 -> 12288: 96 tiles of 256 rows on one CTA
-# per SM, about 40 of a tile's 64 k blocks per CTA). The last four run on SM pairs
-# (tcgen05 cta_group::2, 256 x 256 tiles, stream-K over 76 pairs: 5.05, 8.3, 1.26 and
-# 4.1 tiles per pair, so most pairs hold a split tile; ragged rows, and last tiles whose
+# (16 x 4096 -> 40960: 320 tiles; 64 x 4096 -> 12288). 200 x 4096 -> 12288 and the last
+# four run on SM pairs (tcgen05 cta_group::2, whole 256 x 256 tiles: 48 of them on 48
+# pairs, then 5.05, 8.3, 1.26 and 4.1 tiles per pair; ragged rows, and last tiles whose
 # second half lies past N).
 @pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 200, 300), (16, 4096, 4096), (37, 384, 1234),
                                       (100, 256, 384), (300, 512, 256), (2048, 1024, 512), (300, 384, 1234),
