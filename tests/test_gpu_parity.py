@@ -58,11 +58,13 @@ def test_philox_words_bit_exact():
 # (16 x 4096 -> 40960: 320 tiles; 64 x 4096 -> 12288). 200 x 4096 -> 12288 and the last
 # four run on SM pairs (tcgen05 cta_group::2, whole 256 x 256 tiles: 48 of them on 48
 # pairs, then 5.05, 8.3, 1.26 and 4.1 tiles per pair; ragged rows, and last tiles whose
-# second half lies past N).
+# second half lies past N); 512 x 1024 -> 4096 and 300 x 512 -> 4800 with 32 and 38
+# tiles, the fewest that take the pairs.
 @pytest.mark.parametrize("rows,k,n", [(1, 64, 128), (5, 200, 300), (16, 4096, 4096), (37, 384, 1234),
                                       (100, 256, 384), (300, 512, 256), (2048, 1024, 512), (300, 384, 1234),
                                       (513, 4096, 384), (16, 4096, 12288), (16, 12288, 4096), (16, 4096, 40960),
-                                      (200, 4096, 12288), (64, 4096, 12288), (2048, 512, 12288), (1000, 256, 40000), (512, 1024, 12288), (300, 384, 40000)])
+                                      (200, 4096, 12288), (64, 4096, 12288), (2048, 512, 12288), (1000, 256, 40000), (512, 1024, 12288), (300, 384, 40000),
+                                      (512, 1024, 4096), (300, 512, 4800)])
 def test_linear_bf16_tcgen05(rows, k, n):
     """y = x W^T added onto a nonzero output (the residual stream's mode), against
     float64; a second call on the same inputs gives the same bits (every split tile is
